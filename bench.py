@@ -1,0 +1,377 @@
+#!/usr/bin/env python
+"""KDA forward benchmark: tokens/s of the whole hot path on one GB300 per rank.
+
+A step is one pass of the whole path over one batch: kda_gate (decay and beta
+from their pre-activations) then kda_chunk_fwd (chunked KDA forward with the
+final state), on the 16384-token, 64-head, K=V=128 BF16 workload by default.
+Inputs are resident in HBM when the timed region starts and are larger than
+L2, so no flush is needed between steps.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--mode bf16_tc|fp32_exact]
+    python bench.py --impl reference ...   # the FP64 CPU oracle, on a bounded sample
+
+Under torchrun (N > 1) every rank runs the same workload on its own GPU (weak
+scaling: independent batches, no data-path collective); the timing is the
+maximum over ranks and rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "KDA chunk-forward tokens/s at H=64,K=V=128,T=16384; % of roofline"
+UNIT = "tokens/s"
+DEFAULT_WORKLOAD = "single_16384_bf16"
+HBM_FALLBACK_GBS = 6800.0
+# The pages' H200 chunk-forward p50 at 16384 tokens, 64 heads x 128, original
+# intermediates ("Add opt-in FP32 KDA chunk computation", section Validation).
+H200_CHUNK_US_16384 = 4050.976
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--mode", choices=["bf16_tc", "fp32_exact"], default=None)
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            d = json.load(fh)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return HBM_FALLBACK_GBS, "fallback"
+
+
+def kernel_traffic(kernel_key: str):
+    """DRAM bytes per launch from a committed ncu summary, if it still matches
+    the kernel source; None otherwise."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as fh:
+            d = json.load(fh)
+    except Exception:
+        return None
+    ent = d.get(kernel_key)
+    if not ent:
+        return None
+    src = os.path.join(ROOT, ent["source"])
+    try:
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    except Exception:
+        return None
+    return ent["dram_bytes_per_launch"] if sha == ent["source_sha256_16"] else None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="kda_clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.gpu_index), "-lms", "50"], stdout=self.out,
+                stderr=subprocess.DEVNULL)
+            time.sleep(0.15)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [s.strip() for s in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(nm)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def algorithmic_bytes(T, H, K, V, N, qkv_bytes, out_bytes):
+    """Compulsory HBM bytes of one kda_chunk_fwd launch: read q, k, v, g (FP32),
+    beta (FP32); write out and the FP32 final state."""
+    per_token_head = (2 * K + V) * qkv_bytes + 4 * K + 4 + V * out_bytes
+    return T * H * per_token_head + N * H * K * V * 4
+
+
+def gate_bytes(T, H, K):
+    return T * H * K * (4 + 4) + T * H * (4 + 4)
+
+
+def workload_config(w, mode):
+    return {"workload": w.name, "T": None, "N": None, "H": w.H, "K": w.K, "V": w.V,
+            "qkv_dtype": str(w.qkv_dtype).replace("torch.", ""), "g_beta_dtype": "float32",
+            "mode": mode, "chunk": 64,
+            "l2": "inputs larger than L2 (no flush needed)", "parallelism": "replicas"}
+
+
+def run_reference(args):
+    """The FP64 CPU oracle, timed on the host cores over bounded samples."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import numpy as np
+    import oracle
+    from kimi_delta_attention_10_gb300.inputs import WORKLOAD_BY_NAME, workload_inputs
+
+    w = WORKLOAD_BY_NAME[args.workload]
+    x = workload_inputs(w)
+    heads_per_step = 2
+    f64 = lambda t: t.float().numpy().astype(np.float64)
+
+    def sample(step):
+        hs = [(2 * step + i) % w.H for i in range(heads_per_step)]
+        return (f64(x.q[:, hs]), f64(x.k[:, hs]), f64(x.v[:, hs]), f64(x.f[:, hs]),
+                f64(x.A_log[hs]), f64(x.dt_bias[hs]), f64(x.b[:, hs]))
+
+    def one(step):
+        arrs = sample(step)
+        t0 = time.perf_counter()
+        oracle.reference(*arrs, x.cu_seqlens.numpy(), x.scale)
+        return time.perf_counter() - t0
+
+    for s in range(args.warmup):
+        one(s)
+    total = 0.0
+    for s in range(args.steps):
+        total += one(args.warmup + s)
+    tokens = x.T * heads_per_step / w.H * args.steps
+    value = tokens / total
+    cfg = workload_config(w, "fp64_oracle")
+    cfg["T"], cfg["N"] = x.T, x.N
+    sample_desc = (f"{heads_per_step} of {w.H} heads x all {x.T} tokens per step "
+                   f"(gate + recurrence), value scaled to whole tokens")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": cfg,
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.default_threads(),
+                             "kind": "oracle", "sample": sample_desc},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def cpu_baseline(x, w, budget_heads=8):
+    import numpy as np
+    import oracle
+    hs = list(range(min(budget_heads, w.H)))
+    f64 = lambda t: t.float().numpy().astype(np.float64)
+    arrs = (f64(x.q[:, hs]), f64(x.k[:, hs]), f64(x.v[:, hs]), f64(x.f[:, hs]),
+            f64(x.A_log[hs]), f64(x.dt_bias[hs]), f64(x.b[:, hs]))
+    t0 = time.perf_counter()
+    oracle.reference(*arrs, x.cu_seqlens.numpy(), x.scale)
+    dt = time.perf_counter() - t0
+    return {"value": x.T * len(hs) / w.H / dt, "unit": UNIT, "cores": oracle.default_threads(),
+            "kind": "oracle",
+            "sample": f"FP64 oracle (gate + token recurrence) on heads 0-{len(hs) - 1} of {w.H}, "
+                      f"all {x.T} tokens ({dt:.2f} s wall); value scaled to whole tokens"}
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+        return
+
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    import __graft_entry__
+    __graft_entry__.build()
+    from kimi_delta_attention_10_gb300 import kda_chunk_fwd, kda_gate
+    from kimi_delta_attention_10_gb300.inputs import WORKLOAD_BY_NAME, workload_inputs
+
+    mode = args.mode or "fp32_exact"
+    w = WORKLOAD_BY_NAME[args.workload]
+    x = workload_inputs(w)
+    T, H, K, V, N = x.T, w.H, w.K, w.V, x.N
+    out_dtype = torch.float32 if mode == "fp32_exact" else x.v.dtype
+    d = {n: getattr(x, n).to(dev) for n in ("q", "k", "v", "f", "A_log", "dt_bias", "b",
+                                            "cu_seqlens")}
+    cu_host = x.cu_seqlens.tolist()
+    g = torch.empty(T, H, K, device=dev)
+    beta = torch.empty(T, H, device=dev)
+    out = torch.empty(T, H, V, dtype=out_dtype, device=dev)
+    fs = torch.empty(N, H, K, V, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        kda_gate(d["f"], d["A_log"], d["dt_bias"], d["b"], g_out=g, beta_out=beta)
+        if ev is not None:
+            ev[1].record(stream)
+        kda_chunk_fwd(d["q"], d["k"], d["v"], g, beta, d["cu_seqlens"], x.scale, mode=mode,
+                      out=out, final_state=fs, cu_seqlens_host=cu_host)
+        if ev is not None:
+            ev[2].record(stream)
+
+    def barrier():
+        if world > 1:
+            t = torch.ones(1, device=dev)
+            dist.all_reduce(t)
+        torch.cuda.synchronize(dev)
+
+    for _ in range(args.warmup):
+        step()
+    barrier()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    gpu_index = local_rank
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    if vis and all(s.strip().isdigit() for s in vis.split(",")):
+        gpu_index = int(vis.split(",")[local_rank])
+    clocks = ClockSampler(gpu_index)
+    clocks.start()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    barrier()
+    start.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    end.record(stream)
+    barrier()
+    clk = clocks.stop()
+    ms = start.elapsed_time(end)
+    gate_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    chunk_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    if world > 1:
+        t = torch.tensor([ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # End to end through the public API: pinned host inputs copied in, result copied out.
+    e2e = None
+    if not args.no_e2e:
+        host_in = {n: t.pin_memory() for n, t in
+                   ((n, getattr(x, n)) for n in ("q", "k", "v", "f", "A_log", "dt_bias", "b",
+                                                 "cu_seqlens"))}
+        host_out = torch.empty(T, H, V, dtype=out_dtype).pin_memory()
+        host_fs = torch.empty(N, H, K, V).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+        d2h = host_out.numel() * host_out.element_size() + host_fs.numel() * 4
+
+        def e2e_step():
+            for n, t in host_in.items():
+                d[n].copy_(t, non_blocking=True)
+            step()
+            host_out.copy_(out, non_blocking=True)
+            host_fs.copy_(fs, non_blocking=True)
+
+        for _ in range(max(1, min(args.warmup, 3))):
+            e2e_step()
+        barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+        barrier()
+        ems = e0.elapsed_time(e1)
+        if world > 1:
+            t = torch.tensor([ems], device=dev, dtype=torch.float64)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ems = float(t.item())
+        e2e = {"value": world * T * args.steps / (ems * 1e-3), "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    if rank == 0:
+        qkv_bytes = x.q.element_size()
+        out_bytes = out.element_size()
+        alg = algorithmic_bytes(T, H, K, V, N, qkv_bytes, out_bytes)
+        avg_chunk_s = statistics.mean(chunk_ms) * 1e-3
+        peak, peak_src = measured_peaks()
+        achieved = alg / avg_chunk_s / 1e9
+        kernel_key = f"kda_chunk_fwd:{mode}:{w.name}"
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "traffic": kernel_traffic(kernel_key),
+                "kernel": f"kda_chunk_fwd ({mode})", "peak_source": f"{peak_src} hbm_gbs",
+                "algorithmic_bytes_per_launch": alg,
+                "avg_launch_ms": avg_chunk_s * 1e3}
+        cfg = workload_config(w, mode)
+        cfg["T"], cfg["N"] = T, N
+        value = world * T * args.steps / (ms * 1e-3)
+        chunk_tps = T / avg_chunk_s
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "f32" if mode == "fp32_exact" else "bf16", "data": "synthetic",
+                "config": cfg, "roofline": roof,
+                "kernels": {"kda_gate_ms": statistics.mean(gate_ms),
+                            "kda_chunk_fwd_ms": statistics.mean(chunk_ms),
+                            "kda_chunk_fwd_p50_ms": statistics.median(chunk_ms),
+                            "kda_chunk_fwd_max_ms": max(chunk_ms),
+                            "kda_gate_GBps": gate_bytes(T, H, K) / statistics.mean(gate_ms) / 1e6,
+                            "chunk_only_tokens_per_s": chunk_tps,
+                            "context_h200_chunk_only_ratio": chunk_tps / (
+                                16384 / (H200_CHUNK_US_16384 * 1e-6))},
+                "gpu_launches": 2 * args.steps,
+                "clocks": clk, "e2e": e2e}
+        if world == 1 and not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(x, w)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,141 @@
+/*
+ * kda.h -- C ABI of the GB300 (sm_103a) Kimi Delta Attention forward library
+ * (libkda_gb300.so).
+ *
+ * The method: the gated delta-rule recurrence of Kimi Delta Attention with a
+ * per-channel log-space decay,
+ *
+ *     S_t = (I - beta_t k_t k_t^T) Diag(exp g_t) S_{t-1} + beta_t k_t v_t^T,
+ *     o_t = scale * S_t^T q_t,
+ *
+ * over packed variable-length sequences, computed in chunks of 64 tokens.
+ * Page references are to XTuner's pull requests "Add opt-in FP32 KDA chunk
+ * computation" (#2301) and "GLM-5.3-Flash F6.2: KDA correctness and FLA
+ * sequence parallelism" (#2153).
+ *
+ * Conventions shared by every entry point
+ *   - Every array argument is a DEVICE pointer unless its name ends in
+ *     `_host`.  Arrays are dense, row-major, in the layout given per argument,
+ *     owned by the caller, and must stay valid until the stream reaches the
+ *     launched work.  The library allocates no device memory and keeps no
+ *     mutable global state; calls on different streams are independent.
+ *   - Every device pointer must be 16-byte aligned (KDA_ERR_ALIGNMENT).
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *     default stream).  The library never synchronises.
+ *   - Argument errors are detected on the host before anything is launched:
+ *     the call returns a non-zero kda_status and launches nothing.  A CUDA
+ *     launch failure returns KDA_ERR_CUDA.  Errors that only the device can
+ *     see (offsets that contradict T when no host mirror of cu_seqlens is
+ *     given) are written to `*status_dev` when it is non-NULL: the kernel
+ *     stores the first error code there and skips the bad unit; read it after
+ *     the stream has reached the work.  The library never traps.
+ */
+#ifndef KDA_GB300_H
+#define KDA_GB300_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t. */
+typedef struct CUstream_st* kda_stream_t;
+
+typedef enum {
+    KDA_OK = 0,
+    KDA_ERR_INVALID_ARG = 1,   /* NULL pointer, bad size, bad enum, bad offsets    */
+    KDA_ERR_UNSUPPORTED = 2,   /* valid but not implemented (e.g. K != 128)       */
+    KDA_ERR_ALIGNMENT = 3,     /* a device pointer is not 16-byte aligned          */
+    KDA_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed             */
+    KDA_ERR_TIMEOUT = 5,       /* device: a bounded wait gave up (status word)     */
+    KDA_ERR_DEVICE_ARG = 6     /* device: offsets outside [0, T] (status word)     */
+} kda_status;
+
+typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype;
+
+typedef enum {
+    /* BF16 tensor-core operands with FP32 accumulation; output rel-L2 error
+     * against the FP64 recurrence is held below 3e-3. */
+    KDA_MODE_BF16_TC = 0,
+    /* FP32 arithmetic throughout (IEEE FP32, no TF32), output rel-L2 error
+     * below 1e-5 with F32 output.  This is the counterpart of the pages'
+     * opt-in FP32 chunk intermediates ("Add opt-in FP32 KDA chunk
+     * computation", section Change), without their TF32 caveat. */
+    KDA_MODE_FP32_EXACT = 1
+} kda_mode;
+
+/*
+ * kda_gate -- log-space decay and write strength from their pre-activations.
+ *
+ *   g[t,h,c]  = -exp(A_log[h]) * softplus(f[t,h,c] + dt_bias[h,c])
+ *   beta[t,h] = 1 / (1 + exp(-b[t,h]))
+ *
+ * The decay is computed outside the chunk kernel with FP32 A_log/dt_bias and
+ * beta is a sigmoid of its logits ("GLM-5.3-Flash F6.2: KDA correctness and
+ * FLA sequence parallelism", fused-gate commit).
+ *
+ *   f       [T, H, K]  f_dtype (F32 or BF16)   gate pre-activation
+ *   A_log   [H]        F32
+ *   dt_bias [H, K]     F32
+ *   b       [T, H]     b_dtype (F32 or BF16)   beta logits
+ *   g_out   [T, H, K]  F32  (written)          every value < 0
+ *   beta_out[T, H]     F32  (written)          every value in (0, 1)
+ * Requires T >= 0, H >= 1, 1 <= K and K % 4 == 0.  T == 0 launches nothing.
+ */
+kda_status kda_gate(const void* f, int32_t f_dtype, const float* A_log, const float* dt_bias,
+                    const void* b, int32_t b_dtype, int64_t T, int32_t H, int32_t K,
+                    float* g_out, float* beta_out, kda_stream_t stream);
+
+/*
+ * kda_chunk_fwd -- chunked KDA forward over packed sequences.
+ *
+ * Sequence n covers rows cu_seqlens[n] .. cu_seqlens[n+1]-1 of every tensor
+ * ("packed offsets": "Add opt-in FP32 KDA chunk computation", section
+ * Change).  Each sequence starts from a zero state; chunks of 64 tokens start
+ * at the sequence start, the last one possibly shorter.
+ *
+ *   q, k       [T, H, K]  qkv_dtype (F32 or BF16)
+ *   v          [T, H, V]  qkv_dtype
+ *   g          [T, H, K]  F32   log-space decay, must be <= 0 (kda_gate's output)
+ *   beta       [T, H]     F32   write strength in [0, 1]
+ *   cu_seqlens [N+1]      int32 device copy of the offsets, cu[0] = 0, cu[N] = T,
+ *                                non-decreasing
+ *   cu_seqlens_host [N+1] int32 HOST mirror of the same offsets, or NULL.  When
+ *                                given it is validated on the host (bad offsets
+ *                                -> KDA_ERR_INVALID_ARG, nothing launched);
+ *                                when NULL the kernel checks each sequence's
+ *                                range against [0, T] and reports
+ *                                KDA_ERR_DEVICE_ARG through status_dev.
+ *   N >= 0 sequences, T >= 0 tokens, H >= 1 heads, K = V = 128 (else
+ *   KDA_ERR_UNSUPPORTED).
+ *   scale      output scale (typically 1/sqrt(K)).
+ *   qk_l2norm  1: q and k are L2-normalised per (token, head) inside the op,
+ *              x / sqrt(sum x^2 + 1e-6) in FP32 ("Add opt-in FP32 KDA chunk
+ *              computation", section Change); 0: used as given.
+ *   mode       kda_mode.
+ *   out        [T, H, V]  out_dtype (F32 or BF16), written for every covered row.
+ *   final_state [N, H, K, V] F32, or NULL: the state after each sequence's
+ *              last token (zero for an empty sequence).
+ *   status_dev one device int32 or NULL; the kernel writes a kda_status there
+ *              only on a device-detected error (the caller zeroes it).
+ */
+kda_status kda_chunk_fwd(const void* q, const void* k, const void* v, int32_t qkv_dtype,
+                         const float* g, const float* beta,
+                         const int32_t* cu_seqlens, const int32_t* cu_seqlens_host,
+                         int32_t N, int64_t T, int32_t H, int32_t K, int32_t V,
+                         float scale, int32_t qk_l2norm, int32_t mode,
+                         void* out, int32_t out_dtype, float* final_state,
+                         int32_t* status_dev, kda_stream_t stream);
+
+/* Static text for a kda_status value ("unknown status" otherwise). */
+const char* kda_status_string(int32_t status);
+
+/* ABI revision of this header; bumped on any incompatible change. */
+int32_t kda_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_GB300_H */

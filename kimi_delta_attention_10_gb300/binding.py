@@ -1,0 +1,155 @@
+"""ctypes binding of libkda_gb300.so (include/kda.h): argument marshalling only.
+
+Every computation runs in the library's CUDA kernels; PyTorch provides the
+device memory and the stream.  There is no fallback: if the library is
+missing, or a tensor is not on a CUDA device, the call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional, Sequence, Tuple
+
+import torch
+
+from . import _build
+
+KDA_OK = 0
+KDA_ERR_INVALID_ARG = 1
+KDA_ERR_UNSUPPORTED = 2
+KDA_ERR_ALIGNMENT = 3
+KDA_ERR_CUDA = 4
+KDA_ERR_TIMEOUT = 5
+KDA_ERR_DEVICE_ARG = 6
+
+KDA_F32 = 0
+KDA_BF16 = 1
+
+KDA_MODE_BF16_TC = 0
+KDA_MODE_FP32_EXACT = 1
+
+MODES = {"bf16_tc": KDA_MODE_BF16_TC, "fp32_exact": KDA_MODE_FP32_EXACT}
+
+# Every symbol include/kda.h declares.
+EXPORTS = ("kda_gate", "kda_chunk_fwd", "kda_status_string", "kda_abi_version")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class KDAError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} (status {status})")
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
+    """Load libkda_gb300.so (optionally building it first)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build.LIB_PATH
+        if not os.path.exists(path):
+            if not build_if_missing:
+                raise RuntimeError(
+                    f"{path} is missing: build it with kimi_delta_attention_10_gb300._build.build()")
+            _build.build()
+        lib = ctypes.CDLL(path)
+        vp, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+        lib.kda_gate.argtypes = [vp, i32, vp, vp, vp, i32, i64, i32, i32, vp, vp, vp]
+        lib.kda_gate.restype = i32
+        lib.kda_chunk_fwd.argtypes = [vp, vp, vp, i32, vp, vp, vp, vp, i32, i64, i32, i32, i32,
+                                      ctypes.c_float, i32, i32, vp, i32, vp, vp, vp]
+        lib.kda_chunk_fwd.restype = i32
+        lib.kda_status_string.argtypes = [i32]
+        lib.kda_status_string.restype = ctypes.c_char_p
+        lib.kda_abi_version.argtypes = []
+        lib.kda_abi_version.restype = i32
+        _lib = lib
+        return lib
+
+
+def status_string(status: int) -> str:
+    return load_library().kda_status_string(int(status)).decode()
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return KDA_F32
+    if t.dtype == torch.bfloat16:
+        return KDA_BF16
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _dev_ptr(t: Optional[torch.Tensor], name: str) -> Optional[int]:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise RuntimeError(f"{name} must be a CUDA tensor (the library has no CPU path)")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def _stream_handle(stream: Optional[torch.cuda.Stream], device) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    return s.cuda_stream
+
+
+def kda_gate(f: torch.Tensor, A_log: torch.Tensor, dt_bias: torch.Tensor, b: torch.Tensor,
+             g_out: Optional[torch.Tensor] = None, beta_out: Optional[torch.Tensor] = None,
+             stream: Optional[torch.cuda.Stream] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """g = -exp(A_log[h]) * softplus(f + dt_bias), beta = sigmoid(b) (FP32 outputs)."""
+    lib = load_library()
+    T, H, K = f.shape
+    if g_out is None:
+        g_out = torch.empty((T, H, K), dtype=torch.float32, device=f.device)
+    if beta_out is None:
+        beta_out = torch.empty((T, H), dtype=torch.float32, device=f.device)
+    st = lib.kda_gate(_dev_ptr(f, "f"), _dtype_code(f), _dev_ptr(A_log, "A_log"),
+                      _dev_ptr(dt_bias, "dt_bias"), _dev_ptr(b, "b"), _dtype_code(b), T, H, K,
+                      _dev_ptr(g_out, "g_out"), _dev_ptr(beta_out, "beta_out"),
+                      _stream_handle(stream, f.device))
+    if st != KDA_OK:
+        raise KDAError(st, "kda_gate")
+    return g_out, beta_out
+
+
+def kda_chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor,
+                  beta: torch.Tensor, cu_seqlens: torch.Tensor, scale: Optional[float] = None,
+                  mode: str = "bf16_tc", out: Optional[torch.Tensor] = None,
+                  out_dtype: Optional[torch.dtype] = None, output_final_state: bool = True,
+                  final_state: Optional[torch.Tensor] = None,
+                  cu_seqlens_host: Optional[Sequence[int]] = None, qk_l2norm: bool = True,
+                  status: Optional[torch.Tensor] = None,
+                  stream: Optional[torch.cuda.Stream] = None):
+    """Chunked KDA forward.  Returns (out [T,H,V], final_state [N,H,K,V] or None)."""
+    lib = load_library()
+    T, H, K = q.shape
+    V = v.shape[2]
+    N = cu_seqlens.numel() - 1
+    if scale is None:
+        scale = K ** -0.5
+    if out is None:
+        out = torch.empty((T, H, V), dtype=out_dtype or v.dtype, device=q.device)
+    if final_state is None and output_final_state:
+        final_state = torch.empty((N, H, K, V), dtype=torch.float32, device=q.device)
+    host_arr = None
+    if cu_seqlens_host is not None:
+        host_arr = (ctypes.c_int32 * len(cu_seqlens_host))(*[int(x) for x in cu_seqlens_host])
+    st = lib.kda_chunk_fwd(
+        _dev_ptr(q, "q"), _dev_ptr(k, "k"), _dev_ptr(v, "v"), _dtype_code(q),
+        _dev_ptr(g, "g"), _dev_ptr(beta, "beta"), _dev_ptr(cu_seqlens, "cu_seqlens"),
+        ctypes.cast(host_arr, ctypes.c_void_p) if host_arr is not None else None,
+        N, T, H, K, V, float(scale), 1 if qk_l2norm else 0, MODES[mode],
+        _dev_ptr(out, "out"), _dtype_code(out), _dev_ptr(final_state, "final_state"),
+        _dev_ptr(status, "status"), _stream_handle(stream, q.device))
+    if st != KDA_OK:
+        raise KDAError(st, "kda_chunk_fwd")
+    return out, final_state

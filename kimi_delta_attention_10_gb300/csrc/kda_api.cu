@@ -1,0 +1,101 @@
+// Host side of the C ABI declared in include/kda.h: argument validation and
+// dispatch.  Nothing is launched unless every host-visible check passes.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kda.h"
+#include "kda_internal.cuh"
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool valid_dtype(int32_t d) { return d == KDA_F32 || d == KDA_BF16; }
+
+}  // namespace
+
+namespace kda {
+
+int device_sm_count()
+{
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return sms;
+}
+
+}  // namespace kda
+
+extern "C" {
+
+int32_t kda_abi_version(void) { return 1; }
+
+const char* kda_status_string(int32_t s)
+{
+    switch (s) {
+        case KDA_OK: return "ok";
+        case KDA_ERR_INVALID_ARG: return "invalid argument";
+        case KDA_ERR_UNSUPPORTED: return "unsupported shape, dtype or mode";
+        case KDA_ERR_ALIGNMENT: return "device pointer not 16-byte aligned";
+        case KDA_ERR_CUDA: return "CUDA error";
+        case KDA_ERR_TIMEOUT: return "device wait timed out";
+        case KDA_ERR_DEVICE_ARG: return "device saw offsets outside [0, T]";
+        default: return "unknown status";
+    }
+}
+
+kda_status kda_gate(const void* f, int32_t f_dtype, const float* A_log, const float* dt_bias,
+                    const void* b, int32_t b_dtype, int64_t T, int32_t H, int32_t K,
+                    float* g_out, float* beta_out, kda_stream_t stream)
+{
+    if (T < 0 || H < 1 || K < 1) return KDA_ERR_INVALID_ARG;
+    if (!valid_dtype(f_dtype) || !valid_dtype(b_dtype)) return KDA_ERR_INVALID_ARG;
+    if (K % 4 != 0) return KDA_ERR_UNSUPPORTED;
+    if (!f || !A_log || !dt_bias || !b || !g_out || !beta_out) return KDA_ERR_INVALID_ARG;
+    if (!aligned16(f) || !aligned16(A_log) || !aligned16(dt_bias) || !aligned16(b) ||
+        !aligned16(g_out) || !aligned16(beta_out))
+        return KDA_ERR_ALIGNMENT;
+    if (T == 0) return KDA_OK;
+    cudaError_t e = kda::launch_gate(f, f_dtype == KDA_BF16, A_log, dt_bias, b,
+                                     b_dtype == KDA_BF16, T, H, K, g_out, beta_out,
+                                     reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+kda_status kda_chunk_fwd(const void* q, const void* k, const void* v, int32_t qkv_dtype,
+                         const float* g, const float* beta,
+                         const int32_t* cu_seqlens, const int32_t* cu_seqlens_host,
+                         int32_t N, int64_t T, int32_t H, int32_t K, int32_t V,
+                         float scale, int32_t qk_l2norm, int32_t mode,
+                         void* out, int32_t out_dtype, float* final_state,
+                         int32_t* status_dev, kda_stream_t stream)
+{
+    if (N < 0 || T < 0 || H < 1 || K < 1 || V < 1) return KDA_ERR_INVALID_ARG;
+    if (T > INT32_MAX) return KDA_ERR_UNSUPPORTED;
+    if (!valid_dtype(qkv_dtype) || !valid_dtype(out_dtype)) return KDA_ERR_INVALID_ARG;
+    if (mode != KDA_MODE_BF16_TC && mode != KDA_MODE_FP32_EXACT) return KDA_ERR_INVALID_ARG;
+    if (qk_l2norm != 0 && qk_l2norm != 1) return KDA_ERR_INVALID_ARG;
+    if (K != kda::kHeadK || V != kda::kHeadV) return KDA_ERR_UNSUPPORTED;
+    if (!cu_seqlens) return KDA_ERR_INVALID_ARG;
+    if (T > 0 && (!q || !k || !v || !g || !beta || !out)) return KDA_ERR_INVALID_ARG;
+    const void* ptrs[] = {q, k, v, g, beta, cu_seqlens, out, final_state, status_dev};
+    for (const void* p : ptrs)
+        if (p && !aligned16(p)) return KDA_ERR_ALIGNMENT;
+    if (cu_seqlens_host) {
+        if (cu_seqlens_host[0] != 0 || (int64_t)cu_seqlens_host[N] != T)
+            return KDA_ERR_INVALID_ARG;
+        for (int32_t n = 0; n < N; ++n)
+            if (cu_seqlens_host[n + 1] < cu_seqlens_host[n]) return KDA_ERR_INVALID_ARG;
+    }
+    if (mode == KDA_MODE_BF16_TC) return KDA_ERR_UNSUPPORTED;  // tensor-core path: not built yet
+    if (N == 0) return KDA_OK;
+
+    kda::ChunkArgs a;
+    a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.cu_seqlens = cu_seqlens;
+    a.N = N; a.T = T; a.H = H; a.scale = scale; a.l2norm = qk_l2norm;
+    a.out = out; a.final_state = final_state; a.status = status_dev;
+    a.qkv_bf16 = qkv_dtype == KDA_BF16; a.out_bf16 = out_dtype == KDA_BF16;
+    cudaError_t e = kda::launch_chunk_fp32(a, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+}  // extern "C"

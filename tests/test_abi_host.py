@@ -1,0 +1,116 @@
+"""Host-side checks of the C ABI (no GPU needed, no kernel launched).
+
+Every negative case below is rejected by the host validation in kda_api.cu
+before any CUDA call, so fake (never dereferenced) pointer values are safe."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from kimi_delta_attention_10_gb300 import _build, binding
+
+ROOT = os.path.abspath(os.path.join(os.path.dirname(__file__), ".."))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return binding.load_library()
+
+
+def declared_symbols():
+    text = open(os.path.join(ROOT, "include", "kda.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kda_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_exports():
+    assert declared_symbols() == sorted(binding.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+
+
+def test_abi_version_and_status_strings(lib):
+    assert lib.kda_abi_version() == 1
+    assert binding.status_string(0) == "ok"
+    for s in range(1, 7):
+        assert binding.status_string(s) not in ("ok", "unknown status")
+    assert binding.status_string(99) == "unknown status"
+
+
+# A fake, 16-byte-aligned device address that is never dereferenced.
+P = 0x10000
+MIS = 0x10004
+
+
+def chunk(lib, **kw):
+    a = dict(q=P, k=P, v=P, qkv=1, g=P, beta=P, cu=P, cu_host=None, N=1, T=10, H=2, K=128,
+             V=128, scale=0.1, l2=1, mode=1, out=P, out_dt=1, fs=None, status=None, stream=None)
+    a.update(kw)
+    host = a["cu_host"]
+    if host is not None:
+        host = ctypes.cast((ctypes.c_int32 * len(host))(*host), ctypes.c_void_p)
+    return lib.kda_chunk_fwd(a["q"], a["k"], a["v"], a["qkv"], a["g"], a["beta"], a["cu"], host,
+                             a["N"], a["T"], a["H"], a["K"], a["V"], a["scale"], a["l2"],
+                             a["mode"], a["out"], a["out_dt"], a["fs"], a["status"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(qkv=7), binding.KDA_ERR_INVALID_ARG),
+    (dict(out_dt=-1), binding.KDA_ERR_INVALID_ARG),
+    (dict(mode=5), binding.KDA_ERR_INVALID_ARG),
+    (dict(l2=2), binding.KDA_ERR_INVALID_ARG),
+    (dict(K=64), binding.KDA_ERR_UNSUPPORTED),
+    (dict(K=16, V=24), binding.KDA_ERR_UNSUPPORTED),     # the pages' rectangular case
+    (dict(V=64), binding.KDA_ERR_UNSUPPORTED),
+    (dict(N=-1), binding.KDA_ERR_INVALID_ARG),
+    (dict(T=-3), binding.KDA_ERR_INVALID_ARG),
+    (dict(H=0), binding.KDA_ERR_INVALID_ARG),
+    (dict(q=None), binding.KDA_ERR_INVALID_ARG),
+    (dict(out=None), binding.KDA_ERR_INVALID_ARG),
+    (dict(cu=None), binding.KDA_ERR_INVALID_ARG),
+    (dict(q=MIS), binding.KDA_ERR_ALIGNMENT),
+    (dict(g=MIS), binding.KDA_ERR_ALIGNMENT),
+    (dict(fs=MIS), binding.KDA_ERR_ALIGNMENT),
+    (dict(status=MIS), binding.KDA_ERR_ALIGNMENT),
+    (dict(cu_host=[0, 9]), binding.KDA_ERR_INVALID_ARG),           # last != T
+    (dict(cu_host=[1, 10]), binding.KDA_ERR_INVALID_ARG),          # first != 0
+    (dict(N=2, cu_host=[0, 7, 5]), binding.KDA_ERR_INVALID_ARG),   # decreasing (and last != T)
+    (dict(N=3, cu_host=[0, 7, 5, 10]), binding.KDA_ERR_INVALID_ARG),
+])
+def test_chunk_fwd_rejects_bad_arguments(lib, kw, expect):
+    assert chunk(lib, **kw) == expect
+
+
+def gate(lib, **kw):
+    a = dict(f=P, fdt=0, A=P, dt=P, b=P, bdt=0, T=10, H=2, K=128, g=P, beta=P, stream=None)
+    a.update(kw)
+    return lib.kda_gate(a["f"], a["fdt"], a["A"], a["dt"], a["b"], a["bdt"], a["T"], a["H"],
+                        a["K"], a["g"], a["beta"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(fdt=3), binding.KDA_ERR_INVALID_ARG),
+    (dict(bdt=3), binding.KDA_ERR_INVALID_ARG),
+    (dict(K=6), binding.KDA_ERR_UNSUPPORTED),
+    (dict(H=0), binding.KDA_ERR_INVALID_ARG),
+    (dict(T=-1), binding.KDA_ERR_INVALID_ARG),
+    (dict(f=None), binding.KDA_ERR_INVALID_ARG),
+    (dict(beta=None), binding.KDA_ERR_INVALID_ARG),
+    (dict(g=MIS), binding.KDA_ERR_ALIGNMENT),
+    (dict(A=MIS), binding.KDA_ERR_ALIGNMENT),
+    (dict(T=0), binding.KDA_OK),                                    # nothing to do
+])
+def test_gate_rejects_bad_arguments(lib, kw, expect):
+    assert gate(lib, **kw) == expect
+
+
+def test_binding_refuses_cpu_tensors(lib):
+    import torch
+    x = torch.zeros(4, 2, 128)
+    with pytest.raises(RuntimeError, match="CUDA tensor"):
+        binding.kda_gate(x, torch.zeros(2), torch.zeros(2, 128), torch.zeros(4, 2))
