@@ -81,7 +81,8 @@ typedef enum {
  *   b       [T, H]     b_dtype (F32 or BF16)   beta logits
  *   g_out   [T, H, K]  F32  (written)          every value < 0
  *   beta_out[T, H]     F32  (written)          every value in (0, 1)
- * Requires T >= 0, H >= 1, 1 <= K and K % 4 == 0.  T == 0 launches nothing.
+ * Requires T >= 0, H >= 1, 1 <= K and K % 4 == 0.  T == 0 launches nothing and
+ * accepts NULL tensor pointers.
  */
 kda_status kda_gate(const void* f, int32_t f_dtype, const float* A_log, const float* dt_bias,
                     const void* b, int32_t b_dtype, int64_t T, int32_t H, int32_t K,

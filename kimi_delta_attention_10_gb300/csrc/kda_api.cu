@@ -50,11 +50,11 @@ kda_status kda_gate(const void* f, int32_t f_dtype, const float* A_log, const fl
     if (T < 0 || H < 1 || K < 1) return KDA_ERR_INVALID_ARG;
     if (!valid_dtype(f_dtype) || !valid_dtype(b_dtype)) return KDA_ERR_INVALID_ARG;
     if (K % 4 != 0) return KDA_ERR_UNSUPPORTED;
+    if (T == 0) return KDA_OK;   // nothing to do; empty tensors may have NULL data
     if (!f || !A_log || !dt_bias || !b || !g_out || !beta_out) return KDA_ERR_INVALID_ARG;
     if (!aligned16(f) || !aligned16(A_log) || !aligned16(dt_bias) || !aligned16(b) ||
         !aligned16(g_out) || !aligned16(beta_out))
         return KDA_ERR_ALIGNMENT;
-    if (T == 0) return KDA_OK;
     cudaError_t e = kda::launch_gate(f, f_dtype == KDA_BF16, A_log, dt_bias, b,
                                      b_dtype == KDA_BF16, T, H, K, g_out, beta_out,
                                      reinterpret_cast<cudaStream_t>(stream));

@@ -104,6 +104,7 @@ def gate(lib, **kw):
     (dict(g=MIS), binding.KDA_ERR_ALIGNMENT),
     (dict(A=MIS), binding.KDA_ERR_ALIGNMENT),
     (dict(T=0), binding.KDA_OK),                                    # nothing to do
+    (dict(T=0, f=None, b=None, g=None, beta=None), binding.KDA_OK),  # empty tensors
 ])
 def test_gate_rejects_bad_arguments(lib, kw, expect):
     assert gate(lib, **kw) == expect
