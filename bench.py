@@ -240,7 +240,7 @@ def main():
     from kimi_delta_attention_10_gb300 import kda_chunk_fwd, kda_gate
     from kimi_delta_attention_10_gb300.inputs import WORKLOAD_BY_NAME, workload_inputs
 
-    mode = args.mode or "fp32_exact"
+    mode = args.mode or "bf16_tc"
     w = WORKLOAD_BY_NAME[args.workload]
     x = workload_inputs(w)
     T, H, K, V, N = x.T, w.H, w.K, w.V, x.N

@@ -86,7 +86,6 @@ kda_status kda_chunk_fwd(const void* q, const void* k, const void* v, int32_t qk
         for (int32_t n = 0; n < N; ++n)
             if (cu_seqlens_host[n + 1] < cu_seqlens_host[n]) return KDA_ERR_INVALID_ARG;
     }
-    if (mode == KDA_MODE_BF16_TC) return KDA_ERR_UNSUPPORTED;  // tensor-core path: not built yet
     if (N == 0) return KDA_OK;
 
     kda::ChunkArgs a;
@@ -94,7 +93,9 @@ kda_status kda_chunk_fwd(const void* q, const void* k, const void* v, int32_t qk
     a.N = N; a.T = T; a.H = H; a.scale = scale; a.l2norm = qk_l2norm;
     a.out = out; a.final_state = final_state; a.status = status_dev;
     a.qkv_bf16 = qkv_dtype == KDA_BF16; a.out_bf16 = out_dtype == KDA_BF16;
-    cudaError_t e = kda::launch_chunk_fp32(a, reinterpret_cast<cudaStream_t>(stream));
+    cudaError_t e = (mode == KDA_MODE_BF16_TC)
+                        ? kda::launch_chunk_tc(a, reinterpret_cast<cudaStream_t>(stream))
+                        : kda::launch_chunk_fp32(a, reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 

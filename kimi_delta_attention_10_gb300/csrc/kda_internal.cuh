@@ -38,6 +38,7 @@ cudaError_t launch_gate(const void* f, bool f_bf16, const float* A_log, const fl
                         float* g_out, float* beta_out, cudaStream_t stream);
 
 cudaError_t launch_chunk_fp32(const ChunkArgs& a, cudaStream_t stream);
+cudaError_t launch_chunk_tc(const ChunkArgs& a, cudaStream_t stream);
 
 int device_sm_count();
 

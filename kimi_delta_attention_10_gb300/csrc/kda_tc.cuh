@@ -1,0 +1,190 @@
+// Blackwell (sm_103a) tensor-core primitives: tcgen05 MMA with operands in
+// shared memory and accumulators in tensor memory (TMEM), mbarrier waits with
+// an iteration bound, and the 128-byte-swizzled shared-memory tile layout the
+// MMA descriptors describe.  Inline PTX only.
+#pragma once
+
+#include <stdint.h>
+
+namespace kda {
+namespace tc {
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ---------------------------------------------------------------- layouts
+//
+// SW128 tile: rows of 128 bytes, 8-row atoms of 1024 bytes, the 16-byte chunk
+// j of row r stored at chunk position j ^ (r % 8).  A matrix wider than 128
+// bytes along its contiguous dimension is stored as consecutive "blocks" of
+// 128-byte rows: block b holds bytes [128 b, 128 b + 128) of every row.
+//   offset(row, byte) = (byte / 128) * rows * 128 + sw128(row, byte % 128)
+// Every block must start 1024-byte aligned.
+__device__ __forceinline__ uint32_t sw128(uint32_t row, uint32_t byte_in_row)
+{
+    return (row >> 3) * 1024u + (row & 7u) * 128u +
+           ((((byte_in_row >> 4) ^ (row & 7u)) << 4) | (byte_in_row & 15u));
+}
+
+__device__ __forceinline__ uint32_t sw128_tile(uint32_t rows, uint32_t row, uint32_t byte)
+{
+    return (byte >> 7) * rows * 128u + sw128(row, byte & 127u);
+}
+
+// Shared-memory matrix descriptor, SWIZZLE_128B.
+//   bits 0-13 start >> 4, 16-29 leading byte offset >> 4, 32-45 stride byte
+//   offset >> 4, 46-47 version (1), 61-63 layout (2 = 128-byte swizzle).
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo)
+{
+    return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+// K-major operand (rows = M or N index, K contiguous) of `rows` rows.  k-step
+// `s` covers 32 bytes of K (16 BF16 or 8 TF32 elements).
+__device__ __forceinline__ uint64_t desc_kmajor(uint32_t base, uint32_t rows, uint32_t s)
+{
+    const uint32_t start = base + (s >> 2) * rows * 128u + (s & 3u) * 32u;
+    return desc_sw128(start, 16u, 1024u);
+}
+
+// MN-major BF16 operand whose MN extent is exactly 64 elements (one 128-byte
+// row per K index): rows are K indices.  k-step `s` covers K rows 16 s .. 16 s + 15.
+__device__ __forceinline__ uint64_t desc_mnmajor64(uint32_t base, uint32_t s)
+{
+    return desc_sw128(base + s * 2048u, 8192u, 1024u);
+}
+
+// Instruction descriptor (kind::f16 with BF16 operands, or kind::tf32), FP32 D.
+//   bits 4-5 D format (1 = F32), 7-9 A format, 10-12 B format (1 = BF16,
+//   2 = TF32), 15/16 A/B major (0 = K, 1 = MN), 17-22 N >> 3, 24-28 M >> 4.
+constexpr uint32_t kFmtBF16 = 1, kFmtTF32 = 2;
+__host__ __device__ constexpr uint32_t idesc(uint32_t fmt, uint32_t M, uint32_t N,
+                                             bool a_mn = false, bool b_mn = false)
+{
+    return (1u << 4) | (fmt << 7) | (fmt << 10) | ((a_mn ? 1u : 0u) << 15) |
+           ((b_mn ? 1u : 0u) << 16) | ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+
+// ---------------------------------------------------------------- MMA
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t id,
+                                         uint32_t acc)
+{
+    asm volatile(
+        "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(id), "r"(acc));
+}
+
+__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t id,
+                                         uint32_t acc)
+{
+    asm volatile(
+        "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(id), "r"(acc));
+}
+
+// Arrives once on `mbar` when every MMA this thread issued before has completed.
+__device__ __forceinline__ void commit(uint64_t* mbar)
+{
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+            smem_u32(mbar))
+        : "memory");
+}
+
+// ---------------------------------------------------------------- fences
+__device__ __forceinline__ void fence_before_sync()
+{
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void fence_after_sync()
+{
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// Makes this thread's generic-proxy shared-memory writes visible to the MMA.
+__device__ __forceinline__ void fence_async_smem()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// ---------------------------------------------------------------- mbarrier
+__device__ __forceinline__ void mbar_init(uint64_t* m, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(m)), "r"(count)
+                 : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* m, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        "selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(m)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Waits for phase `parity` to complete; gives up after `max_iter` polls.
+__device__ __forceinline__ bool mbar_wait(uint64_t* m, uint32_t parity, uint32_t max_iter)
+{
+    for (uint32_t i = 0; i < max_iter; ++i)
+        if (mbar_try_wait(m, parity)) return true;
+    return false;
+}
+
+// ---------------------------------------------------------------- TMEM
+// Executed by one whole warp; the TMEM address is written to *dst.
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols)
+{
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(dst)),
+                 "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish()
+{
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols)
+{
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr),
+                 "r"(ncols)
+                 : "memory");
+}
+
+// Warp-collective: thread t of warp w reads TMEM lane 32 (w % 4) + t,
+// columns [col, col + 32) of `taddr` (taddr's lane field = 32 (w % 4)).
+// Waits for the load before returning.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&r)[32])
+{
+    uint32_t* u = reinterpret_cast<uint32_t*>(r);
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
+        "tcgen05.wait::ld.sync.aligned;\n"
+        : "=r"(u[0]), "=r"(u[1]), "=r"(u[2]), "=r"(u[3]), "=r"(u[4]), "=r"(u[5]), "=r"(u[6]),
+          "=r"(u[7]), "=r"(u[8]), "=r"(u[9]), "=r"(u[10]), "=r"(u[11]), "=r"(u[12]),
+          "=r"(u[13]), "=r"(u[14]), "=r"(u[15]), "=r"(u[16]), "=r"(u[17]), "=r"(u[18]),
+          "=r"(u[19]), "=r"(u[20]), "=r"(u[21]), "=r"(u[22]), "=r"(u[23]), "=r"(u[24]),
+          "=r"(u[25]), "=r"(u[26]), "=r"(u[27]), "=r"(u[28]), "=r"(u[29]), "=r"(u[30]),
+          "=r"(u[31])
+        : "r"(taddr)
+        : "memory");
+}
+
+__device__ __forceinline__ uint32_t tmem_addr(uint32_t base, uint32_t lane, uint32_t col)
+{
+    return base + (lane << 16) + col;
+}
+
+}  // namespace tc
+}  // namespace kda

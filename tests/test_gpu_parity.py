@@ -61,14 +61,17 @@ def test_gate_extremes_and_bf16_inputs():
         assert np.max(np.abs(beta.cpu().double().numpy() - b_ref) / b_ref) < 2e-6
 
 
-@pytest.mark.parametrize("mode", ["fp32_exact"])
+MODES = ["fp32_exact", "bf16_tc"]
+OUT_DTYPE = {"fp32_exact": torch.float32, "bf16_tc": None}   # None: the activation dtype
+
+
+@pytest.mark.parametrize("mode", MODES)
 @pytest.mark.parametrize("wi", range(len(WORKLOADS)))
 def test_chunk_matches_oracle(wi, mode):
     """Full path (gate + chunk) on each workload; all heads on the small ones,
     sampled heads on the 16384-token and packed 32768-token workloads."""
     x = inputs(wi)
-    out_dtype = torch.float32 if mode == "fp32_exact" else None
-    out, S, _, _ = gpu_pipeline(x, mode, out_dtype=out_dtype)
+    out, S, _, _ = gpu_pipeline(x, mode, out_dtype=OUT_DTYPE[mode])
     heads = SAMPLED_HEADS if x.T > 4096 else None
     o_ref, S_ref, _, _ = oracle_pipeline(x, heads)
     sel = slice(None) if heads is None else heads
@@ -84,23 +87,25 @@ def _small(lens, H=4, seed=0, dtype=torch.bfloat16):
     return make_inputs(lens, H, 128, 128, dtype, seed)
 
 
+@pytest.mark.parametrize("mode", MODES)
 @pytest.mark.parametrize("lens", [[1], [63], [64], [65], [127, 128], [129, 0, 3], [0], [200, 1, 64]])
-def test_chunk_edge_lengths(lens):
+def test_chunk_edge_lengths(lens, mode):
     x = _small(lens, seed=sum(lens) + len(lens))
-    out, S, _, _ = gpu_pipeline(x, "fp32_exact", out_dtype=torch.float32)
+    out, S, _, _ = gpu_pipeline(x, mode, out_dtype=OUT_DTYPE[mode])
     o_ref, S_ref, _, _ = oracle_pipeline(x)
     if x.T:
-        assert rel_l2(out.double().numpy(), o_ref) <= 1e-5
-    assert rel_l2(S.double().numpy(), S_ref) <= 1e-5
+        assert rel_l2(out.double().numpy(), o_ref) <= TOL[mode]
+    assert rel_l2(S.double().numpy(), S_ref) <= TOL[mode]
     for n, L in enumerate(lens):
         if L == 0:
             assert torch.count_nonzero(S[n]) == 0
 
 
-def test_packing_is_bitwise_per_sequence():
+@pytest.mark.parametrize("mode", MODES)
+def test_packing_is_bitwise_per_sequence(mode):
     lens = [70, 5, 129]
     x = _small(lens, seed=3)
-    out, S, _, _ = gpu_pipeline(x, "fp32_exact", out_dtype=torch.float32)
+    out, S, _, _ = gpu_pipeline(x, mode, out_dtype=OUT_DTYPE[mode])
     cu = x.cu_seqlens.tolist()
     d = device_inputs(x)
     g, beta = kda_gate(d["f"], d["A_log"], d["dt_bias"], d["b"])
@@ -109,15 +114,16 @@ def test_packing_is_bitwise_per_sequence():
         cu1 = torch.tensor([0, z - a], dtype=torch.int32, device="cuda")
         o1, S1 = kda_chunk_fwd(d["q"][a:z].contiguous(), d["k"][a:z].contiguous(),
                                d["v"][a:z].contiguous(), g[a:z].contiguous(),
-                               beta[a:z].contiguous(), cu1, x.scale, mode="fp32_exact",
-                               out_dtype=torch.float32)
+                               beta[a:z].contiguous(), cu1, x.scale, mode=mode,
+                               out_dtype=OUT_DTYPE[mode])
         assert torch.equal(o1.cpu(), out[a:z]) and torch.equal(S1.cpu()[0], S[n])
 
 
-def test_deterministic_and_head_permutation():
+@pytest.mark.parametrize("mode", MODES)
+def test_deterministic_and_head_permutation(mode):
     x = _small([150, 40], H=6, seed=4)
-    out1, S1, _, _ = gpu_pipeline(x, "fp32_exact", out_dtype=torch.float32)
-    out2, S2, _, _ = gpu_pipeline(x, "fp32_exact", out_dtype=torch.float32)
+    out1, S1, _, _ = gpu_pipeline(x, mode, out_dtype=OUT_DTYPE[mode])
+    out2, S2, _, _ = gpu_pipeline(x, mode, out_dtype=OUT_DTYPE[mode])
     assert torch.equal(out1, out2) and torch.equal(S1, S2)
     perm = torch.tensor([3, 0, 5, 1, 4, 2])
     xp = _small([150, 40], H=6, seed=4)
@@ -125,23 +131,24 @@ def test_deterministic_and_head_permutation():
         setattr(xp, name, getattr(xp, name)[:, perm].contiguous())
     xp.A_log = xp.A_log[perm].contiguous()
     xp.dt_bias = xp.dt_bias[perm].contiguous()
-    outp, Sp, _, _ = gpu_pipeline(xp, "fp32_exact", out_dtype=torch.float32)
+    outp, Sp, _, _ = gpu_pipeline(xp, mode, out_dtype=OUT_DTYPE[mode])
     assert torch.equal(outp, out1[:, perm]) and torch.equal(Sp, S1[:, perm])
 
 
-def test_without_l2norm_on_prenormalised_inputs():
+@pytest.mark.parametrize("mode", MODES)
+def test_without_l2norm_on_prenormalised_inputs(mode):
     x = _small([90], H=2, seed=6, dtype=torch.float32)
     x.q = x.q / torch.sqrt((x.q * x.q).sum(-1, keepdim=True))
     x.k = x.k / torch.sqrt((x.k * x.k).sum(-1, keepdim=True))
     d = device_inputs(x)
     g, beta = kda_gate(d["f"], d["A_log"], d["dt_bias"], d["b"])
     out, S = kda_chunk_fwd(d["q"], d["k"], d["v"], g, beta, d["cu_seqlens"], x.scale,
-                           mode="fp32_exact", qk_l2norm=False)
+                           mode=mode, qk_l2norm=False)
     g_ref, b_ref = oracle.gate(f64(x.f), f64(x.A_log), f64(x.dt_bias), f64(x.b))
     o_ref, S_ref = oracle.forward(f64(x.q), f64(x.k), f64(x.v), g_ref, b_ref,
                                   x.cu_seqlens.numpy(), x.scale, l2norm=False)
-    assert rel_l2(out.cpu().double().numpy(), o_ref) <= 1e-5
-    assert rel_l2(S.cpu().double().numpy(), S_ref) <= 1e-5
+    assert rel_l2(out.cpu().double().numpy(), o_ref) <= TOL[mode]
+    assert rel_l2(S.cpu().double().numpy(), S_ref) <= TOL[mode]
 
 
 def test_bf16_output_in_fp32_mode():
@@ -153,7 +160,8 @@ def test_bf16_output_in_fp32_mode():
     assert rel_l2(S.double().numpy(), S_ref) <= 1e-5
 
 
-def test_device_detects_bad_offsets_without_host_mirror():
+@pytest.mark.parametrize("mode", MODES)
+def test_device_detects_bad_offsets_without_host_mirror(mode):
     """Offsets past T with no host mirror: the kernel reports through the status
     word, skips that sequence, and computes the others."""
     x = _small([40, 30], H=2, seed=8)
@@ -162,10 +170,10 @@ def test_device_detects_bad_offsets_without_host_mirror():
     bad = torch.tensor([0, 40, 90], dtype=torch.int32, device="cuda")   # 90 > T = 70
     status = torch.zeros(4, dtype=torch.int32, device="cuda")
     out = torch.zeros(70, 2, 128, device="cuda")
-    kda_chunk_fwd(d["q"], d["k"], d["v"], g, beta, bad, x.scale, mode="fp32_exact", out=out,
+    kda_chunk_fwd(d["q"], d["k"], d["v"], g, beta, bad, x.scale, mode=mode, out=out,
                   status=status)
     torch.cuda.synchronize()
     assert int(status[0]) == 6
     o_ref, _, _, _ = oracle_pipeline(x)
-    assert rel_l2(out[:40].cpu().double().numpy(), o_ref[:40]) <= 1e-5
+    assert rel_l2(out[:40].cpu().double().numpy(), o_ref[:40]) <= TOL[mode]
     assert torch.count_nonzero(out[40:]) == 0
