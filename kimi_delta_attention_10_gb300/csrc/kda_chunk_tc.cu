@@ -3,28 +3,35 @@
 // One CTA (256 threads) per (sequence, head); chunks of 64 tokens in order.
 // The state is carried transposed, S^T (V x K = 128 x 128): its FP32 master
 // lives in registers (thread (v, half) holds S^T[v][64 half .. 64 half + 63])
-// and a BF16 copy in shared memory is the A operand of the next chunk's MMAs.
-// Every MMA has M = 128 (the V or K dimension) so D occupies all 128 TMEM lanes.
+// and an FP16 copy in shared memory is the A operand of the next chunk's MMAs.
 //
 // Per chunk (the chunk solve of "Add opt-in FP32 KDA chunk computation",
-// sections Problem and Change, in its WY form):
-//   prep (CUDA cores)  q^, k^ (L2 norm), a = e^g, A_kk, A_qk (overflow-safe
-//                      factors, as in the FP32 kernel), T = (I + A_kk)^-1
-//                      by 16x16 blocks, X = beta k^ o e^G, Q' = q^ o e^G,
-//                      K'' = k^ o e^{G_last - G}, d = e^{G_last}
-//   MMA (TF32)         W^T = X^T T^T,  U^T = (beta V)^T T^T
-//   MMA (BF16)         [W S]^T = S^T W^T,  [Q' S]^T = S^T Q'^T
-//   epilogue           Delta^T = U^T - [W S]^T
-//   MMA (TF32)         O^T += Delta^T Aqk^T,  P^T = Delta^T K''
-//   epilogue           out = scale O;  S^T <- S^T Diag(d) + P^T
+// sections Problem and Change, in its WY form), with G the in-chunk prefix of
+// the log-decay g and a_t = e^{g_t}:
+//   A_kk[i][j] = beta_i sum_c k^_ic k^_jc e^{G_ic - G_jc}   (j < i)
+//   A_qk[i][j] =        sum_c q^_ic k^_jc e^{G_ic - G_jc}   (j <= i)
+//   T' = (I + A_kk)^-1 diag(beta)
+//   W = T' (K^ o e^G),  U = T' V
+//   Delta = U - W S,  O = scale [(Q^ o e^G) S + A_qk Delta]
+//   S <- Diag(e^{G_last}) S + (K^ o e^{G_last - G})^T Delta
 //
-// Operand precision: the state-side products (W S, Q' S) take BF16 operands;
-// every product inside the chunk (T, Delta, A_qk, K'') takes TF32 operands,
-// because BF16 rounding there alone costs about 1.6e-3 of output rel-L2 (FP64
-// emulation of this algorithm), which with a BF16 output would exceed the
-// 3e-3 budget.  Accumulation is FP32 in TMEM throughout.
+// Pair sums on tensor cores without overflow.  e^{G_i - G_j} is never formed
+// as e^{G_i} e^{-G_j} (in-chunk decays reach e^{-1000}).  The 64 tokens are
+// split as a binary tree: at level s (blocks of 2s tokens, midpoint m), every
+// pair with j in the lower half and i in the upper half of one block factors as
+//   e^{G_i - G_j} = (prod_{t=m}^{i} a_t) (prod_{t=j+1}^{m-1} a_t),
+// both factors <= 1.  Each level is then a product of "left" rows
+// (k^_i or q^_i times the upper factor) with "right" rows (k^_j times the
+// lower factor) over the 128 channels; levels 32/16, 8/4, 2/1 are three
+// M=128, N=64, K=128 MMAs.  Every pair i > j belongs to exactly one level.
+//
+// Operands are FP16 (11-bit significand, as TF32, whose precision the
+// intra-chunk products need: BF16 operands there cost ~1.6e-3 of output
+// rel-L2 each in an FP64 emulation of this algorithm).  In this problem FP16
+// underflow only drops contributions far below the error budget.
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <stdint.h>
 
 #include "kda_internal.cuh"
@@ -39,36 +46,44 @@ constexpr int C = kChunk;     // 64
 constexpr int DK = kHeadK;    // 128
 constexpr int DV = kHeadV;    // 128
 constexpr int NT = 256;
-constexpr int LDW = 132;      // fp32 work-row stride (floats)
 constexpr int LDA = C + 1;
 constexpr int SB = 16;
 constexpr int NB = C / SB;
 constexpr uint32_t kWaitIters = 1u << 22;   // polls before a wait gives up
 
 // Shared memory map (bytes from a 1024-aligned base).
-constexpr uint32_t WORK_BYTES = C * LDW * 4;              // 33792 = 33 KiB
-constexpr uint32_t OFF_ST = 0;                            // S^T bf16 [128][128]   32 KiB
-constexpr uint32_t OFF_QW = OFF_ST + 32768;               // q work -> Q' bf16 | T tf32
-constexpr uint32_t OFF_KW = OFF_QW + WORK_BYTES;          // k work -> X^T tf32 -> W bf16 (MN)
-constexpr uint32_t OFF_AW = OFF_KW + WORK_BYTES;          // e^g -> k^ o bwd -> K''^T tf32
-constexpr uint32_t OFF_VW = OFF_AW + WORK_BYTES;          // v work -> (beta V)^T tf32 -> Delta^T
-constexpr uint32_t OFF_AQK = OFF_VW + WORK_BYTES;         // A_qk tf32 [64][64]    16 KiB
-constexpr uint32_t OFF_AKK = OFF_AQK + 16384;             // A_kk fp32 [64][65]
-constexpr uint32_t OFF_TF = OFF_AKK + C * LDA * 4;        // T fp32 [64][65]
-constexpr uint32_t OFF_BLK = OFF_TF + C * LDA * 4;        // blk fp32 [4][128]
-constexpr uint32_t OFF_DEC = OFF_BLK + NB * DK * 4;       // d fp32 [128]
-constexpr uint32_t OFF_BETA = OFF_DEC + DK * 4;           // beta fp32 [64]
-constexpr uint32_t OFF_BAR = OFF_BETA + C * 4;            // 3 mbarriers + TMEM slot + flag
+constexpr uint32_t OFF_ST = 0;          // S^T fp16 K-major [128 v][128 c]            32 KiB
+constexpr uint32_t OFF_SQ = 32768;      // q staging [64][128] 16-bit -> V^T fp16 K-major [128 v][64 j]
+constexpr uint32_t OFF_SK = 49152;      // k staging -> W fp16 MN-major [128 c][64 i]
+constexpr uint32_t OFF_SV = 65536;      // v staging [64][128] 16-bit
+constexpr uint32_t OFF_SG = 81920;      // g staging fp32 [64][128] -> Delta^T fp16 K-major [128 v][64 j]
+constexpr uint32_t OFF_AOP = 114688;    // pair-sum operands: A MN-major 2 x 16 KiB, B MN-major 16 KiB
+constexpr uint32_t AOP_B = OFF_AOP + 32768;
+constexpr uint32_t OFF_AKK = OFF_AOP;                 // after the pair sums: A_kk fp32 [64][65]
+constexpr uint32_t OFF_TF = OFF_AOP + C * LDA * 4;    //                      T fp32 [64][65]
+constexpr uint32_t OFF_AQK = OFF_AOP + 33792;         //                      A_qk fp16 K-major [64 i][64 j]
+constexpr uint32_t OFF_TP = OFF_AOP + 41984;          //                      T' fp16 K-major [64 i][64 j]
+constexpr uint32_t OFF_XT = OFF_AOP + 50176;          // X'^T fp16 K-major [128 c][64 j]
+constexpr uint32_t OFF_QP = OFF_XT + 16384;           // Q' fp16 MN-major [128 c][64 i]
+constexpr uint32_t OFF_KT = OFF_QP + 16384;           // K''^T fp16 K-major [128 c][64 j]
+constexpr uint32_t OFF_RQ = OFF_KT + 16384;           // 1/|q_t|           fp32 [64]
+constexpr uint32_t OFF_RK = OFF_RQ + 256;             // 1/|k_t|           fp32 [64]
+constexpr uint32_t OFF_DQK = OFF_RK + 256;            // q^_t . k^_t       fp32 [64]
+constexpr uint32_t OFF_BETA = OFF_DQK + 256;          // beta              fp32 [64]
+constexpr uint32_t OFF_DEC = OFF_BETA + 256;          // e^{G_last}        fp32 [128]
+constexpr uint32_t OFF_TOT = OFF_DEC + 512;           // half-chunk decay  fp32 [2][128]
+constexpr uint32_t OFF_BAR = OFF_TOT + 1024;          // 4 mbarriers + TMEM slot
 constexpr uint32_t SMEM_USED = OFF_BAR + 64;
-constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;         // + alignment slack
+constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;     // + alignment slack
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
-static_assert(OFF_QW % 1024 == 0 && OFF_KW % 1024 == 0 && OFF_AW % 1024 == 0 &&
-              OFF_VW % 1024 == 0 && OFF_AQK % 1024 == 0, "SW128 tiles need 1024-B alignment");
-constexpr uint32_t OFF_QP = OFF_QW;                        // Q' bf16 [64][128], 16 KiB
-constexpr uint32_t OFF_TT = OFF_QW + 16384;                // T tf32 [64][64], 16 KiB
+static_assert(OFF_TF + C * LDA * 4 <= OFF_AQK && OFF_TP + 8192 <= OFF_XT, "pair-sum region");
+static_assert(OFF_AQK % 1024 == 0 && OFF_TP % 1024 == 0 && OFF_XT % 1024 == 0 &&
+              OFF_QP % 1024 == 0 && OFF_KT % 1024 == 0 && AOP_B % 1024 == 0,
+              "SW128 tiles need 1024-B alignment");
 
 // TMEM columns.
-constexpr uint32_t TM_WS = 0, TM_O = 64, TM_P = 128, TM_W = 256, TM_U = 320, TM_COLS = 512;
+constexpr uint32_t TM_WS = 0, TM_O = 64, TM_P = 128, TM_A = 256, TM_W = 256, TM_U = 320;
+constexpr uint32_t TM_COLS = 512;
 
 __device__ __forceinline__ float warp_sum(float x)
 {
@@ -77,32 +92,160 @@ __device__ __forceinline__ float warp_sum(float x)
     return x;
 }
 
-// 8 consecutive input elements -> float.
-__device__ __forceinline__ void load8(const __nv_bfloat16* p, float (&x)[8])
+// Staging keeps 16-bit activations: BF16 inputs as they are, FP32 inputs
+// rounded to FP16 (the operands are FP16 anyway).
+template <typename TIn> struct Stage;
+template <> struct Stage<__nv_bfloat16> {
+    __device__ static float to_f32(uint16_t x) { return __uint_as_float((uint32_t)x << 16); }
+};
+template <> struct Stage<float> {
+    __device__ static float to_f32(uint16_t x) { return __half2float(__ushort_as_half(x)); }
+};
+
+__device__ __forceinline__ uint32_t pack_h2(float lo, float hi)
 {
-    const uint4 u = __ldg(reinterpret_cast<const uint4*>(p));
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        x[2 * i] = __uint_as_float(w[i] << 16);
-        x[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
-    }
-}
-__device__ __forceinline__ void load8(const float* p, float (&x)[8])
-{
-    const float4 a = __ldg(reinterpret_cast<const float4*>(p));
-    const float4 b = __ldg(reinterpret_cast<const float4*>(p + 4));
-    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
-    x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+    const __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&v);
 }
 
 __device__ __forceinline__ void store_out(float* p, float x) { *p = x; }
 __device__ __forceinline__ void store_out(__nv_bfloat16* p, float x) { *p = __float2bfloat16_rn(x); }
 
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi)
+// 8 FP16 values at MN indices m .. m+7 (m % 8 == 0) of K row `row` of a
+// 128-byte-swizzled tile whose 64-element MN groups are `gbytes` apart.
+__device__ __forceinline__ void st8(unsigned char* tile, uint32_t gbytes, int row, int m,
+                                    const float* v)
 {
-    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<const uint32_t*>(&v);
+    uint4 pk;
+    pk.x = pack_h2(v[0], v[1]);
+    pk.y = pack_h2(v[2], v[3]);
+    pk.z = pack_h2(v[4], v[5]);
+    pk.w = pack_h2(v[6], v[7]);
+    *reinterpret_cast<uint4*>(tile + (m >> 6) * gbytes + sw128(row, (m & 63) * 2)) = pk;
+}
+
+// One 16-byte piece of a chunk row, global -> staging (rows >= L are zero).
+template <typename TIn> struct Loader;
+template <> struct Loader<__nv_bfloat16> {
+    static constexpr int kPieces = DK / 8;          // 16-byte pieces per 128-element row
+    __device__ static uint4 load(const __nv_bfloat16* row, int piece)
+    {
+        return __ldg(reinterpret_cast<const uint4*>(row) + piece);
+    }
+    __device__ static void store(unsigned char* stage, int r, int piece, uint4 x)
+    {
+        *reinterpret_cast<uint4*>(stage + r * 256 + piece * 16) = x;
+    }
+};
+template <> struct Loader<float> {
+    static constexpr int kPieces = DK / 4;
+    __device__ static uint4 load(const float* row, int piece)
+    {
+        return __ldg(reinterpret_cast<const uint4*>(row) + piece);
+    }
+    __device__ static void store(unsigned char* stage, int r, int piece, uint4 x)
+    {
+        uint2 hx;
+        hx.x = pack_h2(__uint_as_float(x.x), __uint_as_float(x.y));
+        hx.y = pack_h2(__uint_as_float(x.z), __uint_as_float(x.w));
+        *reinterpret_cast<uint2*>(stage + r * 256 + piece * 8) = hx;
+    }
+};
+
+// Writes one level's left (upper-half) and right (lower-half) operand rows for
+// channel c over this thread's 32 tokens (a, kh, qh hold tokens 32 hh + u).
+// Level S <= 16: both halves of every 2S-block lie in this thread's 32 tokens,
+// and its 16 upper (and 16 lower) tokens have level indices 16 hh .. 16 hh + 15.
+template <int S>
+__device__ __forceinline__ void level_operands(unsigned char* sm, int c, int hh, int mo, int no,
+                                               const float (&a)[32], const float (&kh)[32],
+                                               const float (&qh)[32])
+{
+    float lk[16], lq[16], rr[16];
+#pragma unroll
+    for (int b = 0; b < 16 / S; ++b) {
+        const int lo = 2 * S * b, up = lo + S;       // local token indices
+        float p = 1.f;
+#pragma unroll
+        for (int x = 0; x < S; ++x) {                // upper: forward from the midpoint
+            p *= a[up + x];
+            lk[S * b + x] = kh[up + x] * p;
+            lq[S * b + x] = qh[up + x] * p;
+        }
+        p = 1.f;
+#pragma unroll
+        for (int x = S - 1; x >= 0; --x) {           // lower: backward to the midpoint
+            rr[S * b + x] = kh[lo + x] * p;
+            p *= a[lo + x];
+        }
+    }
+    unsigned char* A = sm + OFF_AOP;
+    unsigned char* B = sm + AOP_B;
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+        st8(A, 16384, c, mo + 16 * hh + 8 * q, lk + 8 * q);
+        st8(A, 16384, c, mo + 32 + 16 * hh + 8 * q, lq + 8 * q);
+        st8(B, 16384, c, no + 16 * hh + 8 * q, rr + 8 * q);
+    }
+}
+
+// Level 32: the upper half (tokens 32..63) is thread hh = 1, the lower hh = 0.
+__device__ __forceinline__ void level32_operands(unsigned char* sm, int c, int hh,
+                                                 const float (&a)[32], const float (&kh)[32],
+                                                 const float (&qh)[32])
+{
+    unsigned char* A = sm + OFF_AOP;
+    unsigned char* B = sm + AOP_B;
+    float v1[32], v2[32];
+    if (hh == 1) {
+        float p = 1.f;
+#pragma unroll
+        for (int x = 0; x < 32; ++x) {
+            p *= a[x];
+            v1[x] = kh[x] * p;
+            v2[x] = qh[x] * p;
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            st8(A, 16384, c, 8 * q, v1 + 8 * q);
+            st8(A, 16384, c, 32 + 8 * q, v2 + 8 * q);
+        }
+    } else {
+        float p = 1.f;
+#pragma unroll
+        for (int x = 31; x >= 0; --x) {
+            v1[x] = kh[x] * p;
+            p *= a[x];
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) st8(B, 16384, c, 8 * q, v1 + 8 * q);
+    }
+}
+
+// Pair sums of level S for the 32 TMEM lanes of this warp: lane u is upper
+// token index u of the level; columns [16 hf, 16 hf + 16) of the level's 32
+// right (lower-half) tokens.  k rows go to A_kk (times beta_i), q rows to A_qk.
+template <int S>
+__device__ __forceinline__ void extract_level(unsigned char* sm, uint32_t taddr, int u, int hf,
+                                              bool qrows)
+{
+    float r[16];
+    tmem_ld16(taddr, r);
+    const int bi = u / S;
+    const int i = bi * 2 * S + S + (u % S);
+    float (*akk)[LDA] = reinterpret_cast<float (*)[LDA]>(sm + OFF_AKK);
+    const float beta_i = reinterpret_cast<const float*>(sm + OFF_BETA)[i];
+#pragma unroll
+    for (int x = 0; x < 16; ++x) {
+        const int nn = 16 * hf + x;
+        if (nn / S == bi) {
+            const int j = (nn / S) * 2 * S + (nn % S);
+            if (qrows)
+                *reinterpret_cast<__half*>(sm + OFF_AQK + sw128(i, j * 2)) = __float2half_rn(r[x]);
+            else
+                akk[i][j] = beta_i * r[x];
+        }
+    }
 }
 
 template <typename TIn, typename TOut>
@@ -114,21 +257,25 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(ChunkArgs args)
     unsigned char* sm = smem_raw + pad;
     const uint32_t sb = raw_s + pad;                      // shared-window address of sm
 
-    float (*Qw)[LDW] = reinterpret_cast<float (*)[LDW]>(sm + OFF_QW);
-    float (*Kw)[LDW] = reinterpret_cast<float (*)[LDW]>(sm + OFF_KW);
-    float (*Aw)[LDW] = reinterpret_cast<float (*)[LDW]>(sm + OFF_AW);
-    float (*Vw)[LDW] = reinterpret_cast<float (*)[LDW]>(sm + OFF_VW);
     float (*akk)[LDA] = reinterpret_cast<float (*)[LDA]>(sm + OFF_AKK);
     float (*Tf)[LDA] = reinterpret_cast<float (*)[LDA]>(sm + OFF_TF);
-    float (*blk)[DK] = reinterpret_cast<float (*)[DK]>(sm + OFF_BLK);
-    float* dec = reinterpret_cast<float*>(sm + OFF_DEC);
+    const uint16_t* sq = reinterpret_cast<const uint16_t*>(sm + OFF_SQ);
+    const uint16_t* sk = reinterpret_cast<const uint16_t*>(sm + OFF_SK);
+    const uint16_t* sv = reinterpret_cast<const uint16_t*>(sm + OFF_SV);
+    const float* sg = reinterpret_cast<const float*>(sm + OFF_SG);
+    float* rq = reinterpret_cast<float*>(sm + OFF_RQ);
+    float* rk = reinterpret_cast<float*>(sm + OFF_RK);
+    float* dqk = reinterpret_cast<float*>(sm + OFF_DQK);
     float* sbeta = reinterpret_cast<float*>(sm + OFF_BETA);
-    uint64_t* bar = reinterpret_cast<uint64_t*>(sm + OFF_BAR);   // [0] prep, [1] S1, [2] S3
+    float* dec = reinterpret_cast<float*>(sm + OFF_DEC);
+    float* tot = reinterpret_cast<float*>(sm + OFF_TOT);
+    uint64_t* bar = reinterpret_cast<uint64_t*>(sm + OFF_BAR);   // [0] pairs [1] W/U [2] S1 [3] S3
     uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + OFF_BAR + 32);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int quad = warp & 3, half = warp >> 2;
-    const int row = 32 * quad + lane;                     // TMEM lane = V (or K) index
+    const int row = 32 * quad + lane;                     // TMEM lane
+    const int ch = tid & 127, hh = tid >> 7;              // channel / token-half ownership
     const int n = blockIdx.x / args.H, h = blockIdx.x % args.H;
     const int H = args.H;
 
@@ -141,6 +288,8 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(ChunkArgs args)
     const TIn* __restrict__ gk = static_cast<const TIn*>(args.k);
     const TIn* __restrict__ gv = static_cast<const TIn*>(args.v);
     TOut* __restrict__ out = static_cast<TOut*>(args.out);
+    using LD = Loader<TIn>;
+    using ST = Stage<TIn>;
 
     // ---- setup: zero S^T, TMEM allocation, barriers
     for (int e = tid; e < 32768 / 16; e += NT)
@@ -150,7 +299,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(ChunkArgs args)
         tmem_relinquish();
     }
     if (tid == 0) {
-        for (int b = 0; b < 3; ++b) mbar_init(&bar[b], 1);
+        for (int b = 0; b < 4; ++b) mbar_init(&bar[b], 1);
         fence_mbar_init();
     }
     fence_async_smem();
@@ -164,140 +313,190 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(ChunkArgs args)
 #pragma unroll
     for (int c = 0; c < 64; ++c) S[c] = 0.f;
     bool failed = false;
-    int last_bar = -1;                                     // last barrier committed to
-    uint32_t phase = 0;
+    int last_bar = -1;
+    uint32_t ph[4] = {0, 0, 0, 0};                         // next phase parity per barrier
 
-    for (int t0 = bos; t0 < eos && !failed; t0 += C, phase ^= 1u) {
+    for (int t0 = bos; t0 < eos; t0 += C) {
         const int L = min(C, eos - t0);
 
-        // ---- P1: load the chunk (rows >= L: zero, decay factor 1); zero A_qk
-        for (int e = tid; e < C * (DK / 8); e += NT) {
-            const int r = e / (DK / 8), c8 = (e % (DK / 8)) * 8;
-            float xq[8], xk[8], xv[8], xa[8];
-            if (r < L) {
-                const int64_t off = ((int64_t)(t0 + r) * H + h) * DK + c8;
-                load8(gq + off, xq);
-                load8(gk + off, xk);
-                load8(gv + ((int64_t)(t0 + r) * H + h) * DV + c8, xv);
-                const float4 g0 = __ldg(reinterpret_cast<const float4*>(args.g + off));
-                const float4 g1 = __ldg(reinterpret_cast<const float4*>(args.g + off + 4));
-                xa[0] = expf(g0.x); xa[1] = expf(g0.y); xa[2] = expf(g0.z); xa[3] = expf(g0.w);
-                xa[4] = expf(g1.x); xa[5] = expf(g1.y); xa[6] = expf(g1.z); xa[7] = expf(g1.w);
-            } else {
+        // ---- 1: load the chunk into staging (all loads issued before the stores)
+        {
+            constexpr int P = LD::kPieces;                 // pieces per row
+            constexpr int NQ = C * P / NT;                 // pieces per thread per tensor
+            uint4 xq[NQ], xk[NQ], xv[NQ], xg[8];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) { xq[i] = 0.f; xk[i] = 0.f; xv[i] = 0.f; xa[i] = 1.f; }
+            for (int u = 0; u < NQ; ++u) {
+                const int e = tid + u * NT, r = e / P, pc = e % P;
+                if (r < L) {
+                    const int64_t off = ((int64_t)(t0 + r) * H + h) * DK;
+                    xq[u] = LD::load(gq + off, pc);
+                    xk[u] = LD::load(gk + off, pc);
+                    xv[u] = LD::load(gv + off, pc);
+                } else {
+                    xq[u] = xk[u] = xv[u] = make_uint4(0, 0, 0, 0);
+                }
             }
 #pragma unroll
-            for (int i = 0; i < 8; i += 4) {
-                *reinterpret_cast<float4*>(&Qw[r][c8 + i]) = make_float4(xq[i], xq[i + 1], xq[i + 2], xq[i + 3]);
-                *reinterpret_cast<float4*>(&Kw[r][c8 + i]) = make_float4(xk[i], xk[i + 1], xk[i + 2], xk[i + 3]);
-                *reinterpret_cast<float4*>(&Vw[r][c8 + i]) = make_float4(xv[i], xv[i + 1], xv[i + 2], xv[i + 3]);
-                *reinterpret_cast<float4*>(&Aw[r][c8 + i]) = make_float4(xa[i], xa[i + 1], xa[i + 2], xa[i + 3]);
+            for (int u = 0; u < 8; ++u) {
+                const int e = tid + u * NT, r = e / 32, pc = e % 32;
+                xg[u] = (r < L) ? __ldg(reinterpret_cast<const uint4*>(
+                                      args.g + ((int64_t)(t0 + r) * H + h) * DK) + pc)
+                                : make_uint4(0, 0, 0, 0);
+            }
+            const float bt = (tid < L) ? args.beta[(int64_t)(t0 + tid) * H + h] : 0.f;
+#pragma unroll
+            for (int u = 0; u < NQ; ++u) {
+                const int e = tid + u * NT, r = e / P, pc = e % P;
+                LD::store(sm + OFF_SQ, r, pc, xq[u]);
+                LD::store(sm + OFF_SK, r, pc, xk[u]);
+                LD::store(sm + OFF_SV, r, pc, xv[u]);
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                reinterpret_cast<uint4*>(sm + OFF_SG)[tid + u * NT] = xg[u];
+            if (tid < C) sbeta[tid] = bt;
+        }
+        __syncthreads();
+
+        // ---- 2: row norms and q^ . k^ (warp per row)
+        for (int r = warp; r < C; r += NT / 32) {
+            float s2q = 0.f, s2k = 0.f, sqk = 0.f;
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                const float x = ST::to_f32(sq[r * DK + lane + 32 * m]);
+                const float y = ST::to_f32(sk[r * DK + lane + 32 * m]);
+                s2q += x * x;
+                s2k += y * y;
+                sqk += x * y;
+            }
+            s2q = warp_sum(s2q);
+            s2k = warp_sum(s2k);
+            sqk = warp_sum(sqk);
+            if (lane == 0) {
+                const float iq = args.l2norm ? 1.f / sqrtf(s2q + 1e-6f) : 1.f;
+                const float ik = args.l2norm ? 1.f / sqrtf(s2k + 1e-6f) : 1.f;
+                rq[r] = iq;
+                rk[r] = ik;
+                dqk[r] = iq * ik * sqk;
             }
         }
-        if (tid < C) sbeta[tid] = tid < L ? args.beta[(int64_t)(t0 + tid) * H + h] : 0.f;
-        for (int e = tid; e < 16384 / 16; e += NT)
+        __syncthreads();
+
+        // ---- 3: per channel (thread ch, tokens 32 hh .. 32 hh + 31)
+        float a[32], kh[32], qh[32];
+        {
+#pragma unroll
+            for (int u = 0; u < 32; ++u) {
+                const int t = 32 * hh + u;
+                a[u] = expf(sg[t * DK + ch]);
+                kh[u] = ST::to_f32(sk[t * DK + ch]) * rk[t];
+                qh[u] = ST::to_f32(sq[t * DK + ch]) * rq[t];
+            }
+            float p = 1.f;
+#pragma unroll
+            for (int u = 0; u < 32; ++u) p *= a[u];
+            tot[hh * DK + ch] = p;
+        }
+        __syncthreads();
+        {
+            // X'^T = k^ o e^G, Q' = q^ o e^G, K''^T = k^ o e^{G_last - G} (rows of channel ch)
+            const float before = hh ? tot[ch] : 1.f;          // decay of tokens before my half
+            const float after = hh ? 1.f : tot[DK + ch];      // decay of tokens after my half
+            if (hh == 0) dec[ch] = tot[ch] * tot[DK + ch];
+            float x1[32], x2[32];
+            float p = before;
+#pragma unroll
+            for (int u = 0; u < 32; ++u) {
+                p *= a[u];
+                x1[u] = kh[u] * p;
+                x2[u] = qh[u] * p;
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                st8(sm + OFF_XT, 0, ch, 32 * hh + 8 * q, x1 + 8 * q);
+                st8(sm + OFF_QP, 0, ch, 32 * hh + 8 * q, x2 + 8 * q);
+            }
+            p = after;
+#pragma unroll
+            for (int u = 31; u >= 0; --u) {
+                x1[u] = kh[u] * p;
+                p *= a[u];
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) st8(sm + OFF_KT, 0, ch, 32 * hh + 8 * q, x1 + 8 * q);
+        }
+
+        // ---- 4: pair sums, three rounds of (left x right) MMAs over the channels
+#pragma unroll
+        for (int rnd = 0; rnd < 3; ++rnd) {
+            if (rnd == 0) {
+                level32_operands(sm, ch, hh, a, kh, qh);
+                level_operands<16>(sm, ch, hh, 64, 32, a, kh, qh);
+            } else if (rnd == 1) {
+                level_operands<8>(sm, ch, hh, 0, 0, a, kh, qh);
+                level_operands<4>(sm, ch, hh, 64, 32, a, kh, qh);
+            } else {
+                level_operands<2>(sm, ch, hh, 0, 0, a, kh, qh);
+                level_operands<1>(sm, ch, hh, 64, 32, a, kh, qh);
+            }
+            fence_async_smem();
+            fence_before_sync();
+            __syncthreads();
+            if (tid == 0) {
+                fence_after_sync();
+                constexpr uint32_t id = idesc(kFmtF16, 128, 64, true, true);
+#pragma unroll
+                for (int s = 0; s < 8; ++s)
+                    mma_f16(tmem + TM_A + 64 * rnd, desc_mnmajor128(sb + OFF_AOP, 16384, s),
+                            desc_mnmajor64(sb + AOP_B, s), id, s > 0);
+                commit(&bar[0]);
+            }
+            if (rnd == 0) {
+                // V^T fp16 K-major [v][j] into the q staging (q is no longer read)
+                float vv[32];
+#pragma unroll
+                for (int u = 0; u < 32; ++u) vv[u] = ST::to_f32(sv[(32 * hh + u) * DV + ch]);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) st8(sm + OFF_SQ, 0, ch, 32 * hh + 8 * q, vv + 8 * q);
+            }
+            last_bar = 0;
+            {
+                const bool ok = mbar_wait(&bar[0], ph[0], kWaitIters);
+                ph[0] ^= 1u;
+                if (__syncthreads_or(!ok)) { failed = true; break; }
+            }
+            fence_after_sync();
+        }
+        if (failed) break;
+
+        // ---- 5: extract A_kk (fp32) and A_qk (fp16 operand) from TMEM
+        for (int e = tid; e < 8192 / 16; e += NT)
             reinterpret_cast<uint4*>(sm + OFF_AQK)[e] = make_uint4(0, 0, 0, 0);
         __syncthreads();
-
-        // ---- P2: L2 normalisation (warp per row)
-        if (args.l2norm) {
-            for (int r = warp; r < C; r += NT / 32) {
-                float sq = 0.f, sk = 0.f;
+        {
+            const bool second = quad >= 2, qrows = (quad & 1) != 0;
 #pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                    const float x = Qw[r][lane + 32 * m], y = Kw[r][lane + 32 * m];
-                    sq += x * x;
-                    sk += y * y;
-                }
-                sq = warp_sum(sq);
-                sk = warp_sum(sk);
-                const float iq = 1.f / sqrtf(sq + 1e-6f), ik = 1.f / sqrtf(sk + 1e-6f);
-#pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                    Qw[r][lane + 32 * m] *= iq;
-                    Kw[r][lane + 32 * m] *= ik;
+            for (int rnd = 0; rnd < 3; ++rnd) {
+                const uint32_t ta = tlane + TM_A + 64 * rnd + (second ? 32 : 0) + 16 * half;
+                if (rnd == 0) {
+                    if (second) extract_level<16>(sm, ta, lane, half, qrows);
+                    else extract_level<32>(sm, ta, lane, half, qrows);
+                } else if (rnd == 1) {
+                    if (second) extract_level<4>(sm, ta, lane, half, qrows);
+                    else extract_level<8>(sm, ta, lane, half, qrows);
+                } else {
+                    if (second) extract_level<1>(sm, ta, lane, half, qrows);
+                    else extract_level<2>(sm, ta, lane, half, qrows);
                 }
             }
-            __syncthreads();
+            if (tid < C)
+                *reinterpret_cast<__half*>(sm + OFF_AQK + sw128(tid, tid * 2)) = __float2half_rn(dqk[tid]);
         }
-
-        // ---- P3: pairs inside one 16-token block (running products of a_t)
-        for (int j = warp; j < C; j += NT / 32) {
-            const int bend = (j / SB) * SB + SB;
-            float kp[4];
-#pragma unroll
-            for (int m = 0; m < 4; ++m) kp[m] = Kw[j][lane + 32 * m];
-            for (int i = j; i < bend; ++i) {
-                float skk = 0.f, sqk = 0.f;
-#pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                    const int c = lane + 32 * m;
-                    if (i > j) kp[m] *= Aw[i][c];
-                    skk += Kw[i][c] * kp[m];
-                    sqk += Qw[i][c] * kp[m];
-                }
-                skk = warp_sum(skk);
-                sqk = warp_sum(sqk);
-                if (lane == 0) {
-                    akk[i][j] = (i > j) ? sbeta[i] * skk : 0.f;
-                    *reinterpret_cast<float*>(sm + OFF_AQK + sw128_tile(64, i, j * 4)) = sqk;
-                }
-            }
-        }
+        fence_before_sync();
         __syncthreads();
 
-        // ---- P4: per channel, products inside each block (fwd / bwd / totals)
-        if (tid < DK) {
-            const int c = tid;
-            float tot = 1.f;
-            for (int I = 0; I < NB; ++I) {
-                float av[SB], kk[SB];
-                float p = 1.f;
-#pragma unroll
-                for (int u = 0; u < SB; ++u) {
-                    const int r = I * SB + u;
-                    av[u] = Aw[r][c];
-                    kk[u] = Kw[r][c];
-                    p *= av[u];
-                    Qw[r][c] *= p;
-                    Kw[r][c] = kk[u] * p;
-                }
-                blk[I][c] = p;
-                tot *= p;
-                float pb = 1.f;
-#pragma unroll
-                for (int u = SB - 1; u >= 0; --u) {
-                    Aw[I * SB + u][c] = kk[u] * pb;
-                    pb *= av[u];
-                }
-            }
-            dec[c] = tot;
-        }
-        __syncthreads();
-
-        // ---- P5: pairs in different blocks
-        for (int e = tid; e < 6 * SB * SB; e += NT) {
-            const int pi = e / (SB * SB);
-            const int I = pi == 0 ? 1 : (pi < 3 ? 2 : 3);
-            const int J = pi == 0 ? 0 : (pi < 3 ? pi - 1 : pi - 3);
-            const int i = I * SB + (e % (SB * SB)) / SB;
-            const int j = J * SB + e % SB;
-            float skk = 0.f, sqk = 0.f;
-            for (int c = 0; c < DK; ++c) {
-                float mid = 1.f;
-                for (int M = J + 1; M < I; ++M) mid *= blk[M][c];
-                const float kb = Aw[j][c] * mid;
-                skk += Kw[i][c] * kb;
-                sqk += Qw[i][c] * kb;
-            }
-            akk[i][j] = sbeta[i] * skk;
-            *reinterpret_cast<float*>(sm + OFF_AQK + sw128_tile(64, i, j * 4)) = sqk;
-        }
-        __syncthreads();
-
-        // ---- P6: T = (I + A_kk)^-1 by 16x16 blocks
-        if (warp < NB && lane < SB) {          // diagonal blocks, one warp each
+        // ---- 6: T = (I + A_kk)^-1 by 16x16 blocks, then T' = T diag(beta) (fp16)
+        if (warp < NB && lane < SB) {
             const int b = warp * SB, m = lane;
             float tcol[SB];
 #pragma unroll
@@ -312,200 +511,138 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(ChunkArgs args)
         }
         __syncthreads();
         for (int d = 1; d < NB; ++d) {
-            // Y_IJ = sum_{M=J}^{I-1} A_IM T_MJ, kept in the unused block (J, I) of Tf
             for (int e = tid; e < (NB - d) * SB * SB; e += NT) {
                 const int J = e / (SB * SB), I = J + d;
                 const int r = (e % (SB * SB)) / SB, cc = e % SB;
                 float acc = 0.f;
                 for (int M = J; M < I; ++M)
+#pragma unroll
                     for (int k = 0; k < SB; ++k)
                         acc += akk[I * SB + r][M * SB + k] * Tf[M * SB + k][J * SB + cc];
-                Tf[J * SB + r][I * SB + cc] = acc;
+                Tf[J * SB + r][I * SB + cc] = acc;        // Y_IJ, in the unused block (J, I)
             }
             __syncthreads();
-            // T_IJ = -T_II Y_IJ
             for (int e = tid; e < (NB - d) * SB * SB; e += NT) {
                 const int J = e / (SB * SB), I = J + d;
                 const int r = (e % (SB * SB)) / SB, cc = e % SB;
                 float acc = 0.f;
-                for (int k = 0; k <= r; ++k) acc += Tf[I * SB + r][I * SB + k] * Tf[J * SB + k][I * SB + cc];
+#pragma unroll
+                for (int k = 0; k < SB; ++k)
+                    if (k <= r) acc += Tf[I * SB + r][I * SB + k] * Tf[J * SB + k][I * SB + cc];
                 Tf[I * SB + r][J * SB + cc] = -acc;
             }
             __syncthreads();
         }
-
-        // ---- P7: MMA operands.  Read everything needed into registers first.
         {
-            // X^T[c][j] = beta_j k^_jc e^{G_jc}, K''^T[c][j] = k^_jc e^{G_last,c - G_jc},
-            // Q'[i][c] = q^_ic e^{G_ic}, (beta V)^T[v][j]; T tf32.
-            float xv[32], kv[32];
+            // T'[i][j] = T[i][j] beta_j (j <= i), row i, 8 columns per store
 #pragma unroll
-            for (int u = 0; u < 32; ++u) {
-                const int e = tid + u * NT;
-                const int j = e / DK, c = e % DK, J = j / SB;
-                float pre = 1.f, post = 1.f;
-                for (int M = 0; M < J; ++M) pre *= blk[M][c];
-                for (int M = J + 1; M < NB; ++M) post *= blk[M][c];
-                xv[u] = sbeta[j] * Kw[j][c] * pre;
-                kv[u] = Aw[j][c] * post;
-                Qw[j][c] *= pre;                          // Q' in place (fp32)
-            }
-            __syncthreads();
+            for (int u = 0; u < 2; ++u) {
+                const int e = tid + u * NT;                  // 512 pieces of 8
+                const int i = e / 8, j0 = (e % 8) * 8;
+                float v8[8];
 #pragma unroll
-            for (int u = 0; u < 32; ++u) {
-                const int e = tid + u * NT;
-                const int j = e / DK, c = e % DK;
-                *reinterpret_cast<float*>(sm + OFF_KW + sw128_tile(128, c, j * 4)) = xv[u];
-                *reinterpret_cast<float*>(sm + OFF_AW + sw128_tile(128, c, j * 4)) = kv[u];
-            }
-            float vv[32];
-#pragma unroll
-            for (int u = 0; u < 32; ++u) {
-                const int e = tid + u * NT;
-                const int j = e / DV, m = e % DV;
-                vv[u] = sbeta[j] * Vw[j][m];
-            }
-            __syncthreads();
-#pragma unroll
-            for (int u = 0; u < 32; ++u) {
-                const int e = tid + u * NT;
-                const int j = e / DV, m = e % DV;
-                *reinterpret_cast<float*>(sm + OFF_VW + sw128_tile(128, m, j * 4)) = vv[u];
-            }
-        }
-        __syncthreads();
-        // Q' bf16 K-major [64 i][128 c] (Q' fp32 still in Qw rows; written to the
-        // first 16 KiB of the same region after a register round trip).
-        {
-            uint32_t qp[16];
-#pragma unroll
-            for (int u = 0; u < 16; ++u) {
-                const int e = tid + u * NT;
-                const int i = e / 64, c2 = (e % 64) * 2;
-                qp[u] = pack_bf16(Qw[i][c2], Qw[i][c2 + 1]);
-            }
-            float tt[16];
-#pragma unroll
-            for (int u = 0; u < 16; ++u) {
-                const int e = tid + u * NT;
-                const int i = e / 64, j = e % 64;
-                tt[u] = (j <= i) ? Tf[i][j] : 0.f;
-            }
-            __syncthreads();
-#pragma unroll
-            for (int u = 0; u < 16; ++u) {
-                const int e = tid + u * NT;
-                const int i = e / 64, c2 = (e % 64) * 2;
-                *reinterpret_cast<uint32_t*>(sm + OFF_QP + sw128_tile(64, i, c2 * 2)) = qp[u];
-                const int j = e % 64;
-                *reinterpret_cast<float*>(sm + OFF_TT + sw128_tile(64, i, j * 4)) = tt[u];
+                for (int x = 0; x < 8; ++x) {
+                    const int j = j0 + x;
+                    v8[x] = (j <= i) ? Tf[i][j] * sbeta[j] : 0.f;
+                }
+                st8(sm + OFF_TP, 0, i, j0, v8);
             }
         }
         fence_async_smem();
         fence_before_sync();
         __syncthreads();
 
-        // ---- P8: W^T = X^T T^T, U^T = (beta V)^T T^T  (TF32)
+        // ---- 7: W^T = X'^T T'^T, U^T = V^T T'^T
         if (tid == 0) {
             fence_after_sync();
-            constexpr uint32_t id = idesc(kFmtTF32, 128, 64);
+            constexpr uint32_t id = idesc(kFmtF16, 128, 64);
 #pragma unroll
-            for (int s = 0; s < 8; ++s)
-                mma_tf32(tmem + TM_W, desc_kmajor(sb + OFF_KW, 128, s), desc_kmajor(sb + OFF_TT, 64, s), id, s > 0);
+            for (int s = 0; s < 4; ++s)
+                mma_f16(tmem + TM_W, desc_kmajor(sb + OFF_XT, 128, s), desc_kmajor(sb + OFF_TP, 64, s), id, s > 0);
 #pragma unroll
-            for (int s = 0; s < 8; ++s)
-                mma_tf32(tmem + TM_U, desc_kmajor(sb + OFF_VW, 128, s), desc_kmajor(sb + OFF_TT, 64, s), id, s > 0);
-            commit(&bar[0]);
-        }
-        last_bar = 0;
-        {
-            const bool ok = mbar_wait(&bar[0], phase, kWaitIters);
-            if (__syncthreads_or(!ok)) { failed = true; break; }
-        }
-        fence_after_sync();
-        // W bf16, MN-major [c][i] (row c = TMEM lane, 32 tokens per half)
-        {
-            float w[32];
-            tmem_ld32(tlane + TM_W + 32 * half, w);
-            unsigned char* dst = sm + OFF_KW;
-#pragma unroll
-            for (int q8 = 0; q8 < 4; ++q8) {
-                uint4 pk;
-                pk.x = pack_bf16(w[8 * q8 + 0], w[8 * q8 + 1]);
-                pk.y = pack_bf16(w[8 * q8 + 2], w[8 * q8 + 3]);
-                pk.z = pack_bf16(w[8 * q8 + 4], w[8 * q8 + 5]);
-                pk.w = pack_bf16(w[8 * q8 + 6], w[8 * q8 + 7]);
-                *reinterpret_cast<uint4*>(dst + sw128(row, (32 * half + 8 * q8) * 2)) = pk;
-            }
-        }
-        fence_async_smem();
-        fence_before_sync();
-        __syncthreads();
-
-        // ---- S1: [W S]^T = S^T W^T, [Q' S]^T = S^T Q'^T  (BF16)
-        if (tid == 0) {
-            fence_after_sync();
-            constexpr uint32_t idw = idesc(kFmtBF16, 128, 64, false, true);
-            constexpr uint32_t idq = idesc(kFmtBF16, 128, 64);
-#pragma unroll
-            for (int s = 0; s < 8; ++s)
-                mma_bf16(tmem + TM_WS, desc_kmajor(sb + OFF_ST, 128, s), desc_mnmajor64(sb + OFF_KW, s), idw, s > 0);
-#pragma unroll
-            for (int s = 0; s < 8; ++s)
-                mma_bf16(tmem + TM_O, desc_kmajor(sb + OFF_ST, 128, s), desc_kmajor(sb + OFF_QP, 64, s), idq, s > 0);
+            for (int s = 0; s < 4; ++s)
+                mma_f16(tmem + TM_U, desc_kmajor(sb + OFF_SQ, 128, s), desc_kmajor(sb + OFF_TP, 64, s), id, s > 0);
             commit(&bar[1]);
         }
         last_bar = 1;
         {
-            const bool ok = mbar_wait(&bar[1], phase, kWaitIters);
+            const bool ok = mbar_wait(&bar[1], ph[1], kWaitIters);
+            ph[1] ^= 1u;
             if (__syncthreads_or(!ok)) { failed = true; break; }
         }
         fence_after_sync();
-        // Delta^T[v][i] = U^T[v][i] - [W S]^T[v][i], TF32 operand K-major [v][i]
         {
-            float ws[32], uu[32];
-            tmem_ld32(tlane + TM_WS + 32 * half, ws);
-            tmem_ld32(tlane + TM_U + 32 * half, uu);
-            unsigned char* dst = sm + OFF_VW;
+            // W fp16 MN-major [c][i] into the k staging (row c = TMEM lane)
+            float w[32];
+            tmem_ld32(tlane + TM_W + 32 * half, w);
 #pragma unroll
-            for (int q4 = 0; q4 < 8; ++q4) {
-                const float4 dv = make_float4(uu[4 * q4] - ws[4 * q4], uu[4 * q4 + 1] - ws[4 * q4 + 1],
-                                              uu[4 * q4 + 2] - ws[4 * q4 + 2], uu[4 * q4 + 3] - ws[4 * q4 + 3]);
-                *reinterpret_cast<float4*>(dst + sw128_tile(128, row, (32 * half + 4 * q4) * 4)) = dv;
-            }
+            for (int q = 0; q < 4; ++q) st8(sm + OFF_SK, 0, row, 32 * half + 8 * q, w + 8 * q);
         }
         fence_async_smem();
         fence_before_sync();
         __syncthreads();
 
-        // ---- S3: O^T += Delta^T Aqk^T, P^T = Delta^T K''  (TF32)
+        // ---- 8: [W S]^T = S^T W^T, [Q' S]^T = S^T Q'^T
         if (tid == 0) {
             fence_after_sync();
-            constexpr uint32_t ido = idesc(kFmtTF32, 128, 64);
-            constexpr uint32_t idp = idesc(kFmtTF32, 128, 128);
+            constexpr uint32_t id = idesc(kFmtF16, 128, 64, false, true);
 #pragma unroll
             for (int s = 0; s < 8; ++s)
-                mma_tf32(tmem + TM_O, desc_kmajor(sb + OFF_VW, 128, s), desc_kmajor(sb + OFF_AQK, 64, s), ido, 1);
+                mma_f16(tmem + TM_WS, desc_kmajor(sb + OFF_ST, 128, s), desc_mnmajor64(sb + OFF_SK, s), id, s > 0);
 #pragma unroll
             for (int s = 0; s < 8; ++s)
-                mma_tf32(tmem + TM_P, desc_kmajor(sb + OFF_VW, 128, s), desc_kmajor(sb + OFF_AW, 128, s), idp, s > 0);
+                mma_f16(tmem + TM_O, desc_kmajor(sb + OFF_ST, 128, s), desc_mnmajor64(sb + OFF_QP, s), id, s > 0);
             commit(&bar[2]);
         }
         last_bar = 2;
         {
-            const bool ok = mbar_wait(&bar[2], phase, kWaitIters);
+            const bool ok = mbar_wait(&bar[2], ph[2], kWaitIters);
+            ph[2] ^= 1u;
             if (__syncthreads_or(!ok)) { failed = true; break; }
         }
         fence_after_sync();
-        // out = scale * O;  S^T <- S^T Diag(d) + P^T;  BF16 copy of S^T for the next chunk
         {
+            // Delta^T[v][i] = U^T[v][i] - [W S]^T[v][i], fp16 K-major [v][i]
+            float ws[32], uu[32];
+            tmem_ld32(tlane + TM_WS + 32 * half, ws);
+            tmem_ld32(tlane + TM_U + 32 * half, uu);
+#pragma unroll
+            for (int x = 0; x < 32; ++x) uu[x] -= ws[x];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) st8(sm + OFF_SG, 0, row, 32 * half + 8 * q, uu + 8 * q);
+        }
+        fence_async_smem();
+        fence_before_sync();
+        __syncthreads();
+
+        // ---- 9: O^T += Delta^T A_qk^T, P^T = Delta^T K''
+        if (tid == 0) {
+            fence_after_sync();
+            constexpr uint32_t ido = idesc(kFmtF16, 128, 64);
+            constexpr uint32_t idp = idesc(kFmtF16, 128, 128);
+#pragma unroll
+            for (int s = 0; s < 4; ++s)
+                mma_f16(tmem + TM_O, desc_kmajor(sb + OFF_SG, 128, s), desc_kmajor(sb + OFF_AQK, 64, s), ido, 1);
+#pragma unroll
+            for (int s = 0; s < 4; ++s)
+                mma_f16(tmem + TM_P, desc_kmajor(sb + OFF_SG, 128, s), desc_kmajor(sb + OFF_KT, 128, s), idp, s > 0);
+            commit(&bar[3]);
+        }
+        last_bar = 3;
+        {
+            const bool ok = mbar_wait(&bar[3], ph[3], kWaitIters);
+            ph[3] ^= 1u;
+            if (__syncthreads_or(!ok)) { failed = true; break; }
+        }
+        fence_after_sync();
+        {
+            // out = scale O;  S^T <- S^T Diag(d) + P^T;  fp16 copy of S^T
             float o[32];
             tmem_ld32(tlane + TM_O + 32 * half, o);
-            const int v = row;
 #pragma unroll
             for (int u = 0; u < 32; ++u) {
                 const int i = 32 * half + u;
-                if (i < L) store_out(out + ((int64_t)(t0 + i) * H + h) * DV + v, args.scale * o[u]);
+                if (i < L) store_out(out + ((int64_t)(t0 + i) * H + h) * DV + row, args.scale * o[u]);
             }
             float p[32];
 #pragma unroll
@@ -517,15 +654,14 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(ChunkArgs args)
                     S[32 * part + u] = S[32 * part + u] * dec[c] + p[u];
                 }
             }
-            unsigned char* dst = sm + OFF_ST;
 #pragma unroll
-            for (int q8 = 0; q8 < 8; ++q8) {
+            for (int q = 0; q < 8; ++q) {
                 uint4 pk;
-                pk.x = pack_bf16(S[8 * q8 + 0], S[8 * q8 + 1]);
-                pk.y = pack_bf16(S[8 * q8 + 2], S[8 * q8 + 3]);
-                pk.z = pack_bf16(S[8 * q8 + 4], S[8 * q8 + 5]);
-                pk.w = pack_bf16(S[8 * q8 + 6], S[8 * q8 + 7]);
-                *reinterpret_cast<uint4*>(dst + sw128_tile(128, row, (64 * half + 8 * q8) * 2)) = pk;
+                pk.x = pack_h2(S[8 * q + 0], S[8 * q + 1]);
+                pk.y = pack_h2(S[8 * q + 2], S[8 * q + 3]);
+                pk.z = pack_h2(S[8 * q + 4], S[8 * q + 5]);
+                pk.w = pack_h2(S[8 * q + 6], S[8 * q + 7]);
+                *reinterpret_cast<uint4*>(sm + OFF_ST + sw128_tile(128, row, (64 * half + 8 * q) * 2)) = pk;
             }
         }
         fence_async_smem();
@@ -536,7 +672,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(ChunkArgs args)
     if (failed) {
         if (tid == 0) report_status(args.status, KDA_ERR_TIMEOUT);
         // let the MMAs still in flight finish before the TMEM is released
-        if (last_bar >= 0) mbar_wait(&bar[last_bar], phase, kWaitIters);
+        if (last_bar >= 0) mbar_wait(&bar[last_bar], ph[last_bar] ^ 1u, kWaitIters);
     } else if (args.final_state != nullptr) {
         float* fs = args.final_state + ((int64_t)n * H + h) * DK * DV;
 #pragma unroll

@@ -57,10 +57,18 @@ __device__ __forceinline__ uint64_t desc_mnmajor64(uint32_t base, uint32_t s)
     return desc_sw128(base + s * 2048u, 8192u, 1024u);
 }
 
-// Instruction descriptor (kind::f16 with BF16 operands, or kind::tf32), FP32 D.
-//   bits 4-5 D format (1 = F32), 7-9 A format, 10-12 B format (1 = BF16,
-//   2 = TF32), 15/16 A/B major (0 = K, 1 = MN), 17-22 N >> 3, 24-28 M >> 4.
-constexpr uint32_t kFmtBF16 = 1, kFmtTF32 = 2;
+// MN-major 16-bit operand with an MN extent of 128 elements: two 64-element
+// groups, each stored as K rows of 128 bytes; group 1 starts `group_bytes`
+// after group 0.  k-step `s` covers K rows 16 s .. 16 s + 15.
+__device__ __forceinline__ uint64_t desc_mnmajor128(uint32_t base, uint32_t group_bytes, uint32_t s)
+{
+    return desc_sw128(base + s * 2048u, group_bytes, 1024u);
+}
+
+// Instruction descriptor (kind::f16 with F16 or BF16 operands, or kind::tf32), FP32 D.
+//   bits 4-5 D format (1 = F32), 7-9 A format, 10-12 B format (0 = F16,
+//   1 = BF16, 2 = TF32), 15/16 A/B major (0 = K, 1 = MN), 17-22 N >> 3, 24-28 M >> 4.
+constexpr uint32_t kFmtF16 = 0, kFmtBF16 = 1, kFmtTF32 = 2;
 __host__ __device__ constexpr uint32_t idesc(uint32_t fmt, uint32_t M, uint32_t N,
                                              bool a_mn = false, bool b_mn = false)
 {
@@ -76,6 +84,14 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b
         "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
         "l"(a), "l"(b), "r"(id), "r"(acc));
+}
+
+// kind::f16 with F16 operands uses the same instruction as BF16; the format
+// lives in the instruction descriptor.
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t id,
+                                        uint32_t acc)
+{
+    mma_bf16(d_tmem, a, b, id, acc);
 }
 
 __device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t id,
@@ -177,6 +193,21 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&r)[32])
           "=r"(u[19]), "=r"(u[20]), "=r"(u[21]), "=r"(u[22]), "=r"(u[23]), "=r"(u[24]),
           "=r"(u[25]), "=r"(u[26]), "=r"(u[27]), "=r"(u[28]), "=r"(u[29]), "=r"(u[30]),
           "=r"(u[31])
+        : "r"(taddr)
+        : "memory");
+}
+
+// As tmem_ld32 for 16 columns.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&r)[16])
+{
+    uint32_t* u = reinterpret_cast<uint32_t*>(r);
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n"
+        "tcgen05.wait::ld.sync.aligned;\n"
+        : "=r"(u[0]), "=r"(u[1]), "=r"(u[2]), "=r"(u[3]), "=r"(u[4]), "=r"(u[5]), "=r"(u[6]),
+          "=r"(u[7]), "=r"(u[8]), "=r"(u[9]), "=r"(u[10]), "=r"(u[11]), "=r"(u[12]),
+          "=r"(u[13]), "=r"(u[14]), "=r"(u[15])
         : "r"(taddr)
         : "memory");
 }
