@@ -147,6 +147,22 @@ def gate_bytes(T, H, K):
     return T * H * K * (4 + 4) + T * H * (4 + 4)
 
 
+def max_over_ranks(x: float, device) -> float:
+    """Maximum of a per-rank float over the process group (identity without one)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(world: int, units_per_rank_step: int, steps: int, ms: float) -> float:
+    """Units processed by all ranks per second (weak scaling: every rank runs a batch)."""
+    return world * units_per_rank_step * steps / (ms * 1e-3)
+
+
 def workload_config(w, mode):
     return {"workload": w.name, "T": None, "N": None, "H": w.H, "K": w.K, "V": w.V,
             "qkv_dtype": str(w.qkv_dtype).replace("torch.", ""), "g_beta_dtype": "float32",
@@ -290,13 +306,9 @@ def main():
     end.record(stream)
     barrier()
     clk = clocks.stop()
-    ms = start.elapsed_time(end)
+    ms = max_over_ranks(start.elapsed_time(end), dev)
     gate_ms = [e[0].elapsed_time(e[1]) for e in evs]
     chunk_ms = [e[1].elapsed_time(e[2]) for e in evs]
-    if world > 1:
-        t = torch.tensor([ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
 
     # End to end through the public API: pinned host inputs copied in, result copied out.
     e2e = None
@@ -326,12 +338,8 @@ def main():
             e2e_step()
         e1.record(stream)
         barrier()
-        ems = e0.elapsed_time(e1)
-        if world > 1:
-            t = torch.tensor([ems], device=dev, dtype=torch.float64)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ems = float(t.item())
-        e2e = {"value": world * T * args.steps / (ems * 1e-3), "unit": UNIT,
+        ems = max_over_ranks(e0.elapsed_time(e1), dev)
+        e2e = {"value": whole_job_rate(world, T, args.steps, ems), "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
     if rank == 0:
@@ -349,7 +357,7 @@ def main():
                 "avg_launch_ms": avg_chunk_s * 1e3}
         cfg = workload_config(w, mode)
         cfg["T"], cfg["N"] = T, N
-        value = world * T * args.steps / (ms * 1e-3)
+        value = whole_job_rate(world, T, args.steps, ms)
         chunk_tps = T / avg_chunk_s
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,

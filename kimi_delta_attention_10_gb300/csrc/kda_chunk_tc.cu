@@ -54,16 +54,17 @@ constexpr uint32_t kWaitIters = 1u << 22;   // polls before a wait gives up
 // Shared memory map (bytes from a 1024-aligned base).
 constexpr uint32_t OFF_ST = 0;          // S^T fp16 K-major [128 v][128 c]            32 KiB
 constexpr uint32_t OFF_SQ = 32768;      // q staging [64][128] 16-bit -> V^T fp16 K-major [128 v][64 j]
-constexpr uint32_t OFF_SK = 49152;      // k staging -> W fp16 MN-major [128 c][64 i]
-constexpr uint32_t OFF_SV = 65536;      // v staging [64][128] 16-bit
-constexpr uint32_t OFF_SG = 81920;      // g staging fp32 [64][128] -> Delta^T fp16 K-major [128 v][64 j]
-constexpr uint32_t OFF_AOP = 114688;    // pair-sum operands: A MN-major 2 x 16 KiB, B MN-major 16 KiB
+constexpr uint32_t OFF_SV = 49152;      // v staging [64][128] 16-bit
+constexpr uint32_t OFF_SK = 65536;      // k staging -> pair-sum buffer 2 (A part 0) -> W fp16 MN-major
+constexpr uint32_t OFF_SG = 81920;      // g staging fp32 -> pair-sum buffer 2 (A part 1, B)
+constexpr uint32_t OFF_AOP = 114688;    // pair-sum buffer 1: A MN-major 2 x 16 KiB, B MN-major 16 KiB
 constexpr uint32_t AOP_B = OFF_AOP + 32768;
+constexpr uint32_t OFF_AOP2 = OFF_SK;   // pair-sum buffer 2 (after the k and g staging are read)
 constexpr uint32_t OFF_AKK = OFF_AOP;                 // after the pair sums: A_kk fp32 [64][65]
 constexpr uint32_t OFF_TF = OFF_AOP + C * LDA * 4;    //                      T fp32 [64][65]
 constexpr uint32_t OFF_AQK = OFF_AOP + 33792;         //                      A_qk fp16 K-major [64 i][64 j]
 constexpr uint32_t OFF_TP = OFF_AOP + 41984;          //                      T' fp16 K-major [64 i][64 j]
-constexpr uint32_t OFF_XT = OFF_AOP + 50176;          // X'^T fp16 K-major [128 c][64 j]
+constexpr uint32_t OFF_XT = OFF_AOP + 50176;          // X'^T fp16 K-major [128 c][64 j] -> Delta^T [128 v][64 j]
 constexpr uint32_t OFF_QP = OFF_XT + 16384;           // Q' fp16 MN-major [128 c][64 i]
 constexpr uint32_t OFF_KT = OFF_QP + 16384;           // K''^T fp16 K-major [128 c][64 j]
 constexpr uint32_t OFF_RQ = OFF_KT + 16384;           // 1/|q_t|           fp32 [64]
@@ -72,25 +73,19 @@ constexpr uint32_t OFF_DQK = OFF_RK + 256;            // q^_t . k^_t       fp32 
 constexpr uint32_t OFF_BETA = OFF_DQK + 256;          // beta              fp32 [64]
 constexpr uint32_t OFF_DEC = OFF_BETA + 256;          // e^{G_last}        fp32 [128]
 constexpr uint32_t OFF_TOT = OFF_DEC + 512;           // half-chunk decay  fp32 [2][128]
-constexpr uint32_t OFF_BAR = OFF_TOT + 1024;          // 4 mbarriers + TMEM slot
+constexpr uint32_t OFF_BAR = OFF_TOT + 1024;          // 6 mbarriers + TMEM slot
 constexpr uint32_t SMEM_USED = OFF_BAR + 64;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;     // + alignment slack
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 static_assert(OFF_TF + C * LDA * 4 <= OFF_AQK && OFF_TP + 8192 <= OFF_XT, "pair-sum region");
 static_assert(OFF_AQK % 1024 == 0 && OFF_TP % 1024 == 0 && OFF_XT % 1024 == 0 &&
-              OFF_QP % 1024 == 0 && OFF_KT % 1024 == 0 && AOP_B % 1024 == 0,
+              OFF_QP % 1024 == 0 && OFF_KT % 1024 == 0 && AOP_B % 1024 == 0 &&
+                  OFF_AOP2 + 49152 == OFF_AOP,
               "SW128 tiles need 1024-B alignment");
 
 // TMEM columns.
 constexpr uint32_t TM_WS = 0, TM_O = 64, TM_P = 128, TM_A = 256, TM_W = 256, TM_U = 320;
 constexpr uint32_t TM_COLS = 512;
-
-__device__ __forceinline__ float warp_sum(float x)
-{
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-    return x;
-}
 
 // Staging keeps 16-bit activations: BF16 inputs as they are, FP32 inputs
 // rounded to FP16 (the operands are FP16 anyway).
@@ -157,7 +152,7 @@ template <> struct Loader<float> {
 // Level S <= 16: both halves of every 2S-block lie in this thread's 32 tokens,
 // and its 16 upper (and 16 lower) tokens have level indices 16 hh .. 16 hh + 15.
 template <int S>
-__device__ __forceinline__ void level_operands(unsigned char* sm, int c, int hh, int mo, int no,
+__device__ __forceinline__ void level_operands(unsigned char* buf, int c, int hh, int mo, int no,
                                                const float (&a)[32], const float (&kh)[32],
                                                const float (&qh)[32])
 {
@@ -179,8 +174,8 @@ __device__ __forceinline__ void level_operands(unsigned char* sm, int c, int hh,
             p *= a[lo + x];
         }
     }
-    unsigned char* A = sm + OFF_AOP;
-    unsigned char* B = sm + AOP_B;
+    unsigned char* A = buf;
+    unsigned char* B = buf + 32768;
 #pragma unroll
     for (int q = 0; q < 2; ++q) {
         st8(A, 16384, c, mo + 16 * hh + 8 * q, lk + 8 * q);
@@ -190,12 +185,12 @@ __device__ __forceinline__ void level_operands(unsigned char* sm, int c, int hh,
 }
 
 // Level 32: the upper half (tokens 32..63) is thread hh = 1, the lower hh = 0.
-__device__ __forceinline__ void level32_operands(unsigned char* sm, int c, int hh,
+__device__ __forceinline__ void level32_operands(unsigned char* buf, int c, int hh,
                                                  const float (&a)[32], const float (&kh)[32],
                                                  const float (&qh)[32])
 {
-    unsigned char* A = sm + OFF_AOP;
-    unsigned char* B = sm + AOP_B;
+    unsigned char* A = buf;
+    unsigned char* B = buf + 32768;
     float v1[32], v2[32];
     if (hh == 1) {
         float p = 1.f;
@@ -223,14 +218,13 @@ __device__ __forceinline__ void level32_operands(unsigned char* sm, int c, int h
 }
 
 // Pair sums of level S for the 32 TMEM lanes of this warp: lane u is upper
-// token index u of the level; columns [16 hf, 16 hf + 16) of the level's 32
-// right (lower-half) tokens.  k rows go to A_kk (times beta_i), q rows to A_qk.
+// token index u of the level; r holds columns [16 hf, 16 hf + 16) of the
+// level's 32 right (lower-half) tokens.  k rows go to A_kk (times beta_i), q
+// rows to A_qk.  Writes only entries j < i.
 template <int S>
-__device__ __forceinline__ void extract_level(unsigned char* sm, uint32_t taddr, int u, int hf,
+__device__ __forceinline__ void extract_level(unsigned char* sm, const float* r, int u, int hf,
                                               bool qrows)
 {
-    float r[16];
-    tmem_ld16(taddr, r);
     const int bi = u / S;
     const int i = bi * 2 * S + S + (u % S);
     float (*akk)[LDA] = reinterpret_cast<float (*)[LDA]>(sm + OFF_AKK);
@@ -259,8 +253,8 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(ChunkArgs args)
 
     float (*akk)[LDA] = reinterpret_cast<float (*)[LDA]>(sm + OFF_AKK);
     float (*Tf)[LDA] = reinterpret_cast<float (*)[LDA]>(sm + OFF_TF);
-    const uint16_t* sq = reinterpret_cast<const uint16_t*>(sm + OFF_SQ);
     const uint16_t* sk = reinterpret_cast<const uint16_t*>(sm + OFF_SK);
+    const uint16_t* sq = reinterpret_cast<const uint16_t*>(sm + OFF_SQ);
     const uint16_t* sv = reinterpret_cast<const uint16_t*>(sm + OFF_SV);
     const float* sg = reinterpret_cast<const float*>(sm + OFF_SG);
     float* rq = reinterpret_cast<float*>(sm + OFF_RQ);
@@ -269,8 +263,9 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(ChunkArgs args)
     float* sbeta = reinterpret_cast<float*>(sm + OFF_BETA);
     float* dec = reinterpret_cast<float*>(sm + OFF_DEC);
     float* tot = reinterpret_cast<float*>(sm + OFF_TOT);
-    uint64_t* bar = reinterpret_cast<uint64_t*>(sm + OFF_BAR);   // [0] pairs [1] W/U [2] S1 [3] S3
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + OFF_BAR + 32);
+    // [0..2] pair-sum rounds, [3] W/U, [4] state products, [5] output/state update
+    uint64_t* bar = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + OFF_BAR + 56);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int quad = warp & 3, half = warp >> 2;
@@ -290,6 +285,10 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(ChunkArgs args)
     TOut* __restrict__ out = static_cast<TOut*>(args.out);
     using LD = Loader<TIn>;
     using ST = Stage<TIn>;
+    constexpr int P = LD::kPieces;                         // 16-byte pieces per row
+    constexpr int NQ = C * P / NT;                         // pieces per thread per tensor
+    // 16-bit inputs: the next chunk's loads are issued while this chunk computes.
+    constexpr bool kPrefetch = sizeof(TIn) == 2;
 
     // ---- setup: zero S^T, TMEM allocation, barriers
     for (int e = tid; e < 32768 / 16; e += NT)
@@ -299,7 +298,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(ChunkArgs args)
         tmem_relinquish();
     }
     if (tid == 0) {
-        for (int b = 0; b < 4; ++b) mbar_init(&bar[b], 1);
+        for (int b = 0; b < 6; ++b) mbar_init(&bar[b], 1);
         fence_mbar_init();
     }
     fence_async_smem();
@@ -314,15 +313,51 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(ChunkArgs args)
     for (int c = 0; c < 64; ++c) S[c] = 0.f;
     bool failed = false;
     int last_bar = -1;
-    uint32_t ph[4] = {0, 0, 0, 0};                         // next phase parity per barrier
+    uint32_t phase = 0;                                    // every barrier completes once per chunk
 
-    for (int t0 = bos; t0 < eos; t0 += C) {
+    // 16-bit inputs: each staging region receives the next chunk by cp.async as
+    // soon as its last reader in this chunk is done.  FP32 inputs are converted
+    // to FP16 on the way in, through registers, at the top of each chunk.
+    auto async_rows16 = [&](uint32_t off, const TIn* base, int tc) {
+        const int Lc = min(C, eos - tc);
+#pragma unroll
+        for (int u = 0; u < C * 16 / NT; ++u) {
+            const int e = tid + u * NT, r = e >> 4, pc = e & 15;
+            const bool ok = r < Lc;
+            const TIn* src = base + ((int64_t)(tc + (ok ? r : 0)) * H + h) * DK + pc * 8;
+            cp_async16(sm + off + r * 256 + pc * 16, src, ok);
+        }
+    };
+    auto async_g = [&](int tc) {
+        const int Lc = min(C, eos - tc);
+#pragma unroll
+        for (int u = 0; u < C * 32 / NT; ++u) {
+            const int e = tid + u * NT, r = e >> 5, pc = e & 31;
+            const bool ok = r < Lc;
+            const float* src = args.g + ((int64_t)(tc + (ok ? r : 0)) * H + h) * DK + pc * 4;
+            cp_async16(sm + OFF_SG + e * 16, src, ok);
+        }
+    };
+    float xb = 0.f;                                        // beta of this thread's row (tid < 64)
+    auto load_beta = [&](int tc) {
+        xb = (tid < min(C, eos - tc)) ? args.beta[(int64_t)(tc + tid) * H + h] : 0.f;
+    };
+    if (kPrefetch && bos < eos) {
+        async_rows16(OFF_SQ, gq, bos);
+        async_rows16(OFF_SK, gk, bos);
+        async_rows16(OFF_SV, gv, bos);
+        async_g(bos);
+        cp_async_commit();
+        load_beta(bos);
+    }
+
+    for (int t0 = bos; t0 < eos; t0 += C, phase ^= 1u) {
         const int L = min(C, eos - t0);
 
-        // ---- 1: load the chunk into staging (all loads issued before the stores)
-        {
-            constexpr int P = LD::kPieces;                 // pieces per row
-            constexpr int NQ = C * P / NT;                 // pieces per thread per tensor
+        // ---- 1: the chunk in staging (rows >= L zero, decay 1)
+        if (kPrefetch) {
+            cp_async_wait_all();
+        } else {
             uint4 xq[NQ], xk[NQ], xv[NQ], xg[8];
 #pragma unroll
             for (int u = 0; u < NQ; ++u) {
@@ -343,7 +378,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(ChunkArgs args)
                                       args.g + ((int64_t)(t0 + r) * H + h) * DK) + pc)
                                 : make_uint4(0, 0, 0, 0);
             }
-            const float bt = (tid < L) ? args.beta[(int64_t)(t0 + tid) * H + h] : 0.f;
+            load_beta(t0);
 #pragma unroll
             for (int u = 0; u < NQ; ++u) {
                 const int e = tid + u * NT, r = e / P, pc = e % P;
@@ -352,27 +387,40 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(ChunkArgs args)
                 LD::store(sm + OFF_SV, r, pc, xv[u]);
             }
 #pragma unroll
-            for (int u = 0; u < 8; ++u)
-                reinterpret_cast<uint4*>(sm + OFF_SG)[tid + u * NT] = xg[u];
-            if (tid < C) sbeta[tid] = bt;
+            for (int u = 0; u < 8; ++u) reinterpret_cast<uint4*>(sm + OFF_SG)[tid + u * NT] = xg[u];
         }
+        if (tid < C) sbeta[tid] = xb;
         __syncthreads();
+        const bool more = kPrefetch && t0 + C < eos;       // a next chunk to prefetch
 
-        // ---- 2: row norms and q^ . k^ (warp per row)
-        for (int r = warp; r < C; r += NT / 32) {
+        // ---- 2: row norms and q^ . k^ (4 threads per row, 32 channels each)
+        {
+            const int r = tid >> 2, p4 = tid & 3;
             float s2q = 0.f, s2k = 0.f, sqk = 0.f;
 #pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                const float x = ST::to_f32(sq[r * DK + lane + 32 * m]);
-                const float y = ST::to_f32(sk[r * DK + lane + 32 * m]);
-                s2q += x * x;
-                s2k += y * y;
-                sqk += x * y;
+            for (int i4 = 0; i4 < 4; ++i4) {
+                const int piece = p4 + 4 * ((i4 + r) & 3);   // 16-byte piece of the row
+                const uint4 uq = *reinterpret_cast<const uint4*>(sm + OFF_SQ + r * 256 + piece * 16);
+                const uint4 uk = *reinterpret_cast<const uint4*>(sm + OFF_SK + r * 256 + piece * 16);
+                const uint32_t wq[4] = {uq.x, uq.y, uq.z, uq.w}, wk[4] = {uk.x, uk.y, uk.z, uk.w};
+#pragma unroll
+                for (int w2 = 0; w2 < 4; ++w2) {
+                    const float q0 = ST::to_f32((uint16_t)(wq[w2] & 0xffffu));
+                    const float q1 = ST::to_f32((uint16_t)(wq[w2] >> 16));
+                    const float k0 = ST::to_f32((uint16_t)(wk[w2] & 0xffffu));
+                    const float k1 = ST::to_f32((uint16_t)(wk[w2] >> 16));
+                    s2q += q0 * q0 + q1 * q1;
+                    s2k += k0 * k0 + k1 * k1;
+                    sqk += q0 * k0 + q1 * k1;
+                }
             }
-            s2q = warp_sum(s2q);
-            s2k = warp_sum(s2k);
-            sqk = warp_sum(sqk);
-            if (lane == 0) {
+#pragma unroll
+            for (int o = 1; o < 4; o <<= 1) {
+                s2q += __shfl_xor_sync(0xffffffffu, s2q, o);
+                s2k += __shfl_xor_sync(0xffffffffu, s2k, o);
+                sqk += __shfl_xor_sync(0xffffffffu, sqk, o);
+            }
+            if (p4 == 0) {
                 const float iq = args.l2norm ? 1.f / sqrtf(s2q + 1e-6f) : 1.f;
                 const float ik = args.l2norm ? 1.f / sqrtf(s2k + 1e-6f) : 1.f;
                 rq[r] = iq;
@@ -426,68 +474,79 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(ChunkArgs args)
             for (int q = 0; q < 4; ++q) st8(sm + OFF_KT, 0, ch, 32 * hh + 8 * q, x1 + 8 * q);
         }
 
-        // ---- 4: pair sums, three rounds of (left x right) MMAs over the channels
-#pragma unroll
-        for (int rnd = 0; rnd < 3; ++rnd) {
-            if (rnd == 0) {
-                level32_operands(sm, ch, hh, a, kh, qh);
-                level_operands<16>(sm, ch, hh, 64, 32, a, kh, qh);
-            } else if (rnd == 1) {
-                level_operands<8>(sm, ch, hh, 0, 0, a, kh, qh);
-                level_operands<4>(sm, ch, hh, 64, 32, a, kh, qh);
-            } else {
-                level_operands<2>(sm, ch, hh, 0, 0, a, kh, qh);
-                level_operands<1>(sm, ch, hh, 64, 32, a, kh, qh);
-            }
+        // ---- 4: pair sums: three (left x right) MMAs over the channels, the
+        // operands of a round written while the previous round's MMA runs
+        constexpr uint32_t id_pairs = idesc(kFmtF16, 128, 64, true, true);
+        auto issue_round = [&](int rnd, uint32_t buf) {
             fence_async_smem();
             fence_before_sync();
             __syncthreads();
             if (tid == 0) {
                 fence_after_sync();
-                constexpr uint32_t id = idesc(kFmtF16, 128, 64, true, true);
 #pragma unroll
                 for (int s = 0; s < 8; ++s)
-                    mma_f16(tmem + TM_A + 64 * rnd, desc_mnmajor128(sb + OFF_AOP, 16384, s),
-                            desc_mnmajor64(sb + AOP_B, s), id, s > 0);
-                commit(&bar[0]);
+                    mma_f16(tmem + TM_A + 64 * rnd, desc_mnmajor128(sb + buf, 16384, s),
+                            desc_mnmajor64(sb + buf + 32768, s), id_pairs, s > 0);
+                commit(&bar[rnd]);
             }
-            if (rnd == 0) {
-                // V^T fp16 K-major [v][j] into the q staging (q is no longer read)
-                float vv[32];
+        };
+        auto wait_round = [&](int rnd) -> bool {
+            last_bar = rnd;
+            const bool ok = mbar_wait(&bar[rnd], phase, kWaitIters);
+            return __syncthreads_or(!ok) == 0;
+        };
+        level32_operands(sm + OFF_AOP, ch, hh, a, kh, qh);
+        level_operands<16>(sm + OFF_AOP, ch, hh, 64, 32, a, kh, qh);
+        issue_round(0, OFF_AOP);
+        {
+            // V^T fp16 K-major [v][j] into the q staging (q is no longer read)
+            float vv[32];
 #pragma unroll
-                for (int u = 0; u < 32; ++u) vv[u] = ST::to_f32(sv[(32 * hh + u) * DV + ch]);
+            for (int u = 0; u < 32; ++u) vv[u] = ST::to_f32(sv[(32 * hh + u) * DV + ch]);
 #pragma unroll
-                for (int q = 0; q < 4; ++q) st8(sm + OFF_SQ, 0, ch, 32 * hh + 8 * q, vv + 8 * q);
-            }
-            last_bar = 0;
-            {
-                const bool ok = mbar_wait(&bar[0], ph[0], kWaitIters);
-                ph[0] ^= 1u;
-                if (__syncthreads_or(!ok)) { failed = true; break; }
-            }
-            fence_after_sync();
+            for (int q = 0; q < 4; ++q) st8(sm + OFF_SQ, 0, ch, 32 * hh + 8 * q, vv + 8 * q);
         }
-        if (failed) break;
+        level_operands<8>(sm + OFF_AOP2, ch, hh, 0, 0, a, kh, qh);
+        level_operands<4>(sm + OFF_AOP2, ch, hh, 64, 32, a, kh, qh);
+        issue_round(1, OFF_AOP2);
+        if (more) { async_rows16(OFF_SV, gv, t0 + C); cp_async_commit(); }
+        if (!wait_round(0)) { failed = true; break; }
+        level_operands<2>(sm + OFF_AOP, ch, hh, 0, 0, a, kh, qh);
+        level_operands<1>(sm + OFF_AOP, ch, hh, 64, 32, a, kh, qh);
+        issue_round(2, OFF_AOP);
+        if (!wait_round(1)) { failed = true; break; }
+        if (more) { async_g(t0 + C); cp_async_commit(); load_beta(t0 + C); }
+        if (!wait_round(2)) { failed = true; break; }
+        fence_after_sync();
 
-        // ---- 5: extract A_kk (fp32) and A_qk (fp16 operand) from TMEM
-        for (int e = tid; e < 8192 / 16; e += NT)
-            reinterpret_cast<uint4*>(sm + OFF_AQK)[e] = make_uint4(0, 0, 0, 0);
-        __syncthreads();
+        // ---- 5: A_kk (fp32) and A_qk (fp16 operand) from TMEM.  The strictly
+        // upper part of A_qk is zeroed here, disjoint from the entries written.
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int e = tid + u * NT;                       // 512 pieces of 8 columns
+            const int i = e >> 3, p8 = e & 7;
+            unsigned char* dst = sm + OFF_AQK + sw128(i, p8 * 16);
+            if (8 * p8 > i) {
+                *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
+            } else if (8 * p8 + 7 > i) {
+#pragma unroll
+                for (int x = 0; x < 8; ++x)
+                    if (8 * p8 + x > i) reinterpret_cast<__half*>(dst)[x] = __float2half_rn(0.f);
+            }
+        }
         {
             const bool second = quad >= 2, qrows = (quad & 1) != 0;
-#pragma unroll
-            for (int rnd = 0; rnd < 3; ++rnd) {
-                const uint32_t ta = tlane + TM_A + 64 * rnd + (second ? 32 : 0) + 16 * half;
-                if (rnd == 0) {
-                    if (second) extract_level<16>(sm, ta, lane, half, qrows);
-                    else extract_level<32>(sm, ta, lane, half, qrows);
-                } else if (rnd == 1) {
-                    if (second) extract_level<4>(sm, ta, lane, half, qrows);
-                    else extract_level<8>(sm, ta, lane, half, qrows);
-                } else {
-                    if (second) extract_level<1>(sm, ta, lane, half, qrows);
-                    else extract_level<2>(sm, ta, lane, half, qrows);
-                }
+            const uint32_t tb = tlane + TM_A + (second ? 32 : 0) + 16 * half;
+            float r[48];
+            tmem_ld16x3(tb, tb + 64, tb + 128, r);
+            if (second) {
+                extract_level<16>(sm, r, lane, half, qrows);
+                extract_level<4>(sm, r + 16, lane, half, qrows);
+                extract_level<1>(sm, r + 32, lane, half, qrows);
+            } else {
+                extract_level<32>(sm, r, lane, half, qrows);
+                extract_level<8>(sm, r + 16, lane, half, qrows);
+                extract_level<2>(sm, r + 32, lane, half, qrows);
             }
             if (tid < C)
                 *reinterpret_cast<__half*>(sm + OFF_AQK + sw128(tid, tid * 2)) = __float2half_rn(dqk[tid]);
@@ -495,7 +554,8 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(ChunkArgs args)
         fence_before_sync();
         __syncthreads();
 
-        // ---- 6: T = (I + A_kk)^-1 by 16x16 blocks, then T' = T diag(beta) (fp16)
+        // ---- 6: T = (I + A_kk)^-1: 16x16 diagonal blocks, then the 32- and
+        // 64-row merges T_BA = -T_B A_BA T_A.  Y scratch lives in unused upper blocks.
         if (warp < NB && lane < SB) {
             const int b = warp * SB, m = lane;
             float tcol[SB];
@@ -510,26 +570,67 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(ChunkArgs args)
             for (int i = 0; i < SB; ++i) Tf[b + i][b + m] = tcol[i];
         }
         __syncthreads();
-        for (int d = 1; d < NB; ++d) {
-            for (int e = tid; e < (NB - d) * SB * SB; e += NT) {
-                const int J = e / (SB * SB), I = J + d;
-                const int r = (e % (SB * SB)) / SB, cc = e % SB;
-                float acc = 0.f;
-                for (int M = J; M < I; ++M)
+        {
+            // 32-row merges for blocks (1,0) and (3,2): Y = A_{I,I-1} T_{I-1,I-1}
 #pragma unroll
-                    for (int k = 0; k < SB; ++k)
-                        acc += akk[I * SB + r][M * SB + k] * Tf[M * SB + k][J * SB + cc];
-                Tf[J * SB + r][I * SB + cc] = acc;        // Y_IJ, in the unused block (J, I)
+            for (int u = 0; u < 2; ++u) {
+                const int e = tid + u * NT, I = 1 + 2 * (e >> 8), J = I - 1;
+                const int r = (e >> 4) & 15, cc = e & 15;
+                float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+                for (int k = 0; k < SB; k += 2) {
+                    s0 += akk[I * SB + r][J * SB + k] * Tf[J * SB + k][J * SB + cc];
+                    s1 += akk[I * SB + r][J * SB + k + 1] * Tf[J * SB + k + 1][J * SB + cc];
+                }
+                Tf[J * SB + r][I * SB + cc] = s0 + s1;
             }
             __syncthreads();
-            for (int e = tid; e < (NB - d) * SB * SB; e += NT) {
-                const int J = e / (SB * SB), I = J + d;
-                const int r = (e % (SB * SB)) / SB, cc = e % SB;
-                float acc = 0.f;
 #pragma unroll
-                for (int k = 0; k < SB; ++k)
-                    if (k <= r) acc += Tf[I * SB + r][I * SB + k] * Tf[J * SB + k][I * SB + cc];
-                Tf[I * SB + r][J * SB + cc] = -acc;
+            for (int u = 0; u < 2; ++u) {
+                const int e = tid + u * NT, I = 1 + 2 * (e >> 8), J = I - 1;
+                const int r = (e >> 4) & 15, cc = e & 15;
+                float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+                for (int k = 0; k < SB; k += 2) {
+                    s0 += Tf[I * SB + r][I * SB + k] * Tf[J * SB + k][I * SB + cc];
+                    s1 += Tf[I * SB + r][I * SB + k + 1] * Tf[J * SB + k + 1][I * SB + cc];
+                }
+                Tf[I * SB + r][J * SB + cc] = -(s0 + s1);
+            }
+            __syncthreads();
+            // 64-row merge: Y = A[32:64, 0:32] T[0:32, 0:32], kept in Tf[0:32, 32:64]
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int e = tid + u * NT, r = e >> 5, cc = e & 31;
+                const int k0 = cc < SB ? 0 : SB;            // T[0:32,0:32] is zero above its blocks
+                float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll
+                for (int k = 0; k < 32; k += 4) {
+                    if (k >= k0) {
+                        s0 += akk[32 + r][k] * Tf[k][cc];
+                        s1 += akk[32 + r][k + 1] * Tf[k + 1][cc];
+                        s2 += akk[32 + r][k + 2] * Tf[k + 2][cc];
+                        s3 += akk[32 + r][k + 3] * Tf[k + 3][cc];
+                    }
+                }
+                Tf[r][32 + cc] = (s0 + s1) + (s2 + s3);
+            }
+            __syncthreads();
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int e = tid + u * NT, r = e >> 5, cc = e & 31;
+                const int k1 = r < SB ? SB : 32;            // T[32:64,32:64] likewise
+                float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll
+                for (int k = 0; k < 32; k += 4) {
+                    if (k < k1) {
+                        s0 += Tf[32 + r][32 + k] * Tf[k][32 + cc];
+                        s1 += Tf[32 + r][32 + k + 1] * Tf[k + 1][32 + cc];
+                        s2 += Tf[32 + r][32 + k + 2] * Tf[k + 2][32 + cc];
+                        s3 += Tf[32 + r][32 + k + 3] * Tf[k + 3][32 + cc];
+                    }
+                }
+                Tf[32 + r][cc] = -((s0 + s1) + (s2 + s3));
             }
             __syncthreads();
         }
@@ -562,14 +663,14 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(ChunkArgs args)
 #pragma unroll
             for (int s = 0; s < 4; ++s)
                 mma_f16(tmem + TM_U, desc_kmajor(sb + OFF_SQ, 128, s), desc_kmajor(sb + OFF_TP, 64, s), id, s > 0);
-            commit(&bar[1]);
+            commit(&bar[3]);
         }
-        last_bar = 1;
+        last_bar = 3;
         {
-            const bool ok = mbar_wait(&bar[1], ph[1], kWaitIters);
-            ph[1] ^= 1u;
+            const bool ok = mbar_wait(&bar[3], phase, kWaitIters);
             if (__syncthreads_or(!ok)) { failed = true; break; }
         }
+        if (more) { async_rows16(OFF_SQ, gq, t0 + C); cp_async_commit(); }
         fence_after_sync();
         {
             // W fp16 MN-major [c][i] into the k staging (row c = TMEM lane)
@@ -592,24 +693,24 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(ChunkArgs args)
 #pragma unroll
             for (int s = 0; s < 8; ++s)
                 mma_f16(tmem + TM_O, desc_kmajor(sb + OFF_ST, 128, s), desc_mnmajor64(sb + OFF_QP, s), id, s > 0);
-            commit(&bar[2]);
+            commit(&bar[4]);
         }
-        last_bar = 2;
+        last_bar = 4;
         {
-            const bool ok = mbar_wait(&bar[2], ph[2], kWaitIters);
-            ph[2] ^= 1u;
+            const bool ok = mbar_wait(&bar[4], phase, kWaitIters);
             if (__syncthreads_or(!ok)) { failed = true; break; }
         }
+        if (more) { async_rows16(OFF_SK, gk, t0 + C); cp_async_commit(); }
         fence_after_sync();
         {
             // Delta^T[v][i] = U^T[v][i] - [W S]^T[v][i], fp16 K-major [v][i]
             float ws[32], uu[32];
-            tmem_ld32(tlane + TM_WS + 32 * half, ws);
             tmem_ld32(tlane + TM_U + 32 * half, uu);
+            tmem_ld32(tlane + TM_WS + 32 * half, ws);
 #pragma unroll
             for (int x = 0; x < 32; ++x) uu[x] -= ws[x];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) st8(sm + OFF_SG, 0, row, 32 * half + 8 * q, uu + 8 * q);
+            for (int q = 0; q < 4; ++q) st8(sm + OFF_XT, 0, row, 32 * half + 8 * q, uu + 8 * q);
         }
         fence_async_smem();
         fence_before_sync();
@@ -622,16 +723,15 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(ChunkArgs args)
             constexpr uint32_t idp = idesc(kFmtF16, 128, 128);
 #pragma unroll
             for (int s = 0; s < 4; ++s)
-                mma_f16(tmem + TM_O, desc_kmajor(sb + OFF_SG, 128, s), desc_kmajor(sb + OFF_AQK, 64, s), ido, 1);
+                mma_f16(tmem + TM_O, desc_kmajor(sb + OFF_XT, 128, s), desc_kmajor(sb + OFF_AQK, 64, s), ido, 1);
 #pragma unroll
             for (int s = 0; s < 4; ++s)
-                mma_f16(tmem + TM_P, desc_kmajor(sb + OFF_SG, 128, s), desc_kmajor(sb + OFF_KT, 128, s), idp, s > 0);
-            commit(&bar[3]);
+                mma_f16(tmem + TM_P, desc_kmajor(sb + OFF_XT, 128, s), desc_kmajor(sb + OFF_KT, 128, s), idp, s > 0);
+            commit(&bar[5]);
         }
-        last_bar = 3;
+        last_bar = 5;
         {
-            const bool ok = mbar_wait(&bar[3], ph[3], kWaitIters);
-            ph[3] ^= 1u;
+            const bool ok = mbar_wait(&bar[5], phase, kWaitIters);
             if (__syncthreads_or(!ok)) { failed = true; break; }
         }
         fence_after_sync();
@@ -649,10 +749,8 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(ChunkArgs args)
             for (int part = 0; part < 2; ++part) {
                 tmem_ld32(tlane + TM_P + 64 * half + 32 * part, p);
 #pragma unroll
-                for (int u = 0; u < 32; ++u) {
-                    const int c = 64 * half + 32 * part + u;
-                    S[32 * part + u] = S[32 * part + u] * dec[c] + p[u];
-                }
+                for (int u = 0; u < 32; ++u)
+                    S[32 * part + u] = S[32 * part + u] * dec[64 * half + 32 * part + u] + p[u];
             }
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
@@ -669,10 +767,12 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(ChunkArgs args)
         __syncthreads();
     }
 
+    if (kPrefetch) cp_async_wait_all();
     if (failed) {
         if (tid == 0) report_status(args.status, KDA_ERR_TIMEOUT);
         // let the MMAs still in flight finish before the TMEM is released
-        if (last_bar >= 0) mbar_wait(&bar[last_bar], ph[last_bar] ^ 1u, kWaitIters);
+        for (int b = 0; b <= 5; ++b)
+            if (b <= last_bar) mbar_wait(&bar[b], phase, kWaitIters);
     } else if (args.final_state != nullptr) {
         float* fs = args.final_state + ((int64_t)n * H + h) * DK * DV;
 #pragma unroll

@@ -1,0 +1,75 @@
+"""bench.py host logic on the CPU: the multi-rank reduction (gloo, world size 2),
+the whole-job rate, and the reference arm's JSON line."""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+ROOT = os.path.abspath(os.path.join(os.path.dirname(__file__), ".."))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        per_rank_ms = [12.5, 40.0][rank]
+        out[rank] = bench.max_over_ranks(per_rank_ms, "cpu")
+    finally:
+        dist.destroy_process_group()
+
+
+def test_max_over_ranks_gloo_two_ranks():
+    world, port = 2, _free_port()
+    mgr = mp.get_context("spawn").Manager()
+    out = mgr.dict()
+    mp.start_processes(_rank_main, args=(world, port, out), nprocs=world, join=True,
+                       start_method="spawn")
+    assert dict(out) == {0: 40.0, 1: 40.0}
+
+
+def test_max_over_ranks_without_group():
+    assert bench.max_over_ranks(3.25, "cpu") == 3.25
+
+
+def test_whole_job_rate_is_weak_scaling():
+    # 2 ranks x 16384 tokens x 10 steps in 1 s
+    assert bench.whole_job_rate(2, 16384, 10, 1000.0) == pytest.approx(327680.0)
+
+
+def _run_bench(args, env_extra):
+    env = dict(os.environ, **env_extra)
+    return subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), *args],
+                          capture_output=True, text=True, env=env, timeout=600, cwd=ROOT)
+
+
+def test_reference_arm_prints_one_json_line():
+    r = _run_bench(["--impl", "reference", "--workload", "packed_37_28_f32", "--steps", "2",
+                    "--warmup", "1"], {"RANK": "0"})
+    assert r.returncode == 0, r.stderr
+    lines = [l for l in r.stdout.splitlines() if l.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["value"] > 0 and d["unit"] == "tokens/s"
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+    assert d["config"]["workload"] == "packed_37_28_f32"
+
+
+def test_reference_arm_other_ranks_exit_quietly():
+    r = _run_bench(["--impl", "reference", "--workload", "packed_37_28_f32", "--steps", "1",
+                    "--warmup", "0"], {"RANK": "1"})
+    assert r.returncode == 0 and r.stdout.strip() == ""
