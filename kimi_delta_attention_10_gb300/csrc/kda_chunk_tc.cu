@@ -46,7 +46,7 @@ constexpr int C = kChunk;     // 64
 constexpr int DK = kHeadK;    // 128
 constexpr int DV = kHeadV;    // 128
 constexpr int NT = 256;
-constexpr int LDA = C + 1;
+constexpr int LDA = C + 4;     // fp32 row stride of A_kk and T: 16-byte aligned rows
 constexpr int SB = 16;
 constexpr int NB = C / SB;
 constexpr uint32_t kWaitIters = 1u << 22;   // polls before a wait gives up
@@ -60,11 +60,11 @@ constexpr uint32_t OFF_SG = 81920;      // g staging fp32 -> pair-sum buffer 2 (
 constexpr uint32_t OFF_AOP = 114688;    // pair-sum buffer 1: A MN-major 2 x 16 KiB, B MN-major 16 KiB
 constexpr uint32_t AOP_B = OFF_AOP + 32768;
 constexpr uint32_t OFF_AOP2 = OFF_SK;   // pair-sum buffer 2 (after the k and g staging are read)
-constexpr uint32_t OFF_AKK = OFF_AOP;                 // after the pair sums: A_kk fp32 [64][65]
-constexpr uint32_t OFF_TF = OFF_AOP + C * LDA * 4;    //                      T fp32 [64][65]
-constexpr uint32_t OFF_AQK = OFF_AOP + 33792;         //                      A_qk fp16 K-major [64 i][64 j]
-constexpr uint32_t OFF_TP = OFF_AOP + 41984;          //                      T' fp16 K-major [64 i][64 j]
-constexpr uint32_t OFF_XT = OFF_AOP + 50176;          // X'^T fp16 K-major [128 c][64 j] -> Delta^T [128 v][64 j]
+constexpr uint32_t OFF_AKK = OFF_AOP;                 // after the pair sums: A_kk fp32 [64][68]
+constexpr uint32_t OFF_TF = OFF_AOP + C * LDA * 4;    //                      T fp32 [64][68]
+constexpr uint32_t OFF_AQK = OFF_AOP + 34816;         //                      A_qk fp16 K-major [64 i][64 j]
+constexpr uint32_t OFF_TP = OFF_AOP + 43008;          //                      T' fp16 K-major [64 i][64 j]
+constexpr uint32_t OFF_XT = OFF_AOP + 51200;          // X'^T fp16 K-major [128 c][64 j] -> Delta^T [128 v][64 j]
 constexpr uint32_t OFF_QP = OFF_XT + 16384;           // Q' fp16 MN-major [128 c][64 i]
 constexpr uint32_t OFF_KT = OFF_QP + 16384;           // K''^T fp16 K-major [128 c][64 j]
 constexpr uint32_t OFF_RQ = OFF_KT + 16384;           // 1/|q_t|           fp32 [64]
@@ -219,25 +219,64 @@ __device__ __forceinline__ void level32_operands(unsigned char* buf, int c, int 
 
 // Pair sums of level S for the 32 TMEM lanes of this warp: lane u is upper
 // token index u of the level; r holds columns [16 hf, 16 hf + 16) of the
-// level's 32 right (lower-half) tokens.  k rows go to A_kk (times beta_i), q
-// rows to A_qk.  Writes only entries j < i.
+// level's 32 right (lower-half) tokens.  The valid columns of a lane are one
+// contiguous run of j (the lower half of its block), written with vector
+// stores: k rows to A_kk (times beta_i), q rows to A_qk.  Only entries j < i.
 template <int S>
 __device__ __forceinline__ void extract_level(unsigned char* sm, const float* r, int u, int hf,
                                               bool qrows)
 {
-    const int bi = u / S;
+    constexpr int W = S < 16 ? S : 16;                    // valid columns per lane
+    constexpr int NCASE = S < 16 ? 16 / S : 1;            // blocks per 16-column window
+    const int bi = u / S;                                 // block of this lane's token
     const int i = bi * 2 * S + S + (u % S);
-    float (*akk)[LDA] = reinterpret_cast<float (*)[LDA]>(sm + OFF_AKK);
-    const float beta_i = reinterpret_cast<const float*>(sm + OFF_BETA)[i];
+    int j0;
+    bool valid;
+    if (S == 32) { j0 = 16 * hf; valid = true; }
+    else if (S == 16) { j0 = 32 * bi; valid = (bi == hf); }
+    else { j0 = 2 * S * bi; valid = ((bi * S) >> 4) == hf; }
+    if (!valid) return;
+    float v[W];
+    const int cs = (S < 16) ? (bi & (NCASE - 1)) : 0;     // which block of the window
 #pragma unroll
-    for (int x = 0; x < 16; ++x) {
-        const int nn = 16 * hf + x;
-        if (nn / S == bi) {
-            const int j = (nn / S) * 2 * S + (nn % S);
-            if (qrows)
-                *reinterpret_cast<__half*>(sm + OFF_AQK + sw128(i, j * 2)) = __float2half_rn(r[x]);
-            else
-                akk[i][j] = beta_i * r[x];
+    for (int x = 0; x < W; ++x) {
+        float t = r[x];
+#pragma unroll
+        for (int c = 1; c < NCASE; ++c) t = (cs == c) ? r[c * S + x] : t;
+        v[x] = t;
+    }
+    if (qrows) {
+        unsigned char* dst = sm + OFF_AQK + sw128(i, j0 * 2);
+        if constexpr (W >= 8) {
+#pragma unroll
+            for (int q = 0; q < W / 8; ++q) {
+                uint4 pk;
+                pk.x = pack_h2(v[8 * q + 0], v[8 * q + 1]);
+                pk.y = pack_h2(v[8 * q + 2], v[8 * q + 3]);
+                pk.z = pack_h2(v[8 * q + 4], v[8 * q + 5]);
+                pk.w = pack_h2(v[8 * q + 6], v[8 * q + 7]);
+                *reinterpret_cast<uint4*>(sm + OFF_AQK + sw128(i, (j0 + 8 * q) * 2)) = pk;
+            }
+        } else if constexpr (W == 4) {
+            *reinterpret_cast<uint2*>(dst) = make_uint2(pack_h2(v[0], v[1]), pack_h2(v[2], v[3]));
+        } else if constexpr (W == 2) {
+            *reinterpret_cast<uint32_t*>(dst) = pack_h2(v[0], v[1]);
+        } else {
+            *reinterpret_cast<__half*>(dst) = __float2half_rn(v[0]);
+        }
+    } else {
+        const float beta_i = reinterpret_cast<const float*>(sm + OFF_BETA)[i];
+        float* dst = reinterpret_cast<float*>(sm + OFF_AKK) + i * LDA + j0;
+        if constexpr (W >= 4) {
+#pragma unroll
+            for (int q = 0; q < W / 4; ++q)
+                reinterpret_cast<float4*>(dst)[q] =
+                    make_float4(beta_i * v[4 * q], beta_i * v[4 * q + 1], beta_i * v[4 * q + 2],
+                                beta_i * v[4 * q + 3]);
+        } else if constexpr (W == 2) {
+            *reinterpret_cast<float2*>(dst) = make_float2(beta_i * v[0], beta_i * v[1]);
+        } else {
+            *dst = beta_i * v[0];
         }
     }
 }
@@ -572,65 +611,58 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(ChunkArgs args)
         __syncthreads();
         {
             // 32-row merges for blocks (1,0) and (3,2): Y = A_{I,I-1} T_{I-1,I-1}
+            // (one 2x1 micro-tile per thread; Y kept in the unused block (I-1, I))
+            {
+                const int blk = tid >> 7, I = 1 + 2 * blk, J = I - 1;
+                const int r2 = ((tid >> 4) & 7) * 2, cc = tid & 15;
+                float y0 = 0.f, y1 = 0.f;
 #pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                const int e = tid + u * NT, I = 1 + 2 * (e >> 8), J = I - 1;
-                const int r = (e >> 4) & 15, cc = e & 15;
-                float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-                for (int k = 0; k < SB; k += 2) {
-                    s0 += akk[I * SB + r][J * SB + k] * Tf[J * SB + k][J * SB + cc];
-                    s1 += akk[I * SB + r][J * SB + k + 1] * Tf[J * SB + k + 1][J * SB + cc];
+                for (int k = 0; k < SB; ++k) {
+                    const float t = Tf[J * SB + k][J * SB + cc];
+                    y0 += akk[I * SB + r2][J * SB + k] * t;
+                    y1 += akk[I * SB + r2 + 1][J * SB + k] * t;
                 }
-                Tf[J * SB + r][I * SB + cc] = s0 + s1;
+                Tf[J * SB + r2][I * SB + cc] = y0;
+                Tf[J * SB + r2 + 1][I * SB + cc] = y1;
+                __syncthreads();
+                float t0 = 0.f, t1 = 0.f;
+#pragma unroll
+                for (int k = 0; k < SB; ++k) {
+                    const float y = Tf[J * SB + k][I * SB + cc];
+                    t0 += Tf[I * SB + r2][I * SB + k] * y;
+                    t1 += Tf[I * SB + r2 + 1][I * SB + k] * y;
+                }
+                Tf[I * SB + r2][J * SB + cc] = -t0;
+                Tf[I * SB + r2 + 1][J * SB + cc] = -t1;
             }
             __syncthreads();
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                const int e = tid + u * NT, I = 1 + 2 * (e >> 8), J = I - 1;
-                const int r = (e >> 4) & 15, cc = e & 15;
-                float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-                for (int k = 0; k < SB; k += 2) {
-                    s0 += Tf[I * SB + r][I * SB + k] * Tf[J * SB + k][I * SB + cc];
-                    s1 += Tf[I * SB + r][I * SB + k + 1] * Tf[J * SB + k + 1][I * SB + cc];
+            // 64-row merge: Y = A[32:64, 0:32] T[0:32, 0:32] (kept in Tf[0:32, 32:64]),
+            // then T[32:64, 0:32] = -T[32:64, 32:64] Y; one 2x2 micro-tile per thread
+            {
+                const int r2 = (tid >> 4) * 2, c2 = (tid & 15) * 2;
+                const int k0 = c2 < SB ? 0 : SB;            // T[0:32,0:32] is zero above its blocks
+                float y00 = 0.f, y01 = 0.f, y10 = 0.f, y11 = 0.f;
+#pragma unroll 8
+                for (int k = k0; k < 32; ++k) {
+                    const float2 t = *reinterpret_cast<const float2*>(&Tf[k][c2]);
+                    const float a0 = akk[32 + r2][k], a1 = akk[32 + r2 + 1][k];
+                    y00 += a0 * t.x; y01 += a0 * t.y;
+                    y10 += a1 * t.x; y11 += a1 * t.y;
                 }
-                Tf[I * SB + r][J * SB + cc] = -(s0 + s1);
-            }
-            __syncthreads();
-            // 64-row merge: Y = A[32:64, 0:32] T[0:32, 0:32], kept in Tf[0:32, 32:64]
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int e = tid + u * NT, r = e >> 5, cc = e & 31;
-                const int k0 = cc < SB ? 0 : SB;            // T[0:32,0:32] is zero above its blocks
-                float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
-#pragma unroll
-                for (int k = 0; k < 32; k += 4) {
-                    if (k >= k0) {
-                        s0 += akk[32 + r][k] * Tf[k][cc];
-                        s1 += akk[32 + r][k + 1] * Tf[k + 1][cc];
-                        s2 += akk[32 + r][k + 2] * Tf[k + 2][cc];
-                        s3 += akk[32 + r][k + 3] * Tf[k + 3][cc];
-                    }
+                *reinterpret_cast<float2*>(&Tf[r2][32 + c2]) = make_float2(y00, y01);
+                *reinterpret_cast<float2*>(&Tf[r2 + 1][32 + c2]) = make_float2(y10, y11);
+                __syncthreads();
+                const int k1 = r2 < SB ? SB : 32;            // T[32:64,32:64] likewise
+                float t00 = 0.f, t01 = 0.f, t10 = 0.f, t11 = 0.f;
+#pragma unroll 8
+                for (int k = 0; k < k1; ++k) {
+                    const float2 y = *reinterpret_cast<const float2*>(&Tf[k][32 + c2]);
+                    const float b0 = Tf[32 + r2][32 + k], b1 = Tf[32 + r2 + 1][32 + k];
+                    t00 += b0 * y.x; t01 += b0 * y.y;
+                    t10 += b1 * y.x; t11 += b1 * y.y;
                 }
-                Tf[r][32 + cc] = (s0 + s1) + (s2 + s3);
-            }
-            __syncthreads();
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int e = tid + u * NT, r = e >> 5, cc = e & 31;
-                const int k1 = r < SB ? SB : 32;            // T[32:64,32:64] likewise
-                float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
-#pragma unroll
-                for (int k = 0; k < 32; k += 4) {
-                    if (k < k1) {
-                        s0 += Tf[32 + r][32 + k] * Tf[k][32 + cc];
-                        s1 += Tf[32 + r][32 + k + 1] * Tf[k + 1][32 + cc];
-                        s2 += Tf[32 + r][32 + k + 2] * Tf[k + 2][32 + cc];
-                        s3 += Tf[32 + r][32 + k + 3] * Tf[k + 3][32 + cc];
-                    }
-                }
-                Tf[32 + r][cc] = -((s0 + s1) + (s2 + s3));
+                *reinterpret_cast<float2*>(&Tf[32 + r2][c2]) = make_float2(-t00, -t01);
+                *reinterpret_cast<float2*>(&Tf[32 + r2 + 1][c2]) = make_float2(-t10, -t11);
             }
             __syncthreads();
         }
