@@ -397,19 +397,25 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(ChunkArgs args)
         if (kPrefetch) {
             cp_async_wait_all();
         } else {
-            uint4 xq[NQ], xk[NQ], xv[NQ], xg[8];
+            // one tensor at a time keeps the FP32 path's registers low
+            auto rows_via_regs = [&](const TIn* base, uint32_t off) {
+                uint4 x[NQ];
 #pragma unroll
-            for (int u = 0; u < NQ; ++u) {
-                const int e = tid + u * NT, r = e / P, pc = e % P;
-                if (r < L) {
-                    const int64_t off = ((int64_t)(t0 + r) * H + h) * DK;
-                    xq[u] = LD::load(gq + off, pc);
-                    xk[u] = LD::load(gk + off, pc);
-                    xv[u] = LD::load(gv + off, pc);
-                } else {
-                    xq[u] = xk[u] = xv[u] = make_uint4(0, 0, 0, 0);
+                for (int u = 0; u < NQ; ++u) {
+                    const int e = tid + u * NT, r = e / P, pc = e % P;
+                    x[u] = (r < L) ? LD::load(base + ((int64_t)(t0 + r) * H + h) * DK, pc)
+                                   : make_uint4(0, 0, 0, 0);
                 }
-            }
+#pragma unroll
+                for (int u = 0; u < NQ; ++u) {
+                    const int e = tid + u * NT, r = e / P, pc = e % P;
+                    LD::store(sm + off, r, pc, x[u]);
+                }
+            };
+            rows_via_regs(gq, OFF_SQ);
+            rows_via_regs(gk, OFF_SK);
+            rows_via_regs(gv, OFF_SV);
+            uint4 xg[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
                 const int e = tid + u * NT, r = e / 32, pc = e % 32;
@@ -418,13 +424,6 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(ChunkArgs args)
                                 : make_uint4(0, 0, 0, 0);
             }
             load_beta(t0);
-#pragma unroll
-            for (int u = 0; u < NQ; ++u) {
-                const int e = tid + u * NT, r = e / P, pc = e % P;
-                LD::store(sm + OFF_SQ, r, pc, xq[u]);
-                LD::store(sm + OFF_SK, r, pc, xk[u]);
-                LD::store(sm + OFF_SV, r, pc, xv[u]);
-            }
 #pragma unroll
             for (int u = 0; u < 8; ++u) reinterpret_cast<uint4*>(sm + OFF_SG)[tid + u * NT] = xg[u];
         }
@@ -553,6 +552,14 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(ChunkArgs args)
         level_operands<2>(sm + OFF_AOP, ch, hh, 0, 0, a, kh, qh);
         level_operands<1>(sm + OFF_AOP, ch, hh, 64, 32, a, kh, qh);
         issue_round(2, OFF_AOP);
+        if (tid == 0) {
+            // [Q' S]^T = S^T Q'^T needs only this chunk's Q' and the state entering
+            // it; its completion is covered by the next commit (W/U).
+            constexpr uint32_t idq = idesc(kFmtF16, 128, 64, false, true);
+#pragma unroll
+            for (int s = 0; s < 8; ++s)
+                mma_f16(tmem + TM_O, desc_kmajor(sb + OFF_ST, 128, s), desc_mnmajor64(sb + OFF_QP, s), idq, s > 0);
+        }
         if (!wait_round(1)) { failed = true; break; }
         if (more) { async_g(t0 + C); cp_async_commit(); load_beta(t0 + C); }
         if (!wait_round(2)) { failed = true; break; }
@@ -715,16 +722,13 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(ChunkArgs args)
         fence_before_sync();
         __syncthreads();
 
-        // ---- 8: [W S]^T = S^T W^T, [Q' S]^T = S^T Q'^T
+        // ---- 8: [W S]^T = S^T W^T
         if (tid == 0) {
             fence_after_sync();
             constexpr uint32_t id = idesc(kFmtF16, 128, 64, false, true);
 #pragma unroll
             for (int s = 0; s < 8; ++s)
                 mma_f16(tmem + TM_WS, desc_kmajor(sb + OFF_ST, 128, s), desc_mnmajor64(sb + OFF_SK, s), id, s > 0);
-#pragma unroll
-            for (int s = 0; s < 8; ++s)
-                mma_f16(tmem + TM_O, desc_kmajor(sb + OFF_ST, 128, s), desc_mnmajor64(sb + OFF_QP, s), id, s > 0);
             commit(&bar[4]);
         }
         last_bar = 4;
@@ -771,10 +775,13 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(ChunkArgs args)
             // out = scale O;  S^T <- S^T Diag(d) + P^T;  fp16 copy of S^T
             float o[32];
             tmem_ld32(tlane + TM_O + 32 * half, o);
+            const int64_t ostride = (int64_t)H * DV;
+            TOut* op = out + ((int64_t)(t0 + 32 * half) * H + h) * DV + row;
+            const int nrows = min(32, L - 32 * half);
 #pragma unroll
             for (int u = 0; u < 32; ++u) {
-                const int i = 32 * half + u;
-                if (i < L) store_out(out + ((int64_t)(t0 + i) * H + h) * DV + row, args.scale * o[u]);
+                if (u < nrows) store_out(op, args.scale * o[u]);
+                op += ostride;
             }
             float p[32];
 #pragma unroll
