@@ -43,7 +43,7 @@ _lib = None
 MUTATIONS = {
     "none": 0, "no_erase": 1, "decay_after": 2, "read_before": 3, "transposed_read": 4,
     "no_l2norm": 5, "beta_on_v_only": 6, "gate_no_alog": 7, "gate_bias_head0": 8,
-    "skip_scale": 9,
+    "skip_scale": 9, "ignore_init": 10,
 }
 
 L2_EPS = 1e-6
@@ -75,7 +75,7 @@ def _load():
             lib.kda_oracle_forward.argtypes = [
                 d, d, d, d, d, i32p, ctypes.c_int32, ctypes.c_int64, ctypes.c_int32,
                 ctypes.c_int32, ctypes.c_int32, ctypes.c_double, ctypes.c_int32,
-                ctypes.c_double, d, d, ctypes.c_int32, ctypes.c_int32]
+                ctypes.c_double, d, d, d, ctypes.c_int32, ctypes.c_int32]
             lib.kda_oracle_forward.restype = ctypes.c_int
             lib.kda_oracle_default_threads.restype = ctypes.c_int32
             _lib = lib
@@ -110,10 +110,11 @@ def gate(f, A_log, dt_bias, b, mutation: int = 0) -> Tuple[np.ndarray, np.ndarra
 
 def forward(q, k, v, g, beta, cu_seqlens, scale: float, l2norm: bool = True,
             eps: float = L2_EPS, final_state: bool = True, nthreads: int = 0,
-            mutation: int = 0) -> Tuple[np.ndarray, Optional[np.ndarray]]:
+            mutation: int = 0, initial_state=None) -> Tuple[np.ndarray, Optional[np.ndarray]]:
     """Token-by-token FP64 KDA forward.
 
-    q, k: [T,H,K]; v: [T,H,V]; g: [T,H,K]; beta: [T,H]; cu_seqlens: [N+1].
+    q, k: [T,H,K]; v: [T,H,V]; g: [T,H,K]; beta: [T,H]; cu_seqlens: [N+1];
+    initial_state: [N,H,K,V] or None (zero).
     Returns o [T,H,V] and final_state [N,H,K,V] (or None)."""
     q = _f64(q); k = _f64(k); v = _f64(v); g = _f64(g); beta = _f64(beta)
     cu = np.ascontiguousarray(np.asarray(cu_seqlens, dtype=np.int32))
@@ -124,10 +125,15 @@ def forward(q, k, v, g, beta, cu_seqlens, scale: float, l2norm: bool = True,
     assert beta.shape == (T, H)
     o = np.zeros((T, H, V), np.float64)
     S = np.zeros((N, H, K, V), np.float64) if final_state else None
+    init = None
+    if initial_state is not None:
+        init = _f64(initial_state)
+        assert init.shape == (N, H, K, V)
     rc = _load().kda_oracle_forward(
         _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
         cu.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), N, T, H, K, V, float(scale),
-        1 if l2norm else 0, float(eps), _ptr(o),
+        1 if l2norm else 0, float(eps),
+        _ptr(init) if init is not None else ctypes.POINTER(ctypes.c_double)(), _ptr(o),
         _ptr(S) if S is not None else ctypes.POINTER(ctypes.c_double)(),
         int(nthreads), int(mutation))
     if rc != 0:
@@ -136,13 +142,13 @@ def forward(q, k, v, g, beta, cu_seqlens, scale: float, l2norm: bool = True,
 
 
 def reference(q, k, v, f, A_log, dt_bias, b, cu_seqlens, scale: float,
-              nthreads: int = 0, mutation: int = 0):
+              nthreads: int = 0, mutation: int = 0, initial_state=None):
     """The whole path from raw draws: FP64 gate, then the FP64 forward.
 
     Returns (o, final_state, g, beta)."""
     g, beta = gate(f, A_log, dt_bias, b, mutation=mutation)
     o, S = forward(q, k, v, g, beta, cu_seqlens, scale, nthreads=nthreads,
-                   mutation=mutation)
+                   mutation=mutation, initial_state=initial_state)
     return o, S, g, beta
 
 

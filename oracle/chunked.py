@@ -60,8 +60,9 @@ def chunk_step(Q, Kk, Vv, g, b, S0, scale):
 
 
 def forward_chunked(q, k, v, g, beta, cu_seqlens, scale: float, C: int = 64,
-                    l2norm: bool = True, eps: float = L2_EPS):
-    """Chunked FP64 forward over packed sequences.  Shapes as the token oracle."""
+                    l2norm: bool = True, eps: float = L2_EPS, initial_state=None):
+    """Chunked FP64 forward over packed sequences.  Shapes as the token oracle;
+    initial_state [N,H,K,V] or None (zero)."""
     q = np.asarray(q, np.float64); k = np.asarray(k, np.float64)
     v = np.asarray(v, np.float64); g = np.asarray(g, np.float64)
     beta = np.asarray(beta, np.float64)
@@ -73,7 +74,8 @@ def forward_chunked(q, k, v, g, beta, cu_seqlens, scale: float, C: int = 64,
     for n in range(len(cu) - 1):
         bos, eos = cu[n], cu[n + 1]
         for h in range(H):
-            S = np.zeros((K, V))
+            S = (np.zeros((K, V)) if initial_state is None
+                 else np.array(initial_state[n, h], np.float64))
             for c0 in range(bos, eos, C):
                 c1 = min(c0 + C, eos)
                 Q = q[c0:c1, h]

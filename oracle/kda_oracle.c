@@ -16,7 +16,7 @@
  *     the HF reference forward; beta passes through a sigmoid).
  *
  *   forward, for each packed sequence n (rows cu[n] .. cu[n+1]-1) and head h,
- *   from S = 0 (a K x V matrix):
+ *   from S = initial_state[n,h] (a K x V matrix; zero when none is given):
  *          q^ = q / sqrt(sum q^2 + eps),  k^ likewise   (L2 normalisation
  *               inside the op: "Add opt-in FP32 KDA chunk computation",
  *               section Change)
@@ -53,7 +53,8 @@ enum {
     MUT_BETA_ON_V_ONLY = 6,  /* S += k (beta v - S^T k)^T                     */
     MUT_GATE_NO_ALOG = 7,    /* gate without the -exp(A_log) factor (= -softplus) */
     MUT_GATE_BIAS_HEAD0 = 8, /* gate uses dt_bias of head 0 for every head    */
-    MUT_SKIP_SCALE = 9       /* drop the output scale                         */
+    MUT_SKIP_SCALE = 9,      /* drop the output scale                         */
+    MUT_IGNORE_INIT = 10     /* start every sequence from zero despite an initial state */
 };
 
 static double softplus(double x) { return x > 30.0 ? x : log1p(exp(x)); }
@@ -80,6 +81,7 @@ void kda_oracle_gate(const double* f, const double* A_log, const double* dt_bias
 typedef struct {
     const double *q, *k, *v, *g, *beta;
     const int32_t* cu;
+    const double* init;
     int32_t N, H, K, V;
     double scale, eps;
     int32_t l2norm, mutation;
@@ -104,7 +106,10 @@ static void run_unit(job_t* J, int64_t unit, double* S, double* r, double* qn, d
     const int32_t n = (int32_t)(unit / J->H), h = (int32_t)(unit % J->H);
     const int32_t K = J->K, V = J->V, H = J->H;
     const int mut = J->mutation;
-    memset(S, 0, sizeof(double) * (size_t)K * V);
+    if (J->init && mut != MUT_IGNORE_INIT)
+        memcpy(S, J->init + unit * (int64_t)K * V, sizeof(double) * (size_t)K * V);
+    else
+        memset(S, 0, sizeof(double) * (size_t)K * V);
     for (int64_t t = J->cu[n]; t < J->cu[n + 1]; ++t) {
         const double* qt = J->q + (t * H + h) * (int64_t)K;
         const double* kt = J->k + (t * H + h) * (int64_t)K;
@@ -186,21 +191,20 @@ static void* worker(void* arg)
     return NULL;
 }
 
-/* Returns 0 on success, -1 on bad arguments.  o: [T,H,V]; final_state:
- * [N,H,K,V] or NULL.  nthreads <= 0 uses every online core.  Rows of o that
- * no sequence covers are left untouched. */
+/* Returns 0 on success, -1 on bad arguments.  o: [T,H,V]; initial_state and
+ * final_state: [N,H,K,V] or NULL.  nthreads <= 0 uses every online core. */
 int kda_oracle_forward(const double* q, const double* k, const double* v, const double* g,
                        const double* beta, const int32_t* cu_seqlens, int32_t N, int64_t T,
                        int32_t H, int32_t K, int32_t V, double scale, int32_t l2norm,
-                       double eps, double* o, double* final_state, int32_t nthreads,
-                       int32_t mutation)
+                       double eps, const double* initial_state, double* o,
+                       double* final_state, int32_t nthreads, int32_t mutation)
 {
     if (N < 0 || H <= 0 || K <= 0 || V <= 0 || T < 0) return -1;
     if (cu_seqlens[0] != 0 || cu_seqlens[N] != T) return -1;
     for (int32_t n = 0; n < N; ++n)
         if (cu_seqlens[n + 1] < cu_seqlens[n]) return -1;
     job_t J;
-    J.q = q; J.k = k; J.v = v; J.g = g; J.beta = beta; J.cu = cu_seqlens;
+    J.q = q; J.k = k; J.v = v; J.g = g; J.beta = beta; J.cu = cu_seqlens; J.init = initial_state;
     J.N = N; J.H = H; J.K = K; J.V = V; J.scale = scale; J.eps = eps;
     J.l2norm = l2norm; J.mutation = mutation; J.o = o; J.final_state = final_state;
     J.n_units = (int64_t)N * H; J.next_unit = 0;

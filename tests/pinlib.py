@@ -262,6 +262,62 @@ def pin_numpy_matrix_form(mutation=0):
     return max(oracle.rel_l2(o, o2), oracle.rel_l2(S, S2)), 1e-13
 
 
+def pin_initial_state_decay(mutation=0):
+    """beta = 0 from an initial state S0: the state only decays, so
+    o_t = scale * sum_c q^_tc e^{G_tc} S0[c, :] and S_T = Diag(e^{G_T}) S0."""
+    rng = _rng(12)
+    lens = [9, 4]
+    T, H, K, V = sum(lens), 2, 6, 5
+    q, k, v = _qkv(rng, T, H, K, V)
+    g = -rng.uniform(0.0, 1.5, (T, H, K))
+    S0 = rng.standard_normal((len(lens), H, K, V))
+    cu = _cu(lens)
+    o, S = oracle.forward(q, k, v, g, np.zeros((T, H)), cu, 0.7, mutation=mutation,
+                          initial_state=S0)
+    qn = q / np.sqrt(np.sum(q * q, -1, keepdims=True) + oracle.L2_EPS)
+    o_ref = np.zeros_like(o)
+    S_ref = np.zeros_like(S)
+    for n in range(len(lens)):
+        a, z = cu[n], cu[n + 1]
+        G = np.cumsum(g[a:z], axis=0)                                  # [t, h, c]
+        o_ref[a:z] = 0.7 * np.einsum("thc,thc,hcm->thm", qn[a:z], np.exp(G), S0[n])
+        S_ref[n] = np.exp(G[-1])[:, :, None] * S0[n]
+    return max(oracle.rel_l2(o, o_ref), oracle.rel_l2(S, S_ref)), 1e-13
+
+
+def pin_split_sequence(mutation=0):
+    """Running a sequence in two pieces, the second from the first's final state
+    (chunked WY form), equals one run of the whole (token loop)."""
+    rng = _rng(13)
+    T, H, K, V = 70, 2, 16, 16
+    cut = 29
+    q, k, v = _qkv(rng, T, H, K, V)
+    f, A_log, dt_bias, b = _gate_draws(rng, T, H, K)
+    g, beta = oracle.gate(f, A_log, dt_bias, b)
+    o, S = oracle.forward(q, k, v, g, beta, [0, T], 0.3, mutation=mutation)
+    o1, S1 = oracle.forward(q[:cut], k[:cut], v[:cut], g[:cut], beta[:cut], [0, cut], 0.3,
+                            mutation=mutation)
+    o2, S2 = chunked.forward_chunked(q[cut:], k[cut:], v[cut:], g[cut:], beta[cut:],
+                                     [0, T - cut], 0.3, C=16, initial_state=S1)
+    err = max(oracle.rel_l2(np.concatenate([o1, o2]), o), oracle.rel_l2(S2, S))
+    return err, 1e-12
+
+
+def pin_chunked_with_initial_state(mutation=0):
+    """The chunked WY form from an initial state agrees with the token loop."""
+    rng = _rng(14)
+    lens = [37, 28]
+    T, H, K, V = sum(lens), 2, 16, 16
+    q, k, v = _qkv(rng, T, H, K, V)
+    f, A_log, dt_bias, b = _gate_draws(rng, T, H, K)
+    g, beta = oracle.gate(f, A_log, dt_bias, b)
+    S0 = 0.3 * rng.standard_normal((len(lens), H, K, V))
+    cu = _cu(lens)
+    o, S = oracle.forward(q, k, v, g, beta, cu, 0.2, mutation=mutation, initial_state=S0)
+    oc, Sc = chunked.forward_chunked(q, k, v, g, beta, cu, 0.2, C=64, initial_state=S0)
+    return max(oracle.rel_l2(o, oc), oracle.rel_l2(S, Sc)), 1e-12
+
+
 PINS = {
     "scalar_exact": pin_scalar_exact,
     "beta_zero": pin_beta_zero,
@@ -275,6 +331,9 @@ PINS = {
     "scale": pin_scale,
     "gate_special_values": pin_gate_special_values,
     "numpy_matrix_form": pin_numpy_matrix_form,
+    "initial_state_decay": pin_initial_state_decay,
+    "split_sequence": pin_split_sequence,
+    "chunked_with_initial_state": pin_chunked_with_initial_state,
 }
 
 
