@@ -1,9 +1,11 @@
 #!/usr/bin/env python
 """KDA forward benchmark: tokens/s of the whole hot path on one GB300 per rank.
 
-A step is one pass of the whole path over one batch: kda_gate (decay and beta
-from their pre-activations) then kda_chunk_fwd (chunked KDA forward with the
-final state), on the 16384-token, 64-head, K=V=128 BF16 workload by default.
+A step is one pass of the whole path over one batch: the decay and beta from
+their pre-activations and the chunked KDA forward with the final state, on the
+16384-token, 64-head, K=V=128 BF16 workload by default.  The default step is
+kda_gate followed by kda_chunk_fwd; --fused times one launch of
+kda_chunk_fwd_gated (the gate fused into the chunk prologue) instead.
 Inputs are resident in HBM when the timed region starts and are larger than
 L2, so no flush is needed between steps.
 
@@ -48,6 +50,8 @@ def parse_args():
     p.add_argument("--workload", default=DEFAULT_WORKLOAD)
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--fused", action="store_true",
+                   help="time kda_chunk_fwd_gated instead of kda_gate + kda_chunk_fwd")
     return p.parse_args()
 
 
@@ -253,7 +257,7 @@ def main():
 
     import __graft_entry__
     __graft_entry__.build()
-    from kimi_delta_attention_10_gb300 import kda_chunk_fwd, kda_gate
+    from kimi_delta_attention_10_gb300 import kda_chunk_fwd, kda_chunk_fwd_gated, kda_gate
     from kimi_delta_attention_10_gb300.inputs import WORKLOAD_BY_NAME, workload_inputs
 
     mode = args.mode or "bf16_tc"
@@ -273,11 +277,17 @@ def main():
     def step(ev=None):
         if ev is not None:
             ev[0].record(stream)
-        kda_gate(d["f"], d["A_log"], d["dt_bias"], d["b"], g_out=g, beta_out=beta)
+        if (not args.fused):
+            kda_gate(d["f"], d["A_log"], d["dt_bias"], d["b"], g_out=g, beta_out=beta)
         if ev is not None:
             ev[1].record(stream)
-        kda_chunk_fwd(d["q"], d["k"], d["v"], g, beta, d["cu_seqlens"], x.scale, mode=mode,
-                      out=out, final_state=fs, cu_seqlens_host=cu_host)
+        if (not args.fused):
+            kda_chunk_fwd(d["q"], d["k"], d["v"], g, beta, d["cu_seqlens"], x.scale, mode=mode,
+                          out=out, final_state=fs, cu_seqlens_host=cu_host)
+        else:
+            kda_chunk_fwd_gated(d["q"], d["k"], d["v"], d["f"], d["A_log"], d["dt_bias"],
+                                d["b"], d["cu_seqlens"], x.scale, mode=mode, out=out,
+                                final_state=fs, cu_seqlens_host=cu_host)
         if ev is not None:
             ev[2].record(stream)
 
@@ -349,14 +359,16 @@ def main():
         avg_chunk_s = statistics.mean(chunk_ms) * 1e-3
         peak, peak_src = measured_peaks()
         achieved = alg / avg_chunk_s / 1e9
-        kernel_key = f"kda_chunk_fwd:{mode}:{w.name}"
+        kname = "kda_chunk_fwd" if (not args.fused) else "kda_chunk_fwd_gated"
+        kernel_key = f"{kname}:{mode}:{w.name}"
         roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "traffic": kernel_traffic(kernel_key),
-                "kernel": f"kda_chunk_fwd ({mode})", "peak_source": f"{peak_src} hbm_gbs",
+                "kernel": f"{kname} ({mode})", "peak_source": f"{peak_src} hbm_gbs",
                 "algorithmic_bytes_per_launch": alg,
                 "avg_launch_ms": avg_chunk_s * 1e3}
         cfg = workload_config(w, mode)
         cfg["T"], cfg["N"] = T, N
+        cfg["step"] = "kda_gate + kda_chunk_fwd" if (not args.fused) else "kda_chunk_fwd_gated"
         value = whole_job_rate(world, T, args.steps, ms)
         chunk_tps = T / avg_chunk_s
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
@@ -364,16 +376,17 @@ def main():
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": "f32" if mode == "fp32_exact" else "bf16", "data": "synthetic",
                 "config": cfg, "roofline": roof,
-                "kernels": {"kda_gate_ms": statistics.mean(gate_ms),
-                            "kda_chunk_fwd_ms": statistics.mean(chunk_ms),
-                            "kda_chunk_fwd_p50_ms": statistics.median(chunk_ms),
-                            "kda_chunk_fwd_max_ms": max(chunk_ms),
-                            "kda_gate_GBps": gate_bytes(T, H, K) / statistics.mean(gate_ms) / 1e6,
-                            "chunk_only_tokens_per_s": chunk_tps,
-                            "context_h200_chunk_only_ratio": chunk_tps / (
+                "kernels": {f"{kname}_ms": statistics.mean(chunk_ms),
+                            f"{kname}_p50_ms": statistics.median(chunk_ms),
+                            f"{kname}_max_ms": max(chunk_ms),
+                            "chunk_tokens_per_s": chunk_tps,
+                            "context_h200_chunk_fwd_ratio": chunk_tps / (
                                 16384 / (H200_CHUNK_US_16384 * 1e-6))},
-                "gpu_launches": 2 * args.steps,
+                "gpu_launches": (2 if (not args.fused) else 1) * args.steps,
                 "clocks": clk, "e2e": e2e}
+        if (not args.fused):
+            line["kernels"]["kda_gate_ms"] = statistics.mean(gate_ms)
+            line["kernels"]["kda_gate_GBps"] = gate_bytes(T, H, K) / statistics.mean(gate_ms) / 1e6
         if world == 1 and not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(x, w)
         print(json.dumps(line), flush=True)

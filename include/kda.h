@@ -116,8 +116,12 @@ kda_status kda_gate(const void* f, int32_t f_dtype, const float* A_log, const fl
  *              computation", section Change); 0: used as given.
  *   mode       kda_mode.
  *   out        [T, H, V]  out_dtype (F32 or BF16), written for every covered row.
+ *   initial_state [N, H, K, V] F32, or NULL (every sequence starts from zero):
+ *              the state each sequence starts from (the pages' wrapper lacks
+ *              one: "Add opt-in FP32 KDA chunk computation", section Change).
  *   final_state [N, H, K, V] F32, or NULL: the state after each sequence's
- *              last token (zero for an empty sequence).
+ *              last token (the initial state for an empty sequence).
+ *              final_state may alias initial_state.
  *   status_dev one device int32 or NULL; the kernel writes a kda_status there
  *              only on a device-detected error (the caller zeroes it).
  */
@@ -126,13 +130,58 @@ kda_status kda_chunk_fwd(const void* q, const void* k, const void* v, int32_t qk
                          const int32_t* cu_seqlens, const int32_t* cu_seqlens_host,
                          int32_t N, int64_t T, int32_t H, int32_t K, int32_t V,
                          float scale, int32_t qk_l2norm, int32_t mode,
-                         void* out, int32_t out_dtype, float* final_state,
-                         int32_t* status_dev, kda_stream_t stream);
+                         void* out, int32_t out_dtype, const float* initial_state,
+                         float* final_state, int32_t* status_dev, kda_stream_t stream);
+
+/*
+ * kda_chunk_fwd_gated -- kda_chunk_fwd with the gate fused into its prologue.
+ *
+ * Takes the gate's inputs instead of g and beta and forms, per element,
+ *   g = -exp(A_log[h]) * softplus(f + dt_bias[h,c]),  beta = sigmoid(b)
+ * exactly as kda_gate does (same FP32 arithmetic, so the result equals
+ * kda_gate followed by kda_chunk_fwd bit for bit), without writing g or beta
+ * to memory.  The pages compute the gate outside the chunk kernel ("GLM-5.3-
+ * Flash F6.2: KDA correctness and FLA sequence parallelism", fused-gate
+ * commit); fusing it here removes that launch and its round trip of g.
+ *
+ *   f       [T, H, K]  F32 (KDA_ERR_UNSUPPORTED otherwise)
+ *   A_log   [H] F32, dt_bias [H, K] F32
+ *   b       [T, H]     F32 or BF16 (b_dtype)
+ * Every other argument as kda_chunk_fwd.
+ */
+kda_status kda_chunk_fwd_gated(const void* q, const void* k, const void* v, int32_t qkv_dtype,
+                               const void* f, int32_t f_dtype, const float* A_log,
+                               const float* dt_bias, const void* b, int32_t b_dtype,
+                               const int32_t* cu_seqlens, const int32_t* cu_seqlens_host,
+                               int32_t N, int64_t T, int32_t H, int32_t K, int32_t V,
+                               float scale, int32_t qk_l2norm, int32_t mode,
+                               void* out, int32_t out_dtype, const float* initial_state,
+                               float* final_state, int32_t* status_dev, kda_stream_t stream);
+
+/*
+ * kda_recurrent_step -- one token of the recurrence for each of N sequences
+ * (the decode step: the pages' serving path runs the FP32 recurrence token by
+ * token, "Add opt-in FP32 KDA chunk computation", section Problem).
+ *
+ *   q, k  [N, H, K], v [N, H, V]  qkv_dtype (F32 or BF16): token n of sequence n
+ *   g     [N, H, K] F32 log-decay (<= 0), beta [N, H] F32
+ *   state [N, H, K, V] F32, read and overwritten in place:
+ *           S <- (I - beta k^ k^^T) Diag(e^g) S + beta k^ v^T
+ *   out   [N, H, V] out_dtype: scale * S^T q^ with the updated S
+ * IEEE FP32 arithmetic; q and k are L2-normalised when qk_l2norm = 1.
+ * K = V = 128 (else KDA_ERR_UNSUPPORTED).  N = 0 launches nothing.
+ */
+kda_status kda_recurrent_step(const void* q, const void* k, const void* v, int32_t qkv_dtype,
+                              const float* g, const float* beta, int32_t N, int32_t H,
+                              int32_t K, int32_t V, float scale, int32_t qk_l2norm,
+                              float* state, void* out, int32_t out_dtype,
+                              kda_stream_t stream);
 
 /* Static text for a kda_status value ("unknown status" otherwise). */
 const char* kda_status_string(int32_t status);
 
-/* ABI revision of this header; bumped on any incompatible change. */
+/* ABI revision of this header; bumped on any incompatible change (2: initial
+ * state argument of kda_chunk_fwd; kda_chunk_fwd_gated; kda_recurrent_step). */
 int32_t kda_abi_version(void);
 
 #ifdef __cplusplus

@@ -32,7 +32,8 @@ KDA_MODE_FP32_EXACT = 1
 MODES = {"bf16_tc": KDA_MODE_BF16_TC, "fp32_exact": KDA_MODE_FP32_EXACT}
 
 # Every symbol include/kda.h declares.
-EXPORTS = ("kda_gate", "kda_chunk_fwd", "kda_status_string", "kda_abi_version")
+EXPORTS = ("kda_gate", "kda_chunk_fwd", "kda_chunk_fwd_gated", "kda_recurrent_step",
+           "kda_status_string", "kda_abi_version")
 
 _lock = threading.Lock()
 _lib = None
@@ -65,8 +66,15 @@ def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.kda_gate.argtypes = [vp, i32, vp, vp, vp, i32, i64, i32, i32, vp, vp, vp]
         lib.kda_gate.restype = i32
         lib.kda_chunk_fwd.argtypes = [vp, vp, vp, i32, vp, vp, vp, vp, i32, i64, i32, i32, i32,
-                                      ctypes.c_float, i32, i32, vp, i32, vp, vp, vp]
+                                      ctypes.c_float, i32, i32, vp, i32, vp, vp, vp, vp]
         lib.kda_chunk_fwd.restype = i32
+        lib.kda_chunk_fwd_gated.argtypes = [vp, vp, vp, i32, vp, i32, vp, vp, vp, i32, vp, vp,
+                                            i32, i64, i32, i32, i32, ctypes.c_float, i32, i32,
+                                            vp, i32, vp, vp, vp, vp]
+        lib.kda_chunk_fwd_gated.restype = i32
+        lib.kda_recurrent_step.argtypes = [vp, vp, vp, i32, vp, vp, i32, i32, i32, i32,
+                                           ctypes.c_float, i32, vp, vp, i32, vp]
+        lib.kda_recurrent_step.restype = i32
         lib.kda_status_string.argtypes = [i32]
         lib.kda_status_string.restype = ctypes.c_char_p
         lib.kda_abi_version.argtypes = []
@@ -121,11 +129,30 @@ def kda_gate(f: torch.Tensor, A_log: torch.Tensor, dt_bias: torch.Tensor, b: tor
     return g_out, beta_out
 
 
+def _chunk_outputs(q, v, cu_seqlens, out, out_dtype, output_final_state, final_state):
+    T, H, K = q.shape
+    V = v.shape[2]
+    N = cu_seqlens.numel() - 1
+    if out is None:
+        out = torch.empty((T, H, V), dtype=out_dtype or v.dtype, device=q.device)
+    if final_state is None and output_final_state:
+        final_state = torch.empty((N, H, K, V), dtype=torch.float32, device=q.device)
+    return out, final_state
+
+
+def _host_offsets(cu_seqlens_host):
+    if cu_seqlens_host is None:
+        return None, None
+    arr = (ctypes.c_int32 * len(cu_seqlens_host))(*[int(x) for x in cu_seqlens_host])
+    return arr, ctypes.cast(arr, ctypes.c_void_p)
+
+
 def kda_chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor,
                   beta: torch.Tensor, cu_seqlens: torch.Tensor, scale: Optional[float] = None,
                   mode: str = "bf16_tc", out: Optional[torch.Tensor] = None,
                   out_dtype: Optional[torch.dtype] = None, output_final_state: bool = True,
                   final_state: Optional[torch.Tensor] = None,
+                  initial_state: Optional[torch.Tensor] = None,
                   cu_seqlens_host: Optional[Sequence[int]] = None, qk_l2norm: bool = True,
                   status: Optional[torch.Tensor] = None,
                   stream: Optional[torch.cuda.Stream] = None):
@@ -136,20 +163,72 @@ def kda_chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Te
     N = cu_seqlens.numel() - 1
     if scale is None:
         scale = K ** -0.5
-    if out is None:
-        out = torch.empty((T, H, V), dtype=out_dtype or v.dtype, device=q.device)
-    if final_state is None and output_final_state:
-        final_state = torch.empty((N, H, K, V), dtype=torch.float32, device=q.device)
-    host_arr = None
-    if cu_seqlens_host is not None:
-        host_arr = (ctypes.c_int32 * len(cu_seqlens_host))(*[int(x) for x in cu_seqlens_host])
+    out, final_state = _chunk_outputs(q, v, cu_seqlens, out, out_dtype, output_final_state,
+                                      final_state)
+    keep, host = _host_offsets(cu_seqlens_host)
     st = lib.kda_chunk_fwd(
         _dev_ptr(q, "q"), _dev_ptr(k, "k"), _dev_ptr(v, "v"), _dtype_code(q),
-        _dev_ptr(g, "g"), _dev_ptr(beta, "beta"), _dev_ptr(cu_seqlens, "cu_seqlens"),
-        ctypes.cast(host_arr, ctypes.c_void_p) if host_arr is not None else None,
+        _dev_ptr(g, "g"), _dev_ptr(beta, "beta"), _dev_ptr(cu_seqlens, "cu_seqlens"), host,
         N, T, H, K, V, float(scale), 1 if qk_l2norm else 0, MODES[mode],
-        _dev_ptr(out, "out"), _dtype_code(out), _dev_ptr(final_state, "final_state"),
-        _dev_ptr(status, "status"), _stream_handle(stream, q.device))
+        _dev_ptr(out, "out"), _dtype_code(out), _dev_ptr(initial_state, "initial_state"),
+        _dev_ptr(final_state, "final_state"), _dev_ptr(status, "status"),
+        _stream_handle(stream, q.device))
     if st != KDA_OK:
         raise KDAError(st, "kda_chunk_fwd")
     return out, final_state
+
+
+def kda_chunk_fwd_gated(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, f: torch.Tensor,
+                        A_log: torch.Tensor, dt_bias: torch.Tensor, b: torch.Tensor,
+                        cu_seqlens: torch.Tensor, scale: Optional[float] = None,
+                        mode: str = "bf16_tc", out: Optional[torch.Tensor] = None,
+                        out_dtype: Optional[torch.dtype] = None, output_final_state: bool = True,
+                        final_state: Optional[torch.Tensor] = None,
+                        initial_state: Optional[torch.Tensor] = None,
+                        cu_seqlens_host: Optional[Sequence[int]] = None, qk_l2norm: bool = True,
+                        status: Optional[torch.Tensor] = None,
+                        stream: Optional[torch.cuda.Stream] = None):
+    """Chunked KDA forward with the gate (g, beta from f, A_log, dt_bias, b) fused in."""
+    lib = load_library()
+    T, H, K = q.shape
+    V = v.shape[2]
+    N = cu_seqlens.numel() - 1
+    if scale is None:
+        scale = K ** -0.5
+    out, final_state = _chunk_outputs(q, v, cu_seqlens, out, out_dtype, output_final_state,
+                                      final_state)
+    keep, host = _host_offsets(cu_seqlens_host)
+    st = lib.kda_chunk_fwd_gated(
+        _dev_ptr(q, "q"), _dev_ptr(k, "k"), _dev_ptr(v, "v"), _dtype_code(q),
+        _dev_ptr(f, "f"), _dtype_code(f), _dev_ptr(A_log, "A_log"), _dev_ptr(dt_bias, "dt_bias"),
+        _dev_ptr(b, "b"), _dtype_code(b), _dev_ptr(cu_seqlens, "cu_seqlens"), host,
+        N, T, H, K, V, float(scale), 1 if qk_l2norm else 0, MODES[mode],
+        _dev_ptr(out, "out"), _dtype_code(out), _dev_ptr(initial_state, "initial_state"),
+        _dev_ptr(final_state, "final_state"), _dev_ptr(status, "status"),
+        _stream_handle(stream, q.device))
+    if st != KDA_OK:
+        raise KDAError(st, "kda_chunk_fwd_gated")
+    return out, final_state
+
+
+def kda_recurrent_step(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor,
+                       beta: torch.Tensor, state: torch.Tensor, scale: Optional[float] = None,
+                       out: Optional[torch.Tensor] = None, out_dtype: Optional[torch.dtype] = None,
+                       qk_l2norm: bool = True, stream: Optional[torch.cuda.Stream] = None):
+    """One decode token per sequence: q, k [N,H,K], v [N,H,V], g [N,H,K], beta [N,H];
+    state [N,H,K,V] FP32 is updated in place.  Returns out [N,H,V]."""
+    lib = load_library()
+    N, H, K = q.shape
+    V = v.shape[2]
+    if scale is None:
+        scale = K ** -0.5
+    if out is None:
+        out = torch.empty((N, H, V), dtype=out_dtype or v.dtype, device=q.device)
+    st = lib.kda_recurrent_step(
+        _dev_ptr(q, "q"), _dev_ptr(k, "k"), _dev_ptr(v, "v"), _dtype_code(q),
+        _dev_ptr(g, "g"), _dev_ptr(beta, "beta"), N, H, K, V, float(scale),
+        1 if qk_l2norm else 0, _dev_ptr(state, "state"), _dev_ptr(out, "out"),
+        _dtype_code(out), _stream_handle(stream, q.device))
+    if st != KDA_OK:
+        raise KDAError(st, "kda_recurrent_step")
+    return out

@@ -27,7 +27,7 @@ int device_sm_count()
 
 extern "C" {
 
-int32_t kda_abi_version(void) { return 1; }
+int32_t kda_abi_version(void) { return 2; }
 
 const char* kda_status_string(int32_t s)
 {
@@ -61,13 +61,16 @@ kda_status kda_gate(const void* f, int32_t f_dtype, const float* A_log, const fl
     return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
-kda_status kda_chunk_fwd(const void* q, const void* k, const void* v, int32_t qkv_dtype,
-                         const float* g, const float* beta,
-                         const int32_t* cu_seqlens, const int32_t* cu_seqlens_host,
-                         int32_t N, int64_t T, int32_t H, int32_t K, int32_t V,
-                         float scale, int32_t qk_l2norm, int32_t mode,
-                         void* out, int32_t out_dtype, float* final_state,
-                         int32_t* status_dev, kda_stream_t stream)
+namespace {
+
+// Shared validation of the chunk entry points (everything but g/beta vs the
+// gate inputs).  Returns KDA_OK when a launch may proceed.
+kda_status check_chunk(const void* q, const void* k, const void* v, int32_t qkv_dtype,
+                       const int32_t* cu_seqlens, const int32_t* cu_seqlens_host, int32_t N,
+                       int64_t T, int32_t H, int32_t K, int32_t V, int32_t qk_l2norm,
+                       int32_t mode, const void* out, int32_t out_dtype,
+                       const float* initial_state, const float* final_state,
+                       const int32_t* status_dev)
 {
     if (N < 0 || T < 0 || H < 1 || K < 1 || V < 1) return KDA_ERR_INVALID_ARG;
     if (T > INT32_MAX) return KDA_ERR_UNSUPPORTED;
@@ -76,8 +79,8 @@ kda_status kda_chunk_fwd(const void* q, const void* k, const void* v, int32_t qk
     if (qk_l2norm != 0 && qk_l2norm != 1) return KDA_ERR_INVALID_ARG;
     if (K != kda::kHeadK || V != kda::kHeadV) return KDA_ERR_UNSUPPORTED;
     if (!cu_seqlens) return KDA_ERR_INVALID_ARG;
-    if (T > 0 && (!q || !k || !v || !g || !beta || !out)) return KDA_ERR_INVALID_ARG;
-    const void* ptrs[] = {q, k, v, g, beta, cu_seqlens, out, final_state, status_dev};
+    if (T > 0 && (!q || !k || !v || !out)) return KDA_ERR_INVALID_ARG;
+    const void* ptrs[] = {q, k, v, cu_seqlens, out, initial_state, final_state, status_dev};
     for (const void* p : ptrs)
         if (p && !aligned16(p)) return KDA_ERR_ALIGNMENT;
     if (cu_seqlens_host) {
@@ -86,16 +89,105 @@ kda_status kda_chunk_fwd(const void* q, const void* k, const void* v, int32_t qk
         for (int32_t n = 0; n < N; ++n)
             if (cu_seqlens_host[n + 1] < cu_seqlens_host[n]) return KDA_ERR_INVALID_ARG;
     }
-    if (N == 0) return KDA_OK;
+    return KDA_OK;
+}
 
-    kda::ChunkArgs a;
-    a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.cu_seqlens = cu_seqlens;
-    a.N = N; a.T = T; a.H = H; a.scale = scale; a.l2norm = qk_l2norm;
-    a.out = out; a.final_state = final_state; a.status = status_dev;
-    a.qkv_bf16 = qkv_dtype == KDA_BF16; a.out_bf16 = out_dtype == KDA_BF16;
+kda_status launch_chunk(const kda::ChunkArgs& a, int32_t mode, kda_stream_t stream)
+{
+    if (a.N == 0) return KDA_OK;
     cudaError_t e = (mode == KDA_MODE_BF16_TC)
                         ? kda::launch_chunk_tc(a, reinterpret_cast<cudaStream_t>(stream))
                         : kda::launch_chunk_fp32(a, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+kda::ChunkArgs chunk_args(const void* q, const void* k, const void* v, int32_t qkv_dtype,
+                          const int32_t* cu_seqlens, int32_t N, int64_t T, int32_t H,
+                          float scale, int32_t qk_l2norm, void* out, int32_t out_dtype,
+                          const float* initial_state, float* final_state, int32_t* status_dev)
+{
+    kda::ChunkArgs a = {};
+    a.q = q; a.k = k; a.v = v; a.cu_seqlens = cu_seqlens;
+    a.N = N; a.T = T; a.H = H; a.scale = scale; a.l2norm = qk_l2norm;
+    a.out = out; a.final_state = final_state; a.status = status_dev;
+    a.qkv_bf16 = qkv_dtype == KDA_BF16; a.out_bf16 = out_dtype == KDA_BF16;
+    a.initial_state = initial_state;
+    return a;
+}
+
+}  // namespace
+
+kda_status kda_chunk_fwd(const void* q, const void* k, const void* v, int32_t qkv_dtype,
+                         const float* g, const float* beta,
+                         const int32_t* cu_seqlens, const int32_t* cu_seqlens_host,
+                         int32_t N, int64_t T, int32_t H, int32_t K, int32_t V,
+                         float scale, int32_t qk_l2norm, int32_t mode,
+                         void* out, int32_t out_dtype, const float* initial_state,
+                         float* final_state, int32_t* status_dev, kda_stream_t stream)
+{
+    kda_status st = check_chunk(q, k, v, qkv_dtype, cu_seqlens, cu_seqlens_host, N, T, H, K, V,
+                                qk_l2norm, mode, out, out_dtype, initial_state, final_state,
+                                status_dev);
+    if (st != KDA_OK) return st;
+    if (T > 0 && (!g || !beta)) return KDA_ERR_INVALID_ARG;
+    if ((g && !aligned16(g)) || (beta && !aligned16(beta))) return KDA_ERR_ALIGNMENT;
+    kda::ChunkArgs a = chunk_args(q, k, v, qkv_dtype, cu_seqlens, N, T, H, scale, qk_l2norm, out,
+                                  out_dtype, initial_state, final_state, status_dev);
+    a.g = g; a.beta = beta; a.gated = false;
+    return launch_chunk(a, mode, stream);
+}
+
+kda_status kda_chunk_fwd_gated(const void* q, const void* k, const void* v, int32_t qkv_dtype,
+                               const void* f, int32_t f_dtype, const float* A_log,
+                               const float* dt_bias, const void* b, int32_t b_dtype,
+                               const int32_t* cu_seqlens, const int32_t* cu_seqlens_host,
+                               int32_t N, int64_t T, int32_t H, int32_t K, int32_t V,
+                               float scale, int32_t qk_l2norm, int32_t mode,
+                               void* out, int32_t out_dtype, const float* initial_state,
+                               float* final_state, int32_t* status_dev, kda_stream_t stream)
+{
+    kda_status st = check_chunk(q, k, v, qkv_dtype, cu_seqlens, cu_seqlens_host, N, T, H, K, V,
+                                qk_l2norm, mode, out, out_dtype, initial_state, final_state,
+                                status_dev);
+    if (st != KDA_OK) return st;
+    if (!valid_dtype(f_dtype) || !valid_dtype(b_dtype)) return KDA_ERR_INVALID_ARG;
+    if (f_dtype != KDA_F32) return KDA_ERR_UNSUPPORTED;
+    if (!A_log || !dt_bias) return KDA_ERR_INVALID_ARG;
+    if (T > 0 && (!f || !b)) return KDA_ERR_INVALID_ARG;
+    const void* ptrs[] = {f, A_log, dt_bias, b};
+    for (const void* p : ptrs)
+        if (p && !aligned16(p)) return KDA_ERR_ALIGNMENT;
+    kda::ChunkArgs a = chunk_args(q, k, v, qkv_dtype, cu_seqlens, N, T, H, scale, qk_l2norm, out,
+                                  out_dtype, initial_state, final_state, status_dev);
+    a.gated = true;
+    a.f = static_cast<const float*>(f);
+    a.A_log = A_log;
+    a.dt_bias = dt_bias;
+    a.b = b;
+    a.b_bf16 = b_dtype == KDA_BF16;
+    return launch_chunk(a, mode, stream);
+}
+
+kda_status kda_recurrent_step(const void* q, const void* k, const void* v, int32_t qkv_dtype,
+                              const float* g, const float* beta, int32_t N, int32_t H,
+                              int32_t K, int32_t V, float scale, int32_t qk_l2norm,
+                              float* state, void* out, int32_t out_dtype,
+                              kda_stream_t stream)
+{
+    if (N < 0 || H < 1 || K < 1 || V < 1) return KDA_ERR_INVALID_ARG;
+    if (!valid_dtype(qkv_dtype) || !valid_dtype(out_dtype)) return KDA_ERR_INVALID_ARG;
+    if (qk_l2norm != 0 && qk_l2norm != 1) return KDA_ERR_INVALID_ARG;
+    if (K != kda::kHeadK || V != kda::kHeadV) return KDA_ERR_UNSUPPORTED;
+    if (N == 0) return KDA_OK;
+    if (!q || !k || !v || !g || !beta || !state || !out) return KDA_ERR_INVALID_ARG;
+    const void* ptrs[] = {q, k, v, g, beta, state, out};
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return KDA_ERR_ALIGNMENT;
+    kda::StepArgs a = {};
+    a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.N = N; a.H = H; a.scale = scale;
+    a.l2norm = qk_l2norm; a.state = state; a.out = out;
+    a.qkv_bf16 = qkv_dtype == KDA_BF16; a.out_bf16 = out_dtype == KDA_BF16;
+    cudaError_t e = kda::launch_recurrent_step(a, reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 

@@ -71,7 +71,7 @@ __device__ __forceinline__ float warp_sum(float x)
 __device__ __forceinline__ void store_out(float* p, float x) { *p = x; }
 __device__ __forceinline__ void store_out(__nv_bfloat16* p, float x) { *p = __float2bfloat16_rn(x); }
 
-template <typename TIn, typename TOut>
+template <typename TIn, typename TOut, bool kGated>
 __global__ void __launch_bounds__(NT, 1) chunk_fp32_kernel(ChunkArgs args)
 {
     extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -96,7 +96,15 @@ __global__ void __launch_bounds__(NT, 1) chunk_fp32_kernel(ChunkArgs args)
     const float* __restrict__ g = args.g;
     TOut* __restrict__ out = static_cast<TOut*>(args.out);
 
-    for (int i = tid; i < DK * BV; i += NT) sm.s[i / BV][i % BV] = 0.f;
+    if (args.initial_state != nullptr) {
+        const float* s0 = args.initial_state + ((int64_t)n * H + h) * DK * kHeadV;
+        for (int i = tid; i < DK * BV; i += NT)
+            sm.s[i / BV][i % BV] = s0[(int64_t)(i / BV) * kHeadV + v0 + i % BV];
+    } else {
+        for (int i = tid; i < DK * BV; i += NT) sm.s[i / BV][i % BV] = 0.f;
+    }
+    const float* __restrict__ graw = kGated ? args.f : g;
+    const float lamneg = kGated ? -expf(args.A_log[h]) : 0.f;
 
     for (int t0 = bos; t0 < eos; t0 += C) {
         const int L = min(C, eos - t0);
@@ -110,7 +118,8 @@ __global__ void __launch_bounds__(NT, 1) chunk_fp32_kernel(ChunkArgs args)
                 const int64_t off = ((int64_t)(t0 + r) * H + h) * DK + c;
                 qv = load_as_float(q + off);
                 kv = load_as_float(k + off);
-                av = expf(g[off]);
+                av = expf(kGated ? gate_decay(graw[off], args.dt_bias[(int64_t)h * DK + c], lamneg)
+                                 : graw[off]);
             }
             sm.q[r][c] = qv;
             sm.k[r][c] = kv;
@@ -122,7 +131,19 @@ __global__ void __launch_bounds__(NT, 1) chunk_fp32_kernel(ChunkArgs args)
             if (r < L) vv = load_as_float(v + ((int64_t)(t0 + r) * H + h) * kHeadV + v0 + m);
             sm.v[r][m] = vv;
         }
-        if (tid < C) sm.beta[tid] = tid < L ? args.beta[(int64_t)(t0 + tid) * H + h] : 0.f;
+        if (tid < C) {
+            float bt = 0.f;
+            if (tid < L) {
+                const int64_t i = (int64_t)(t0 + tid) * H + h;
+                if (kGated)
+                    bt = gate_sigmoid(args.b_bf16
+                                          ? __bfloat162float(static_cast<const __nv_bfloat16*>(args.b)[i])
+                                          : static_cast<const float*>(args.b)[i]);
+                else
+                    bt = args.beta[i];
+            }
+            sm.beta[tid] = bt;
+        }
         __syncthreads();
 
         // ---- 2. L2 normalisation of q and k rows (one warp per row)
@@ -294,28 +315,34 @@ __global__ void __launch_bounds__(NT, 1) chunk_fp32_kernel(ChunkArgs args)
     }
 }
 
-template <typename TIn, typename TOut>
+template <typename TIn, typename TOut, bool kGated>
 cudaError_t launch_typed(const ChunkArgs& a, cudaStream_t stream)
 {
     const size_t smem = sizeof(Smem);
-    cudaError_t e = cudaFuncSetAttribute(chunk_fp32_kernel<TIn, TOut>,
+    cudaError_t e = cudaFuncSetAttribute(chunk_fp32_kernel<TIn, TOut, kGated>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const int64_t units = (int64_t)a.N * a.H * NVS;
     if (units > INT32_MAX) return cudaErrorInvalidConfiguration;
-    chunk_fp32_kernel<TIn, TOut><<<(unsigned)units, NT, smem, stream>>>(a);
+    chunk_fp32_kernel<TIn, TOut, kGated><<<(unsigned)units, NT, smem, stream>>>(a);
     return cudaGetLastError();
+}
+
+template <bool kGated>
+cudaError_t launch_gated(const ChunkArgs& a, cudaStream_t stream)
+{
+    if (a.qkv_bf16)
+        return a.out_bf16 ? launch_typed<__nv_bfloat16, __nv_bfloat16, kGated>(a, stream)
+                          : launch_typed<__nv_bfloat16, float, kGated>(a, stream);
+    return a.out_bf16 ? launch_typed<float, __nv_bfloat16, kGated>(a, stream)
+                      : launch_typed<float, float, kGated>(a, stream);
 }
 
 }  // namespace
 
 cudaError_t launch_chunk_fp32(const ChunkArgs& a, cudaStream_t stream)
 {
-    if (a.qkv_bf16)
-        return a.out_bf16 ? launch_typed<__nv_bfloat16, __nv_bfloat16>(a, stream)
-                          : launch_typed<__nv_bfloat16, float>(a, stream);
-    return a.out_bf16 ? launch_typed<float, __nv_bfloat16>(a, stream)
-                      : launch_typed<float, float>(a, stream);
+    return a.gated ? launch_gated<true>(a, stream) : launch_gated<false>(a, stream);
 }
 
 }  // namespace kda

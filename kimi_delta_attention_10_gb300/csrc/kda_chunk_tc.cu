@@ -281,7 +281,7 @@ __device__ __forceinline__ void extract_level(unsigned char* sm, const float* r,
     }
 }
 
-template <typename TIn, typename TOut>
+template <typename TIn, typename TOut, bool kGated>
 __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(ChunkArgs args)
 {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -329,9 +329,33 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(ChunkArgs args)
     // 16-bit inputs: the next chunk's loads are issued while this chunk computes.
     constexpr bool kPrefetch = sizeof(TIn) == 2;
 
-    // ---- setup: zero S^T, TMEM allocation, barriers
-    for (int e = tid; e < 32768 / 16; e += NT)
-        reinterpret_cast<uint4*>(sm + OFF_ST)[e] = make_uint4(0, 0, 0, 0);
+    // fused gate: g and beta formed from f, A_log, dt_bias and b (as kda_gate does)
+    const float* __restrict__ graw = kGated ? args.f : args.g;
+    float lamneg = 0.f, dtb = 0.f;
+    if (kGated) {
+        lamneg = -expf(args.A_log[h]);
+        dtb = args.dt_bias[(int64_t)h * DK + ch];
+    }
+
+    // ---- setup: the entering state (zero, or the caller's), TMEM, barriers
+    float S[64];                                           // S^T[row][64 half + c]
+    if (args.initial_state != nullptr) {
+        const float* s0 = args.initial_state + ((int64_t)n * H + h) * DK * DV;
+#pragma unroll
+        for (int u = 0; u < 64; ++u) S[u] = s0[(int64_t)(64 * half + u) * DV + row];
+    } else {
+#pragma unroll
+        for (int u = 0; u < 64; ++u) S[u] = 0.f;
+    }
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        uint4 pk;
+        pk.x = pack_h2(S[8 * q + 0], S[8 * q + 1]);
+        pk.y = pack_h2(S[8 * q + 2], S[8 * q + 3]);
+        pk.z = pack_h2(S[8 * q + 4], S[8 * q + 5]);
+        pk.w = pack_h2(S[8 * q + 6], S[8 * q + 7]);
+        *reinterpret_cast<uint4*>(sm + OFF_ST + sw128_tile(128, row, (64 * half + 8 * q) * 2)) = pk;
+    }
     if (warp == 0) {
         tmem_alloc(tslot, TM_COLS);
         tmem_relinquish();
@@ -347,9 +371,6 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(ChunkArgs args)
     const uint32_t tmem = *tslot;
     const uint32_t tlane = tmem + ((uint32_t)(32 * quad) << 16);
 
-    float S[64];                                           // S^T[row][64 half + c]
-#pragma unroll
-    for (int c = 0; c < 64; ++c) S[c] = 0.f;
     bool failed = false;
     int last_bar = -1;
     uint32_t phase = 0;                                    // every barrier completes once per chunk
@@ -373,13 +394,22 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(ChunkArgs args)
         for (int u = 0; u < C * 32 / NT; ++u) {
             const int e = tid + u * NT, r = e >> 5, pc = e & 31;
             const bool ok = r < Lc;
-            const float* src = args.g + ((int64_t)(tc + (ok ? r : 0)) * H + h) * DK + pc * 4;
+            const float* src = graw + ((int64_t)(tc + (ok ? r : 0)) * H + h) * DK + pc * 4;
             cp_async16(sm + OFF_SG + e * 16, src, ok);
         }
     };
     float xb = 0.f;                                        // beta of this thread's row (tid < 64)
     auto load_beta = [&](int tc) {
-        xb = (tid < min(C, eos - tc)) ? args.beta[(int64_t)(tc + tid) * H + h] : 0.f;
+        xb = 0.f;
+        if (tid < min(C, eos - tc)) {
+            const int64_t i = (int64_t)(tc + tid) * H + h;
+            if (kGated)
+                xb = gate_sigmoid(args.b_bf16
+                                      ? __bfloat162float(static_cast<const __nv_bfloat16*>(args.b)[i])
+                                      : static_cast<const float*>(args.b)[i]);
+            else
+                xb = args.beta[i];
+        }
     };
     if (kPrefetch && bos < eos) {
         async_rows16(OFF_SQ, gq, bos);
@@ -420,7 +450,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(ChunkArgs args)
             for (int u = 0; u < 8; ++u) {
                 const int e = tid + u * NT, r = e / 32, pc = e % 32;
                 xg[u] = (r < L) ? __ldg(reinterpret_cast<const uint4*>(
-                                      args.g + ((int64_t)(t0 + r) * H + h) * DK) + pc)
+                                      graw + ((int64_t)(t0 + r) * H + h) * DK) + pc)
                                 : make_uint4(0, 0, 0, 0);
             }
             load_beta(t0);
@@ -474,7 +504,9 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(ChunkArgs args)
 #pragma unroll
             for (int u = 0; u < 32; ++u) {
                 const int t = 32 * hh + u;
-                a[u] = expf(sg[t * DK + ch]);
+                const float gv = sg[t * DK + ch];
+                // rows past the sequence end hold 0: decay 1 in both forms
+                a[u] = expf(kGated ? (t < L ? gate_decay(gv, dtb, lamneg) : 0.f) : gv);
                 kh[u] = ST::to_f32(sk[t * DK + ch]) * rk[t];
                 qh[u] = ST::to_f32(sq[t * DK + ch]) * rq[t];
             }
@@ -822,28 +854,34 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(ChunkArgs args)
     if (warp == 0) tmem_dealloc(tmem, TM_COLS);
 }
 
-template <typename TIn, typename TOut>
+template <typename TIn, typename TOut, bool kGated>
 cudaError_t launch_typed(const ChunkArgs& a, cudaStream_t stream)
 {
-    cudaError_t e = cudaFuncSetAttribute(chunk_tc_kernel<TIn, TOut>,
+    cudaError_t e = cudaFuncSetAttribute(chunk_tc_kernel<TIn, TOut, kGated>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;
     const int64_t units = (int64_t)a.N * a.H;
     if (units > INT32_MAX) return cudaErrorInvalidConfiguration;
-    chunk_tc_kernel<TIn, TOut><<<(unsigned)units, NT, SMEM_BYTES, stream>>>(a);
+    chunk_tc_kernel<TIn, TOut, kGated><<<(unsigned)units, NT, SMEM_BYTES, stream>>>(a);
     return cudaGetLastError();
+}
+
+template <bool kGated>
+cudaError_t launch_gated(const ChunkArgs& a, cudaStream_t stream)
+{
+    if (a.qkv_bf16)
+        return a.out_bf16 ? launch_typed<__nv_bfloat16, __nv_bfloat16, kGated>(a, stream)
+                          : launch_typed<__nv_bfloat16, float, kGated>(a, stream);
+    return a.out_bf16 ? launch_typed<float, __nv_bfloat16, kGated>(a, stream)
+                      : launch_typed<float, float, kGated>(a, stream);
 }
 
 }  // namespace
 
 cudaError_t launch_chunk_tc(const ChunkArgs& a, cudaStream_t stream)
 {
-    if (a.qkv_bf16)
-        return a.out_bf16 ? launch_typed<__nv_bfloat16, __nv_bfloat16>(a, stream)
-                          : launch_typed<__nv_bfloat16, float>(a, stream);
-    return a.out_bf16 ? launch_typed<float, __nv_bfloat16>(a, stream)
-                      : launch_typed<float, float>(a, stream);
+    return a.gated ? launch_gated<true>(a, stream) : launch_gated<false>(a, stream);
 }
 
 }  // namespace kda

@@ -17,12 +17,6 @@
 namespace kda {
 namespace {
 
-__device__ __forceinline__ float softplus_f32(float x)
-{
-    // log(1 + e^x); above 20 the correction e^-x is below FP32 resolution.
-    return x > 20.f ? x : log1pf(expf(x));
-}
-
 __device__ __forceinline__ float4 load4(const float* p, int64_t i)
 {
     return __ldcs(reinterpret_cast<const float4*>(p + i));
@@ -59,16 +53,16 @@ __global__ void __launch_bounds__(256) gate_kernel(const TF* __restrict__ f,
         const float4 x = load4(f, i4 * 4);
         const float4 db = __ldg(reinterpret_cast<const float4*>(dt_bias + (int64_t)h * K + c));
         float4 r;
-        r.x = lam * softplus_f32(x.x + db.x);
-        r.y = lam * softplus_f32(x.y + db.y);
-        r.z = lam * softplus_f32(x.z + db.z);
-        r.w = lam * softplus_f32(x.w + db.w);
+        r.x = gate_decay(x.x, db.x, lam);
+        r.y = gate_decay(x.y, db.y, lam);
+        r.z = gate_decay(x.z, db.z, lam);
+        r.w = gate_decay(x.w, db.w, lam);
         __stcs(reinterpret_cast<float4*>(g_out + i4 * 4), r);
     }
     const int64_t nb = T * H;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nb; i += stride) {
         const float x = load_as_float(b + i);
-        beta_out[i] = 1.f / (1.f + expf(-x));
+        beta_out[i] = gate_sigmoid(x);
     }
 }
 

@@ -30,6 +30,31 @@ struct ChunkArgs {
     int32_t* status;
     bool qkv_bf16;
     bool out_bf16;
+    const float* initial_state;   // [N,H,K,V] or nullptr
+    // Gate fused into the prologue (kda_chunk_fwd_gated): g and beta are then
+    // formed from f, A_log, dt_bias and b, and the g/beta pointers are unused.
+    bool gated;
+    const float* f;
+    const float* A_log;
+    const float* dt_bias;
+    const void* b;
+    bool b_bf16;
+};
+
+struct StepArgs {
+    const void* q;
+    const void* k;
+    const void* v;
+    const float* g;
+    const float* beta;
+    int32_t N;
+    int32_t H;
+    float scale;
+    int32_t l2norm;
+    float* state;
+    void* out;
+    bool qkv_bf16;
+    bool out_bf16;
 };
 
 // Each launcher returns cudaSuccess or the launch error.
@@ -39,6 +64,7 @@ cudaError_t launch_gate(const void* f, bool f_bf16, const float* A_log, const fl
 
 cudaError_t launch_chunk_fp32(const ChunkArgs& a, cudaStream_t stream);
 cudaError_t launch_chunk_tc(const ChunkArgs& a, cudaStream_t stream);
+cudaError_t launch_recurrent_step(const StepArgs& a, cudaStream_t stream);
 
 int device_sm_count();
 
@@ -46,6 +72,21 @@ int device_sm_count();
 __device__ __forceinline__ void report_status(int32_t* status, int32_t code)
 {
     if (status != nullptr) atomicCAS(status, 0, code);
+}
+
+// The gate's FP32 arithmetic, shared by kda_gate and the fused prologues so
+// that both give identical values: g = lamneg * softplus(x), lamneg = -exp(A_log).
+__device__ __forceinline__ float gate_softplus(float x)
+{
+    // log(1 + e^x); above 20 the correction e^-x is below FP32 resolution.
+    return x > 20.f ? x : log1pf(expf(x));
+}
+__device__ __forceinline__ float gate_sigmoid(float x) { return 1.f / (1.f + expf(-x)); }
+// g from its pre-activation f, dt_bias and lamneg = -exp(A_log[h]); the explicit
+// roundings keep the product from being contracted into a later expf.
+__device__ __forceinline__ float gate_decay(float f, float dt_bias, float lamneg)
+{
+    return __fmul_rn(lamneg, gate_softplus(__fadd_rn(f, dt_bias)));
 }
 
 __device__ __forceinline__ float load_as_float(const float* p) { return *p; }

@@ -35,7 +35,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.kda_abi_version() == 1
+    assert lib.kda_abi_version() == 2
     assert binding.status_string(0) == "ok"
     for s in range(1, 7):
         assert binding.status_string(s) not in ("ok", "unknown status")
@@ -49,14 +49,16 @@ MIS = 0x10004
 
 def chunk(lib, **kw):
     a = dict(q=P, k=P, v=P, qkv=1, g=P, beta=P, cu=P, cu_host=None, N=1, T=10, H=2, K=128,
-             V=128, scale=0.1, l2=1, mode=1, out=P, out_dt=1, fs=None, status=None, stream=None)
+             V=128, scale=0.1, l2=1, mode=1, out=P, out_dt=1, s0=None, fs=None, status=None,
+             stream=None)
     a.update(kw)
     host = a["cu_host"]
     if host is not None:
         host = ctypes.cast((ctypes.c_int32 * len(host))(*host), ctypes.c_void_p)
     return lib.kda_chunk_fwd(a["q"], a["k"], a["v"], a["qkv"], a["g"], a["beta"], a["cu"], host,
                              a["N"], a["T"], a["H"], a["K"], a["V"], a["scale"], a["l2"],
-                             a["mode"], a["out"], a["out_dt"], a["fs"], a["status"], a["stream"])
+                             a["mode"], a["out"], a["out_dt"], a["s0"], a["fs"], a["status"],
+                             a["stream"])
 
 
 @pytest.mark.parametrize("kw,expect", [
@@ -76,6 +78,7 @@ def chunk(lib, **kw):
     (dict(q=MIS), binding.KDA_ERR_ALIGNMENT),
     (dict(g=MIS), binding.KDA_ERR_ALIGNMENT),
     (dict(fs=MIS), binding.KDA_ERR_ALIGNMENT),
+    (dict(s0=MIS), binding.KDA_ERR_ALIGNMENT),
     (dict(status=MIS), binding.KDA_ERR_ALIGNMENT),
     (dict(cu_host=[0, 9]), binding.KDA_ERR_INVALID_ARG),           # last != T
     (dict(cu_host=[1, 10]), binding.KDA_ERR_INVALID_ARG),          # first != 0
@@ -115,3 +118,47 @@ def test_binding_refuses_cpu_tensors(lib):
     x = torch.zeros(4, 2, 128)
     with pytest.raises(RuntimeError, match="CUDA tensor"):
         binding.kda_gate(x, torch.zeros(2), torch.zeros(2, 128), torch.zeros(4, 2))
+
+
+def gated(lib, **kw):
+    a = dict(q=P, k=P, v=P, qkv=1, f=P, fdt=0, A=P, dt=P, b=P, bdt=0, cu=P, N=1, T=10, H=2,
+             K=128, V=128, mode=0, out=P, out_dt=1, s0=None, fs=None)
+    a.update(kw)
+    return lib.kda_chunk_fwd_gated(a["q"], a["k"], a["v"], a["qkv"], a["f"], a["fdt"], a["A"],
+                                   a["dt"], a["b"], a["bdt"], a["cu"], None, a["N"], a["T"],
+                                   a["H"], a["K"], a["V"], 0.1, 1, a["mode"], a["out"],
+                                   a["out_dt"], a["s0"], a["fs"], None, None)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(fdt=1), binding.KDA_ERR_UNSUPPORTED),        # BF16 f is not supported
+    (dict(fdt=4), binding.KDA_ERR_INVALID_ARG),
+    (dict(bdt=4), binding.KDA_ERR_INVALID_ARG),
+    (dict(A=None), binding.KDA_ERR_INVALID_ARG),
+    (dict(f=None), binding.KDA_ERR_INVALID_ARG),
+    (dict(b=MIS), binding.KDA_ERR_ALIGNMENT),
+    (dict(K=64), binding.KDA_ERR_UNSUPPORTED),
+    (dict(mode=3), binding.KDA_ERR_INVALID_ARG),
+])
+def test_chunk_fwd_gated_rejects_bad_arguments(lib, kw, expect):
+    assert gated(lib, **kw) == expect
+
+
+def step(lib, **kw):
+    a = dict(q=P, k=P, v=P, qkv=1, g=P, beta=P, N=4, H=2, K=128, V=128, state=P, out=P, out_dt=1)
+    a.update(kw)
+    return lib.kda_recurrent_step(a["q"], a["k"], a["v"], a["qkv"], a["g"], a["beta"], a["N"],
+                                  a["H"], a["K"], a["V"], 0.1, 1, a["state"], a["out"],
+                                  a["out_dt"], None)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(N=-1), binding.KDA_ERR_INVALID_ARG),
+    (dict(N=0, q=None), binding.KDA_OK),               # nothing to do
+    (dict(V=64), binding.KDA_ERR_UNSUPPORTED),
+    (dict(state=None), binding.KDA_ERR_INVALID_ARG),
+    (dict(state=MIS), binding.KDA_ERR_ALIGNMENT),
+    (dict(qkv=9), binding.KDA_ERR_INVALID_ARG),
+])
+def test_recurrent_step_rejects_bad_arguments(lib, kw, expect):
+    assert step(lib, **kw) == expect
