@@ -10,10 +10,12 @@
 // the log-decay g and a_t = e^{g_t}:
 //   A_kk[i][j] = beta_i sum_c k^_ic k^_jc e^{G_ic - G_jc}   (j < i)
 //   A_qk[i][j] =        sum_c q^_ic k^_jc e^{G_ic - G_jc}   (j <= i)
-//   T' = (I + A_kk)^-1 diag(beta)
-//   W = T' (K^ o e^G),  U = T' V
-//   Delta = U - W S,  O = scale [(Q^ o e^G) S + A_qk Delta]
+//   T' = (I + A_kk)^-1 diag(beta),  X' = K^ o e^G
+//   Delta = T' (V - X' S)          (= U - W S with W = T' X', U = T' V)
+//   O = scale [(Q^ o e^G) S + A_qk Delta]
 //   S <- Diag(e^{G_last}) S + (K^ o e^{G_last - G})^T Delta
+// X' S needs only the state entering the chunk, so its MMA runs beside the
+// pair sums; once T' is known a single MMA gives Delta.
 //
 // Pair sums on tensor cores without overflow.  e^{G_i - G_j} is never formed
 // as e^{G_i} e^{-G_j} (in-chunk decays reach e^{-1000}).  The 64 tokens are
@@ -53,9 +55,9 @@ constexpr uint32_t kWaitIters = 1u << 22;   // polls before a wait gives up
 
 // Shared memory map (bytes from a 1024-aligned base).
 constexpr uint32_t OFF_ST = 0;          // S^T fp16 K-major [128 v][128 c]            32 KiB
-constexpr uint32_t OFF_SQ = 32768;      // q staging [64][128] 16-bit -> V^T fp16 K-major [128 v][64 j]
+constexpr uint32_t OFF_SQ = 32768;      // q staging [64][128] 16-bit -> V^T -> Y^T = (V - X'S)^T fp16 K-major [128 v][64 j]
 constexpr uint32_t OFF_SV = 49152;      // v staging [64][128] 16-bit
-constexpr uint32_t OFF_SK = 65536;      // k staging -> pair-sum buffer 2 (A part 0) -> W fp16 MN-major
+constexpr uint32_t OFF_SK = 65536;      // k staging -> pair-sum buffer 2 (A part 0)
 constexpr uint32_t OFF_SG = 81920;      // g staging fp32 -> pair-sum buffer 2 (A part 1, B)
 constexpr uint32_t OFF_AOP = 114688;    // pair-sum buffer 1: A MN-major 2 x 16 KiB, B MN-major 16 KiB
 constexpr uint32_t AOP_B = OFF_AOP + 32768;
@@ -64,7 +66,7 @@ constexpr uint32_t OFF_AKK = OFF_AOP;                 // after the pair sums: A_
 constexpr uint32_t OFF_TF = OFF_AOP + C * LDA * 4;    //                      T fp32 [64][68]
 constexpr uint32_t OFF_AQK = OFF_AOP + 34816;         //                      A_qk fp16 K-major [64 i][64 j]
 constexpr uint32_t OFF_TP = OFF_AOP + 43008;          //                      T' fp16 K-major [64 i][64 j]
-constexpr uint32_t OFF_XT = OFF_AOP + 51200;          // X'^T fp16 K-major [128 c][64 j] -> Delta^T [128 v][64 j]
+constexpr uint32_t OFF_XT = OFF_AOP + 51200;          // X'^T fp16 [128 c][64 j] -> Delta^T K-major [128 v][64 j]
 constexpr uint32_t OFF_QP = OFF_XT + 16384;           // Q' fp16 MN-major [128 c][64 i]
 constexpr uint32_t OFF_KT = OFF_QP + 16384;           // K''^T fp16 K-major [128 c][64 j]
 constexpr uint32_t OFF_RQ = OFF_KT + 16384;           // 1/|q_t|           fp32 [64]
@@ -73,7 +75,7 @@ constexpr uint32_t OFF_DQK = OFF_RK + 256;            // q^_t . k^_t       fp32 
 constexpr uint32_t OFF_BETA = OFF_DQK + 256;          // beta              fp32 [64]
 constexpr uint32_t OFF_DEC = OFF_BETA + 256;          // e^{G_last}        fp32 [128]
 constexpr uint32_t OFF_TOT = OFF_DEC + 512;           // half-chunk decay  fp32 [2][128]
-constexpr uint32_t OFF_BAR = OFF_TOT + 1024;          // 6 mbarriers + TMEM slot
+constexpr uint32_t OFF_BAR = OFF_TOT + 1024;          // 5 mbarriers + TMEM slot
 constexpr uint32_t SMEM_USED = OFF_BAR + 64;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;     // + alignment slack
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
@@ -84,7 +86,7 @@ static_assert(OFF_AQK % 1024 == 0 && OFF_TP % 1024 == 0 && OFF_XT % 1024 == 0 &&
               "SW128 tiles need 1024-B alignment");
 
 // TMEM columns.
-constexpr uint32_t TM_WS = 0, TM_O = 64, TM_P = 128, TM_A = 256, TM_W = 256, TM_U = 320;
+constexpr uint32_t TM_XS = 0, TM_O = 64, TM_P = 128, TM_A = 256;   // TM_XS: [X'S]^T, then Delta^T
 constexpr uint32_t TM_COLS = 512;
 
 // Staging keeps 16-bit activations: BF16 inputs as they are, FP32 inputs
@@ -302,7 +304,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(ChunkArgs args)
     float* sbeta = reinterpret_cast<float*>(sm + OFF_BETA);
     float* dec = reinterpret_cast<float*>(sm + OFF_DEC);
     float* tot = reinterpret_cast<float*>(sm + OFF_TOT);
-    // [0..2] pair-sum rounds, [3] W/U, [4] state products, [5] output/state update
+    // [0..2] pair-sum rounds, [3] Delta, [4] output/state update
     uint64_t* bar = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
     uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + OFF_BAR + 56);
 
@@ -361,7 +363,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(ChunkArgs args)
         tmem_relinquish();
     }
     if (tid == 0) {
-        for (int b = 0; b < 6; ++b) mbar_init(&bar[b], 1);
+        for (int b = 0; b < 5; ++b) mbar_init(&bar[b], 1);
         fence_mbar_init();
     }
     fence_async_smem();
@@ -568,6 +570,17 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(ChunkArgs args)
         level32_operands(sm + OFF_AOP, ch, hh, a, kh, qh);
         level_operands<16>(sm + OFF_AOP, ch, hh, 64, 32, a, kh, qh);
         issue_round(0, OFF_AOP);
+        if (tid == 0) {
+            // [X'S]^T = S^T X'^T and [Q'S]^T = S^T Q'^T need only this chunk's X', Q'
+            // and the entering state; the next commit covers them.
+            constexpr uint32_t ids = idesc(kFmtF16, 128, 64, false, true);
+#pragma unroll
+            for (int s = 0; s < 8; ++s)
+                mma_f16(tmem + TM_XS, desc_kmajor(sb + OFF_ST, 128, s), desc_mnmajor64(sb + OFF_XT, s), ids, s > 0);
+#pragma unroll
+            for (int s = 0; s < 8; ++s)
+                mma_f16(tmem + TM_O, desc_kmajor(sb + OFF_ST, 128, s), desc_mnmajor64(sb + OFF_QP, s), ids, s > 0);
+        }
         {
             // V^T fp16 K-major [v][j] into the q staging (q is no longer read)
             float vv[32];
@@ -584,16 +597,13 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(ChunkArgs args)
         level_operands<2>(sm + OFF_AOP, ch, hh, 0, 0, a, kh, qh);
         level_operands<1>(sm + OFF_AOP, ch, hh, 64, 32, a, kh, qh);
         issue_round(2, OFF_AOP);
-        if (tid == 0) {
-            // [Q' S]^T = S^T Q'^T needs only this chunk's Q' and the state entering
-            // it; its completion is covered by the next commit (W/U).
-            constexpr uint32_t idq = idesc(kFmtF16, 128, 64, false, true);
-#pragma unroll
-            for (int s = 0; s < 8; ++s)
-                mma_f16(tmem + TM_O, desc_kmajor(sb + OFF_ST, 128, s), desc_mnmajor64(sb + OFF_QP, s), idq, s > 0);
-        }
         if (!wait_round(1)) { failed = true; break; }
-        if (more) { async_g(t0 + C); cp_async_commit(); load_beta(t0 + C); }
+        if (more) {                   // k and g staging (pair-sum buffer 2) are free now
+            async_g(t0 + C);
+            async_rows16(OFF_SK, gk, t0 + C);
+            cp_async_commit();
+            load_beta(t0 + C);
+        }
         if (!wait_round(2)) { failed = true; break; }
         fence_after_sync();
 
@@ -629,6 +639,26 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(ChunkArgs args)
             if (tid < C)
                 *reinterpret_cast<__half*>(sm + OFF_AQK + sw128(tid, tid * 2)) = __float2half_rn(dqk[tid]);
         }
+        {
+            // Y^T[v][j] = V^T[v][j] - [X'S]^T[v][j], in place over the V^T tile
+            float xs[32], y[32];
+            tmem_ld32(tlane + TM_XS + 32 * half, xs);
+            unsigned char* rowp = sm + OFF_SQ;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const uint4 pk = *reinterpret_cast<const uint4*>(rowp + sw128(row, (32 * half + 8 * q) * 2));
+                const uint32_t w4[4] = {pk.x, pk.y, pk.z, pk.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 vf = __half22float2(*reinterpret_cast<const __half2*>(&w4[e]));
+                    y[8 * q + 2 * e] = vf.x - xs[8 * q + 2 * e];
+                    y[8 * q + 2 * e + 1] = vf.y - xs[8 * q + 2 * e + 1];
+                }
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) st8(rowp, 0, row, 32 * half + 8 * q, y + 8 * q);
+        }
+        fence_async_smem();
         fence_before_sync();
         __syncthreads();
 
@@ -724,16 +754,13 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(ChunkArgs args)
         fence_before_sync();
         __syncthreads();
 
-        // ---- 7: W^T = X'^T T'^T, U^T = V^T T'^T
+        // ---- 7: Delta^T = Y^T T'^T
         if (tid == 0) {
             fence_after_sync();
             constexpr uint32_t id = idesc(kFmtF16, 128, 64);
 #pragma unroll
             for (int s = 0; s < 4; ++s)
-                mma_f16(tmem + TM_W, desc_kmajor(sb + OFF_XT, 128, s), desc_kmajor(sb + OFF_TP, 64, s), id, s > 0);
-#pragma unroll
-            for (int s = 0; s < 4; ++s)
-                mma_f16(tmem + TM_U, desc_kmajor(sb + OFF_SQ, 128, s), desc_kmajor(sb + OFF_TP, 64, s), id, s > 0);
+                mma_f16(tmem + TM_XS, desc_kmajor(sb + OFF_SQ, 128, s), desc_kmajor(sb + OFF_TP, 64, s), id, s > 0);
             commit(&bar[3]);
         }
         last_bar = 3;
@@ -744,41 +771,11 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(ChunkArgs args)
         if (more) { async_rows16(OFF_SQ, gq, t0 + C); cp_async_commit(); }
         fence_after_sync();
         {
-            // W fp16 MN-major [c][i] into the k staging (row c = TMEM lane)
-            float w[32];
-            tmem_ld32(tlane + TM_W + 32 * half, w);
+            // Delta^T fp16 K-major [v][i] into the X'^T tile (last read by the X'S MMA)
+            float dl[32];
+            tmem_ld32(tlane + TM_XS + 32 * half, dl);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) st8(sm + OFF_SK, 0, row, 32 * half + 8 * q, w + 8 * q);
-        }
-        fence_async_smem();
-        fence_before_sync();
-        __syncthreads();
-
-        // ---- 8: [W S]^T = S^T W^T
-        if (tid == 0) {
-            fence_after_sync();
-            constexpr uint32_t id = idesc(kFmtF16, 128, 64, false, true);
-#pragma unroll
-            for (int s = 0; s < 8; ++s)
-                mma_f16(tmem + TM_WS, desc_kmajor(sb + OFF_ST, 128, s), desc_mnmajor64(sb + OFF_SK, s), id, s > 0);
-            commit(&bar[4]);
-        }
-        last_bar = 4;
-        {
-            const bool ok = mbar_wait(&bar[4], phase, kWaitIters);
-            if (__syncthreads_or(!ok)) { failed = true; break; }
-        }
-        if (more) { async_rows16(OFF_SK, gk, t0 + C); cp_async_commit(); }
-        fence_after_sync();
-        {
-            // Delta^T[v][i] = U^T[v][i] - [W S]^T[v][i], fp16 K-major [v][i]
-            float ws[32], uu[32];
-            tmem_ld32(tlane + TM_U + 32 * half, uu);
-            tmem_ld32(tlane + TM_WS + 32 * half, ws);
-#pragma unroll
-            for (int x = 0; x < 32; ++x) uu[x] -= ws[x];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) st8(sm + OFF_XT, 0, row, 32 * half + 8 * q, uu + 8 * q);
+            for (int q = 0; q < 4; ++q) st8(sm + OFF_XT, 0, row, 32 * half + 8 * q, dl + 8 * q);
         }
         fence_async_smem();
         fence_before_sync();
@@ -795,11 +792,11 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(ChunkArgs args)
 #pragma unroll
             for (int s = 0; s < 4; ++s)
                 mma_f16(tmem + TM_P, desc_kmajor(sb + OFF_XT, 128, s), desc_kmajor(sb + OFF_KT, 128, s), idp, s > 0);
-            commit(&bar[5]);
+            commit(&bar[4]);
         }
-        last_bar = 5;
+        last_bar = 4;
         {
-            const bool ok = mbar_wait(&bar[5], phase, kWaitIters);
+            const bool ok = mbar_wait(&bar[4], phase, kWaitIters);
             if (__syncthreads_or(!ok)) { failed = true; break; }
         }
         fence_after_sync();
@@ -842,7 +839,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(ChunkArgs args)
     if (failed) {
         if (tid == 0) report_status(args.status, KDA_ERR_TIMEOUT);
         // let the MMAs still in flight finish before the TMEM is released
-        for (int b = 0; b <= 5; ++b)
+        for (int b = 0; b <= 4; ++b)
             if (b <= last_bar) mbar_wait(&bar[b], phase, kWaitIters);
     } else if (args.final_state != nullptr) {
         float* fs = args.final_state + ((int64_t)n * H + h) * DK * DV;
