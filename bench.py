@@ -4,8 +4,11 @@
 A step is one pass of the whole path over one batch: the decay and beta from
 their pre-activations and the chunked KDA forward with the final state, on the
 16384-token, 64-head, K=V=128 BF16 workload by default.  The default step is
-kda_gate followed by kda_chunk_fwd; --fused times one launch of
-kda_chunk_fwd_gated (the gate fused into the chunk prologue) instead.
+kda_gate followed by kda_chunk_fwd; --fused times one call of
+kda_chunk_fwd_gated (the gate fused into the chunk preparation) instead.  The
+BF16 tensor-core path runs in two phases through a preallocated workspace
+(plan, chunk preparation, state scan: three launches per chunk call);
+--single-pass times the single-pass kernel (no workspace) instead.
 Inputs are resident in HBM when the timed region starts and are larger than
 L2, so no flush is needed between steps.
 
@@ -52,6 +55,8 @@ def parse_args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--fused", action="store_true",
                    help="time kda_chunk_fwd_gated instead of kda_gate + kda_chunk_fwd")
+    p.add_argument("--single-pass", action="store_true",
+                   help="BF16 tensor-core path without a workspace (one kernel per call)")
     return p.parse_args()
 
 
@@ -66,8 +71,8 @@ def measured_peaks():
 
 
 def kernel_traffic(kernel_key: str):
-    """DRAM bytes per launch from a committed ncu summary, if it still matches
-    the kernel source; None otherwise."""
+    """DRAM bytes per chunk call (summed over its launches) from a committed ncu
+    summary, if it still matches the kernel sources; None otherwise."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as fh:
@@ -77,12 +82,13 @@ def kernel_traffic(kernel_key: str):
     ent = d.get(kernel_key)
     if not ent:
         return None
-    src = os.path.join(ROOT, ent["source"])
+    h = hashlib.sha256()
     try:
-        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        for src in ent["sources"]:
+            h.update(open(os.path.join(ROOT, src), "rb").read())
     except Exception:
         return None
-    return ent["dram_bytes_per_launch"] if sha == ent["source_sha256_16"] else None
+    return ent["dram_bytes_per_call"] if h.hexdigest()[:16] == ent["sources_sha256_16"] else None
 
 
 class ClockSampler:
@@ -257,10 +263,12 @@ def main():
 
     import __graft_entry__
     __graft_entry__.build()
-    from kimi_delta_attention_10_gb300 import kda_chunk_fwd, kda_chunk_fwd_gated, kda_gate
+    from kimi_delta_attention_10_gb300 import (chunk_workspace_size, kda_chunk_fwd,
+                                               kda_chunk_fwd_gated, kda_gate)
     from kimi_delta_attention_10_gb300.inputs import WORKLOAD_BY_NAME, workload_inputs
 
     mode = args.mode or "bf16_tc"
+    two_phase = mode == "bf16_tc" and not args.single_pass
     w = WORKLOAD_BY_NAME[args.workload]
     x = workload_inputs(w)
     T, H, K, V, N = x.T, w.H, w.K, w.V, x.N
@@ -272,6 +280,8 @@ def main():
     beta = torch.empty(T, H, device=dev)
     out = torch.empty(T, H, V, dtype=out_dtype, device=dev)
     fs = torch.empty(N, H, K, V, device=dev)
+    ws = (torch.empty(chunk_workspace_size(N, T, H, K, V), dtype=torch.uint8, device=dev)
+          if two_phase else None)
     stream = torch.cuda.current_stream(dev)
 
     def step(ev=None):
@@ -283,11 +293,11 @@ def main():
             ev[1].record(stream)
         if (not args.fused):
             kda_chunk_fwd(d["q"], d["k"], d["v"], g, beta, d["cu_seqlens"], x.scale, mode=mode,
-                          out=out, final_state=fs, cu_seqlens_host=cu_host)
+                          out=out, final_state=fs, cu_seqlens_host=cu_host, workspace=ws)
         else:
             kda_chunk_fwd_gated(d["q"], d["k"], d["v"], d["f"], d["A_log"], d["dt_bias"],
                                 d["b"], d["cu_seqlens"], x.scale, mode=mode, out=out,
-                                final_state=fs, cu_seqlens_host=cu_host)
+                                final_state=fs, cu_seqlens_host=cu_host, workspace=ws)
         if ev is not None:
             ev[2].record(stream)
 
@@ -360,15 +370,19 @@ def main():
         peak, peak_src = measured_peaks()
         achieved = alg / avg_chunk_s / 1e9
         kname = "kda_chunk_fwd" if (not args.fused) else "kda_chunk_fwd_gated"
-        kernel_key = f"{kname}:{mode}:{w.name}"
+        variant = "two_phase" if two_phase else ("single_pass" if mode == "bf16_tc" else mode)
+        kernel_key = f"{kname}:{variant}:{w.name}"
+        what = {"two_phase": "two-phase call: plan + chunk preparation + state scan",
+                "single_pass": "single-pass kernel"}.get(variant, "FP32-exact kernel")
         roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "traffic": kernel_traffic(kernel_key),
-                "kernel": f"{kname} ({mode})", "peak_source": f"{peak_src} hbm_gbs",
+                "kernel": f"{kname} ({mode}, {what})", "peak_source": f"{peak_src} hbm_gbs",
                 "algorithmic_bytes_per_launch": alg,
                 "avg_launch_ms": avg_chunk_s * 1e3}
         cfg = workload_config(w, mode)
         cfg["T"], cfg["N"] = T, N
         cfg["step"] = "kda_gate + kda_chunk_fwd" if (not args.fused) else "kda_chunk_fwd_gated"
+        cfg["chunk_path"] = variant
         value = whole_job_rate(world, T, args.steps, ms)
         chunk_tps = T / avg_chunk_s
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
@@ -382,7 +396,7 @@ def main():
                             "chunk_tokens_per_s": chunk_tps,
                             "context_h200_chunk_fwd_ratio": chunk_tps / (
                                 16384 / (H200_CHUNK_US_16384 * 1e-6))},
-                "gpu_launches": (2 if (not args.fused) else 1) * args.steps,
+                "gpu_launches": ((0 if args.fused else 1) + (3 if two_phase else 1)) * args.steps,
                 "clocks": clk, "e2e": e2e}
         if (not args.fused):
             line["kernels"]["kda_gate_ms"] = statistics.mean(gate_ms)

@@ -55,8 +55,10 @@ typedef enum {
 typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype;
 
 typedef enum {
-    /* BF16 tensor-core operands with FP32 accumulation; output rel-L2 error
-     * against the FP64 recurrence is held below 3e-3. */
+    /* 16-bit tensor-core operands (FP16: v, and q and k when qk_l2norm = 0,
+     * must lie within its range, |x| < 65504) with FP32 accumulation and an
+     * FP32 state; output rel-L2 error against the FP64 recurrence is held
+     * below 3e-3. */
     KDA_MODE_BF16_TC = 0,
     /* FP32 arithmetic throughout (IEEE FP32, no TF32), output rel-L2 error
      * below 1e-5 with F32 output.  This is the counterpart of the pages'
@@ -87,6 +89,26 @@ typedef enum {
 kda_status kda_gate(const void* f, int32_t f_dtype, const float* A_log, const float* dt_bias,
                     const void* b, int32_t b_dtype, int64_t T, int32_t H, int32_t K,
                     float* g_out, float* beta_out, kda_stream_t stream);
+
+/*
+ * kda_chunk_workspace_size -- bytes of device workspace that kda_chunk_fwd and
+ * kda_chunk_fwd_gated use for a problem of N sequences, T tokens and H heads.
+ *
+ * With a workspace, KDA_MODE_BF16_TC runs in two phases: every (chunk, head)
+ * is first prepared in parallel over the whole GPU (the chunk solve's
+ * state-independent part: pair sums, (I + A_kk)^-1, W, U and the decay
+ * factors) into the workspace, then one pass per (sequence, head) carries the
+ * state through the chunks ("Add opt-in FP32 KDA chunk computation", section
+ * Problem: the chunk solve and the carried state).  Without one it runs a
+ * single pass per (sequence, head) that does all of a chunk's work in order.
+ * KDA_MODE_FP32_EXACT uses no workspace (*bytes_host = 0).
+ *
+ * The size is a bound that holds for every cu_seqlens with these N and T:
+ * a 1 KiB-aligned header of N + 5 int32, plus (T / 64 + N) * H records of
+ * 74240 bytes.  Arguments as kda_chunk_fwd; *bytes_host is host memory.
+ */
+kda_status kda_chunk_workspace_size(int32_t N, int64_t T, int32_t H, int32_t K, int32_t V,
+                                    int32_t mode, int64_t* bytes_host);
 
 /*
  * kda_chunk_fwd -- chunked KDA forward over packed sequences.
@@ -122,6 +144,13 @@ kda_status kda_gate(const void* f, int32_t f_dtype, const float* A_log, const fl
  *   final_state [N, H, K, V] F32, or NULL: the state after each sequence's
  *              last token (the initial state for an empty sequence).
  *              final_state may alias initial_state.
+ *   workspace  device scratch of workspace_bytes bytes, or NULL (see
+ *              kda_chunk_workspace_size).  KDA_MODE_BF16_TC with a workspace
+ *              needs workspace_bytes >= kda_chunk_workspace_size(...) (else
+ *              KDA_ERR_INVALID_ARG); its contents are overwritten and mean
+ *              nothing after the call.  Calls that share one workspace must be
+ *              ordered (same stream, or synchronised): the library does not
+ *              guard it.  Ignored by KDA_MODE_FP32_EXACT.
  *   status_dev one device int32 or NULL; the kernel writes a kda_status there
  *              only on a device-detected error (the caller zeroes it).
  */
@@ -131,7 +160,8 @@ kda_status kda_chunk_fwd(const void* q, const void* k, const void* v, int32_t qk
                          int32_t N, int64_t T, int32_t H, int32_t K, int32_t V,
                          float scale, int32_t qk_l2norm, int32_t mode,
                          void* out, int32_t out_dtype, const float* initial_state,
-                         float* final_state, int32_t* status_dev, kda_stream_t stream);
+                         float* final_state, void* workspace, int64_t workspace_bytes,
+                         int32_t* status_dev, kda_stream_t stream);
 
 /*
  * kda_chunk_fwd_gated -- kda_chunk_fwd with the gate fused into its prologue.
@@ -139,7 +169,8 @@ kda_status kda_chunk_fwd(const void* q, const void* k, const void* v, int32_t qk
  * Takes the gate's inputs instead of g and beta and forms, per element,
  *   g = -exp(A_log[h]) * softplus(f + dt_bias[h,c]),  beta = sigmoid(b)
  * exactly as kda_gate does (same FP32 arithmetic, so the result equals
- * kda_gate followed by kda_chunk_fwd bit for bit), without writing g or beta
+ * kda_gate followed by kda_chunk_fwd bit for bit, given the same workspace
+ * choice), without writing g or beta
  * to memory.  The pages compute the gate outside the chunk kernel ("GLM-5.3-
  * Flash F6.2: KDA correctness and FLA sequence parallelism", fused-gate
  * commit); fusing it here removes that launch and its round trip of g.
@@ -156,7 +187,8 @@ kda_status kda_chunk_fwd_gated(const void* q, const void* k, const void* v, int3
                                int32_t N, int64_t T, int32_t H, int32_t K, int32_t V,
                                float scale, int32_t qk_l2norm, int32_t mode,
                                void* out, int32_t out_dtype, const float* initial_state,
-                               float* final_state, int32_t* status_dev, kda_stream_t stream);
+                               float* final_state, void* workspace, int64_t workspace_bytes,
+                               int32_t* status_dev, kda_stream_t stream);
 
 /*
  * kda_recurrent_step -- one token of the recurrence for each of N sequences
@@ -181,7 +213,8 @@ kda_status kda_recurrent_step(const void* q, const void* k, const void* v, int32
 const char* kda_status_string(int32_t status);
 
 /* ABI revision of this header; bumped on any incompatible change (2: initial
- * state argument of kda_chunk_fwd; kda_chunk_fwd_gated; kda_recurrent_step). */
+ * state argument of kda_chunk_fwd; kda_chunk_fwd_gated; kda_recurrent_step.
+ * 3: workspace arguments; kda_chunk_workspace_size). */
 int32_t kda_abi_version(void);
 
 #ifdef __cplusplus

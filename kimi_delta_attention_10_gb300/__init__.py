@@ -1,8 +1,10 @@
 """GB300 (sm_103a) chunked Kimi Delta Attention forward.
 
 The compute path is libkda_gb300.so (C ABI in include/kda.h), reached through
-``kda_gate``, ``kda_chunk_fwd``, ``kda_chunk_fwd_gated`` and ``kda_recurrent_step``; ``inputs`` holds the seeded synthetic
-workloads.
+``kda_gate``, ``kda_chunk_fwd``, ``kda_chunk_fwd_gated`` and
+``kda_recurrent_step`` (``chunk_workspace_size`` sizes the two-phase path's
+scratch); ``inputs`` holds the seeded synthetic workloads.
 """
-from .binding import (KDAError, kda_chunk_fwd, kda_chunk_fwd_gated, kda_gate,  # noqa: F401
-                      kda_recurrent_step, library_path, load_library, status_string)
+from .binding import (KDAError, chunk_workspace_size, kda_chunk_fwd,  # noqa: F401
+                      kda_chunk_fwd_gated, kda_gate, kda_recurrent_step, library_path,
+                      load_library, status_string)

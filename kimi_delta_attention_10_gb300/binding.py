@@ -32,8 +32,8 @@ KDA_MODE_FP32_EXACT = 1
 MODES = {"bf16_tc": KDA_MODE_BF16_TC, "fp32_exact": KDA_MODE_FP32_EXACT}
 
 # Every symbol include/kda.h declares.
-EXPORTS = ("kda_gate", "kda_chunk_fwd", "kda_chunk_fwd_gated", "kda_recurrent_step",
-           "kda_status_string", "kda_abi_version")
+EXPORTS = ("kda_gate", "kda_chunk_workspace_size", "kda_chunk_fwd", "kda_chunk_fwd_gated",
+           "kda_recurrent_step", "kda_status_string", "kda_abi_version")
 
 _lock = threading.Lock()
 _lib = None
@@ -65,12 +65,15 @@ def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
         vp, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
         lib.kda_gate.argtypes = [vp, i32, vp, vp, vp, i32, i64, i32, i32, vp, vp, vp]
         lib.kda_gate.restype = i32
+        lib.kda_chunk_workspace_size.argtypes = [i32, i64, i32, i32, i32, i32,
+                                                 ctypes.POINTER(i64)]
+        lib.kda_chunk_workspace_size.restype = i32
         lib.kda_chunk_fwd.argtypes = [vp, vp, vp, i32, vp, vp, vp, vp, i32, i64, i32, i32, i32,
-                                      ctypes.c_float, i32, i32, vp, i32, vp, vp, vp, vp]
+                                      ctypes.c_float, i32, i32, vp, i32, vp, vp, vp, i64, vp, vp]
         lib.kda_chunk_fwd.restype = i32
         lib.kda_chunk_fwd_gated.argtypes = [vp, vp, vp, i32, vp, i32, vp, vp, vp, i32, vp, vp,
                                             i32, i64, i32, i32, i32, ctypes.c_float, i32, i32,
-                                            vp, i32, vp, vp, vp, vp]
+                                            vp, i32, vp, vp, vp, i64, vp, vp]
         lib.kda_chunk_fwd_gated.restype = i32
         lib.kda_recurrent_step.argtypes = [vp, vp, vp, i32, vp, vp, i32, i32, i32, i32,
                                            ctypes.c_float, i32, vp, vp, i32, vp]
@@ -140,6 +143,31 @@ def _chunk_outputs(q, v, cu_seqlens, out, out_dtype, output_final_state, final_s
     return out, final_state
 
 
+def chunk_workspace_size(N: int, T: int, H: int, K: int = 128, V: int = 128,
+                         mode: str = "bf16_tc") -> int:
+    """Bytes of workspace the two-phase chunk path needs (0 for fp32_exact)."""
+    out = ctypes.c_int64(0)
+    st = load_library().kda_chunk_workspace_size(N, T, H, K, V, MODES[mode], ctypes.byref(out))
+    if st != KDA_OK:
+        raise KDAError(st, "kda_chunk_workspace_size")
+    return out.value
+
+
+def _workspace(workspace, mode, N, T, H, K, V, device):
+    """(pointer, bytes) for the call: None -> no workspace (single-pass
+    kernel); "auto" -> a fresh buffer of the required size for bf16_tc; a
+    tensor -> its storage."""
+    if workspace is None or mode != "bf16_tc":
+        return None, 0, None
+    if isinstance(workspace, str):
+        if workspace != "auto":
+            raise ValueError("workspace must be None, 'auto' or a CUDA tensor")
+        workspace = torch.empty(chunk_workspace_size(N, T, H, K, V, mode), dtype=torch.uint8,
+                                device=device)
+    ptr = _dev_ptr(workspace, "workspace")
+    return ptr, workspace.numel() * workspace.element_size(), workspace
+
+
 def _host_offsets(cu_seqlens_host):
     if cu_seqlens_host is None:
         return None, None
@@ -155,8 +183,12 @@ def kda_chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Te
                   initial_state: Optional[torch.Tensor] = None,
                   cu_seqlens_host: Optional[Sequence[int]] = None, qk_l2norm: bool = True,
                   status: Optional[torch.Tensor] = None,
-                  stream: Optional[torch.cuda.Stream] = None):
-    """Chunked KDA forward.  Returns (out [T,H,V], final_state [N,H,K,V] or None)."""
+                  stream: Optional[torch.cuda.Stream] = None, workspace="auto"):
+    """Chunked KDA forward.  Returns (out [T,H,V], final_state [N,H,K,V] or None).
+
+    workspace: "auto" (bf16_tc allocates the two-phase path's scratch), a CUDA
+    tensor of at least chunk_workspace_size(...) bytes, or None (single-pass
+    kernel, no scratch)."""
     lib = load_library()
     T, H, K = q.shape
     V = v.shape[2]
@@ -166,12 +198,13 @@ def kda_chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Te
     out, final_state = _chunk_outputs(q, v, cu_seqlens, out, out_dtype, output_final_state,
                                       final_state)
     keep, host = _host_offsets(cu_seqlens_host)
+    ws, ws_bytes, ws_keep = _workspace(workspace, mode, N, T, H, K, V, q.device)
     st = lib.kda_chunk_fwd(
         _dev_ptr(q, "q"), _dev_ptr(k, "k"), _dev_ptr(v, "v"), _dtype_code(q),
         _dev_ptr(g, "g"), _dev_ptr(beta, "beta"), _dev_ptr(cu_seqlens, "cu_seqlens"), host,
         N, T, H, K, V, float(scale), 1 if qk_l2norm else 0, MODES[mode],
         _dev_ptr(out, "out"), _dtype_code(out), _dev_ptr(initial_state, "initial_state"),
-        _dev_ptr(final_state, "final_state"), _dev_ptr(status, "status"),
+        _dev_ptr(final_state, "final_state"), ws, ws_bytes, _dev_ptr(status, "status"),
         _stream_handle(stream, q.device))
     if st != KDA_OK:
         raise KDAError(st, "kda_chunk_fwd")
@@ -187,8 +220,9 @@ def kda_chunk_fwd_gated(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, f: to
                         initial_state: Optional[torch.Tensor] = None,
                         cu_seqlens_host: Optional[Sequence[int]] = None, qk_l2norm: bool = True,
                         status: Optional[torch.Tensor] = None,
-                        stream: Optional[torch.cuda.Stream] = None):
-    """Chunked KDA forward with the gate (g, beta from f, A_log, dt_bias, b) fused in."""
+                        stream: Optional[torch.cuda.Stream] = None, workspace="auto"):
+    """Chunked KDA forward with the gate (g, beta from f, A_log, dt_bias, b) fused in;
+    workspace as kda_chunk_fwd."""
     lib = load_library()
     T, H, K = q.shape
     V = v.shape[2]
@@ -198,13 +232,14 @@ def kda_chunk_fwd_gated(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, f: to
     out, final_state = _chunk_outputs(q, v, cu_seqlens, out, out_dtype, output_final_state,
                                       final_state)
     keep, host = _host_offsets(cu_seqlens_host)
+    ws, ws_bytes, ws_keep = _workspace(workspace, mode, N, T, H, K, V, q.device)
     st = lib.kda_chunk_fwd_gated(
         _dev_ptr(q, "q"), _dev_ptr(k, "k"), _dev_ptr(v, "v"), _dtype_code(q),
         _dev_ptr(f, "f"), _dtype_code(f), _dev_ptr(A_log, "A_log"), _dev_ptr(dt_bias, "dt_bias"),
         _dev_ptr(b, "b"), _dtype_code(b), _dev_ptr(cu_seqlens, "cu_seqlens"), host,
         N, T, H, K, V, float(scale), 1 if qk_l2norm else 0, MODES[mode],
         _dev_ptr(out, "out"), _dtype_code(out), _dev_ptr(initial_state, "initial_state"),
-        _dev_ptr(final_state, "final_state"), _dev_ptr(status, "status"),
+        _dev_ptr(final_state, "final_state"), ws, ws_bytes, _dev_ptr(status, "status"),
         _stream_handle(stream, q.device))
     if st != KDA_OK:
         raise KDAError(st, "kda_chunk_fwd_gated")

@@ -27,7 +27,7 @@ int device_sm_count()
 
 extern "C" {
 
-int32_t kda_abi_version(void) { return 2; }
+int32_t kda_abi_version(void) { return 3; }
 
 const char* kda_status_string(int32_t s)
 {
@@ -92,12 +92,30 @@ kda_status check_chunk(const void* q, const void* k, const void* v, int32_t qkv_
     return KDA_OK;
 }
 
-kda_status launch_chunk(const kda::ChunkArgs& a, int32_t mode, kda_stream_t stream)
+// Workspace checks (BF16_TC only) and dispatch.
+kda_status launch_chunk(kda::ChunkArgs a, int32_t mode, const int32_t* cu_seqlens_host,
+                        void* workspace, int64_t workspace_bytes, kda_stream_t stream)
 {
+    const bool split = mode == KDA_MODE_BF16_TC && workspace != nullptr;
+    if (split) {
+        if (!aligned16(workspace)) return KDA_ERR_ALIGNMENT;
+        if (workspace_bytes < kda::split_workspace_bytes(a.N, a.T, a.H)) return KDA_ERR_INVALID_ARG;
+    }
     if (a.N == 0) return KDA_OK;
-    cudaError_t e = (mode == KDA_MODE_BF16_TC)
-                        ? kda::launch_chunk_tc(a, reinterpret_cast<cudaStream_t>(stream))
-                        : kda::launch_chunk_fp32(a, reinterpret_cast<cudaStream_t>(stream));
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (split) {
+        a.workspace = workspace;
+        int64_t chunks = kda::split_chunk_bound(a.N, a.T);
+        if (cu_seqlens_host) {            // exact count: no idle preparation CTAs
+            chunks = 0;
+            for (int32_t n = 0; n < a.N; ++n)
+                chunks += (cu_seqlens_host[n + 1] - cu_seqlens_host[n] + kda::kChunk - 1) / kda::kChunk;
+        }
+        e = kda::launch_chunk_split(a, chunks, s);
+    } else {
+        e = (mode == KDA_MODE_BF16_TC) ? kda::launch_chunk_tc(a, s) : kda::launch_chunk_fp32(a, s);
+    }
     return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
@@ -117,13 +135,26 @@ kda::ChunkArgs chunk_args(const void* q, const void* k, const void* v, int32_t q
 
 }  // namespace
 
+kda_status kda_chunk_workspace_size(int32_t N, int64_t T, int32_t H, int32_t K, int32_t V,
+                                    int32_t mode, int64_t* bytes_host)
+{
+    if (!bytes_host) return KDA_ERR_INVALID_ARG;
+    if (N < 0 || T < 0 || H < 1 || K < 1 || V < 1) return KDA_ERR_INVALID_ARG;
+    if (mode != KDA_MODE_BF16_TC && mode != KDA_MODE_FP32_EXACT) return KDA_ERR_INVALID_ARG;
+    if (T > INT32_MAX) return KDA_ERR_UNSUPPORTED;
+    if (K != kda::kHeadK || V != kda::kHeadV) return KDA_ERR_UNSUPPORTED;
+    *bytes_host = mode == KDA_MODE_BF16_TC ? kda::split_workspace_bytes(N, T, H) : 0;
+    return KDA_OK;
+}
+
 kda_status kda_chunk_fwd(const void* q, const void* k, const void* v, int32_t qkv_dtype,
                          const float* g, const float* beta,
                          const int32_t* cu_seqlens, const int32_t* cu_seqlens_host,
                          int32_t N, int64_t T, int32_t H, int32_t K, int32_t V,
                          float scale, int32_t qk_l2norm, int32_t mode,
                          void* out, int32_t out_dtype, const float* initial_state,
-                         float* final_state, int32_t* status_dev, kda_stream_t stream)
+                         float* final_state, void* workspace, int64_t workspace_bytes,
+                         int32_t* status_dev, kda_stream_t stream)
 {
     kda_status st = check_chunk(q, k, v, qkv_dtype, cu_seqlens, cu_seqlens_host, N, T, H, K, V,
                                 qk_l2norm, mode, out, out_dtype, initial_state, final_state,
@@ -134,7 +165,7 @@ kda_status kda_chunk_fwd(const void* q, const void* k, const void* v, int32_t qk
     kda::ChunkArgs a = chunk_args(q, k, v, qkv_dtype, cu_seqlens, N, T, H, scale, qk_l2norm, out,
                                   out_dtype, initial_state, final_state, status_dev);
     a.g = g; a.beta = beta; a.gated = false;
-    return launch_chunk(a, mode, stream);
+    return launch_chunk(a, mode, cu_seqlens_host, workspace, workspace_bytes, stream);
 }
 
 kda_status kda_chunk_fwd_gated(const void* q, const void* k, const void* v, int32_t qkv_dtype,
@@ -144,7 +175,8 @@ kda_status kda_chunk_fwd_gated(const void* q, const void* k, const void* v, int3
                                int32_t N, int64_t T, int32_t H, int32_t K, int32_t V,
                                float scale, int32_t qk_l2norm, int32_t mode,
                                void* out, int32_t out_dtype, const float* initial_state,
-                               float* final_state, int32_t* status_dev, kda_stream_t stream)
+                               float* final_state, void* workspace, int64_t workspace_bytes,
+                               int32_t* status_dev, kda_stream_t stream)
 {
     kda_status st = check_chunk(q, k, v, qkv_dtype, cu_seqlens, cu_seqlens_host, N, T, H, K, V,
                                 qk_l2norm, mode, out, out_dtype, initial_state, final_state,
@@ -165,7 +197,7 @@ kda_status kda_chunk_fwd_gated(const void* q, const void* k, const void* v, int3
     a.dt_bias = dt_bias;
     a.b = b;
     a.b_bf16 = b_dtype == KDA_BF16;
-    return launch_chunk(a, mode, stream);
+    return launch_chunk(a, mode, cu_seqlens_host, workspace, workspace_bytes, stream);
 }
 
 kda_status kda_recurrent_step(const void* q, const void* k, const void* v, int32_t qkv_dtype,

@@ -1,0 +1,662 @@
+// Two-phase tensor-core chunked KDA forward (tcgen05, TMEM accumulators), sm_103a.
+//
+// The chunk solve ("Add opt-in FP32 KDA chunk computation", sections Problem
+// and Change, in its WY form) splits into a part that needs only the chunk's
+// own inputs and a short part that needs the state entering the chunk:
+//   prepare:  A_kk, A_qk (pair sums), T' = (I + A_kk)^-1 diag(beta),
+//             W = T' (K^ o e^G),  U = T' V,  Q' = Q^ o e^G,
+//             K'' = K^ o e^{G_last - G},  d = e^{G_last}
+//   scan:     Delta = U - W S
+//             O = scale [Q' S + A_qk Delta]
+//             S <- Diag(d) S + K''^T Delta
+// The preparation of every (chunk, head) is independent, so it runs over the
+// whole problem at once on every SM (chunk_prep_kernel: one CTA per unit, two
+// CTAs per SM); its results go to a caller-provided workspace as one record
+// per unit, already in the 128-byte-swizzled layouts the scan's MMAs read.
+// The scan (chunk_scan_kernel: one CTA per (sequence, head)) then walks the
+// chunks in order with the state on chip, bringing each record in by one bulk
+// copy, double-buffered, while it works on the one before.  A plan kernel
+// first turns cu_seqlens into per-sequence chunk offsets.
+//
+// Record of one unit (bytes):
+//   W       fp16 [128 c][64 i]  (the B operand of [W S]^T = S^T W^T, MN-major)
+//   Q'      fp16 [128 c][64 i]  (B of [Q' S]^T, MN-major)
+//   U^T     fp16 [128 v][64 i]  (row v read by the thread of state row v)
+//   K''^T   fp16 [128 c][64 j]  (B of P^T = Delta^T K'', K-major)
+//   A_qk    fp16 [64 i][64 j]   (B of Delta^T A_qk^T, K-major; strictly upper part 0)
+//   d       fp32 [128]
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "kda_internal.cuh"
+#include "kda_tc.cuh"
+#include "kda_chunk_ops.cuh"
+
+namespace kda {
+
+namespace {
+
+using namespace tc;
+using namespace chunk_ops;
+
+constexpr int DV = kHeadV;
+constexpr uint32_t kWaitIters = 1u << 22;   // polls before a wait gives up
+
+constexpr uint32_t REC_W = 0;
+constexpr uint32_t REC_QP = 16384;
+constexpr uint32_t REC_U = 32768;
+constexpr uint32_t REC_KT = 49152;
+constexpr uint32_t REC_AQK = 65536;
+constexpr uint32_t REC_DEC = 73728;
+constexpr uint32_t REC_BYTES = 74240;
+static_assert(REC_BYTES % 16 == 0 && REC_BYTES < (1u << 20), "bulk copy size");
+
+// Workspace header: int32 [0] = 1 when the plan found offsets outside [0, T]
+// (those sequences get no chunks and are skipped), int32 [4 .. 4 + N] = chunk
+// offsets (chunks of sequences 0 .. n-1).
+constexpr int kHdrOff = 4;
+
+int64_t header_bytes(int32_t N) { return ((int64_t)(kHdrOff + N + 1) * 4 + 1023) / 1024 * 1024; }
+
+// ---------------------------------------------------------------- plan
+__global__ void __launch_bounds__(1024) chunk_plan_kernel(const int32_t* __restrict__ cu, int32_t N,
+                                                          int64_t T, int32_t* __restrict__ hdr,
+                                                          int32_t* status)
+{
+    __shared__ int32_t wsum[32];
+    __shared__ int32_t carry;
+    __shared__ int32_t bad;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    int32_t* off = hdr + kHdrOff;
+    if (tid == 0) {
+        carry = 0;
+        bad = 0;
+        off[0] = 0;
+    }
+    __syncthreads();
+    for (int32_t base = 0; base < N; base += 1024) {
+        const int32_t n = base + tid;
+        int32_t cnt = 0;
+        if (n < N) {
+            const int32_t bos = cu[n], eos = cu[n + 1];
+            if (bos < 0 || eos < bos || (int64_t)eos > T) bad = 1;   // no chunks: skipped
+            else cnt = (eos - bos + kChunk - 1) / kChunk;
+        }
+        int32_t x = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int32_t y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+        }
+        if (lane == 31) wsum[warp] = x;
+        __syncthreads();
+        if (warp == 0) {
+            int32_t w = wsum[lane];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int32_t y = __shfl_up_sync(0xffffffffu, w, o);
+                if (lane >= o) w += y;
+            }
+            wsum[lane] = w;
+        }
+        __syncthreads();
+        const int32_t incl = carry + x + (warp > 0 ? wsum[warp - 1] : 0);
+        if (n < N) off[n + 1] = incl;
+        __syncthreads();
+        if (tid == 1023) carry = incl;
+        __syncthreads();
+    }
+    if (tid == 0) {
+        hdr[0] = bad;
+        if (bad) report_status(status, KDA_ERR_DEVICE_ARG);
+    }
+}
+
+// ---------------------------------------------------------------- prepare
+// Shared memory of one preparation CTA (bytes from a 1024-aligned base).  The
+// staging of q, k and g is dead once every thread holds its channel's values
+// in registers; the pair-sum operands, X'^T and then A_kk / T reuse it.
+constexpr uint32_t P_SQ = 0;           // q staging [64][128] 16-bit
+constexpr uint32_t P_SK = 16384;       // k staging
+constexpr uint32_t P_SG = 32768;       // g (or f) staging fp32 [64][128]
+constexpr uint32_t P_PAIR = 0;         // pair-sum operands: A MN-major 2 x 16 KiB, B 16 KiB
+constexpr uint32_t P_AKK = 0;          // after the pair sums: A_kk fp32 [64][68]
+constexpr uint32_t P_TF = C * LDA * 4; //                      T fp32 [64][68]
+constexpr uint32_t P_XT = 49152;       // X'^T fp16 K-major [128 c][64 j]
+constexpr uint32_t P_SV = 65536;       // v staging -> V^T fp16 K-major [128 v][64 j]
+constexpr uint32_t P_AQK = 81920;      // A_qk fp16 [64 i][64 j]
+constexpr uint32_t P_TP = 90112;       // T' fp16 [64 i][64 j]
+constexpr uint32_t P_RQ = 98304;       // 1/|q_t| fp32 [64]
+constexpr uint32_t P_RK = P_RQ + 256;  // 1/|k_t|
+constexpr uint32_t P_DQK = P_RK + 256; // q^_t . k^_t
+constexpr uint32_t P_BETA = P_DQK + 256;
+constexpr uint32_t P_TOT = P_BETA + 256;   // half-chunk decay fp32 [2][128]
+constexpr uint32_t P_BAR = P_TOT + 1024;   // 4 mbarriers + TMEM slot
+constexpr uint32_t P_SMEM = P_BAR + 64 + 1024;
+static_assert(P_TF + C * LDA * 4 <= P_XT, "A_kk and T fit below X'^T");
+static_assert(P_PAIR + 49152 <= P_XT, "pair-sum operands fit below X'^T");
+static_assert(2 * (P_SMEM + 1024) <= 233472, "two preparation CTAs per SM");
+constexpr uint32_t P_TM_A = 0, P_TM_W = 0, P_TM_U = 64, P_TM_COLS = 256;
+
+template <typename TIn, bool kGated>
+__global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(ChunkArgs args,
+                                                           const int32_t* __restrict__ hdr,
+                                                           unsigned char* __restrict__ records)
+{
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    const uint32_t raw_s = smem_u32(smem_raw);
+    const uint32_t pad = (1024u - (raw_s & 1023u)) & 1023u;
+    unsigned char* sm = smem_raw + pad;
+    const uint32_t sb = raw_s + pad;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int quad = warp & 3, half = warp >> 2;
+    const int row = 32 * quad + lane;                      // TMEM lane
+    const int ch = tid & 127, hh = tid >> 7;               // channel / token-half ownership
+    const int H = args.H;
+
+    const int32_t* off = hdr + kHdrOff;
+    const int64_t unit = blockIdx.x;
+    const int32_t gc = (int32_t)(unit / H);
+    const int h = (int)(unit % H);
+    if (gc >= off[args.N]) return;
+    int lo = 0, hi = args.N - 1;                           // last n with off[n] <= gc
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (off[mid] <= gc) lo = mid;
+        else hi = mid - 1;
+    }
+    const int n = lo;
+    const int bos = args.cu_seqlens[n], eos = args.cu_seqlens[n + 1];
+    const int t0 = bos + (gc - off[n]) * C;
+    const int L = min(C, eos - t0);
+    unsigned char* rec = records + unit * REC_BYTES;
+
+    float (*akk)[LDA] = reinterpret_cast<float (*)[LDA]>(sm + P_AKK);
+    float (*Tf)[LDA] = reinterpret_cast<float (*)[LDA]>(sm + P_TF);
+    const uint16_t* sq = reinterpret_cast<const uint16_t*>(sm + P_SQ);
+    const uint16_t* sk = reinterpret_cast<const uint16_t*>(sm + P_SK);
+    const uint16_t* sv = reinterpret_cast<const uint16_t*>(sm + P_SV);
+    const float* sg = reinterpret_cast<const float*>(sm + P_SG);
+    float* rq = reinterpret_cast<float*>(sm + P_RQ);
+    float* rk = reinterpret_cast<float*>(sm + P_RK);
+    float* dqk = reinterpret_cast<float*>(sm + P_DQK);
+    float* sbeta = reinterpret_cast<float*>(sm + P_BETA);
+    float* tot = reinterpret_cast<float*>(sm + P_TOT);
+    uint64_t* bar = reinterpret_cast<uint64_t*>(sm + P_BAR);   // [0..2] pair rounds, [3] W/U
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + P_BAR + 48);
+
+    const TIn* __restrict__ gq = static_cast<const TIn*>(args.q);
+    const TIn* __restrict__ gk = static_cast<const TIn*>(args.k);
+    const TIn* __restrict__ gv = static_cast<const TIn*>(args.v);
+    const float* __restrict__ graw = kGated ? args.f : args.g;
+    using ST = Stage<TIn>;
+
+    // ---- 1: the chunk in staging (rows >= L zero, decay 1)
+    if constexpr (sizeof(TIn) == 2) {
+#pragma unroll
+        for (int u = 0; u < C * 16 / NT; ++u) {
+            const int e = tid + u * NT, r = e >> 4, pc = e & 15;
+            const bool ok = r < L;
+            const int64_t src = ((int64_t)(t0 + (ok ? r : 0)) * H + h) * DK + pc * 8;
+            cp_async16(sm + P_SQ + r * 256 + pc * 16, gq + src, ok);
+            cp_async16(sm + P_SK + r * 256 + pc * 16, gk + src, ok);
+            cp_async16(sm + P_SV + r * 256 + pc * 16, gv + src, ok);
+        }
+    } else {
+        using LD = Loader<TIn>;
+        constexpr int P = LD::kPieces;
+        auto rows_via_regs = [&](const TIn* base, uint32_t so) {
+            uint4 x[C * P / NT];
+#pragma unroll
+            for (int u = 0; u < C * P / NT; ++u) {
+                const int e = tid + u * NT, r = e / P, pc = e % P;
+                x[u] = (r < L) ? LD::load(base + ((int64_t)(t0 + r) * H + h) * DK, pc)
+                               : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int u = 0; u < C * P / NT; ++u) {
+                const int e = tid + u * NT;
+                LD::store(sm + so, e / P, e % P, x[u]);
+            }
+        };
+        rows_via_regs(gq, P_SQ);
+        rows_via_regs(gk, P_SK);
+        rows_via_regs(gv, P_SV);
+    }
+#pragma unroll
+    for (int u = 0; u < C * 32 / NT; ++u) {
+        const int e = tid + u * NT, r = e >> 5, pc = e & 31;
+        const bool ok = r < L;
+        cp_async16(sm + P_SG + e * 16, graw + ((int64_t)(t0 + (ok ? r : 0)) * H + h) * DK + pc * 4,
+                   ok);
+    }
+    cp_async_commit();
+    float lamneg = 0.f, dtb = 0.f;
+    if (kGated) {
+        lamneg = -expf(args.A_log[h]);
+        dtb = args.dt_bias[(int64_t)h * DK + ch];
+    }
+    if (tid < C) {
+        float xb = 0.f;
+        if (tid < L) {
+            const int64_t i = (int64_t)(t0 + tid) * H + h;
+            if (kGated)
+                xb = gate_sigmoid(args.b_bf16
+                                      ? __bfloat162float(static_cast<const __nv_bfloat16*>(args.b)[i])
+                                      : static_cast<const float*>(args.b)[i]);
+            else
+                xb = args.beta[i];
+        }
+        sbeta[tid] = xb;
+    }
+    if (warp == 0) {
+        tmem_alloc(tslot, P_TM_COLS);
+        tmem_relinquish();
+    }
+    if (tid == 0) {
+        for (int b = 0; b < 4; ++b) mbar_init(&bar[b], 1);
+        fence_mbar_init();
+    }
+    cp_async_wait_all();
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tmem = *tslot;
+    const uint32_t tlane = tmem + ((uint32_t)(32 * quad) << 16);
+
+    // ---- 2: row norms and q^ . k^
+    chunk_norms<TIn>(sm + P_SQ, sm + P_SK, rq, rk, dqk, args.l2norm != 0, tid);
+    __syncthreads();
+
+    // ---- 3: per channel (thread ch, tokens 32 hh .. 32 hh + 31)
+    float a[32], kh[32], qh[32];
+    {
+#pragma unroll
+        for (int u = 0; u < 32; ++u) {
+            const int t = 32 * hh + u;
+            const float gv_ = sg[t * DK + ch];
+            a[u] = expf(kGated ? (t < L ? gate_decay(gv_, dtb, lamneg) : 0.f) : gv_);
+            kh[u] = ST::to_f32(sk[t * DK + ch]) * rk[t];
+            qh[u] = ST::to_f32(sq[t * DK + ch]) * rq[t];
+        }
+        float p = 1.f;
+#pragma unroll
+        for (int u = 0; u < 32; ++u) p *= a[u];
+        tot[hh * DK + ch] = p;
+    }
+    __syncthreads();
+    {
+        const float before = hh ? tot[ch] : 1.f;
+        const float after = hh ? 1.f : tot[DK + ch];
+        if (hh == 0) reinterpret_cast<float*>(rec + REC_DEC)[ch] = tot[ch] * tot[DK + ch];
+        channel_rows(sm + P_XT, rec + REC_QP, rec + REC_KT, ch, hh, before, after, a, kh, qh);
+    }
+
+    // ---- 4: pair sums, three rounds through one operand buffer
+    bool failed = false;
+    int last_bar = -1;
+    constexpr uint32_t id_pairs = idesc(kFmtF16, 128, 64, true, true);
+    auto issue_round = [&](int rnd) {
+        fence_async_smem();
+        fence_before_sync();
+        __syncthreads();
+        if (tid == 0) {
+            fence_after_sync();
+#pragma unroll
+            for (int s = 0; s < 8; ++s)
+                mma_f16(tmem + P_TM_A + 64 * rnd, desc_mnmajor128(sb + P_PAIR, 16384, s),
+                        desc_mnmajor64(sb + P_PAIR + 32768, s), id_pairs, s > 0);
+            commit(&bar[rnd]);
+        }
+        last_bar = rnd;
+    };
+    auto wait_bar = [&](int b) -> bool {
+        const bool ok = mbar_wait(&bar[b], 0, kWaitIters);
+        return __syncthreads_or(!ok) == 0;
+    };
+    float vv[32];
+    do {
+        level32_operands(sm + P_PAIR, ch, hh, a, kh, qh);
+        level_operands<16>(sm + P_PAIR, ch, hh, 64, 32, a, kh, qh);
+        issue_round(0);
+        if (!wait_bar(0)) { failed = true; break; }
+        level_operands<8>(sm + P_PAIR, ch, hh, 0, 0, a, kh, qh);
+        level_operands<4>(sm + P_PAIR, ch, hh, 64, 32, a, kh, qh);
+        issue_round(1);
+        if (!wait_bar(1)) { failed = true; break; }
+        level_operands<2>(sm + P_PAIR, ch, hh, 0, 0, a, kh, qh);
+        level_operands<1>(sm + P_PAIR, ch, hh, 64, 32, a, kh, qh);
+        issue_round(2);
+        // v column of this thread, read before the barrier that precedes the
+        // in-place V^T writes
+#pragma unroll
+        for (int u = 0; u < 32; ++u) vv[u] = ST::to_f32(sv[(32 * hh + u) * DV + ch]);
+        if (!wait_bar(2)) { failed = true; break; }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) st8(sm + P_SV, 0, ch, 32 * hh + 8 * q, vv + 8 * q);
+        fence_after_sync();
+
+        // ---- 5: A_kk (fp32) and A_qk (fp16) from TMEM
+        aqk_zero_upper(sm + P_AQK, tid);
+        extract_pairs(sm + P_AQK, &akk[0][0], sbeta, dqk, tlane, P_TM_A, tid, warp, lane);
+        fence_before_sync();
+        __syncthreads();
+
+        // ---- 6: T' = (I + A_kk)^-1 diag(beta)
+        chunk_inverse(akk, Tf, sbeta, sm + P_TP, tid, warp, lane);
+        fence_async_smem();
+        fence_before_sync();
+        __syncthreads();
+
+        // ---- 7: W^T = X'^T T'^T, U^T = V^T T'^T
+        if (tid == 0) {
+            fence_after_sync();
+            constexpr uint32_t id = idesc(kFmtF16, 128, 64);
+#pragma unroll
+            for (int s = 0; s < 4; ++s)
+                mma_f16(tmem + P_TM_W, desc_kmajor(sb + P_XT, 128, s), desc_kmajor(sb + P_TP, 64, s),
+                        id, s > 0);
+#pragma unroll
+            for (int s = 0; s < 4; ++s)
+                mma_f16(tmem + P_TM_U, desc_kmajor(sb + P_SV, 128, s), desc_kmajor(sb + P_TP, 64, s),
+                        id, s > 0);
+            commit(&bar[3]);
+        }
+        last_bar = 3;
+        {
+            // A_qk tile to the record while the MMAs run (32 bytes per thread)
+            const uint4* src = reinterpret_cast<const uint4*>(sm + P_AQK);
+            uint4* dst = reinterpret_cast<uint4*>(rec + REC_AQK);
+            dst[tid] = src[tid];
+            dst[tid + NT] = src[tid + NT];
+        }
+        if (!wait_bar(3)) { failed = true; break; }
+        fence_after_sync();
+        {
+            float w[32];
+            tmem_ld32(tlane + P_TM_W + 32 * half, w);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) st8(rec + REC_W, 0, row, 32 * half + 8 * q, w + 8 * q);
+            tmem_ld32(tlane + P_TM_U + 32 * half, w);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) st8(rec + REC_U, 0, row, 32 * half + 8 * q, w + 8 * q);
+        }
+    } while (false);
+
+    if (failed) {
+        if (tid == 0) report_status(args.status, KDA_ERR_TIMEOUT);
+        // let the MMAs still in flight finish before the TMEM is released
+        for (int b = 0; b <= last_bar; ++b) mbar_wait(&bar[b], 0, kWaitIters);
+    }
+    fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, P_TM_COLS);
+}
+
+// ---------------------------------------------------------------- scan
+constexpr uint32_t S_ST = 0;                 // S^T fp16 K-major [128 v][128 c]
+constexpr uint32_t S_DT = 32768;             // Delta^T fp16 K-major [128 v][64 i]
+constexpr uint32_t S_STG = 49152;            // two record stages
+constexpr uint32_t S_STG_STRIDE = 74752;     // REC_BYTES rounded up to 1024
+constexpr uint32_t S_BAR = S_STG + 2 * S_STG_STRIDE;   // full[2], ws, op + TMEM slot
+constexpr uint32_t S_SMEM = S_BAR + 64 + 1024;
+static_assert(S_STG_STRIDE >= REC_BYTES && S_STG_STRIDE % 1024 == 0, "stage alignment");
+static_assert(S_SMEM <= 232448, "shared memory budget");
+constexpr uint32_t S_TM_WS = 0, S_TM_O = 64, S_TM_P = 128, S_TM_COLS = 256;
+
+__device__ __forceinline__ void store_out(float* p, float x) { *p = x; }
+__device__ __forceinline__ void store_out(__nv_bfloat16* p, float x) { *p = __float2bfloat16_rn(x); }
+
+template <typename TOut>
+__global__ void __launch_bounds__(NT, 1) chunk_scan_kernel(ChunkArgs args,
+                                                           const int32_t* __restrict__ hdr,
+                                                           const unsigned char* __restrict__ records)
+{
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    const uint32_t raw_s = smem_u32(smem_raw);
+    const uint32_t pad = (1024u - (raw_s & 1023u)) & 1023u;
+    unsigned char* sm = smem_raw + pad;
+    const uint32_t sb = raw_s + pad;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int quad = warp & 3, half = warp >> 2;
+    const int row = 32 * quad + lane;                      // TMEM lane = state row v
+    const int H = args.H;
+    const int n = blockIdx.x / H, h = blockIdx.x % H;
+
+    const int bos = args.cu_seqlens[n], eos = args.cu_seqlens[n + 1];
+    if (bos < 0 || eos < bos || (int64_t)eos > args.T) return;   // reported by the plan
+    const int nch = (eos - bos + C - 1) / C;
+    const int64_t rstride = (int64_t)H * REC_BYTES;
+    const unsigned char* rec0 = records + ((int64_t)hdr[kHdrOff + n] * H + h) * REC_BYTES;
+    TOut* __restrict__ out = static_cast<TOut*>(args.out);
+    uint64_t* bar = reinterpret_cast<uint64_t*>(sm + S_BAR);   // [0,1] stages, [2] WS, [3] O/P
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + S_BAR + 48);
+
+    // ---- the entering state (zero, or the caller's)
+    float S[64];                                           // S^T[row][64 half + c]
+    if (args.initial_state != nullptr) {
+        const float* s0 = args.initial_state + ((int64_t)n * H + h) * DK * DV;
+#pragma unroll
+        for (int u = 0; u < 64; ++u) S[u] = s0[(int64_t)(64 * half + u) * DV + row];
+    } else {
+#pragma unroll
+        for (int u = 0; u < 64; ++u) S[u] = 0.f;
+    }
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+        *reinterpret_cast<uint4*>(sm + S_ST + sw128_tile(128, row, (64 * half + 8 * q) * 2)) =
+            pack_h8(S + 8 * q);
+    if (warp == 0) {
+        tmem_alloc(tslot, S_TM_COLS);
+        tmem_relinquish();
+    }
+    if (tid == 0) {
+        for (int b = 0; b < 4; ++b) mbar_init(&bar[b], 1);
+        fence_mbar_init();
+    }
+    fence_async_smem();
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tmem = *tslot;
+    const uint32_t tlane = tmem + ((uint32_t)(32 * quad) << 16);
+
+    int issued = 0;                                        // chunks whose record load was issued
+    auto issue_load = [&](int c) {
+        unsigned char* stage = sm + S_STG + (c & 1) * S_STG_STRIDE;
+        mbar_arrive_expect_tx(&bar[c & 1], REC_BYTES);
+        bulk_g2s(stage, rec0 + c * rstride, REC_BYTES, &bar[c & 1]);
+    };
+    if (tid == 0) {
+        for (int c = 0; c < min(2, nch); ++c) issue_load(c);
+    }
+    issued = min(2, nch);
+
+    bool failed = false;
+    int c = 0;
+    int last_mma = -1;                                     // 2: WS committed, 3: O/P committed
+    for (; c < nch; ++c) {
+        const int t0 = bos + c * C, L = min(C, eos - t0);
+        const uint32_t b = c & 1;
+        unsigned char* stage = sm + S_STG + b * S_STG_STRIDE;
+        const uint32_t sst = sb + S_STG + b * S_STG_STRIDE;
+        const uint32_t mpar = c & 1;
+        last_mma = -1;
+        {
+            const bool ok = mbar_wait(&bar[b], (c >> 1) & 1, kWaitIters);
+            if (__syncthreads_or(!ok)) { failed = true; break; }
+        }
+        if (tid == 0) {
+            fence_after_sync();
+            constexpr uint32_t ids = idesc(kFmtF16, 128, 64, false, true);
+#pragma unroll
+            for (int s = 0; s < 8; ++s)
+                mma_f16(tmem + S_TM_WS, desc_kmajor(sb + S_ST, 128, s),
+                        desc_mnmajor64(sst + REC_W, s), ids, s > 0);
+            commit(&bar[2]);
+#pragma unroll
+            for (int s = 0; s < 8; ++s)
+                mma_f16(tmem + S_TM_O, desc_kmajor(sb + S_ST, 128, s),
+                        desc_mnmajor64(sst + REC_QP, s), ids, s > 0);
+        }
+        last_mma = 2;
+        {
+            const bool ok = mbar_wait(&bar[2], mpar, kWaitIters);
+            if (__syncthreads_or(!ok)) { failed = true; break; }
+        }
+        fence_after_sync();
+        {
+            // Delta^T[v][i] = U^T[v][i] - [W S]^T[v][i], fp16 K-major
+            float ws[32], d[8];
+            tmem_ld32(tlane + S_TM_WS + 32 * half, ws);
+            const unsigned char* up = stage + REC_U;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const uint4 pk = *reinterpret_cast<const uint4*>(up + sw128(row, (32 * half + 8 * q) * 2));
+                const uint32_t w4[4] = {pk.x, pk.y, pk.z, pk.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 uf = __half22float2(*reinterpret_cast<const __half2*>(&w4[e]));
+                    d[2 * e] = uf.x - ws[8 * q + 2 * e];
+                    d[2 * e + 1] = uf.y - ws[8 * q + 2 * e + 1];
+                }
+                st8(sm + S_DT, 0, row, 32 * half + 8 * q, d);
+            }
+        }
+        fence_async_smem();
+        fence_before_sync();
+        __syncthreads();
+        if (tid == 0) {
+            fence_after_sync();
+            constexpr uint32_t ido = idesc(kFmtF16, 128, 64);
+            constexpr uint32_t idp = idesc(kFmtF16, 128, 128);
+#pragma unroll
+            for (int s = 0; s < 4; ++s)
+                mma_f16(tmem + S_TM_O, desc_kmajor(sb + S_DT, 128, s),
+                        desc_kmajor(sst + REC_AQK, 64, s), ido, 1);
+#pragma unroll
+            for (int s = 0; s < 4; ++s)
+                mma_f16(tmem + S_TM_P, desc_kmajor(sb + S_DT, 128, s),
+                        desc_kmajor(sst + REC_KT, 128, s), idp, s > 0);
+            commit(&bar[3]);
+        }
+        last_mma = 3;
+        {
+            const bool ok = mbar_wait(&bar[3], mpar, kWaitIters);
+            if (__syncthreads_or(!ok)) { failed = true; break; }
+        }
+        last_mma = -1;
+        fence_after_sync();
+        {
+            // out = scale O;  S^T <- S^T Diag(d) + P^T;  fp16 copy of S^T
+            float o[32];
+            tmem_ld32(tlane + S_TM_O + 32 * half, o);
+            const int64_t ostride = (int64_t)H * DV;
+            TOut* op = out + ((int64_t)(t0 + 32 * half) * H + h) * DV + row;
+            const int nrows = min(32, L - 32 * half);
+#pragma unroll
+            for (int u = 0; u < 32; ++u) {
+                if (u < nrows) store_out(op, args.scale * o[u]);
+                op += ostride;
+            }
+            const float* dec = reinterpret_cast<const float*>(stage + REC_DEC);
+            float p[32];
+#pragma unroll
+            for (int part = 0; part < 2; ++part) {
+                tmem_ld32(tlane + S_TM_P + 64 * half + 32 * part, p);
+#pragma unroll
+                for (int u = 0; u < 32; ++u)
+                    S[32 * part + u] = S[32 * part + u] * dec[64 * half + 32 * part + u] + p[u];
+            }
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                *reinterpret_cast<uint4*>(sm + S_ST + sw128_tile(128, row, (64 * half + 8 * q) * 2)) =
+                    pack_h8(S + 8 * q);
+        }
+        fence_async_smem();
+        fence_before_sync();
+        __syncthreads();
+        // every read of this stage is done: bring in the chunk after next
+        if (c + 2 < nch) {
+            if (tid == 0) issue_load(c + 2);
+            issued = c + 3;
+        }
+    }
+
+    if (failed) {
+        if (tid == 0) report_status(args.status, KDA_ERR_TIMEOUT);
+        // let the copies and MMAs still in flight finish before leaving
+        for (int cc = c; cc < issued; ++cc) mbar_wait(&bar[cc & 1], (cc >> 1) & 1, kWaitIters);
+        if (last_mma == 2 && tid == 0) commit(&bar[3]);   // covers every MMA issued so far
+        if (last_mma >= 2) mbar_wait(&bar[3], c & 1, kWaitIters);
+    } else if (args.final_state != nullptr) {
+        float* fs = args.final_state + ((int64_t)n * H + h) * DK * DV;
+#pragma unroll
+        for (int u = 0; u < 64; ++u) fs[(int64_t)(64 * half + u) * DV + row] = S[u];
+    }
+    fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, S_TM_COLS);
+}
+
+// ---------------------------------------------------------------- launch
+template <typename TIn, bool kGated>
+cudaError_t launch_prep(const ChunkArgs& a, const int32_t* hdr, unsigned char* rec,
+                        int64_t units, cudaStream_t stream)
+{
+    auto kern = chunk_prep_kernel<TIn, kGated>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)P_SMEM);
+    if (e != cudaSuccess) return e;
+    kern<<<(unsigned)units, NT, P_SMEM, stream>>>(a, hdr, rec);
+    return cudaGetLastError();
+}
+
+template <typename TOut>
+cudaError_t launch_scan(const ChunkArgs& a, const int32_t* hdr, const unsigned char* rec,
+                        cudaStream_t stream)
+{
+    auto kern = chunk_scan_kernel<TOut>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)S_SMEM);
+    if (e != cudaSuccess) return e;
+    kern<<<(unsigned)((int64_t)a.N * a.H), NT, S_SMEM, stream>>>(a, hdr, rec);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+int64_t split_chunk_bound(int32_t N, int64_t T) { return T / kChunk + N; }
+
+int64_t split_workspace_bytes(int32_t N, int64_t T, int32_t H)
+{
+    return header_bytes(N) + split_chunk_bound(N, T) * H * (int64_t)REC_BYTES;
+}
+
+cudaError_t launch_chunk_split(const ChunkArgs& a, int64_t chunks, cudaStream_t stream)
+{
+    int32_t* hdr = static_cast<int32_t*>(a.workspace);
+    unsigned char* rec = static_cast<unsigned char*>(a.workspace) + header_bytes(a.N);
+    const int64_t units = chunks * a.H;
+    if (units > INT32_MAX || (int64_t)a.N * a.H > INT32_MAX) return cudaErrorInvalidConfiguration;
+    chunk_plan_kernel<<<1, 1024, 0, stream>>>(a.cu_seqlens, a.N, a.T, hdr, a.status);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    if (units > 0) {
+        if (a.gated)
+            e = a.qkv_bf16 ? launch_prep<__nv_bfloat16, true>(a, hdr, rec, units, stream)
+                           : launch_prep<float, true>(a, hdr, rec, units, stream);
+        else
+            e = a.qkv_bf16 ? launch_prep<__nv_bfloat16, false>(a, hdr, rec, units, stream)
+                           : launch_prep<float, false>(a, hdr, rec, units, stream);
+        if (e != cudaSuccess) return e;
+    }
+    return a.out_bf16 ? launch_scan<__nv_bfloat16>(a, hdr, rec, stream)
+                      : launch_scan<float>(a, hdr, rec, stream);
+}
+
+}  // namespace kda

@@ -39,6 +39,9 @@ struct ChunkArgs {
     const float* dt_bias;
     const void* b;
     bool b_bf16;
+    // Two-phase tensor-core path: caller-provided scratch of at least
+    // split_workspace_bytes(N, T, H) bytes (nullptr: single-pass kernel).
+    void* workspace;
 };
 
 struct StepArgs {
@@ -64,6 +67,10 @@ cudaError_t launch_gate(const void* f, bool f_bf16, const float* A_log, const fl
 
 cudaError_t launch_chunk_fp32(const ChunkArgs& a, cudaStream_t stream);
 cudaError_t launch_chunk_tc(const ChunkArgs& a, cudaStream_t stream);
+// Two-phase path; `chunks` bounds the number of chunks over all sequences.
+cudaError_t launch_chunk_split(const ChunkArgs& a, int64_t chunks, cudaStream_t stream);
+int64_t split_chunk_bound(int32_t N, int64_t T);
+int64_t split_workspace_bytes(int32_t N, int64_t T, int32_t H);
 cudaError_t launch_recurrent_step(const StepArgs& a, cudaStream_t stream);
 
 int device_sm_count();

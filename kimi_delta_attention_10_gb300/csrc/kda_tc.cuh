@@ -156,6 +156,26 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* m, uint32_t parity, uint32_t
     return false;
 }
 
+// Arrives on `m` and adds `bytes` to the transaction count its phase waits for.
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* m, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(m)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+// ---------------------------------------------------------------- bulk copy
+// Global -> shared bulk copy through the async proxy (both addresses 16-byte
+// aligned, `bytes` a multiple of 16); completes `bytes` transactions on `m`.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* m)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+            "r"(smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(m))
+        : "memory");
+}
+
 // ---------------------------------------------------------------- cp.async
 // 16-byte global -> shared copy that bypasses registers; `valid` false fills zeros.
 __device__ __forceinline__ void cp_async16(void* dst, const void* src, bool valid)

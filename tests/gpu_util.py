@@ -8,8 +8,24 @@ import oracle
 from kimi_delta_attention_10_gb300 import kda_chunk_fwd, kda_gate
 from kimi_delta_attention_10_gb300.inputs import KDAInputs
 
-# Output tolerances (rel-L2 against the FP64 oracle).
+# Output tolerances (rel-L2 against the FP64 oracle), per mode.
 TOL = {"fp32_exact": 1e-5, "bf16_tc": 3e-3}
+
+# The library's chunk paths: (mode, workspace).  bf16_tc with a workspace is
+# the two-phase path (prepare every chunk, then scan); without one, the
+# single-pass kernel.
+PATHS = {"fp32_exact": ("fp32_exact", None), "bf16_tc": ("bf16_tc", "auto"),
+         "bf16_tc_1pass": ("bf16_tc", None)}
+OUT_DTYPE = {"fp32_exact": torch.float32, "bf16_tc": None, "bf16_tc_1pass": None}
+
+
+def path_kw(path: str) -> dict:
+    mode, ws = PATHS[path]
+    return dict(mode=mode, workspace=ws)
+
+
+def tol(path: str) -> float:
+    return TOL[PATHS[path][0]]
 
 
 def device_inputs(x: KDAInputs, device="cuda"):
@@ -17,13 +33,14 @@ def device_inputs(x: KDAInputs, device="cuda"):
             ("q", "k", "v", "f", "A_log", "dt_bias", "b", "cu_seqlens")}
 
 
-def gpu_pipeline(x: KDAInputs, mode: str, out_dtype=None, host_mirror=True):
+def gpu_pipeline(x: KDAInputs, path: str, out_dtype=None, host_mirror=True):
     """kda_gate then kda_chunk_fwd on the GPU; CPU copies of (out, final_state, g, beta)."""
     d = device_inputs(x)
     g, beta = kda_gate(d["f"], d["A_log"], d["dt_bias"], d["b"])
     out, S = kda_chunk_fwd(d["q"], d["k"], d["v"], g, beta, d["cu_seqlens"], x.scale,
-                           mode=mode, out_dtype=out_dtype,
-                           cu_seqlens_host=x.cu_seqlens.tolist() if host_mirror else None)
+                           out_dtype=out_dtype,
+                           cu_seqlens_host=x.cu_seqlens.tolist() if host_mirror else None,
+                           **path_kw(path))
     torch.cuda.synchronize()
     return out.cpu(), S.cpu(), g.cpu(), beta.cpu()
 

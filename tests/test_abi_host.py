@@ -35,7 +35,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.kda_abi_version() == 2
+    assert lib.kda_abi_version() == 3
     assert binding.status_string(0) == "ok"
     for s in range(1, 7):
         assert binding.status_string(s) not in ("ok", "unknown status")
@@ -49,16 +49,16 @@ MIS = 0x10004
 
 def chunk(lib, **kw):
     a = dict(q=P, k=P, v=P, qkv=1, g=P, beta=P, cu=P, cu_host=None, N=1, T=10, H=2, K=128,
-             V=128, scale=0.1, l2=1, mode=1, out=P, out_dt=1, s0=None, fs=None, status=None,
-             stream=None)
+             V=128, scale=0.1, l2=1, mode=1, out=P, out_dt=1, s0=None, fs=None, ws=None,
+             ws_bytes=0, status=None, stream=None)
     a.update(kw)
     host = a["cu_host"]
     if host is not None:
         host = ctypes.cast((ctypes.c_int32 * len(host))(*host), ctypes.c_void_p)
     return lib.kda_chunk_fwd(a["q"], a["k"], a["v"], a["qkv"], a["g"], a["beta"], a["cu"], host,
                              a["N"], a["T"], a["H"], a["K"], a["V"], a["scale"], a["l2"],
-                             a["mode"], a["out"], a["out_dt"], a["s0"], a["fs"], a["status"],
-                             a["stream"])
+                             a["mode"], a["out"], a["out_dt"], a["s0"], a["fs"], a["ws"],
+                             a["ws_bytes"], a["status"], a["stream"])
 
 
 @pytest.mark.parametrize("kw,expect", [
@@ -84,9 +84,40 @@ def chunk(lib, **kw):
     (dict(cu_host=[1, 10]), binding.KDA_ERR_INVALID_ARG),          # first != 0
     (dict(N=2, cu_host=[0, 7, 5]), binding.KDA_ERR_INVALID_ARG),   # decreasing (and last != T)
     (dict(N=3, cu_host=[0, 7, 5, 10]), binding.KDA_ERR_INVALID_ARG),
+    (dict(mode=0, ws=MIS, ws_bytes=1 << 40), binding.KDA_ERR_ALIGNMENT),
+    (dict(mode=0, ws=P, ws_bytes=1024), binding.KDA_ERR_INVALID_ARG),   # workspace too small
 ])
 def test_chunk_fwd_rejects_bad_arguments(lib, kw, expect):
     assert chunk(lib, **kw) == expect
+
+
+def workspace_size(lib, N, T, H, K=128, V=128, mode=0):
+    out = ctypes.c_int64(-1)
+    st = lib.kda_chunk_workspace_size(N, T, H, K, V, mode, ctypes.byref(out))
+    return st, out.value
+
+
+def test_workspace_size_bound():
+    """The size covers the worst case of T / 64 + N chunks (every sequence
+    adds at most one partial chunk) and a 1 KiB-aligned offsets header."""
+    lib = binding.load_library()
+    rec = 74240
+    for N, T, H in [(1, 16384, 64), (16, 32768, 64), (3, 65, 4), (0, 0, 1), (5000, 70000, 2)]:
+        st, nbytes = workspace_size(lib, N, T, H)
+        assert st == binding.KDA_OK
+        hdr = -(-(4 * (N + 5)) // 1024) * 1024
+        assert nbytes == hdr + (T // 64 + N) * H * rec
+        # the exact chunk count of any split of T tokens into N sequences is no larger
+        lens = [T // max(N, 1)] * N
+        if N:
+            lens[-1] += T - sum(lens)
+        assert sum(-(-L // 64) for L in lens) <= T // 64 + N
+    assert workspace_size(lib, 2, 100, 3, mode=1) == (binding.KDA_OK, 0)
+    assert workspace_size(lib, 2, 100, 3, K=64)[0] == binding.KDA_ERR_UNSUPPORTED
+    assert workspace_size(lib, -1, 100, 3)[0] == binding.KDA_ERR_INVALID_ARG
+    assert workspace_size(lib, 2, 100, 3, mode=7)[0] == binding.KDA_ERR_INVALID_ARG
+    assert lib.kda_chunk_workspace_size(1, 10, 1, 128, 128, 0, None) == binding.KDA_ERR_INVALID_ARG
+    assert binding.chunk_workspace_size(1, 16384, 64) == workspace_size(lib, 1, 16384, 64)[1]
 
 
 def gate(lib, **kw):
@@ -127,7 +158,8 @@ def gated(lib, **kw):
     return lib.kda_chunk_fwd_gated(a["q"], a["k"], a["v"], a["qkv"], a["f"], a["fdt"], a["A"],
                                    a["dt"], a["b"], a["bdt"], a["cu"], None, a["N"], a["T"],
                                    a["H"], a["K"], a["V"], 0.1, 1, a["mode"], a["out"],
-                                   a["out_dt"], a["s0"], a["fs"], None, None)
+                                   a["out_dt"], a["s0"], a["fs"], a.get("ws"), a.get("ws_bytes", 0),
+                                   None, None)
 
 
 @pytest.mark.parametrize("kw,expect", [
@@ -139,6 +171,7 @@ def gated(lib, **kw):
     (dict(b=MIS), binding.KDA_ERR_ALIGNMENT),
     (dict(K=64), binding.KDA_ERR_UNSUPPORTED),
     (dict(mode=3), binding.KDA_ERR_INVALID_ARG),
+    (dict(ws=P, ws_bytes=100), binding.KDA_ERR_INVALID_ARG),
 ])
 def test_chunk_fwd_gated_rejects_bad_arguments(lib, kw, expect):
     assert gated(lib, **kw) == expect

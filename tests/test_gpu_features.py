@@ -8,12 +8,12 @@ from kimi_delta_attention_10_gb300 import (kda_chunk_fwd, kda_chunk_fwd_gated, k
                                            kda_recurrent_step)
 from kimi_delta_attention_10_gb300.inputs import make_inputs, workload_inputs
 
-from gpu_util import TOL, device_inputs, f64, oracle_pipeline, rel_l2
+from gpu_util import (OUT_DTYPE, PATHS, device_inputs, f64, oracle_pipeline, path_kw, rel_l2,
+                      tol)
 
 pytestmark = pytest.mark.gpu
 
-MODES = ["fp32_exact", "bf16_tc"]
-OUT_DTYPE = {"fp32_exact": torch.float32, "bf16_tc": None}
+MODES = list(PATHS)
 
 
 def _small(lens, H=4, seed=0, dtype=torch.bfloat16):
@@ -28,10 +28,10 @@ def test_gated_equals_gate_then_chunk_bitwise(case, mode):
     d = device_inputs(x)
     g, beta = kda_gate(d["f"], d["A_log"], d["dt_bias"], d["b"])
     o1, s1 = kda_chunk_fwd(d["q"], d["k"], d["v"], g, beta, d["cu_seqlens"], x.scale,
-                           mode=mode, out_dtype=OUT_DTYPE[mode])
+                           out_dtype=OUT_DTYPE[mode], **path_kw(mode))
     o2, s2 = kda_chunk_fwd_gated(d["q"], d["k"], d["v"], d["f"], d["A_log"], d["dt_bias"],
-                                 d["b"], d["cu_seqlens"], x.scale, mode=mode,
-                                 out_dtype=OUT_DTYPE[mode])
+                                 d["b"], d["cu_seqlens"], x.scale, out_dtype=OUT_DTYPE[mode],
+                                 **path_kw(mode))
     torch.cuda.synchronize()
     assert torch.equal(o1, o2) and torch.equal(s1, s2)
 
@@ -41,11 +41,11 @@ def test_gated_matches_oracle(mode):
     x = workload_inputs("single_2048_bf16")
     d = device_inputs(x)
     out, S = kda_chunk_fwd_gated(d["q"], d["k"], d["v"], d["f"], d["A_log"], d["dt_bias"],
-                                 d["b"], d["cu_seqlens"], x.scale, mode=mode,
-                                 out_dtype=OUT_DTYPE[mode], cu_seqlens_host=x.cu_seqlens.tolist())
+                                 d["b"], d["cu_seqlens"], x.scale, out_dtype=OUT_DTYPE[mode],
+                                 cu_seqlens_host=x.cu_seqlens.tolist(), **path_kw(mode))
     o_ref, S_ref, _, _ = oracle_pipeline(x)
-    assert rel_l2(out.cpu().double().numpy(), o_ref) <= TOL[mode]
-    assert rel_l2(S.cpu().double().numpy(), S_ref) <= TOL[mode]
+    assert rel_l2(out.cpu().double().numpy(), o_ref) <= tol(mode)
+    assert rel_l2(S.cpu().double().numpy(), S_ref) <= tol(mode)
 
 
 def test_gated_bf16_beta_logits():
@@ -68,13 +68,13 @@ def test_initial_state_matches_oracle(mode):
     S0 = torch.randn(len(lens), x.H, 128, 128, generator=gen) * 0.2
     d = device_inputs(x)
     g, beta = kda_gate(d["f"], d["A_log"], d["dt_bias"], d["b"])
-    out, S = kda_chunk_fwd(d["q"], d["k"], d["v"], g, beta, d["cu_seqlens"], x.scale, mode=mode,
-                           out_dtype=OUT_DTYPE[mode], initial_state=S0.cuda())
+    out, S = kda_chunk_fwd(d["q"], d["k"], d["v"], g, beta, d["cu_seqlens"], x.scale,
+                           out_dtype=OUT_DTYPE[mode], initial_state=S0.cuda(), **path_kw(mode))
     gr, br = oracle.gate(f64(x.f), f64(x.A_log), f64(x.dt_bias), f64(x.b))
     o_ref, S_ref = oracle.forward(f64(x.q), f64(x.k), f64(x.v), gr, br, x.cu_seqlens.numpy(),
                                   x.scale, initial_state=S0.double().numpy())
-    assert rel_l2(out.cpu().double().numpy(), o_ref) <= TOL[mode]
-    assert rel_l2(S.cpu().double().numpy(), S_ref) <= TOL[mode]
+    assert rel_l2(out.cpu().double().numpy(), o_ref) <= tol(mode)
+    assert rel_l2(S.cpu().double().numpy(), S_ref) <= tol(mode)
     # the empty sequence returns its initial state
     assert torch.equal(S[1].cpu(), S0[1])
 
@@ -86,7 +86,7 @@ def test_split_at_chunk_boundary_is_bitwise(mode):
     x = _small([200], seed=24)
     d = device_inputs(x)
     g, beta = kda_gate(d["f"], d["A_log"], d["dt_bias"], d["b"])
-    kw = dict(mode=mode, out_dtype=OUT_DTYPE[mode])
+    kw = dict(out_dtype=OUT_DTYPE[mode], **path_kw(mode))
     o, S = kda_chunk_fwd(d["q"], d["k"], d["v"], g, beta, d["cu_seqlens"], x.scale, **kw)
     cut = 128
     c1 = torch.tensor([0, cut], dtype=torch.int32, device="cuda")
@@ -130,8 +130,8 @@ def test_chunk_prefill_then_decode_matches_oracle(mode):
     c = torch.tensor([0, pre], dtype=torch.int32, device="cuda")
     _, S = kda_chunk_fwd(d["q"][:pre].contiguous(), d["k"][:pre].contiguous(),
                          d["v"][:pre].contiguous(), g[:pre].contiguous(),
-                         beta[:pre].contiguous(), c, x.scale, mode=mode,
-                         out_dtype=OUT_DTYPE[mode])
+                         beta[:pre].contiguous(), c, x.scale, out_dtype=OUT_DTYPE[mode],
+                         **path_kw(mode))
     outs = []
     for t in range(pre, T):
         sl = lambda z: z[t:t + 1].clone()           # fresh, 16-byte-aligned storage
@@ -139,5 +139,5 @@ def test_chunk_prefill_then_decode_matches_oracle(mode):
                                        x.scale, out_dtype=torch.float32))
     o_ref, S_ref, _, _ = oracle_pipeline(x)
     o_dec = torch.cat(outs).cpu().double().numpy()
-    assert rel_l2(o_dec, o_ref[pre:]) <= TOL[mode]
-    assert rel_l2(S.cpu().double().numpy(), S_ref) <= TOL[mode]
+    assert rel_l2(o_dec, o_ref[pre:]) <= tol(mode)
+    assert rel_l2(S.cpu().double().numpy(), S_ref) <= tol(mode)

@@ -10,7 +10,8 @@ import oracle
 from kimi_delta_attention_10_gb300 import kda_chunk_fwd, kda_gate
 from kimi_delta_attention_10_gb300.inputs import WORKLOADS, make_inputs, workload_inputs
 
-from gpu_util import TOL, device_inputs, f64, gpu_pipeline, oracle_pipeline, rel_l2
+from gpu_util import (OUT_DTYPE, PATHS, device_inputs, f64, gpu_pipeline, oracle_pipeline,
+                      path_kw, rel_l2, tol)
 
 pytestmark = pytest.mark.gpu
 
@@ -61,8 +62,7 @@ def test_gate_extremes_and_bf16_inputs():
         assert np.max(np.abs(beta.cpu().double().numpy() - b_ref) / b_ref) < 2e-6
 
 
-MODES = ["fp32_exact", "bf16_tc"]
-OUT_DTYPE = {"fp32_exact": torch.float32, "bf16_tc": None}   # None: the activation dtype
+MODES = list(PATHS)     # fp32_exact, bf16_tc (two-phase), bf16_tc_1pass (single-pass)
 
 
 @pytest.mark.parametrize("mode", MODES)
@@ -80,7 +80,7 @@ def test_chunk_matches_oracle(wi, mode):
     assert np.isfinite(o_gpu).all() and np.isfinite(S_gpu).all()
     e_o, e_S = rel_l2(o_gpu, o_ref), rel_l2(S_gpu, S_ref)
     print(f"{WORKLOADS[wi].name} {mode}: out rel-L2 {e_o:.3e}, final state rel-L2 {e_S:.3e}")
-    assert e_o <= TOL[mode] and e_S <= TOL[mode]
+    assert e_o <= tol(mode) and e_S <= tol(mode)
 
 
 def _small(lens, H=4, seed=0, dtype=torch.bfloat16):
@@ -94,8 +94,8 @@ def test_chunk_edge_lengths(lens, mode):
     out, S, _, _ = gpu_pipeline(x, mode, out_dtype=OUT_DTYPE[mode])
     o_ref, S_ref, _, _ = oracle_pipeline(x)
     if x.T:
-        assert rel_l2(out.double().numpy(), o_ref) <= TOL[mode]
-    assert rel_l2(S.double().numpy(), S_ref) <= TOL[mode]
+        assert rel_l2(out.double().numpy(), o_ref) <= tol(mode)
+    assert rel_l2(S.double().numpy(), S_ref) <= tol(mode)
     for n, L in enumerate(lens):
         if L == 0:
             assert torch.count_nonzero(S[n]) == 0
@@ -114,8 +114,8 @@ def test_packing_is_bitwise_per_sequence(mode):
         cu1 = torch.tensor([0, z - a], dtype=torch.int32, device="cuda")
         o1, S1 = kda_chunk_fwd(d["q"][a:z].contiguous(), d["k"][a:z].contiguous(),
                                d["v"][a:z].contiguous(), g[a:z].contiguous(),
-                               beta[a:z].contiguous(), cu1, x.scale, mode=mode,
-                               out_dtype=OUT_DTYPE[mode])
+                               beta[a:z].contiguous(), cu1, x.scale,
+                               out_dtype=OUT_DTYPE[mode], **path_kw(mode))
         assert torch.equal(o1.cpu(), out[a:z]) and torch.equal(S1.cpu()[0], S[n])
 
 
@@ -143,12 +143,12 @@ def test_without_l2norm_on_prenormalised_inputs(mode):
     d = device_inputs(x)
     g, beta = kda_gate(d["f"], d["A_log"], d["dt_bias"], d["b"])
     out, S = kda_chunk_fwd(d["q"], d["k"], d["v"], g, beta, d["cu_seqlens"], x.scale,
-                           mode=mode, qk_l2norm=False)
+                           qk_l2norm=False, **path_kw(mode))
     g_ref, b_ref = oracle.gate(f64(x.f), f64(x.A_log), f64(x.dt_bias), f64(x.b))
     o_ref, S_ref = oracle.forward(f64(x.q), f64(x.k), f64(x.v), g_ref, b_ref,
                                   x.cu_seqlens.numpy(), x.scale, l2norm=False)
-    assert rel_l2(out.cpu().double().numpy(), o_ref) <= TOL[mode]
-    assert rel_l2(S.cpu().double().numpy(), S_ref) <= TOL[mode]
+    assert rel_l2(out.cpu().double().numpy(), o_ref) <= tol(mode)
+    assert rel_l2(S.cpu().double().numpy(), S_ref) <= tol(mode)
 
 
 def test_bf16_output_in_fp32_mode():
@@ -170,10 +170,10 @@ def test_device_detects_bad_offsets_without_host_mirror(mode):
     bad = torch.tensor([0, 40, 90], dtype=torch.int32, device="cuda")   # 90 > T = 70
     status = torch.zeros(4, dtype=torch.int32, device="cuda")
     out = torch.zeros(70, 2, 128, device="cuda")
-    kda_chunk_fwd(d["q"], d["k"], d["v"], g, beta, bad, x.scale, mode=mode, out=out,
-                  status=status)
+    kda_chunk_fwd(d["q"], d["k"], d["v"], g, beta, bad, x.scale, out=out, status=status,
+                  **path_kw(mode))
     torch.cuda.synchronize()
     assert int(status[0]) == 6
     o_ref, _, _, _ = oracle_pipeline(x)
-    assert rel_l2(out[:40].cpu().double().numpy(), o_ref[:40]) <= TOL[mode]
+    assert rel_l2(out[:40].cpu().double().numpy(), o_ref[:40]) <= tol(mode)
     assert torch.count_nonzero(out[40:]) == 0
