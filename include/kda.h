@@ -49,7 +49,8 @@ typedef enum {
     KDA_ERR_ALIGNMENT = 3,     /* a device pointer is not 16-byte aligned          */
     KDA_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed             */
     KDA_ERR_TIMEOUT = 5,       /* device: a bounded wait gave up (status word)     */
-    KDA_ERR_DEVICE_ARG = 6     /* device: offsets outside [0, T] (status word)     */
+    KDA_ERR_DEVICE_ARG = 6,    /* device: offsets outside [0, T] (status word)     */
+    KDA_ERR_TOO_LARGE = 7      /* kda_chunk_fwd_static: over its static scratch    */
 } kda_status;
 
 typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype;
@@ -189,6 +190,35 @@ kda_status kda_chunk_fwd_gated(const void* q, const void* k, const void* v, int3
                                void* out, int32_t out_dtype, const float* initial_state,
                                float* final_state, void* workspace, int64_t workspace_bytes,
                                int32_t* status_dev, kda_stream_t stream);
+
+/*
+ * kda_chunk_fwd_static -- kda_chunk_fwd in KDA_MODE_BF16_TC, two-phase, with
+ * the library's own scratch instead of a caller workspace.  The pages have no
+ * counterpart: this is an interface for callers that cannot allocate device
+ * memory per call -- a process whose device-memory budget is fixed up front
+ * (e.g. a server that has handed the rest of HBM to its caches), or C code
+ * with no allocator of its own, for which a cudaMalloc/cudaFree pair per call
+ * would also synchronise the device.
+ *
+ * The scratch is one file-scope device array of 64 MiB in the library, so
+ * the call allocates nothing.  A problem whose kda_chunk_workspace_size(...)
+ * exceeds 64 MiB is rejected with KDA_ERR_TOO_LARGE before anything is
+ * launched (for H = 64: T / 64 + N must not exceed 14).
+ * The first call on a device does set-up (it looks up the array's device
+ * address, which may load the library's device code), so make it before any
+ * stream capture.  Every call on a device uses the same scratch: calls that
+ * overlap in time (on different streams, or from different host threads
+ * without ordering) race on it and give undefined results.  Nothing in the
+ * scratch needs to start at zero.  The result equals kda_chunk_fwd with mode
+ * KDA_MODE_BF16_TC and a workspace, bit for bit.  Arguments as kda_chunk_fwd.
+ */
+kda_status kda_chunk_fwd_static(const void* q, const void* k, const void* v, int32_t qkv_dtype,
+                                const float* g, const float* beta,
+                                const int32_t* cu_seqlens, const int32_t* cu_seqlens_host,
+                                int32_t N, int64_t T, int32_t H, int32_t K, int32_t V,
+                                float scale, int32_t qk_l2norm, void* out, int32_t out_dtype,
+                                const float* initial_state, float* final_state,
+                                int32_t* status_dev, kda_stream_t stream);
 
 /*
  * kda_recurrent_step -- one token of the recurrence for each of N sequences

@@ -22,6 +22,7 @@ KDA_ERR_ALIGNMENT = 3
 KDA_ERR_CUDA = 4
 KDA_ERR_TIMEOUT = 5
 KDA_ERR_DEVICE_ARG = 6
+KDA_ERR_TOO_LARGE = 7
 
 KDA_F32 = 0
 KDA_BF16 = 1
@@ -33,7 +34,7 @@ MODES = {"bf16_tc": KDA_MODE_BF16_TC, "fp32_exact": KDA_MODE_FP32_EXACT}
 
 # Every symbol include/kda.h declares.
 EXPORTS = ("kda_gate", "kda_chunk_workspace_size", "kda_chunk_fwd", "kda_chunk_fwd_gated",
-           "kda_recurrent_step", "kda_status_string", "kda_abi_version")
+           "kda_chunk_fwd_static", "kda_recurrent_step", "kda_status_string", "kda_abi_version")
 
 _lock = threading.Lock()
 _lib = None
@@ -75,6 +76,9 @@ def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
                                             i32, i64, i32, i32, i32, ctypes.c_float, i32, i32,
                                             vp, i32, vp, vp, vp, i64, vp, vp]
         lib.kda_chunk_fwd_gated.restype = i32
+        lib.kda_chunk_fwd_static.argtypes = [vp, vp, vp, i32, vp, vp, vp, vp, i32, i64, i32, i32,
+                                             i32, ctypes.c_float, i32, vp, i32, vp, vp, vp, vp]
+        lib.kda_chunk_fwd_static.restype = i32
         lib.kda_recurrent_step.argtypes = [vp, vp, vp, i32, vp, vp, i32, i32, i32, i32,
                                            ctypes.c_float, i32, vp, vp, i32, vp]
         lib.kda_recurrent_step.restype = i32
@@ -244,6 +248,35 @@ def kda_chunk_fwd_gated(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, f: to
     if st != KDA_OK:
         raise KDAError(st, "kda_chunk_fwd_gated")
     return out, final_state
+
+
+def kda_chunk_fwd_static(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor,
+                         beta: torch.Tensor, cu_seqlens: torch.Tensor, out: torch.Tensor,
+                         scale: Optional[float] = None,
+                         final_state: Optional[torch.Tensor] = None,
+                         initial_state: Optional[torch.Tensor] = None,
+                         cu_seqlens_host: Optional[Sequence[int]] = None, qk_l2norm: bool = True,
+                         status: Optional[torch.Tensor] = None,
+                         stream: Optional[torch.cuda.Stream] = None) -> None:
+    """kda_chunk_fwd (bf16_tc, two-phase) on the library's static scratch: allocates
+    nothing, so `out` (and `final_state`, if wanted) are the caller's.  Problems
+    beyond the 64 MiB scratch raise KDAError(KDA_ERR_TOO_LARGE)."""
+    lib = load_library()
+    T, H, K = q.shape
+    V = v.shape[2]
+    N = cu_seqlens.numel() - 1
+    if scale is None:
+        scale = K ** -0.5
+    keep, host = _host_offsets(cu_seqlens_host)
+    st = lib.kda_chunk_fwd_static(
+        _dev_ptr(q, "q"), _dev_ptr(k, "k"), _dev_ptr(v, "v"), _dtype_code(q),
+        _dev_ptr(g, "g"), _dev_ptr(beta, "beta"), _dev_ptr(cu_seqlens, "cu_seqlens"), host,
+        N, T, H, K, V, float(scale), 1 if qk_l2norm else 0,
+        _dev_ptr(out, "out"), _dtype_code(out), _dev_ptr(initial_state, "initial_state"),
+        _dev_ptr(final_state, "final_state"), _dev_ptr(status, "status"),
+        _stream_handle(stream, q.device))
+    if st != KDA_OK:
+        raise KDAError(st, "kda_chunk_fwd_static")
 
 
 def kda_recurrent_step(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor,

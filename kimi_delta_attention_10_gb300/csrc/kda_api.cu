@@ -39,6 +39,8 @@ const char* kda_status_string(int32_t s)
         case KDA_ERR_CUDA: return "CUDA error";
         case KDA_ERR_TIMEOUT: return "device wait timed out";
         case KDA_ERR_DEVICE_ARG: return "device saw offsets outside [0, T]";
+        case KDA_ERR_TOO_LARGE:
+            return "problem needs more than the 64 MiB static scratch of kda_chunk_fwd_static";
         default: return "unknown status";
     }
 }
@@ -198,6 +200,31 @@ kda_status kda_chunk_fwd_gated(const void* q, const void* k, const void* v, int3
     a.b = b;
     a.b_bf16 = b_dtype == KDA_BF16;
     return launch_chunk(a, mode, cu_seqlens_host, workspace, workspace_bytes, stream);
+}
+
+kda_status kda_chunk_fwd_static(const void* q, const void* k, const void* v, int32_t qkv_dtype,
+                                const float* g, const float* beta,
+                                const int32_t* cu_seqlens, const int32_t* cu_seqlens_host,
+                                int32_t N, int64_t T, int32_t H, int32_t K, int32_t V,
+                                float scale, int32_t qk_l2norm, void* out, int32_t out_dtype,
+                                const float* initial_state, float* final_state,
+                                int32_t* status_dev, kda_stream_t stream)
+{
+    kda_status st = check_chunk(q, k, v, qkv_dtype, cu_seqlens, cu_seqlens_host, N, T, H, K, V,
+                                qk_l2norm, KDA_MODE_BF16_TC, out, out_dtype, initial_state,
+                                final_state, status_dev);
+    if (st != KDA_OK) return st;
+    if (T > 0 && (!g || !beta)) return KDA_ERR_INVALID_ARG;
+    if ((g && !aligned16(g)) || (beta && !aligned16(beta))) return KDA_ERR_ALIGNMENT;
+    if (kda::split_workspace_bytes(N, T, H) > kda::kStaticScratchBytes) return KDA_ERR_TOO_LARGE;
+    if (N == 0) return KDA_OK;
+    void* scratch = nullptr;
+    if (kda::static_scratch(&scratch) != cudaSuccess) return KDA_ERR_CUDA;
+    kda::ChunkArgs a = chunk_args(q, k, v, qkv_dtype, cu_seqlens, N, T, H, scale, qk_l2norm, out,
+                                  out_dtype, initial_state, final_state, status_dev);
+    a.g = g; a.beta = beta; a.gated = false;
+    return launch_chunk(a, KDA_MODE_BF16_TC, cu_seqlens_host, scratch, kda::kStaticScratchBytes,
+                        stream);
 }
 
 kda_status kda_recurrent_step(const void* q, const void* k, const void* v, int32_t qkv_dtype,

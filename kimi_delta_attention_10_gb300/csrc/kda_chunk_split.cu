@@ -30,6 +30,9 @@
 #include <cuda_fp16.h>
 #include <stdint.h>
 
+#include <atomic>
+#include <mutex>
+
 #include "kda_internal.cuh"
 #include "kda_tc.cuh"
 #include "kda_chunk_ops.cuh"
@@ -628,7 +631,38 @@ cudaError_t launch_scan(const ChunkArgs& a, const int32_t* hdr, const unsigned c
     return cudaGetLastError();
 }
 
+// Scratch of the no-allocation entry point (kda_chunk_fwd_static): a
+// file-scope device array, so that call allocates nothing.  Nothing in it has
+// to start at zero: the plan kernel writes the whole header and the
+// preparation writes every record the scan reads.
+__device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::atomic<void*> g_static_scratch_ptr[kMaxDevices];
+std::mutex g_static_scratch_mu;
+
 }  // namespace
+
+cudaError_t static_scratch(void** ptr)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    void* p = g_static_scratch_ptr[dev].load(std::memory_order_acquire);
+    if (p == nullptr) {
+        // set-up, once per device, with that device current
+        std::lock_guard<std::mutex> lock(g_static_scratch_mu);
+        p = g_static_scratch_ptr[dev].load(std::memory_order_relaxed);
+        if (p == nullptr) {
+            e = cudaGetSymbolAddress(&p, g_static_scratch);
+            if (e != cudaSuccess) return e;
+            g_static_scratch_ptr[dev].store(p, std::memory_order_release);
+        }
+    }
+    *ptr = p;
+    return cudaSuccess;
+}
 
 int64_t split_chunk_bound(int32_t N, int64_t T) { return T / kChunk + N; }
 

@@ -71,6 +71,10 @@ cudaError_t launch_chunk_tc(const ChunkArgs& a, cudaStream_t stream);
 cudaError_t launch_chunk_split(const ChunkArgs& a, int64_t chunks, cudaStream_t stream);
 int64_t split_chunk_bound(int32_t N, int64_t T);
 int64_t split_workspace_bytes(int32_t N, int64_t T, int32_t H);
+// The static scratch of kda_chunk_fwd_static and its size; static_scratch()
+// returns its address on the current device (looked up once per device).
+constexpr int64_t kStaticScratchBytes = 64ll << 20;
+cudaError_t static_scratch(void** ptr);
 cudaError_t launch_recurrent_step(const StepArgs& a, cudaStream_t stream);
 
 int device_sm_count();

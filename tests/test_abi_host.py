@@ -37,7 +37,7 @@ def test_library_exports_every_declared_symbol(lib):
 def test_abi_version_and_status_strings(lib):
     assert lib.kda_abi_version() == 3
     assert binding.status_string(0) == "ok"
-    for s in range(1, 7):
+    for s in range(1, 8):
         assert binding.status_string(s) not in ("ok", "unknown status")
     assert binding.status_string(99) == "unknown status"
 
@@ -195,3 +195,41 @@ def step(lib, **kw):
 ])
 def test_recurrent_step_rejects_bad_arguments(lib, kw, expect):
     assert step(lib, **kw) == expect
+
+
+def static(lib, **kw):
+    a = dict(q=P, k=P, v=P, qkv=1, g=P, beta=P, cu=P, N=1, T=10, H=2, K=128, V=128, out=P,
+             out_dt=1)
+    a.update(kw)
+    return lib.kda_chunk_fwd_static(a["q"], a["k"], a["v"], a["qkv"], a["g"], a["beta"], a["cu"],
+                                    None, a["N"], a["T"], a["H"], a["K"], a["V"], 0.1, 1,
+                                    a["out"], a["out_dt"], None, None, None, None)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(K=64), binding.KDA_ERR_UNSUPPORTED),
+    (dict(g=None), binding.KDA_ERR_INVALID_ARG),
+    (dict(beta=MIS), binding.KDA_ERR_ALIGNMENT),
+    # over the 64 MiB static scratch: (T / 64 + N) * H records of 74240 bytes
+    (dict(T=1024, N=1, H=64), binding.KDA_ERR_TOO_LARGE),
+    (dict(T=64 * 14, N=1, H=64), binding.KDA_ERR_TOO_LARGE),
+])
+def test_chunk_fwd_static_rejects_bad_arguments(lib, kw, expect):
+    assert static(lib, **kw) == expect
+
+
+def test_static_scratch_limit_is_the_workspace_bound(lib):
+    """The largest problems the static scratch admits are the ones whose
+    workspace bound fits in 64 MiB."""
+    for H in (1, 8, 64):
+        lo, hi = 0, 1 << 20                   # chunk counts: lo fits, hi does not
+        while hi - lo > 1:
+            mid = (lo + hi) // 2
+            if workspace_size(lib, 1, 64 * mid, H)[1] <= (64 << 20):
+                lo = mid
+            else:
+                hi = mid
+        assert static(lib, T=64 * hi, N=1, H=H) == binding.KDA_ERR_TOO_LARGE
+        # at the limit the call gets past the size check (without a GPU it then
+        # fails at the device set-up instead)
+        assert static(lib, T=64 * lo, N=1, H=H) != binding.KDA_ERR_TOO_LARGE
