@@ -201,7 +201,8 @@ kda_status kda_chunk_fwd_gated(const void* q, const void* k, const void* v, int3
  * would also synchronise the device.
  *
  * The scratch is one file-scope device array of 64 MiB in the library, so
- * the call allocates nothing.  A problem whose kda_chunk_workspace_size(...)
+ * the call allocates nothing; every GPU that loads the library holds those
+ * 64 MiB until the process exits, and they keep the last call's contents.  A problem whose kda_chunk_workspace_size(...)
  * exceeds 64 MiB is rejected with KDA_ERR_TOO_LARGE before anything is
  * launched (for H = 64: T / 64 + N must not exceed 14).
  * The first call on a device does set-up (it looks up the array's device

@@ -635,7 +635,10 @@ cudaError_t launch_scan(const ChunkArgs& a, const int32_t* hdr, const unsigned c
 // file-scope device array, so that call allocates nothing.  Nothing in it has
 // to start at zero: the plan kernel writes the whole header and the
 // preparation writes every record the scan reads.
-__device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+// Every GPU that loads the library holds these bytes until the process exits,
+// and they keep the last call's contents.  In host code the name is only a
+// host-side stand-in: the device address comes from cudaGetSymbolAddress.
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
 
 constexpr int kMaxDevices = 64;
 std::atomic<void*> g_static_scratch_ptr[kMaxDevices];
