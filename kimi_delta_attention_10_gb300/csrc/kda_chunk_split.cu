@@ -18,12 +18,13 @@
 // copy, double-buffered, while it works on the one before.  A plan kernel
 // first turns cu_seqlens into per-sequence chunk offsets.
 //
-// Record of one unit (bytes):
-//   W       fp16 [128 c][64 i]  (the B operand of [W S]^T = S^T W^T, MN-major)
-//   Q'      fp16 [128 c][64 i]  (B of [Q' S]^T, MN-major)
+// Record of one unit (bytes), in this order:
+//   W       fp16 [128 c][64 i]  \ together the MN-major B operand of
+//   Q'      fp16 [128 c][64 i]  / [W S | Q' S]^T = S^T [W; Q']^T (N = 128)
 //   U^T     fp16 [128 v][64 i]  (row v read by the thread of state row v)
-//   K''^T   fp16 [128 c][64 j]  (B of P^T = Delta^T K'', K-major)
-//   A_qk    fp16 [64 i][64 j]   (B of Delta^T A_qk^T, K-major; strictly upper part 0)
+//   A_qk    fp16 [64 i][64 j]   \ together the K-major B operand of
+//   K''^T   fp16 [128 c][64 j]  / [A_qk Delta | K''^T Delta]^T (N = 192);
+//                                 A_qk's strictly upper part is 0
 //   d       fp32 [128]
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
@@ -48,10 +49,10 @@ constexpr int DV = kHeadV;
 constexpr uint32_t kWaitIters = 1u << 22;   // polls before a wait gives up
 
 constexpr uint32_t REC_W = 0;
-constexpr uint32_t REC_QP = 16384;
+constexpr uint32_t REC_QP = 16384;     // = REC_W + 16 KiB: [W; Q'] is one N = 128 operand
 constexpr uint32_t REC_U = 32768;
-constexpr uint32_t REC_KT = 49152;
-constexpr uint32_t REC_AQK = 65536;
+constexpr uint32_t REC_AQK = 49152;
+constexpr uint32_t REC_KT = 57344;     // = REC_AQK + 8 KiB: [A_qk; K''^T] is one N = 192 operand
 constexpr uint32_t REC_DEC = 73728;
 constexpr uint32_t REC_BYTES = 74240;
 static_assert(REC_BYTES % 16 == 0 && REC_BYTES < (1u << 20), "bulk copy size");
@@ -291,14 +292,9 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(ChunkArgs args,
         tot[hh * DK + ch] = p;
     }
     __syncthreads();
-    {
-        const float before = hh ? tot[ch] : 1.f;
-        const float after = hh ? 1.f : tot[DK + ch];
-        if (hh == 0) reinterpret_cast<float*>(rec + REC_DEC)[ch] = tot[ch] * tot[DK + ch];
-        channel_rows(sm + P_XT, rec + REC_QP, rec + REC_KT, ch, hh, before, after, a, kh, qh);
-    }
 
-    // ---- 4: pair sums, three rounds through one operand buffer
+    // ---- 4: pair sums, three rounds through one operand buffer; the
+    // per-channel rows and the zeroing of A_qk's upper part run beside the MMAs
     bool failed = false;
     int last_bar = -1;
     constexpr uint32_t id_pairs = idesc(kFmtF16, 128, 64, true, true);
@@ -325,10 +321,18 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(ChunkArgs args,
         level32_operands(sm + P_PAIR, ch, hh, a, kh, qh);
         level_operands<16>(sm + P_PAIR, ch, hh, 64, 32, a, kh, qh);
         issue_round(0);
+        {
+            // X'^T (shared, over the dead g staging), Q' and K''^T (record), d
+            const float before = hh ? tot[ch] : 1.f;
+            const float after = hh ? 1.f : tot[DK + ch];
+            if (hh == 0) reinterpret_cast<float*>(rec + REC_DEC)[ch] = tot[ch] * tot[DK + ch];
+            channel_rows(sm + P_XT, rec + REC_QP, rec + REC_KT, ch, hh, before, after, a, kh, qh);
+        }
         if (!wait_bar(0)) { failed = true; break; }
         level_operands<8>(sm + P_PAIR, ch, hh, 0, 0, a, kh, qh);
         level_operands<4>(sm + P_PAIR, ch, hh, 64, 32, a, kh, qh);
         issue_round(1);
+        aqk_zero_upper(sm + P_AQK, tid);
         if (!wait_bar(1)) { failed = true; break; }
         level_operands<2>(sm + P_PAIR, ch, hh, 0, 0, a, kh, qh);
         level_operands<1>(sm + P_PAIR, ch, hh, 64, 32, a, kh, qh);
@@ -343,7 +347,6 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(ChunkArgs args,
         fence_after_sync();
 
         // ---- 5: A_kk (fp32) and A_qk (fp16) from TMEM
-        aqk_zero_upper(sm + P_AQK, tid);
         extract_pairs(sm + P_AQK, &akk[0][0], sbeta, dqk, tlane, P_TM_A, tid, warp, lane);
         fence_before_sync();
         __syncthreads();
@@ -400,23 +403,41 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(ChunkArgs args,
 }
 
 // ---------------------------------------------------------------- scan
-constexpr uint32_t S_ST = 0;                 // S^T fp16 K-major [128 v][128 c]
-constexpr uint32_t S_DT = 32768;             // Delta^T fp16 K-major [128 v][64 i]
-constexpr uint32_t S_STG = 49152;            // two record stages
-constexpr uint32_t S_STG_STRIDE = 74752;     // REC_BYTES rounded up to 1024
-constexpr uint32_t S_BAR = S_STG + 2 * S_STG_STRIDE;   // full[2], ws, op + TMEM slot
+// One CTA per (sequence, head): eight epilogue warps (thread = state row v and
+// a half of the columns) and one control warp whose lane 0 issues the bulk
+// copies and the MMAs.  Per chunk c (TMEM region R = 256 (c & 1)):
+//   control:  record c in stage c & 1 (bulk copy, issued a chunk ahead)
+//             [W S | Q' S]^T -> R .. R + 127       (8 MMAs, N = 128)
+//   epilogue: Delta^T = U^T - [W S]^T -> shared (fp16), arrive delta_ready
+//   control:  [O | P]^T += Delta^T [A_qk; K''^T]^T -> R + 64 .. R + 255 (4 MMAs,
+//             N = 192: O accumulates on Q' S, P on zero)
+//   epilogue: S^T <- S^T Diag(d) + P^T, the fp16 copy of S^T for the next
+//             chunk, P zeroed again; arrive s_ready; then chunk c's output,
+//             while the control warp issues chunk c + 1's MMAs into the other
+//             region
+// so the state's chain per chunk is two MMA groups and two short epilogues.
+constexpr int SCAN_THREADS = NT + 32;
+constexpr int kL2Ahead = 4;                   // records prefetched into L2 this many chunks ahead
+constexpr uint32_t kEpiBar = 1;               // named barrier of the 256 epilogue threads
+constexpr uint32_t S_ST = 0;                  // S^T fp16 K-major [128 v][128 c]
+constexpr uint32_t S_DT = 32768;              // Delta^T fp16 K-major [128 v][64 i]
+constexpr uint32_t S_STG = 49152;             // two record stages
+constexpr uint32_t S_STG_STRIDE = 74752;      // REC_BYTES rounded up to 1024
+constexpr uint32_t S_BAR = S_STG + 2 * S_STG_STRIDE;   // 7 mbarriers, TMEM slot, abort flag
 constexpr uint32_t S_SMEM = S_BAR + 64 + 1024;
 static_assert(S_STG_STRIDE >= REC_BYTES && S_STG_STRIDE % 1024 == 0, "stage alignment");
 static_assert(S_SMEM <= 232448, "shared memory budget");
-constexpr uint32_t S_TM_WS = 0, S_TM_O = 64, S_TM_P = 128, S_TM_COLS = 256;
+// TMEM region of one parity: [W S]^T, then O^T, then P^T (contiguous: the
+// MMA groups write R .. R + 127 and R + 64 .. R + 255).
+constexpr uint32_t S_TM_WS = 0, S_TM_O = 64, S_TM_P = 128, S_TM_REGION = 256, S_TM_COLS = 512;
 
 __device__ __forceinline__ void store_out(float* p, float x) { *p = x; }
 __device__ __forceinline__ void store_out(__nv_bfloat16* p, float x) { *p = __float2bfloat16_rn(x); }
 
 template <typename TOut>
-__global__ void __launch_bounds__(NT, 1) chunk_scan_kernel(ChunkArgs args,
-                                                           const int32_t* __restrict__ hdr,
-                                                           const unsigned char* __restrict__ records)
+__global__ void __launch_bounds__(SCAN_THREADS, 1) chunk_scan_kernel(ChunkArgs args,
+                                                                     const int32_t* __restrict__ hdr,
+                                                                     const unsigned char* __restrict__ records)
 {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     const uint32_t raw_s = smem_u32(smem_raw);
@@ -425,7 +446,8 @@ __global__ void __launch_bounds__(NT, 1) chunk_scan_kernel(ChunkArgs args,
     const uint32_t sb = raw_s + pad;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int quad = warp & 3, half = warp >> 2;
+    const bool ctrl = warp == NT / 32;
+    const int quad = warp & 3, half = (warp >> 2) & 1;
     const int row = 32 * quad + lane;                      // TMEM lane = state row v
     const int H = args.H;
     const int n = blockIdx.x / H, h = blockIdx.x % H;
@@ -436,29 +458,35 @@ __global__ void __launch_bounds__(NT, 1) chunk_scan_kernel(ChunkArgs args,
     const int64_t rstride = (int64_t)H * REC_BYTES;
     const unsigned char* rec0 = records + ((int64_t)hdr[kHdrOff + n] * H + h) * REC_BYTES;
     TOut* __restrict__ out = static_cast<TOut*>(args.out);
-    uint64_t* bar = reinterpret_cast<uint64_t*>(sm + S_BAR);   // [0,1] stages, [2] WS, [3] O/P
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + S_BAR + 48);
+    // [0,1] record stages, [2] ws_done, [3] op_done, [4] delta_ready (256),
+    // [5] s_ready (256), [6] drain after a failure
+    uint64_t* bar = reinterpret_cast<uint64_t*>(sm + S_BAR);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + S_BAR + 56);
+    volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(sm + S_BAR + 60);
 
     // ---- the entering state (zero, or the caller's)
     float S[64];                                           // S^T[row][64 half + c]
-    if (args.initial_state != nullptr) {
-        const float* s0 = args.initial_state + ((int64_t)n * H + h) * DK * DV;
+    if (!ctrl) {
+        if (args.initial_state != nullptr) {
+            const float* s0 = args.initial_state + ((int64_t)n * H + h) * DK * DV;
 #pragma unroll
-        for (int u = 0; u < 64; ++u) S[u] = s0[(int64_t)(64 * half + u) * DV + row];
-    } else {
+            for (int u = 0; u < 64; ++u) S[u] = s0[(int64_t)(64 * half + u) * DV + row];
+        } else {
 #pragma unroll
-        for (int u = 0; u < 64; ++u) S[u] = 0.f;
+            for (int u = 0; u < 64; ++u) S[u] = 0.f;
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+            *reinterpret_cast<uint4*>(sm + S_ST + sw128_tile(128, row, (64 * half + 8 * q) * 2)) =
+                pack_h8(S + 8 * q);
     }
-#pragma unroll
-    for (int q = 0; q < 8; ++q)
-        *reinterpret_cast<uint4*>(sm + S_ST + sw128_tile(128, row, (64 * half + 8 * q) * 2)) =
-            pack_h8(S + 8 * q);
     if (warp == 0) {
         tmem_alloc(tslot, S_TM_COLS);
         tmem_relinquish();
     }
     if (tid == 0) {
-        for (int b = 0; b < 4; ++b) mbar_init(&bar[b], 1);
+        for (int b = 0; b < 7; ++b) mbar_init(&bar[b], (b == 4 || b == 5) ? NT : 1);
+        *abort_flag = 0;
         fence_mbar_init();
     }
     fence_async_smem();
@@ -467,139 +495,169 @@ __global__ void __launch_bounds__(NT, 1) chunk_scan_kernel(ChunkArgs args,
     fence_after_sync();
     const uint32_t tmem = *tslot;
     const uint32_t tlane = tmem + ((uint32_t)(32 * quad) << 16);
-
-    int issued = 0;                                        // chunks whose record load was issued
-    auto issue_load = [&](int c) {
-        unsigned char* stage = sm + S_STG + (c & 1) * S_STG_STRIDE;
-        mbar_arrive_expect_tx(&bar[c & 1], REC_BYTES);
-        bulk_g2s(stage, rec0 + c * rstride, REC_BYTES, &bar[c & 1]);
-    };
-    if (tid == 0) {
-        for (int c = 0; c < min(2, nch); ++c) issue_load(c);
+    if (!ctrl) {                                           // P starts from zero in both regions
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            tmem_zero32(tlane + S_TM_REGION * r + S_TM_P + 64 * half);
+            tmem_zero32(tlane + S_TM_REGION * r + S_TM_P + 64 * half + 32);
+        }
     }
-    issued = min(2, nch);
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
 
-    bool failed = false;
-    int c = 0;
-    int last_mma = -1;                                     // 2: WS committed, 3: O/P committed
-    for (; c < nch; ++c) {
-        const int t0 = bos + c * C, L = min(C, eos - t0);
-        const uint32_t b = c & 1;
-        unsigned char* stage = sm + S_STG + b * S_STG_STRIDE;
-        const uint32_t sst = sb + S_STG + b * S_STG_STRIDE;
-        const uint32_t mpar = c & 1;
-        last_mma = -1;
-        {
-            const bool ok = mbar_wait(&bar[b], (c >> 1) & 1, kWaitIters);
-            if (__syncthreads_or(!ok)) { failed = true; break; }
+    // A bounded wait that also gives up once the other role has.
+    auto wait_or_abort = [&](uint64_t* m, uint32_t parity) -> bool {
+        for (uint32_t i = 0; i < kWaitIters; ++i) {
+            if (mbar_try_wait(m, parity)) return true;
+            if ((i & 255u) == 255u && *abort_flag) return false;
         }
-        if (tid == 0) {
-            fence_after_sync();
-            constexpr uint32_t ids = idesc(kFmtF16, 128, 64, false, true);
-#pragma unroll
-            for (int s = 0; s < 8; ++s)
-                mma_f16(tmem + S_TM_WS, desc_kmajor(sb + S_ST, 128, s),
-                        desc_mnmajor64(sst + REC_W, s), ids, s > 0);
-            commit(&bar[2]);
-#pragma unroll
-            for (int s = 0; s < 8; ++s)
-                mma_f16(tmem + S_TM_O, desc_kmajor(sb + S_ST, 128, s),
-                        desc_mnmajor64(sst + REC_QP, s), ids, s > 0);
-        }
-        last_mma = 2;
-        {
-            const bool ok = mbar_wait(&bar[2], mpar, kWaitIters);
-            if (__syncthreads_or(!ok)) { failed = true; break; }
-        }
-        fence_after_sync();
-        {
-            // Delta^T[v][i] = U^T[v][i] - [W S]^T[v][i], fp16 K-major
-            float ws[32], d[8];
-            tmem_ld32(tlane + S_TM_WS + 32 * half, ws);
-            const unsigned char* up = stage + REC_U;
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const uint4 pk = *reinterpret_cast<const uint4*>(up + sw128(row, (32 * half + 8 * q) * 2));
-                const uint32_t w4[4] = {pk.x, pk.y, pk.z, pk.w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float2 uf = __half22float2(*reinterpret_cast<const __half2*>(&w4[e]));
-                    d[2 * e] = uf.x - ws[8 * q + 2 * e];
-                    d[2 * e + 1] = uf.y - ws[8 * q + 2 * e + 1];
+        *abort_flag = 1;
+        return false;
+    };
+
+    if (ctrl) {
+        if (lane == 0) {
+            auto issue_load = [&](int c) {
+                unsigned char* stage = sm + S_STG + (c & 1) * S_STG_STRIDE;
+                mbar_arrive_expect_tx(&bar[c & 1], REC_BYTES);
+                bulk_g2s(stage, rec0 + c * rstride, REC_BYTES, &bar[c & 1]);
+            };
+            for (int c = 0; c < min(2, nch); ++c) issue_load(c);
+            for (int c = 2; c < min(kL2Ahead, nch); ++c) bulk_prefetch_l2(rec0 + c * rstride, REC_BYTES);
+            int issued = min(2, nch), c = 0;
+            bool fail = false, any_mma = false;
+            constexpr uint32_t id1 = idesc(kFmtF16, 128, 128, false, true);
+            constexpr uint32_t id2 = idesc(kFmtF16, 128, 192);
+            for (; c < nch; ++c) {
+                const uint32_t R = tmem + S_TM_REGION * (c & 1);
+                const uint32_t sst = sb + S_STG + (c & 1) * S_STG_STRIDE;
+                if (!wait_or_abort(&bar[c & 1], (c >> 1) & 1)) { fail = true; break; }
+                if (c > 0) {
+                    // chunk c - 1 is finished: S^T is current and its stage is free
+                    if (!wait_or_abort(&bar[5], (c - 1) & 1)) { fail = true; break; }
+                    if (c + 1 < nch) {
+                        issue_load(c + 1);
+                        issued = c + 2;
+                    }
                 }
-                st8(sm + S_DT, 0, row, 32 * half + 8 * q, d);
+                if (c + kL2Ahead < nch) bulk_prefetch_l2(rec0 + (c + kL2Ahead) * rstride, REC_BYTES);
+                fence_after_sync();
+#pragma unroll
+                for (int s = 0; s < 8; ++s)
+                    mma_f16(R + S_TM_WS, desc_kmajor(sb + S_ST, 128, s),
+                            desc_mnmajor128(sst + REC_W, 16384, s), id1, s > 0);
+                commit(&bar[2]);
+                any_mma = true;
+                if (!wait_or_abort(&bar[4], c & 1)) { fail = true; break; }
+                fence_after_sync();
+#pragma unroll
+                for (int s = 0; s < 4; ++s)
+                    mma_f16(R + S_TM_O, desc_kmajor(sb + S_DT, 128, s),
+                            desc_kmajor(sst + REC_AQK, 192, s), id2, 1);
+                commit(&bar[3]);
+            }
+            if (fail) {
+                *abort_flag = 1;
+                report_status(args.status, KDA_ERR_TIMEOUT);
+                // let the MMAs and copies in flight finish before the CTA leaves
+                if (any_mma) {
+                    commit(&bar[6]);
+                    mbar_wait(&bar[6], 0, kWaitIters);
+                }
+                for (int cc = c; cc < issued; ++cc) mbar_wait(&bar[cc & 1], (cc >> 1) & 1, kWaitIters);
             }
         }
-        fence_async_smem();
-        fence_before_sync();
-        __syncthreads();
-        if (tid == 0) {
-            fence_after_sync();
-            constexpr uint32_t ido = idesc(kFmtF16, 128, 64);
-            constexpr uint32_t idp = idesc(kFmtF16, 128, 128);
-#pragma unroll
-            for (int s = 0; s < 4; ++s)
-                mma_f16(tmem + S_TM_O, desc_kmajor(sb + S_DT, 128, s),
-                        desc_kmajor(sst + REC_AQK, 64, s), ido, 1);
-#pragma unroll
-            for (int s = 0; s < 4; ++s)
-                mma_f16(tmem + S_TM_P, desc_kmajor(sb + S_DT, 128, s),
-                        desc_kmajor(sst + REC_KT, 128, s), idp, s > 0);
-            commit(&bar[3]);
-        }
-        last_mma = 3;
-        {
-            const bool ok = mbar_wait(&bar[3], mpar, kWaitIters);
-            if (__syncthreads_or(!ok)) { failed = true; break; }
-        }
-        last_mma = -1;
-        fence_after_sync();
-        {
-            // out = scale O;  S^T <- S^T Diag(d) + P^T;  fp16 copy of S^T
+    } else {
+        // out rows of chunk cc = scale O, from region cc & 1, stored straight
+        // from registers (no shared memory: the MMAs running meanwhile use its
+        // bandwidth): each store instruction writes 32 consecutive V values of
+        // one token.
+        auto store_chunk_out = [&](int cc) {
             float o[32];
-            tmem_ld32(tlane + S_TM_O + 32 * half, o);
+            tmem_ld32(tlane + S_TM_REGION * (cc & 1) + S_TM_O + 32 * half, o);
+            const int tc = bos + cc * C, Lc = min(C, eos - tc);
             const int64_t ostride = (int64_t)H * DV;
-            TOut* op = out + ((int64_t)(t0 + 32 * half) * H + h) * DV + row;
-            const int nrows = min(32, L - 32 * half);
+            TOut* op = out + ((int64_t)(tc + 32 * half) * H + h) * DV + row;
+            const int nrows = min(32, Lc - 32 * half);
 #pragma unroll
             for (int u = 0; u < 32; ++u) {
                 if (u < nrows) store_out(op, args.scale * o[u]);
                 op += ostride;
             }
-            const float* dec = reinterpret_cast<const float*>(stage + REC_DEC);
-            float p[32];
-#pragma unroll
-            for (int part = 0; part < 2; ++part) {
-                tmem_ld32(tlane + S_TM_P + 64 * half + 32 * part, p);
-#pragma unroll
-                for (int u = 0; u < 32; ++u)
-                    S[32 * part + u] = S[32 * part + u] * dec[64 * half + 32 * part + u] + p[u];
+        };
+        bool fail = false;
+        for (int c = 0; c < nch; ++c) {
+            const uint32_t R = tlane + S_TM_REGION * (c & 1);
+            unsigned char* stage = sm + S_STG + (c & 1) * S_STG_STRIDE;
+            {
+                const bool ok = wait_or_abort(&bar[c & 1], (c >> 1) & 1) && wait_or_abort(&bar[2], c & 1);
+                if (named_sync_or(kEpiBar, NT, !ok)) { fail = true; break; }
             }
+            fence_after_sync();
+            {
+                // Delta^T[v][i] = U^T[v][i] - [W S]^T[v][i], fp16 K-major
+                float ws[32], d[8];
+                tmem_ld32(R + S_TM_WS + 32 * half, ws);
+                const unsigned char* up = stage + REC_U;
 #pragma unroll
-            for (int q = 0; q < 8; ++q)
-                *reinterpret_cast<uint4*>(sm + S_ST + sw128_tile(128, row, (64 * half + 8 * q) * 2)) =
-                    pack_h8(S + 8 * q);
-        }
-        fence_async_smem();
-        fence_before_sync();
-        __syncthreads();
-        // every read of this stage is done: bring in the chunk after next
-        if (c + 2 < nch) {
-            if (tid == 0) issue_load(c + 2);
-            issued = c + 3;
-        }
-    }
-
-    if (failed) {
-        if (tid == 0) report_status(args.status, KDA_ERR_TIMEOUT);
-        // let the copies and MMAs still in flight finish before leaving
-        for (int cc = c; cc < issued; ++cc) mbar_wait(&bar[cc & 1], (cc >> 1) & 1, kWaitIters);
-        if (last_mma == 2 && tid == 0) commit(&bar[3]);   // covers every MMA issued so far
-        if (last_mma >= 2) mbar_wait(&bar[3], c & 1, kWaitIters);
-    } else if (args.final_state != nullptr) {
-        float* fs = args.final_state + ((int64_t)n * H + h) * DK * DV;
+                for (int q = 0; q < 4; ++q) {
+                    const uint4 pk = *reinterpret_cast<const uint4*>(up + sw128(row, (32 * half + 8 * q) * 2));
+                    const uint32_t w4[4] = {pk.x, pk.y, pk.z, pk.w};
 #pragma unroll
-        for (int u = 0; u < 64; ++u) fs[(int64_t)(64 * half + u) * DV + row] = S[u];
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 uf = __half22float2(*reinterpret_cast<const __half2*>(&w4[e]));
+                        d[2 * e] = uf.x - ws[8 * q + 2 * e];
+                        d[2 * e + 1] = uf.y - ws[8 * q + 2 * e + 1];
+                    }
+                    st8(sm + S_DT, 0, row, 32 * half + 8 * q, d);
+                }
+            }
+            fence_async_smem();
+            fence_before_sync();
+            mbar_arrive(&bar[4]);
+            {
+                const bool ok = wait_or_abort(&bar[3], c & 1);
+                if (named_sync_or(kEpiBar, NT, !ok)) { fail = true; break; }
+            }
+            fence_after_sync();
+            {
+                // S^T <- S^T Diag(d) + P^T;  fp16 copy of S^T;  P back to zero
+                const float4* dec4 = reinterpret_cast<const float4*>(stage + REC_DEC) + 16 * half;
+                float p[32];
+#pragma unroll
+                for (int part = 0; part < 2; ++part) {
+                    tmem_ld32(R + S_TM_P + 64 * half + 32 * part, p);
+#pragma unroll
+                    for (int u4 = 0; u4 < 8; ++u4) {
+                        const float4 dd = dec4[8 * part + u4];
+                        float* sv = S + 32 * part + 4 * u4;
+                        sv[0] = sv[0] * dd.x + p[4 * u4 + 0];
+                        sv[1] = sv[1] * dd.y + p[4 * u4 + 1];
+                        sv[2] = sv[2] * dd.z + p[4 * u4 + 2];
+                        sv[3] = sv[3] * dd.w + p[4 * u4 + 3];
+                    }
+                    tmem_zero32(R + S_TM_P + 64 * half + 32 * part);
+                }
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    *reinterpret_cast<uint4*>(sm + S_ST + sw128_tile(128, row, (64 * half + 8 * q) * 2)) =
+                        pack_h8(S + 8 * q);
+            }
+            fence_async_smem();
+            fence_before_sync();
+            mbar_arrive(&bar[5]);
+            // this chunk's output, while the control warp issues the next chunk's MMAs
+            store_chunk_out(c);
+        }
+        if (fail) {
+            *abort_flag = 1;
+            if (tid == 0) report_status(args.status, KDA_ERR_TIMEOUT);
+        } else if (args.final_state != nullptr) {
+            float* fs = args.final_state + ((int64_t)n * H + h) * DK * DV;
+#pragma unroll
+            for (int u = 0; u < 64; ++u) fs[(int64_t)(64 * half + u) * DV + row] = S[u];
+        }
     }
     fence_before_sync();
     __syncthreads();
@@ -627,7 +685,7 @@ cudaError_t launch_scan(const ChunkArgs& a, const int32_t* hdr, const unsigned c
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)S_SMEM);
     if (e != cudaSuccess) return e;
-    kern<<<(unsigned)((int64_t)a.N * a.H), NT, S_SMEM, stream>>>(a, hdr, rec);
+    kern<<<(unsigned)((int64_t)a.N * a.H), SCAN_THREADS, S_SMEM, stream>>>(a, hdr, rec);
     return cudaGetLastError();
 }
 

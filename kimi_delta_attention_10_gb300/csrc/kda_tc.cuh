@@ -164,6 +164,30 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* m, uint32_t byte
                  : "memory");
 }
 
+// Plain arrival (count 1) on `m`.
+__device__ __forceinline__ void mbar_arrive(uint64_t* m)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(m)) : "memory");
+}
+
+// Named barrier `id` over `nthreads` threads (whole warps).
+__device__ __forceinline__ void named_sync(uint32_t id, uint32_t nthreads)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+// As named_sync; returns whether any participating thread passed `pred` true.
+__device__ __forceinline__ bool named_sync_or(uint32_t id, uint32_t nthreads, bool pred)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n.reg .pred pi, po;\nsetp.ne.u32 pi, %1, 0;\n"
+        "bar.red.or.pred po, %2, %3, pi;\nselp.u32 %0, 1, 0, po;\n}\n"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(id), "r"(nthreads)
+        : "memory");
+    return r != 0;
+}
+
 // ---------------------------------------------------------------- bulk copy
 // Global -> shared bulk copy through the async proxy (both addresses 16-byte
 // aligned, `bytes` a multiple of 16); completes `bytes` transactions on `m`.
@@ -174,6 +198,12 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
             "r"(smem_u32(dst)),
         "l"(src), "r"(bytes), "r"(smem_u32(m))
         : "memory");
+}
+
+// Hint: bring `bytes` (multiple of 16, 16-byte-aligned address) into L2.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
 // ---------------------------------------------------------------- cp.async
@@ -300,6 +330,19 @@ __device__ __forceinline__ void tmem_ld16x3(uint32_t t0, uint32_t t1, uint32_t t
           "=r"(u[37]), "=r"(u[38]), "=r"(u[39]), "=r"(u[40]), "=r"(u[41]), "=r"(u[42]),
           "=r"(u[43]), "=r"(u[44]), "=r"(u[45]), "=r"(u[46]), "=r"(u[47])
         : "r"(t0), "r"(t1), "r"(t2)
+        : "memory");
+}
+
+// Warp-collective: zeroes TMEM lane 32 (w % 4) + t, columns [col, col + 32)
+// of `taddr`, and waits for the store.
+__device__ __forceinline__ void tmem_zero32(uint32_t taddr)
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,"
+        "%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1};\n"
+        "tcgen05.wait::st.sync.aligned;\n" ::"r"(taddr),
+        "r"(0u)
         : "memory");
 }
 
