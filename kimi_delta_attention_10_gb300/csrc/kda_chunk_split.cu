@@ -533,15 +533,8 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) chunk_scan_kernel(ChunkArgs a
                 const uint32_t R = tmem + S_TM_REGION * (c & 1);
                 const uint32_t sst = sb + S_STG + (c & 1) * S_STG_STRIDE;
                 if (!wait_or_abort(&bar[c & 1], (c >> 1) & 1)) { fail = true; break; }
-                if (c > 0) {
-                    // chunk c - 1 is finished: S^T is current and its stage is free
-                    if (!wait_or_abort(&bar[5], (c - 1) & 1)) { fail = true; break; }
-                    if (c + 1 < nch) {
-                        issue_load(c + 1);
-                        issued = c + 2;
-                    }
-                }
-                if (c + kL2Ahead < nch) bulk_prefetch_l2(rec0 + (c + kL2Ahead) * rstride, REC_BYTES);
+                // chunk c - 1 is finished: S^T is current and its stage is free
+                if (c > 0 && !wait_or_abort(&bar[5], (c - 1) & 1)) { fail = true; break; }
                 fence_after_sync();
 #pragma unroll
                 for (int s = 0; s < 8; ++s)
@@ -549,6 +542,11 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) chunk_scan_kernel(ChunkArgs a
                             desc_mnmajor128(sst + REC_W, 16384, s), id1, s > 0);
                 commit(&bar[2]);
                 any_mma = true;
+                if (c > 0 && c + 1 < nch) {
+                    issue_load(c + 1);
+                    issued = c + 2;
+                }
+                if (c + kL2Ahead < nch) bulk_prefetch_l2(rec0 + (c + kL2Ahead) * rstride, REC_BYTES);
                 if (!wait_or_abort(&bar[4], c & 1)) { fail = true; break; }
                 fence_after_sync();
 #pragma unroll
