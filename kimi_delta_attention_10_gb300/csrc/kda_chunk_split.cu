@@ -19,12 +19,11 @@
 // first turns cu_seqlens into per-sequence chunk offsets.
 //
 // Record of one unit (bytes), in this order:
-//   W       fp16 [128 c][64 i]  \ together the MN-major B operand of
-//   Q'      fp16 [128 c][64 i]  / [W S | Q' S]^T = S^T [W; Q']^T (N = 128)
+//   W       fp16 [128 c][64 i]  (MN-major B of [W S]^T = S^T W^T)
+//   Q'      fp16 [128 c][64 i]  (MN-major B of [Q' S]^T)
 //   U^T     fp16 [128 v][64 i]  (row v read by the thread of state row v)
-//   A_qk    fp16 [64 i][64 j]   \ together the K-major B operand of
-//   K''^T   fp16 [128 c][64 j]  / [A_qk Delta | K''^T Delta]^T (N = 192);
-//                                 A_qk's strictly upper part is 0
+//   A_qk    fp16 [64 i][64 j]   (K-major B of [A_qk Delta]^T; strictly upper part 0)
+//   K''^T   fp16 [128 c][64 j]  (K-major B of [K''^T Delta]^T)
 //   d       fp32 [128]
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
@@ -49,10 +48,10 @@ constexpr int DV = kHeadV;
 constexpr uint32_t kWaitIters = 1u << 22;   // polls before a wait gives up
 
 constexpr uint32_t REC_W = 0;
-constexpr uint32_t REC_QP = 16384;     // = REC_W + 16 KiB: [W; Q'] is one N = 128 operand
+constexpr uint32_t REC_QP = 16384;
 constexpr uint32_t REC_U = 32768;
 constexpr uint32_t REC_AQK = 49152;
-constexpr uint32_t REC_KT = 57344;     // = REC_AQK + 8 KiB: [A_qk; K''^T] is one N = 192 operand
+constexpr uint32_t REC_KT = 57344;
 constexpr uint32_t REC_DEC = 73728;
 constexpr uint32_t REC_BYTES = 74240;
 static_assert(REC_BYTES % 16 == 0 && REC_BYTES < (1u << 20), "bulk copy size");
@@ -416,15 +415,16 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(ChunkArgs args,
 // a half of the columns) and one control warp whose lane 0 issues the bulk
 // copies and the MMAs.  Per chunk c (TMEM region R = 256 (c & 1)):
 //   control:  record c in stage c & 1 (bulk copy, issued a chunk ahead)
-//             [W S | Q' S]^T -> R .. R + 127       (8 MMAs, N = 128)
+//             [W S]^T -> R (8 MMAs, N = 64), commit ws_done; [Q' S]^T -> R + 64
 //   epilogue: Delta^T = U^T - [W S]^T -> shared (fp16), arrive delta_ready
-//   control:  [O | P]^T += Delta^T [A_qk; K''^T]^T -> R + 64 .. R + 255 (4 MMAs,
-//             N = 192: O accumulates on Q' S, P on zero)
-//   epilogue: S^T <- S^T Diag(d) + P^T, the fp16 copy of S^T for the next
-//             chunk, P zeroed again; arrive s_ready; then chunk c's output,
-//             while the control warp issues chunk c + 1's MMAs into the other
-//             region
-// so the state's chain per chunk is two MMA groups and two short epilogues.
+//   control:  P^T = Delta^T K'' (4 MMAs, N = 128), commit p_done; then
+//             O^T += Delta^T A_qk^T on top of Q' S (4 MMAs, N = 64), commit o_done
+//   epilogue: S^T <- S^T Diag(d) + P^T and the fp16 copy of S^T for the next
+//             chunk; O read from TMEM; arrive s_ready; then chunk c's output
+//             rows, stored while the control warp issues chunk c + 1's MMAs
+//             into the other region
+// so the state's chain per chunk is [W S] -> Delta -> P -> S: two short MMA
+// groups and two short epilogues; Q' S and A_qk Delta ride behind them.
 constexpr int SCAN_THREADS = NT + 32;
 constexpr int kL2Ahead = 4;                   // records prefetched into L2 this many chunks ahead
 constexpr uint32_t kEpiBar = 1;               // named barrier of the 256 epilogue threads
@@ -432,12 +432,11 @@ constexpr uint32_t S_ST = 0;                  // S^T fp16 K-major [128 v][128 c]
 constexpr uint32_t S_DT = 32768;              // Delta^T fp16 K-major [128 v][64 i]
 constexpr uint32_t S_STG = 49152;             // two record stages
 constexpr uint32_t S_STG_STRIDE = 74752;      // REC_BYTES rounded up to 1024
-constexpr uint32_t S_BAR = S_STG + 2 * S_STG_STRIDE;   // 7 mbarriers, TMEM slot, abort flag
-constexpr uint32_t S_SMEM = S_BAR + 64 + 1024;
+constexpr uint32_t S_BAR = S_STG + 2 * S_STG_STRIDE;   // 8 mbarriers, TMEM slot, abort flag
+constexpr uint32_t S_SMEM = S_BAR + 128 + 1024;
 static_assert(S_STG_STRIDE >= REC_BYTES && S_STG_STRIDE % 1024 == 0, "stage alignment");
 static_assert(S_SMEM <= 232448, "shared memory budget");
-// TMEM region of one parity: [W S]^T, then O^T, then P^T (contiguous: the
-// MMA groups write R .. R + 127 and R + 64 .. R + 255).
+// TMEM region of one parity: [W S]^T, O^T (on top of [Q' S]^T), P^T.
 constexpr uint32_t S_TM_WS = 0, S_TM_O = 64, S_TM_P = 128, S_TM_REGION = 256, S_TM_COLS = 512;
 
 __device__ __forceinline__ void store_out(float* p, float x) { *p = x; }
@@ -467,11 +466,11 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) chunk_scan_kernel(ChunkArgs a
     const int64_t rstride = (int64_t)H * REC_BYTES;
     const unsigned char* rec0 = records + ((int64_t)hdr[kHdrOff + n] * H + h) * REC_BYTES;
     TOut* __restrict__ out = static_cast<TOut*>(args.out);
-    // [0,1] record stages, [2] ws_done, [3] op_done, [4] delta_ready (256),
-    // [5] s_ready (256), [6] drain after a failure
+    // [0,1] record stages, [2] ws_done, [3] p_done, [4] delta_ready (NT),
+    // [5] s_ready (NT), [6] drain after a failure, [7] o_done
     uint64_t* bar = reinterpret_cast<uint64_t*>(sm + S_BAR);
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + S_BAR + 56);
-    volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(sm + S_BAR + 60);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + S_BAR + 64);
+    volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(sm + S_BAR + 68);
 
     // ---- the entering state (zero, or the caller's)
     float S[64];                                           // S^T[row][64 half + c]
@@ -494,7 +493,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) chunk_scan_kernel(ChunkArgs a
         tmem_relinquish();
     }
     if (tid == 0) {
-        for (int b = 0; b < 7; ++b) mbar_init(&bar[b], (b == 4 || b == 5) ? NT : 1);
+        for (int b = 0; b < 8; ++b) mbar_init(&bar[b], (b == 4 || b == 5) ? NT : 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -504,16 +503,6 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) chunk_scan_kernel(ChunkArgs a
     fence_after_sync();
     const uint32_t tmem = *tslot;
     const uint32_t tlane = tmem + ((uint32_t)(32 * quad) << 16);
-    if (!ctrl) {                                           // P starts from zero in both regions
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-            tmem_zero32(tlane + S_TM_REGION * r + S_TM_P + 64 * half);
-            tmem_zero32(tlane + S_TM_REGION * r + S_TM_P + 64 * half + 32);
-        }
-    }
-    fence_before_sync();
-    __syncthreads();
-    fence_after_sync();
 
     // A bounded wait that also gives up once the other role has.
     auto wait_or_abort = [&](uint64_t* m, uint32_t parity) -> bool {
@@ -536,8 +525,9 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) chunk_scan_kernel(ChunkArgs a
             for (int c = 2; c < min(kL2Ahead, nch); ++c) bulk_prefetch_l2(rec0 + c * rstride, REC_BYTES);
             int issued = min(2, nch), c = 0;
             bool fail = false, any_mma = false;
-            constexpr uint32_t id1 = idesc(kFmtF16, 128, 128, false, true);
-            constexpr uint32_t id2 = idesc(kFmtF16, 128, 192);
+            constexpr uint32_t id_ws = idesc(kFmtF16, 128, 64, false, true);
+            constexpr uint32_t id_p = idesc(kFmtF16, 128, 128);
+            constexpr uint32_t id_o = idesc(kFmtF16, 128, 64);
             for (; c < nch; ++c) {
                 const uint32_t R = tmem + S_TM_REGION * (c & 1);
                 const uint32_t sst = sb + S_STG + (c & 1) * S_STG_STRIDE;
@@ -548,9 +538,13 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) chunk_scan_kernel(ChunkArgs a
 #pragma unroll
                 for (int s = 0; s < 8; ++s)
                     mma_f16(R + S_TM_WS, desc_kmajor(sb + S_ST, 128, s),
-                            desc_mnmajor128(sst + REC_W, 16384, s), id1, s > 0);
+                            desc_mnmajor64(sst + REC_W, s), id_ws, s > 0);
                 commit(&bar[2]);
                 any_mma = true;
+#pragma unroll
+                for (int s = 0; s < 8; ++s)
+                    mma_f16(R + S_TM_O, desc_kmajor(sb + S_ST, 128, s),
+                            desc_mnmajor64(sst + REC_QP, s), id_ws, s > 0);
                 if (c > 0 && c + 1 < nch) {
                     issue_load(c + 1);
                     issued = c + 2;
@@ -560,9 +554,14 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) chunk_scan_kernel(ChunkArgs a
                 fence_after_sync();
 #pragma unroll
                 for (int s = 0; s < 4; ++s)
-                    mma_f16(R + S_TM_O, desc_kmajor(sb + S_DT, 128, s),
-                            desc_kmajor(sst + REC_AQK, 192, s), id2, 1);
+                    mma_f16(R + S_TM_P, desc_kmajor(sb + S_DT, 128, s),
+                            desc_kmajor(sst + REC_KT, 128, s), id_p, s > 0);
                 commit(&bar[3]);
+#pragma unroll
+                for (int s = 0; s < 4; ++s)
+                    mma_f16(R + S_TM_O, desc_kmajor(sb + S_DT, 128, s),
+                            desc_kmajor(sst + REC_AQK, 64, s), id_o, 1);
+                commit(&bar[7]);
             }
             if (fail) {
                 *abort_flag = 1;
@@ -576,13 +575,10 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) chunk_scan_kernel(ChunkArgs a
             }
         }
     } else {
-        // out rows of chunk cc = scale O, from region cc & 1, stored straight
-        // from registers (no shared memory: the MMAs running meanwhile use its
-        // bandwidth): each store instruction writes 32 consecutive V values of
-        // one token.
-        auto store_chunk_out = [&](int cc) {
-            float o[32];
-            tmem_ld32(tlane + S_TM_REGION * (cc & 1) + S_TM_O + 32 * half, o);
+        // out rows of chunk cc = scale O (o: this thread's 32 tokens of its V
+        // column, read from TMEM), stored straight from registers: each store
+        // instruction writes 32 consecutive V values of one token.
+        auto store_chunk_out = [&](int cc, const float (&o)[32]) {
             const int tc = bos + cc * C, Lc = min(C, eos - tc);
             const int64_t ostride = (int64_t)H * DV;
             TOut* op = out + ((int64_t)(tc + 32 * half) * H + h) * DV + row;
@@ -597,8 +593,16 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) chunk_scan_kernel(ChunkArgs a
         for (int c = 0; c < nch; ++c) {
             const uint32_t R = tlane + S_TM_REGION * (c & 1);
             unsigned char* stage = sm + S_STG + (c & 1) * S_STG_STRIDE;
+            uint4 u4[4];                                   // this thread's U^T row piece
             {
-                const bool ok = wait_or_abort(&bar[c & 1], (c >> 1) & 1) && wait_or_abort(&bar[2], c & 1);
+                bool ok = wait_or_abort(&bar[c & 1], (c >> 1) & 1);
+                if (ok) {
+                    const unsigned char* up = stage + REC_U;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        u4[q] = *reinterpret_cast<const uint4*>(up + sw128(row, (32 * half + 8 * q) * 2));
+                    ok = wait_or_abort(&bar[2], c & 1);
+                }
                 if (named_sync_or(kEpiBar, NT, !ok)) { fail = true; break; }
             }
             fence_after_sync();
@@ -606,11 +610,9 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) chunk_scan_kernel(ChunkArgs a
                 // Delta^T[v][i] = U^T[v][i] - [W S]^T[v][i], fp16 K-major
                 float ws[32], d[8];
                 tmem_ld32(R + S_TM_WS + 32 * half, ws);
-                const unsigned char* up = stage + REC_U;
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
-                    const uint4 pk = *reinterpret_cast<const uint4*>(up + sw128(row, (32 * half + 8 * q) * 2));
-                    const uint32_t w4[4] = {pk.x, pk.y, pk.z, pk.w};
+                    const uint32_t w4[4] = {u4[q].x, u4[q].y, u4[q].z, u4[q].w};
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const float2 uf = __half22float2(*reinterpret_cast<const __half2*>(&w4[e]));
@@ -629,33 +631,40 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) chunk_scan_kernel(ChunkArgs a
             }
             fence_after_sync();
             {
-                // S^T <- S^T Diag(d) + P^T;  fp16 copy of S^T;  P back to zero
+                // S^T <- S^T Diag(d) + P^T;  fp16 copy of S^T
                 const float4* dec4 = reinterpret_cast<const float4*>(stage + REC_DEC) + 16 * half;
                 float p[32];
 #pragma unroll
                 for (int part = 0; part < 2; ++part) {
                     tmem_ld32(R + S_TM_P + 64 * half + 32 * part, p);
 #pragma unroll
-                    for (int u4 = 0; u4 < 8; ++u4) {
-                        const float4 dd = dec4[8 * part + u4];
-                        float* sv = S + 32 * part + 4 * u4;
-                        sv[0] = sv[0] * dd.x + p[4 * u4 + 0];
-                        sv[1] = sv[1] * dd.y + p[4 * u4 + 1];
-                        sv[2] = sv[2] * dd.z + p[4 * u4 + 2];
-                        sv[3] = sv[3] * dd.w + p[4 * u4 + 3];
+                    for (int u = 0; u < 8; ++u) {
+                        const float4 f = dec4[8 * part + u];
+                        float* sv = S + 32 * part + 4 * u;
+                        sv[0] = sv[0] * f.x + p[4 * u + 0];
+                        sv[1] = sv[1] * f.y + p[4 * u + 1];
+                        sv[2] = sv[2] * f.z + p[4 * u + 2];
+                        sv[3] = sv[3] * f.w + p[4 * u + 3];
                     }
-                    tmem_zero32(R + S_TM_P + 64 * half + 32 * part);
                 }
 #pragma unroll
                 for (int q = 0; q < 8; ++q)
                     *reinterpret_cast<uint4*>(sm + S_ST + sw128_tile(128, row, (64 * half + 8 * q) * 2)) =
                         pack_h8(S + 8 * q);
             }
+            // this chunk's O leaves TMEM before the next chunk's MMAs start
+            {
+                const bool ok = wait_or_abort(&bar[7], c & 1);
+                if (named_sync_or(kEpiBar, NT, !ok)) { fail = true; break; }
+            }
+            fence_after_sync();
+            float o[32];
+            tmem_ld32(R + S_TM_O + 32 * half, o);
             fence_async_smem();
             fence_before_sync();
             mbar_arrive(&bar[5]);
-            // this chunk's output, while the control warp issues the next chunk's MMAs
-            store_chunk_out(c);
+            // its rows go out while the control warp issues the next chunk's MMAs
+            store_chunk_out(c, o);
         }
         if (fail) {
             *abort_flag = 1;
