@@ -177,3 +177,40 @@ def test_device_detects_bad_offsets_without_host_mirror(mode):
     o_ref, _, _, _ = oracle_pipeline(x)
     assert rel_l2(out[:40].cpu().double().numpy(), o_ref[:40]) <= tol(mode)
     assert torch.count_nonzero(out[40:]) == 0
+
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("host_mirror", [True, False])
+def test_many_short_sequences(mode, host_mirror):
+    """2600 packed sequences of 0..24 tokens: more than one 1024-wide tile of the
+    two-phase path's chunk-offset scan, and a preparation grid sized from the
+    offsets bound when no host mirror is given."""
+    gen = torch.Generator().manual_seed(61)
+    lens = torch.randint(0, 25, (2600,), generator=gen).tolist()
+    x = _small(lens, H=2, seed=62)
+    out, S, _, _ = gpu_pipeline(x, mode, out_dtype=OUT_DTYPE[mode], host_mirror=host_mirror)
+    o_ref, S_ref, _, _ = oracle_pipeline(x)
+    assert rel_l2(out.double().numpy(), o_ref) <= tol(mode)
+    assert rel_l2(S.double().numpy(), S_ref) <= tol(mode)
+    for n, L in enumerate(lens):
+        if L == 0:
+            assert torch.count_nonzero(S[n]) == 0
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_final_state_may_alias_initial_state(mode):
+    lens = [150, 0, 70]
+    x = _small(lens, seed=63)
+    gen = torch.Generator().manual_seed(63)
+    S0 = (torch.randn(len(lens), x.H, 128, 128, generator=gen) * 0.2).cuda()
+    d = device_inputs(x)
+    g, beta = kda_gate(d["f"], d["A_log"], d["dt_bias"], d["b"])
+    kw = dict(out_dtype=OUT_DTYPE[mode], **path_kw(mode))
+    o1, S1 = kda_chunk_fwd(d["q"], d["k"], d["v"], g, beta, d["cu_seqlens"], x.scale,
+                           initial_state=S0, **kw)
+    S_inout = S0.clone()
+    o2, S2 = kda_chunk_fwd(d["q"], d["k"], d["v"], g, beta, d["cu_seqlens"], x.scale,
+                           initial_state=S_inout, final_state=S_inout, **kw)
+    torch.cuda.synchronize()
+    assert S2.data_ptr() == S_inout.data_ptr()
+    assert torch.equal(o1, o2) and torch.equal(S1, S2)
