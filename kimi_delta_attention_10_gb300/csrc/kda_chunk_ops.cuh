@@ -367,6 +367,14 @@ __device__ __forceinline__ void extract_pairs(unsigned char* aqk, float* akk, co
 // unused upper blocks of T); finally T' = T diag(beta) as an FP16 K-major
 // [64 i][64 j] tile.  Entry: A_kk complete and visible (after a CTA barrier).
 // Exit: the T' tile written by this thread (the caller fences and syncs).
+__device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+__device__ __forceinline__ float f4(const float4& v, int e)
+{
+    return e == 0 ? v.x : e == 1 ? v.y : e == 2 ? v.z : v.w;
+}
+
+// Rows of A_kk and T are read 4 columns at a time (16-byte loads along k);
+// every accumulation keeps its k order.
 __device__ __forceinline__ void chunk_inverse(float (*akk)[LDA], float (*Tf)[LDA],
                                               const float* sbeta, unsigned char* tp, int tid,
                                               int warp, int lane)
@@ -378,7 +386,12 @@ __device__ __forceinline__ void chunk_inverse(float (*akk)[LDA], float (*Tf)[LDA
         for (int i = 0; i < SB; ++i) {
             float acc = (i == m) ? 1.f : 0.f;
 #pragma unroll
-            for (int j = 0; j < i; ++j) acc -= akk[b + i][b + j] * tcol[j];
+            for (int q = 0; q < (i + 3) / 4; ++q) {
+                const float4 a4 = ld4(&akk[b + i][b + 4 * q]);
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    if (4 * q + e < i) acc -= f4(a4, e) * tcol[4 * q + e];
+            }
             tcol[i] = (i < m) ? 0.f : acc;
         }
 #pragma unroll
@@ -392,20 +405,30 @@ __device__ __forceinline__ void chunk_inverse(float (*akk)[LDA], float (*Tf)[LDA
         const int r2 = ((tid >> 4) & 7) * 2, cc = tid & 15;
         float y0 = 0.f, y1 = 0.f;
 #pragma unroll
-        for (int k = 0; k < SB; ++k) {
-            const float t = Tf[J * SB + k][J * SB + cc];
-            y0 += akk[I * SB + r2][J * SB + k] * t;
-            y1 += akk[I * SB + r2 + 1][J * SB + k] * t;
+        for (int q = 0; q < SB / 4; ++q) {
+            const float4 a0 = ld4(&akk[I * SB + r2][J * SB + 4 * q]);
+            const float4 a1 = ld4(&akk[I * SB + r2 + 1][J * SB + 4 * q]);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float t = Tf[J * SB + 4 * q + e][J * SB + cc];
+                y0 += f4(a0, e) * t;
+                y1 += f4(a1, e) * t;
+            }
         }
         Tf[J * SB + r2][I * SB + cc] = y0;
         Tf[J * SB + r2 + 1][I * SB + cc] = y1;
         __syncthreads();
         float t0 = 0.f, t1 = 0.f;
 #pragma unroll
-        for (int k = 0; k < SB; ++k) {
-            const float y = Tf[J * SB + k][I * SB + cc];
-            t0 += Tf[I * SB + r2][I * SB + k] * y;
-            t1 += Tf[I * SB + r2 + 1][I * SB + k] * y;
+        for (int q = 0; q < SB / 4; ++q) {
+            const float4 b0 = ld4(&Tf[I * SB + r2][I * SB + 4 * q]);
+            const float4 b1 = ld4(&Tf[I * SB + r2 + 1][I * SB + 4 * q]);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float y = Tf[J * SB + 4 * q + e][I * SB + cc];
+                t0 += f4(b0, e) * y;
+                t1 += f4(b1, e) * y;
+            }
         }
         Tf[I * SB + r2][J * SB + cc] = -t0;
         Tf[I * SB + r2 + 1][J * SB + cc] = -t1;
@@ -417,24 +440,30 @@ __device__ __forceinline__ void chunk_inverse(float (*akk)[LDA], float (*Tf)[LDA
         const int r2 = (tid >> 4) * 2, c2 = (tid & 15) * 2;
         const int k0 = c2 < SB ? 0 : SB;            // T[0:32,0:32] is zero above its blocks
         float y00 = 0.f, y01 = 0.f, y10 = 0.f, y11 = 0.f;
-#pragma unroll 8
-        for (int k = k0; k < 32; ++k) {
-            const float2 t = *reinterpret_cast<const float2*>(&Tf[k][c2]);
-            const float a0 = akk[32 + r2][k], a1 = akk[32 + r2 + 1][k];
-            y00 += a0 * t.x; y01 += a0 * t.y;
-            y10 += a1 * t.x; y11 += a1 * t.y;
+#pragma unroll 2
+        for (int k = k0; k < 32; k += 4) {
+            const float4 a0 = ld4(&akk[32 + r2][k]), a1 = ld4(&akk[32 + r2 + 1][k]);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 t = *reinterpret_cast<const float2*>(&Tf[k + e][c2]);
+                y00 += f4(a0, e) * t.x; y01 += f4(a0, e) * t.y;
+                y10 += f4(a1, e) * t.x; y11 += f4(a1, e) * t.y;
+            }
         }
         *reinterpret_cast<float2*>(&Tf[r2][32 + c2]) = make_float2(y00, y01);
         *reinterpret_cast<float2*>(&Tf[r2 + 1][32 + c2]) = make_float2(y10, y11);
         __syncthreads();
         const int k1 = r2 < SB ? SB : 32;            // T[32:64,32:64] likewise
         float t00 = 0.f, t01 = 0.f, t10 = 0.f, t11 = 0.f;
-#pragma unroll 8
-        for (int k = 0; k < k1; ++k) {
-            const float2 y = *reinterpret_cast<const float2*>(&Tf[k][32 + c2]);
-            const float b0 = Tf[32 + r2][32 + k], b1 = Tf[32 + r2 + 1][32 + k];
-            t00 += b0 * y.x; t01 += b0 * y.y;
-            t10 += b1 * y.x; t11 += b1 * y.y;
+#pragma unroll 2
+        for (int k = 0; k < k1; k += 4) {
+            const float4 b0 = ld4(&Tf[32 + r2][32 + k]), b1 = ld4(&Tf[32 + r2 + 1][32 + k]);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 y = *reinterpret_cast<const float2*>(&Tf[k + e][32 + c2]);
+                t00 += f4(b0, e) * y.x; t01 += f4(b0, e) * y.y;
+                t10 += f4(b1, e) * y.x; t11 += f4(b1, e) * y.y;
+            }
         }
         *reinterpret_cast<float2*>(&Tf[32 + r2][c2]) = make_float2(-t00, -t01);
         *reinterpret_cast<float2*>(&Tf[32 + r2 + 1][c2]) = make_float2(-t10, -t11);
@@ -445,11 +474,14 @@ __device__ __forceinline__ void chunk_inverse(float (*akk)[LDA], float (*Tf)[LDA
     for (int u = 0; u < 2; ++u) {
         const int e = tid + u * NT;                  // 512 pieces of 8
         const int i = e / 8, j0 = (e % 8) * 8;
+        const float4 ta = ld4(&Tf[i][j0]), tb = ld4(&Tf[i][j0 + 4]);
+        const float4 ba = ld4(sbeta + j0), bb = ld4(sbeta + j0 + 4);
         float v8[8];
 #pragma unroll
         for (int x = 0; x < 8; ++x) {
-            const int j = j0 + x;
-            v8[x] = (j <= i) ? Tf[i][j] * sbeta[j] : 0.f;
+            const float tv = x < 4 ? f4(ta, x) : f4(tb, x - 4);
+            const float bv = x < 4 ? f4(ba, x) : f4(bb, x - 4);
+            v8[x] = (j0 + x <= i) ? tv * bv : 0.f;
         }
         st8(tp, 0, i, j0, v8);
     }
