@@ -15,6 +15,8 @@ Contents
     algorithm for the same result.
   * ``exact_scalar`` (submodule): exact rational evaluation of the K = V = 1
     case by its explicit-sum closed form.
+  * ``output_gate`` (submodule): the output gate with gated RMSNorm applied to
+    the attention output, in float64.
 
 Pages followed: XTuner "Add opt-in FP32 KDA chunk computation" (sections
 Problem, Change, Validation: an independent FP64 recurrence is the
