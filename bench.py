@@ -57,6 +57,8 @@ def parse_args():
                    help="time kda_chunk_fwd_gated instead of kda_gate + kda_chunk_fwd")
     p.add_argument("--single-pass", action="store_true",
                    help="BF16 tensor-core path without a workspace (one kernel per call)")
+    p.add_argument("--output-gate", action="store_true",
+                   help="add the output gate with gated RMSNorm (kda_gated_rmsnorm) to the step")
     return p.parse_args()
 
 
@@ -264,7 +266,7 @@ def main():
     import __graft_entry__
     __graft_entry__.build()
     from kimi_delta_attention_10_gb300 import (chunk_workspace_size, kda_chunk_fwd,
-                                               kda_chunk_fwd_gated, kda_gate)
+                                               kda_chunk_fwd_gated, kda_gate, kda_gated_rmsnorm)
     from kimi_delta_attention_10_gb300.inputs import WORKLOAD_BY_NAME, workload_inputs
 
     mode = args.mode or "bf16_tc"
@@ -283,6 +285,12 @@ def main():
     ws = (torch.empty(chunk_workspace_size(N, T, H, K, V), dtype=torch.uint8, device=dev)
           if two_phase else None)
     stream = torch.cuda.current_stream(dev)
+    if args.output_gate:
+        # synthetic output-gate pre-activation and weight (the module's g_b_proj output)
+        gen = torch.Generator().manual_seed(7)
+        zg = torch.randn(T, H, V, generator=gen).to(out_dtype).to(dev)
+        wg = (torch.rand(V, generator=gen) + 0.5).to(dev)
+        yg = torch.empty(T, H, V, dtype=out_dtype, device=dev)
 
     def step(ev=None):
         if ev is not None:
@@ -300,6 +308,10 @@ def main():
                                 final_state=fs, cu_seqlens_host=cu_host, workspace=ws)
         if ev is not None:
             ev[2].record(stream)
+        if args.output_gate:
+            kda_gated_rmsnorm(out, zg, wg, eps=1e-6, out=yg)
+            if ev is not None:
+                ev[3].record(stream)
 
     def barrier():
         if world > 1:
@@ -310,7 +322,7 @@ def main():
     for _ in range(args.warmup):
         step()
     barrier()
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     gpu_index = local_rank
     vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
     if vis and all(s.strip().isdigit() for s in vis.split(",")):
@@ -374,6 +386,8 @@ def main():
                                     db["dt_bias"], db["b"], db["cu_seqlens"], x.scale, mode=mode,
                                     out=outs[b], final_state=fss[b], cu_seqlens_host=cu_host,
                                     workspace=ws)
+            if args.output_gate:                   # y in place of o: the step's result
+                kda_gated_rmsnorm(outs[b], zg, wg, eps=1e-6, out=outs[b])
             ev_comp[b].record(stream)
 
         def download(i):
@@ -446,6 +460,12 @@ def main():
                                 16384 / (H200_CHUNK_US_16384 * 1e-6))},
                 "gpu_launches": ((0 if args.fused else 1) + (3 if two_phase else 1)) * args.steps,
                 "clocks": clk, "e2e": e2e}
+        if args.output_gate:
+            og_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
+            line["kernels"]["kda_gated_rmsnorm_ms"] = og_ms
+            line["kernels"]["kda_gated_rmsnorm_GBps"] = T * H * V * 3 * out.element_size() / og_ms / 1e6
+            line["gpu_launches"] += args.steps
+            cfg["step"] += " + kda_gated_rmsnorm"
         if (not args.fused):
             line["kernels"]["kda_gate_ms"] = statistics.mean(gate_ms)
             line["kernels"]["kda_gate_GBps"] = gate_bytes(T, H, K) / statistics.mean(gate_ms) / 1e6

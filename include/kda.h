@@ -240,12 +240,37 @@ kda_status kda_recurrent_step(const void* q, const void* k, const void* v, int32
                               float* state, void* out, int32_t out_dtype,
                               kda_stream_t stream);
 
+/*
+ * kda_gated_rmsnorm -- the output gate with gated RMSNorm applied to the
+ * attention output, per (token, head) row of V values:
+ *
+ *   y[r, v] = o[r, v] / sqrt(mean_v' o[r, v']^2 + eps) * weight[v] * sigmoid(z[r, v])
+ *
+ * The pages name the low-rank output gate (g_a_proj -> g_b_proj) and the
+ * "gated-norm" wrapper of the KDA module without printing a formula ("GLM-5.3-
+ * Flash F6.2: KDA correctness and FLA sequence parallelism", module and FLA-SP
+ * commits); this is the plain reading of them.
+ *
+ *   o      [rows, V]  o_dtype (F32 or BF16)   attention output, rows = T * H
+ *   z      [rows, V]  z_dtype (F32 or BF16)   output-gate pre-activation
+ *   weight [V]        F32                     per-channel weight, shared by heads
+ *   eps    >= 0
+ *   y      [rows, V]  y_dtype (F32 or BF16)   may alias o when y_dtype == o_dtype
+ * FP32 arithmetic.  V = 128 (else KDA_ERR_UNSUPPORTED); rows = 0 launches
+ * nothing and accepts NULL pointers.
+ */
+kda_status kda_gated_rmsnorm(const void* o, int32_t o_dtype, const void* z, int32_t z_dtype,
+                             const float* weight, int64_t rows, int32_t V, float eps, void* y,
+                             int32_t y_dtype, kda_stream_t stream);
+
 /* Static text for a kda_status value ("unknown status" otherwise). */
 const char* kda_status_string(int32_t status);
 
 /* ABI revision of this header; bumped on any incompatible change (2: initial
  * state argument of kda_chunk_fwd; kda_chunk_fwd_gated; kda_recurrent_step.
- * 3: workspace arguments; kda_chunk_workspace_size). */
+ * 3: workspace arguments; kda_chunk_workspace_size.  Later additions that
+ * change no existing signature keep the number: kda_chunk_fwd_static,
+ * kda_gated_rmsnorm). */
 int32_t kda_abi_version(void);
 
 #ifdef __cplusplus

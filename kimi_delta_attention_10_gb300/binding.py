@@ -34,7 +34,8 @@ MODES = {"bf16_tc": KDA_MODE_BF16_TC, "fp32_exact": KDA_MODE_FP32_EXACT}
 
 # Every symbol include/kda.h declares.
 EXPORTS = ("kda_gate", "kda_chunk_workspace_size", "kda_chunk_fwd", "kda_chunk_fwd_gated",
-           "kda_chunk_fwd_static", "kda_recurrent_step", "kda_status_string", "kda_abi_version")
+           "kda_chunk_fwd_static", "kda_recurrent_step", "kda_gated_rmsnorm", "kda_status_string",
+           "kda_abi_version")
 
 _lock = threading.Lock()
 _lib = None
@@ -82,6 +83,9 @@ def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.kda_recurrent_step.argtypes = [vp, vp, vp, i32, vp, vp, i32, i32, i32, i32,
                                            ctypes.c_float, i32, vp, vp, i32, vp]
         lib.kda_recurrent_step.restype = i32
+        lib.kda_gated_rmsnorm.argtypes = [vp, i32, vp, i32, vp, i64, i32, ctypes.c_float, vp, i32,
+                                          vp]
+        lib.kda_gated_rmsnorm.restype = i32
         lib.kda_status_string.argtypes = [i32]
         lib.kda_status_string.restype = ctypes.c_char_p
         lib.kda_abi_version.argtypes = []
@@ -299,4 +303,23 @@ def kda_recurrent_step(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: tor
         _dtype_code(out), _stream_handle(stream, q.device))
     if st != KDA_OK:
         raise KDAError(st, "kda_recurrent_step")
+    return out
+
+
+def kda_gated_rmsnorm(o: torch.Tensor, z: torch.Tensor, weight: torch.Tensor, eps: float = 1e-6,
+                      out: Optional[torch.Tensor] = None, out_dtype: Optional[torch.dtype] = None,
+                      stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """y = o / sqrt(mean(o^2) + eps) * weight * sigmoid(z) over the last dim (V = 128);
+    o and z of shape [..., V], weight [V] FP32.  Returns y (out if given)."""
+    lib = load_library()
+    V = o.shape[-1]
+    rows = o.numel() // V if V else 0
+    if out is None:
+        out = torch.empty(o.shape, dtype=out_dtype or o.dtype, device=o.device)
+    st = lib.kda_gated_rmsnorm(_dev_ptr(o, "o"), _dtype_code(o), _dev_ptr(z, "z"), _dtype_code(z),
+                               _dev_ptr(weight, "weight"), rows, V, float(eps),
+                               _dev_ptr(out, "out"), _dtype_code(out),
+                               _stream_handle(stream, o.device))
+    if st != KDA_OK:
+        raise KDAError(st, "kda_gated_rmsnorm")
     return out

@@ -250,4 +250,24 @@ kda_status kda_recurrent_step(const void* q, const void* k, const void* v, int32
     return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
+kda_status kda_gated_rmsnorm(const void* o, int32_t o_dtype, const void* z, int32_t z_dtype,
+                             const float* weight, int64_t rows, int32_t V, float eps, void* y,
+                             int32_t y_dtype, kda_stream_t stream)
+{
+    if (rows < 0 || V < 1 || !(eps >= 0.f)) return KDA_ERR_INVALID_ARG;
+    if (!valid_dtype(o_dtype) || !valid_dtype(z_dtype) || !valid_dtype(y_dtype))
+        return KDA_ERR_INVALID_ARG;
+    if (V != kda::kHeadV) return KDA_ERR_UNSUPPORTED;
+    if (rows == 0) return KDA_OK;
+    if (!o || !z || !weight || !y) return KDA_ERR_INVALID_ARG;
+    const void* ptrs[] = {o, z, weight, y};
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return KDA_ERR_ALIGNMENT;
+    if (y == o && y_dtype != o_dtype) return KDA_ERR_INVALID_ARG;
+    cudaError_t e = kda::launch_gated_rmsnorm(o, o_dtype == KDA_BF16, z, z_dtype == KDA_BF16,
+                                              weight, rows, eps, y, y_dtype == KDA_BF16,
+                                              reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
 }  // extern "C"

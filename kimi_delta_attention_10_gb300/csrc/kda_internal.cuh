@@ -76,6 +76,9 @@ int64_t split_workspace_bytes(int32_t N, int64_t T, int32_t H);
 constexpr int64_t kStaticScratchBytes = 64ll << 20;
 cudaError_t static_scratch(void** ptr);
 cudaError_t launch_recurrent_step(const StepArgs& a, cudaStream_t stream);
+cudaError_t launch_gated_rmsnorm(const void* o, bool o_bf16, const void* z, bool z_bf16,
+                                 const float* w, int64_t rows, float eps, void* y, bool y_bf16,
+                                 cudaStream_t stream);
 
 int device_sm_count();
 

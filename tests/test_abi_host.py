@@ -233,3 +233,25 @@ def test_static_scratch_limit_is_the_workspace_bound(lib):
         # at the limit the call gets past the size check (without a GPU it then
         # fails at the device set-up instead)
         assert static(lib, T=64 * lo, N=1, H=H) != binding.KDA_ERR_TOO_LARGE
+
+
+def grms(lib, **kw):
+    a = dict(o=P, odt=1, z=P, zdt=1, w=P, rows=10, V=128, eps=1e-6, y=P, ydt=1)
+    a.update(kw)
+    return lib.kda_gated_rmsnorm(a["o"], a["odt"], a["z"], a["zdt"], a["w"], a["rows"], a["V"],
+                                 a["eps"], a["y"], a["ydt"], None)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(V=64), binding.KDA_ERR_UNSUPPORTED),
+    (dict(rows=-1), binding.KDA_ERR_INVALID_ARG),
+    (dict(eps=-1.0), binding.KDA_ERR_INVALID_ARG),
+    (dict(eps=float("nan")), binding.KDA_ERR_INVALID_ARG),
+    (dict(odt=5), binding.KDA_ERR_INVALID_ARG),
+    (dict(z=None), binding.KDA_ERR_INVALID_ARG),
+    (dict(w=MIS), binding.KDA_ERR_ALIGNMENT),
+    (dict(ydt=0), binding.KDA_ERR_INVALID_ARG),          # y aliases o with another dtype
+    (dict(rows=0, o=None, z=None, w=None, y=None), binding.KDA_OK),
+])
+def test_gated_rmsnorm_rejects_bad_arguments(lib, kw, expect):
+    assert grms(lib, **kw) == expect
