@@ -17,6 +17,8 @@ Contents
     case by its explicit-sum closed form.
   * ``output_gate`` (submodule): the output gate with gated RMSNorm applied to
     the attention output, in float64.
+  * ``backward`` (submodule): the vector-Jacobian product of the recurrence
+    (dq, dk, dv, dg, dbeta, dS_0 from dO and dS_T), token by token in float64.
 
 Pages followed: XTuner "Add opt-in FP32 KDA chunk computation" (sections
 Problem, Change, Validation: an independent FP64 recurrence is the
