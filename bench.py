@@ -59,6 +59,8 @@ def parse_args():
                    help="BF16 tensor-core path without a workspace (one kernel per call)")
     p.add_argument("--output-gate", action="store_true",
                    help="add the output gate with gated RMSNorm (kda_gated_rmsnorm) to the step")
+    p.add_argument("--backward", action="store_true",
+                   help="also time kda_chunk_bwd (the VJP) on the workload, after the step")
     return p.parse_args()
 
 
@@ -153,6 +155,14 @@ def algorithmic_bytes(T, H, K, V, N, qkv_bytes, out_bytes):
     beta (FP32); write out and the FP32 final state."""
     per_token_head = (2 * K + V) * qkv_bytes + 4 * K + 4 + V * out_bytes
     return T * H * per_token_head + N * H * K * V * 4
+
+
+def backward_bytes(T, H, K, V, N, qkv_bytes, dout_bytes):
+    """Compulsory HBM bytes of one kda_chunk_bwd call: read q, k, v, g, beta, dout
+    and the final-state gradient; write dq, dk, dv, dg (FP32), dbeta and the
+    initial-state gradient."""
+    per_token_head = (2 * K + V) * qkv_bytes + 4 * K + 4 + V * dout_bytes + (3 * K + V) * 4 + 4
+    return T * H * per_token_head + 2 * N * H * K * V * 4
 
 
 def gate_bytes(T, H, K):
@@ -265,8 +275,9 @@ def main():
 
     import __graft_entry__
     __graft_entry__.build()
-    from kimi_delta_attention_10_gb300 import (chunk_workspace_size, kda_chunk_fwd,
-                                               kda_chunk_fwd_gated, kda_gate, kda_gated_rmsnorm)
+    from kimi_delta_attention_10_gb300 import (chunk_bwd_workspace_size, chunk_workspace_size,
+                                               kda_chunk_bwd, kda_chunk_fwd, kda_chunk_fwd_gated,
+                                               kda_gate, kda_gated_rmsnorm)
     from kimi_delta_attention_10_gb300.inputs import WORKLOAD_BY_NAME, workload_inputs
 
     mode = args.mode or "bf16_tc"
@@ -424,6 +435,35 @@ def main():
                "copies": "pinned host memory; step i+1's inputs in and step i-1's result out "
                          "overlap step i's compute (two device buffer sets, separate streams)"}
 
+    # The backward (VJP) of the forward on the same inputs, timed on its own.
+    bwd = None
+    if args.backward:
+        from kimi_delta_attention_10_gb300.inputs import make_cotangents
+        dO, dfin, _ = make_cotangents(T, N, H, K, V, 9, dout_dtype=x.v.dtype)
+        dO, dfin = dO.to(dev), dfin.to(dev)
+        bws = torch.empty(chunk_bwd_workspace_size(N, T, H, K, V), dtype=torch.uint8, device=dev)
+
+        def bstep():
+            return kda_chunk_bwd(d["q"], d["k"], d["v"], g, beta, d["cu_seqlens"], dO, x.scale,
+                                 dfinal_state=dfin, cu_seqlens_host=cu_host, workspace=bws)
+
+        bsteps = max(1, min(args.steps, 3))
+        bstep()
+        barrier()
+        b0 = torch.cuda.Event(enable_timing=True)
+        b1 = torch.cuda.Event(enable_timing=True)
+        b0.record(stream)
+        for _ in range(bsteps):
+            bstep()
+        b1.record(stream)
+        barrier()
+        bms = max_over_ranks(b0.elapsed_time(b1), dev) / bsteps
+        balg = backward_bytes(T, H, K, V, N, x.q.element_size(), dO.element_size())
+        bwd = {"call": "kda_chunk_bwd", "steps": bsteps, "ms": bms,
+               "tokens_per_s": whole_job_rate(world, T, 1, bms),
+               "algorithmic_bytes": balg, "achieved_GBps": balg / bms / 1e6,
+               "launches_per_call": 4}         # plan, recurrence VJP, two norm VJPs
+
     if rank == 0:
         qkv_bytes = x.q.element_size()
         out_bytes = out.element_size()
@@ -469,6 +509,10 @@ def main():
         if (not args.fused):
             line["kernels"]["kda_gate_ms"] = statistics.mean(gate_ms)
             line["kernels"]["kda_gate_GBps"] = gate_bytes(T, H, K) / statistics.mean(gate_ms) / 1e6
+        if bwd is not None:
+            peak_b, _ = measured_peaks()
+            bwd["frac_of_hbm_peak"] = bwd["achieved_GBps"] / peak_b
+            line["backward"] = bwd
         if world == 1 and not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(x, w)
         print(json.dumps(line), flush=True)

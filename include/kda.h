@@ -263,6 +263,56 @@ kda_status kda_gated_rmsnorm(const void* o, int32_t o_dtype, const void* z, int3
                              const float* weight, int64_t rows, int32_t V, float eps, void* y,
                              int32_t y_dtype, kda_stream_t stream);
 
+/*
+ * kda_chunk_bwd_workspace_size -- bytes of device scratch kda_chunk_bwd needs
+ * for N sequences of T packed tokens and H heads (K = V = 128, else
+ * KDA_ERR_UNSUPPORTED): the plan header, one K x V FP32 state per chunk per
+ * head (the checkpoints at every chunk start) and 64 states per persistent CTA
+ * (the states inside the chunk being walked backwards).
+ */
+kda_status kda_chunk_bwd_workspace_size(int32_t N, int64_t T, int32_t H, int32_t K, int32_t V,
+                                        int64_t* bytes_host);
+
+/*
+ * kda_chunk_bwd -- the vector-Jacobian product of kda_chunk_fwd: given dout,
+ * the gradient of a scalar loss with respect to every output row, and
+ * dfinal_state, with respect to every final state, returns the gradients with
+ * respect to q, k, v, g, beta and the initial state.  The pages check the
+ * chunked backward against FP64 budgets ("Add opt-in FP32 KDA chunk
+ * computation", section Validation) and print no formula; this is the chain
+ * rule applied by hand to the token recurrence the forward computes,
+ *   S'_t = Diag(e^{g_t}) S_{t-1},  d_t = beta_t (v_t - S'_t^T k^_t),
+ *   S_t = S'_t + k^_t d_t^T,        o_t = scale S_t^T q^_t,
+ * tokens walked backwards per (sequence, head), and then through the L2
+ * normalisation q^ = q / sqrt(|q|^2 + 1e-6) (k alike) when qk_l2norm = 1.
+ *
+ * Inputs are those of kda_chunk_fwd (q, k, v [T,H,K|V] qkv_dtype; g [T,H,K]
+ * and beta [T,H] F32; cu_seqlens device, cu_seqlens_host optional host copy
+ * checked as there; initial_state [N,H,K,V] F32 or NULL for zeros), plus
+ *   dout           [T,H,V]   dout_dtype (F32 or BF16)
+ *   dfinal_state   [N,H,K,V] F32 or NULL (zeros)
+ * Outputs, all F32 and written in full (every token of every sequence):
+ *   dq, dk [T,H,K], dv [T,H,V], dg [T,H,K], dbeta [T,H];
+ *   dinitial_state [N,H,K,V] or NULL (not computed).
+ * No output may alias an input.  workspace: device, 16-byte aligned, at least
+ * kda_chunk_bwd_workspace_size bytes, owned by the caller, contents on entry
+ * irrelevant; calls sharing one workspace must be ordered on one stream.
+ * FP32 arithmetic throughout (the forward is recomputed from the per-chunk
+ * checkpoints, so its rounding matches fp32_exact's token order, not BF16_TC).
+ * Errors as kda_chunk_fwd; offsets outside [0, T] seen on the device set
+ * KDA_ERR_DEVICE_ARG in status_dev and leave those sequences' outputs unwritten.
+ */
+kda_status kda_chunk_bwd(const void* q, const void* k, const void* v, int32_t qkv_dtype,
+                         const float* g, const float* beta,
+                         const int32_t* cu_seqlens, const int32_t* cu_seqlens_host,
+                         int32_t N, int64_t T, int32_t H, int32_t K, int32_t V,
+                         float scale, int32_t qk_l2norm,
+                         const void* dout, int32_t dout_dtype,
+                         const float* initial_state, const float* dfinal_state,
+                         float* dq, float* dk, float* dv, float* dg, float* dbeta,
+                         float* dinitial_state, void* workspace, int64_t workspace_bytes,
+                         int32_t* status_dev, kda_stream_t stream);
+
 /* Static text for a kda_status value ("unknown status" otherwise). */
 const char* kda_status_string(int32_t status);
 
@@ -270,7 +320,7 @@ const char* kda_status_string(int32_t status);
  * state argument of kda_chunk_fwd; kda_chunk_fwd_gated; kda_recurrent_step.
  * 3: workspace arguments; kda_chunk_workspace_size.  Later additions that
  * change no existing signature keep the number: kda_chunk_fwd_static,
- * kda_gated_rmsnorm). */
+ * kda_gated_rmsnorm, kda_chunk_bwd_workspace_size, kda_chunk_bwd). */
 int32_t kda_abi_version(void);
 
 #ifdef __cplusplus

@@ -34,8 +34,8 @@ MODES = {"bf16_tc": KDA_MODE_BF16_TC, "fp32_exact": KDA_MODE_FP32_EXACT}
 
 # Every symbol include/kda.h declares.
 EXPORTS = ("kda_gate", "kda_chunk_workspace_size", "kda_chunk_fwd", "kda_chunk_fwd_gated",
-           "kda_chunk_fwd_static", "kda_recurrent_step", "kda_gated_rmsnorm", "kda_status_string",
-           "kda_abi_version")
+           "kda_chunk_fwd_static", "kda_recurrent_step", "kda_gated_rmsnorm",
+           "kda_chunk_bwd_workspace_size", "kda_chunk_bwd", "kda_status_string", "kda_abi_version")
 
 _lock = threading.Lock()
 _lib = None
@@ -86,6 +86,12 @@ def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.kda_gated_rmsnorm.argtypes = [vp, i32, vp, i32, vp, i64, i32, ctypes.c_float, vp, i32,
                                           vp]
         lib.kda_gated_rmsnorm.restype = i32
+        lib.kda_chunk_bwd_workspace_size.argtypes = [i32, i64, i32, i32, i32, ctypes.POINTER(i64)]
+        lib.kda_chunk_bwd_workspace_size.restype = i32
+        lib.kda_chunk_bwd.argtypes = [vp, vp, vp, i32, vp, vp, vp, vp, i32, i64, i32, i32, i32,
+                                      ctypes.c_float, i32, vp, i32, vp, vp, vp, vp, vp, vp, vp,
+                                      vp, vp, i64, vp, vp]
+        lib.kda_chunk_bwd.restype = i32
         lib.kda_status_string.argtypes = [i32]
         lib.kda_status_string.restype = ctypes.c_char_p
         lib.kda_abi_version.argtypes = []
@@ -323,3 +329,53 @@ def kda_gated_rmsnorm(o: torch.Tensor, z: torch.Tensor, weight: torch.Tensor, ep
     if st != KDA_OK:
         raise KDAError(st, "kda_gated_rmsnorm")
     return out
+
+
+def chunk_bwd_workspace_size(N: int, T: int, H: int, K: int = 128, V: int = 128) -> int:
+    """Bytes of workspace kda_chunk_bwd needs."""
+    out = ctypes.c_int64(0)
+    st = load_library().kda_chunk_bwd_workspace_size(N, T, H, K, V, ctypes.byref(out))
+    if st != KDA_OK:
+        raise KDAError(st, "kda_chunk_bwd_workspace_size")
+    return out.value
+
+
+def kda_chunk_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor,
+                  beta: torch.Tensor, cu_seqlens: torch.Tensor, dout: torch.Tensor,
+                  scale: Optional[float] = None, dfinal_state: Optional[torch.Tensor] = None,
+                  initial_state: Optional[torch.Tensor] = None, want_dinitial: bool = True,
+                  cu_seqlens_host: Optional[Sequence[int]] = None, qk_l2norm: bool = True,
+                  status: Optional[torch.Tensor] = None,
+                  stream: Optional[torch.cuda.Stream] = None, workspace=None):
+    """Backward of kda_chunk_fwd.  Returns FP32 (dq, dk, dv, dg, dbeta, dinitial_state
+    or None).  workspace: None (a fresh buffer) or a CUDA tensor of at least
+    chunk_bwd_workspace_size(...) bytes."""
+    lib = load_library()
+    T, H, K = q.shape
+    V = v.shape[2]
+    N = cu_seqlens.numel() - 1
+    if scale is None:
+        scale = K ** -0.5
+    dev = q.device
+    f32 = dict(dtype=torch.float32, device=dev)
+    dq, dk, dg = (torch.empty((T, H, K), **f32) for _ in range(3))
+    dv = torch.empty((T, H, V), **f32)
+    dbeta = torch.empty((T, H), **f32)
+    dinit = torch.empty((N, H, K, V), **f32) if want_dinitial else None
+    if workspace is None:
+        workspace = torch.empty(chunk_bwd_workspace_size(N, T, H, K, V), dtype=torch.uint8,
+                                device=dev)
+    keep, host = _host_offsets(cu_seqlens_host)
+    st = lib.kda_chunk_bwd(
+        _dev_ptr(q, "q"), _dev_ptr(k, "k"), _dev_ptr(v, "v"), _dtype_code(q),
+        _dev_ptr(g, "g"), _dev_ptr(beta, "beta"), _dev_ptr(cu_seqlens, "cu_seqlens"), host,
+        N, T, H, K, V, float(scale), 1 if qk_l2norm else 0,
+        _dev_ptr(dout, "dout"), _dtype_code(dout), _dev_ptr(initial_state, "initial_state"),
+        _dev_ptr(dfinal_state, "dfinal_state"), _dev_ptr(dq, "dq"), _dev_ptr(dk, "dk"),
+        _dev_ptr(dv, "dv"), _dev_ptr(dg, "dg"), _dev_ptr(dbeta, "dbeta"),
+        _dev_ptr(dinit, "dinitial_state"), _dev_ptr(workspace, "workspace"),
+        workspace.numel() * workspace.element_size(), _dev_ptr(status, "status"),
+        _stream_handle(stream, dev))
+    if st != KDA_OK:
+        raise KDAError(st, "kda_chunk_bwd")
+    return dq, dk, dv, dg, dbeta, dinit

@@ -270,4 +270,48 @@ kda_status kda_gated_rmsnorm(const void* o, int32_t o_dtype, const void* z, int3
     return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
+kda_status kda_chunk_bwd_workspace_size(int32_t N, int64_t T, int32_t H, int32_t K, int32_t V,
+                                        int64_t* bytes_host)
+{
+    if (!bytes_host) return KDA_ERR_INVALID_ARG;
+    if (N < 0 || T < 0 || H < 1 || K < 1 || V < 1) return KDA_ERR_INVALID_ARG;
+    if (T > INT32_MAX) return KDA_ERR_UNSUPPORTED;
+    if (K != kda::kHeadK || V != kda::kHeadV) return KDA_ERR_UNSUPPORTED;
+    *bytes_host = kda::bwd_workspace_bytes(N, T, H);
+    return KDA_OK;
+}
+
+kda_status kda_chunk_bwd(const void* q, const void* k, const void* v, int32_t qkv_dtype,
+                         const float* g, const float* beta,
+                         const int32_t* cu_seqlens, const int32_t* cu_seqlens_host,
+                         int32_t N, int64_t T, int32_t H, int32_t K, int32_t V,
+                         float scale, int32_t qk_l2norm,
+                         const void* dout, int32_t dout_dtype,
+                         const float* initial_state, const float* dfinal_state,
+                         float* dq, float* dk, float* dv, float* dg, float* dbeta,
+                         float* dinitial_state, void* workspace, int64_t workspace_bytes,
+                         int32_t* status_dev, kda_stream_t stream)
+{
+    kda_status st = check_chunk(q, k, v, qkv_dtype, cu_seqlens, cu_seqlens_host, N, T, H, K, V,
+                                qk_l2norm, KDA_MODE_FP32_EXACT, dout, dout_dtype, initial_state,
+                                dfinal_state, status_dev);
+    if (st != KDA_OK) return st;
+    if (T > 0 && (!g || !beta || !dq || !dk || !dv || !dg || !dbeta)) return KDA_ERR_INVALID_ARG;
+    if (N > 0 && !workspace) return KDA_ERR_INVALID_ARG;
+    const void* ptrs[] = {g, beta, dq, dk, dv, dg, dbeta, dinitial_state, workspace};
+    for (const void* p : ptrs)
+        if (p && !aligned16(p)) return KDA_ERR_ALIGNMENT;
+    if (N > 0 && workspace_bytes < kda::bwd_workspace_bytes(N, T, H)) return KDA_ERR_INVALID_ARG;
+    if (N == 0) return KDA_OK;
+    kda::BwdLaunch a = {};
+    a.q = q; a.k = k; a.v = v; a.qkv_bf16 = qkv_dtype == KDA_BF16; a.g = g; a.beta = beta;
+    a.cu = cu_seqlens; a.N = N; a.T = T; a.H = H; a.scale = scale; a.l2norm = qk_l2norm;
+    a.dout = dout; a.dout_bf16 = dout_dtype == KDA_BF16;
+    a.init = initial_state; a.dfinal = dfinal_state;
+    a.dq = dq; a.dk = dk; a.dv = dv; a.dg = dg; a.dbeta = dbeta; a.dinit = dinitial_state;
+    a.workspace = workspace; a.status = status_dev;
+    cudaError_t e = kda::launch_chunk_bwd(a, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
 }  // extern "C"

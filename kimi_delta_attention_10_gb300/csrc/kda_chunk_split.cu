@@ -741,6 +741,16 @@ cudaError_t static_scratch(void** ptr)
     return cudaSuccess;
 }
 
+int64_t chunk_plan_header_bytes(int32_t N) { return header_bytes(N); }
+
+cudaError_t launch_chunk_plan(const int32_t* cu, int32_t N, int64_t T, int32_t* hdr,
+                              int32_t* status, cudaStream_t stream)
+{
+    static_assert(kHdrOff == kPlanOffsets, "plan header layout");
+    chunk_plan_kernel<<<1, 1024, 0, stream>>>(cu, N, T, hdr, status);
+    return cudaGetLastError();
+}
+
 int64_t split_chunk_bound(int32_t N, int64_t T) { return T / kChunk + N; }
 
 int64_t split_workspace_bytes(int32_t N, int64_t T, int32_t H)

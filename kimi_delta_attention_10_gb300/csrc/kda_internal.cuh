@@ -70,6 +70,12 @@ cudaError_t launch_chunk_tc(const ChunkArgs& a, cudaStream_t stream);
 // Two-phase path; `chunks` bounds the number of chunks over all sequences.
 cudaError_t launch_chunk_split(const ChunkArgs& a, int64_t chunks, cudaStream_t stream);
 int64_t split_chunk_bound(int32_t N, int64_t T);
+// The plan kernel: int32 header with [0] = bad-offsets flag and, from
+// [kPlanOffsets], the per-sequence chunk offsets (N + 1 of them).
+constexpr int kPlanOffsets = 4;
+int64_t chunk_plan_header_bytes(int32_t N);
+cudaError_t launch_chunk_plan(const int32_t* cu, int32_t N, int64_t T, int32_t* hdr,
+                              int32_t* status, cudaStream_t stream);
 int64_t split_workspace_bytes(int32_t N, int64_t T, int32_t H);
 // The static scratch of kda_chunk_fwd_static and its size; static_scratch()
 // returns its address on the current device (looked up once per device).
@@ -79,6 +85,36 @@ cudaError_t launch_recurrent_step(const StepArgs& a, cudaStream_t stream);
 cudaError_t launch_gated_rmsnorm(const void* o, bool o_bf16, const void* z, bool z_bf16,
                                  const float* w, int64_t rows, float eps, void* y, bool y_bf16,
                                  cudaStream_t stream);
+
+// Backward (kda_chunk_bwd): FP32 outputs, workspace of bwd_workspace_bytes.
+struct BwdLaunch {
+    const void* q;
+    const void* k;
+    const void* v;
+    bool qkv_bf16;
+    const float* g;
+    const float* beta;
+    const int32_t* cu;
+    int32_t N;
+    int64_t T;
+    int32_t H;
+    float scale;
+    int32_t l2norm;
+    const void* dout;
+    bool dout_bf16;
+    const float* init;     // [N,H,K,V] or nullptr
+    const float* dfinal;   // [N,H,K,V] or nullptr
+    float* dq;
+    float* dk;
+    float* dv;
+    float* dg;
+    float* dbeta;
+    float* dinit;          // or nullptr
+    void* workspace;
+    int32_t* status;
+};
+int64_t bwd_workspace_bytes(int32_t N, int64_t T, int32_t H);
+cudaError_t launch_chunk_bwd(const BwdLaunch& a, cudaStream_t stream);
 
 int device_sm_count();
 

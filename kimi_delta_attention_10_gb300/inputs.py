@@ -150,3 +150,15 @@ def workload_seqlens(w: Workload | str | int) -> List[int]:
         return list(w.seqlens)
     gen = torch.Generator().manual_seed(w.seed)
     return draw_packed_lengths(gen, w.total_tokens, w.max_len)
+
+
+def make_cotangents(T: int, N: int, H: int, K: int, V: int, seed: int,
+                    dout_dtype: torch.dtype = torch.float32):
+    """Seeded draws for a backward call: dout [T,H,V] ~ N(0,1) in ``dout_dtype``,
+    dfinal_state [N,H,K,V] ~ N(0,1) and initial_state [N,H,K,V] ~ N(0, 0.5^2),
+    both FP32, in that order from one generator."""
+    gen = torch.Generator().manual_seed(seed)
+    dout = torch.randn(T, H, V, generator=gen, dtype=torch.float32).to(dout_dtype)
+    dfinal = torch.randn(N, H, K, V, generator=gen, dtype=torch.float32)
+    init = torch.randn(N, H, K, V, generator=gen, dtype=torch.float32) * 0.5
+    return dout, dfinal, init

@@ -255,3 +255,54 @@ def grms(lib, **kw):
 ])
 def test_gated_rmsnorm_rejects_bad_arguments(lib, kw, expect):
     assert grms(lib, **kw) == expect
+
+
+def bwd(lib, **kw):
+    a = dict(q=P, k=P, v=P, qkv=1, g=P, beta=P, cu=P, host=None, N=1, T=100, H=2, K=128, V=128,
+             scale=0.1, l2=1, dout=P, ddt=1, init=None, dfin=None, dq=P, dk=P, dv=P, dg=P, db=P,
+             dinit=None, ws=P, wsb=1 << 40, status=None)
+    a.update(kw)
+    host = a["host"]
+    hp = None
+    if host is not None:
+        arr = (ctypes.c_int32 * len(host))(*host)
+        hp = ctypes.cast(arr, ctypes.c_void_p)
+    return lib.kda_chunk_bwd(a["q"], a["k"], a["v"], a["qkv"], a["g"], a["beta"], a["cu"], hp,
+                             a["N"], a["T"], a["H"], a["K"], a["V"], a["scale"], a["l2"],
+                             a["dout"], a["ddt"], a["init"], a["dfin"], a["dq"], a["dk"], a["dv"],
+                             a["dg"], a["db"], a["dinit"], a["ws"], a["wsb"], a["status"], None)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(K=64), binding.KDA_ERR_UNSUPPORTED),
+    (dict(ddt=5), binding.KDA_ERR_INVALID_ARG),
+    (dict(dout=None), binding.KDA_ERR_INVALID_ARG),
+    (dict(dq=None), binding.KDA_ERR_INVALID_ARG),
+    (dict(db=None), binding.KDA_ERR_INVALID_ARG),
+    (dict(ws=None), binding.KDA_ERR_INVALID_ARG),
+    (dict(ws=MIS), binding.KDA_ERR_ALIGNMENT),
+    (dict(dg=MIS), binding.KDA_ERR_ALIGNMENT),
+    (dict(dinit=MIS), binding.KDA_ERR_ALIGNMENT),
+    (dict(wsb=1024), binding.KDA_ERR_INVALID_ARG),
+    (dict(host=[0, 99]), binding.KDA_ERR_INVALID_ARG),      # cu[N] != T
+    (dict(l2=2), binding.KDA_ERR_INVALID_ARG),
+    (dict(N=0, T=0, ws=None, q=None, k=None, v=None, dout=None, dq=None, dk=None, dv=None,
+          dg=None, db=None), binding.KDA_OK),
+])
+def test_chunk_bwd_rejects_bad_arguments(lib, kw, expect):
+    assert bwd(lib, **kw) == expect
+
+
+def test_bwd_workspace_size(lib):
+    def size(N, T, H):
+        out = ctypes.c_int64(0)
+        assert lib.kda_chunk_bwd_workspace_size(N, T, H, 128, 128, ctypes.byref(out)) == 0
+        return out.value
+    state = 128 * 128 * 4
+    # checkpoints: (T/64 + N) states per head; scratch: 64 states per CTA (<= 256 CTAs)
+    assert size(1, 16384, 64) - size(1, 16384 - 64, 64) == 64 * state
+    assert size(3, 100, 2) - size(3, 100, 1) == (100 // 64 + 3) * state + 3 * 64 * state
+    assert size(1, 64, 256) == size(1, 64, 257) - 2 * state      # CTAs capped at 256
+    out = ctypes.c_int64(0)
+    assert lib.kda_chunk_bwd_workspace_size(1, 64, 1, 64, 128, ctypes.byref(out)) == \
+        binding.KDA_ERR_UNSUPPORTED
