@@ -165,6 +165,15 @@ def backward_bytes(T, H, K, V, N, qkv_bytes, dout_bytes):
     return T * H * per_token_head + 2 * N * H * K * V * 4
 
 
+def chunk_windows(N, H, chunks, sms):
+    """Chunk windows of one two-phase kda_chunk_fwd call: min(4, chunks // 32)
+    when N * H <= the SM count (the rule in kda_chunk_split.cu), else one.
+    The call launches the plan, then one preparation and one scan per window."""
+    if N * H <= sms:
+        return max(1, min(4, chunks // 32))
+    return 1
+
+
 def gate_bytes(T, H, K):
     return T * H * K * (4 + 4) + T * H * (4 + 4)
 
@@ -474,7 +483,10 @@ def main():
         kname = "kda_chunk_fwd" if (not args.fused) else "kda_chunk_fwd_gated"
         variant = "two_phase" if two_phase else ("single_pass" if mode == "bf16_tc" else mode)
         kernel_key = f"{kname}:{variant}:{w.name}"
-        what = {"two_phase": "two-phase call: plan + chunk preparation + state scan",
+        windows = chunk_windows(N, H, sum(-(-L // 64) for L in x.seqlens),
+                                torch.cuda.get_device_properties(dev).multi_processor_count)
+        what = {"two_phase": f"two-phase call: plan, then chunk preparation and state scan "
+                             f"in {windows} chunk window(s)",
                 "single_pass": "single-pass kernel"}.get(variant, "FP32-exact kernel")
         roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "traffic": kernel_traffic(kernel_key),
@@ -498,7 +510,8 @@ def main():
                             "chunk_tokens_per_s": chunk_tps,
                             "context_h200_chunk_fwd_ratio": chunk_tps / (
                                 16384 / (H200_CHUNK_US_16384 * 1e-6))},
-                "gpu_launches": ((0 if args.fused else 1) + (3 if two_phase else 1)) * args.steps,
+                "gpu_launches": ((0 if args.fused else 1) +
+                                 (1 + 2 * windows if two_phase else 1)) * args.steps,
                 "clocks": clk, "e2e": e2e}
         if args.output_gate:
             og_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)

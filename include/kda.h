@@ -104,9 +104,17 @@ kda_status kda_gate(const void* f, int32_t f_dtype, const float* A_log, const fl
  * single pass per (sequence, head) that does all of a chunk's work in order.
  * KDA_MODE_FP32_EXACT uses no workspace (*bytes_host = 0).
  *
+ * When N * H is at most the GPU's SM count (the scan then leaves SMs idle)
+ * and there are at least 64 chunks, the chunks are cut into up to 4 windows
+ * launched as prep(0), scan(0), prep(1), scan(1), ... on the caller's stream,
+ * each preparation after the first with programmatic dependent launch, so
+ * that it runs on the SMs the scan before it leaves free.  Results are bit
+ * for bit those of one window.
+ *
  * The size is a bound that holds for every cu_seqlens with these N and T:
- * a 1 KiB-aligned header of N + 5 int32, plus (T / 64 + N) * H records of
- * 74240 bytes.  Arguments as kda_chunk_fwd; *bytes_host is host memory.
+ * a 1 KiB-aligned header of N + 5 int32, (T / 64 + N) * H records of 74240
+ * bytes, and N * H * K * V FP32 (the state carried between windows).
+ * Arguments as kda_chunk_fwd; *bytes_host is host memory.
  */
 kda_status kda_chunk_workspace_size(int32_t N, int64_t T, int32_t H, int32_t K, int32_t V,
                                     int32_t mode, int64_t* bytes_host);

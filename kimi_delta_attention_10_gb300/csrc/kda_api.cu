@@ -96,7 +96,8 @@ kda_status check_chunk(const void* q, const void* k, const void* v, int32_t qkv_
 
 // Workspace checks (BF16_TC only) and dispatch.
 kda_status launch_chunk(kda::ChunkArgs a, int32_t mode, const int32_t* cu_seqlens_host,
-                        void* workspace, int64_t workspace_bytes, kda_stream_t stream)
+                        void* workspace, int64_t workspace_bytes, kda_stream_t stream,
+                        bool overlap = true)
 {
     const bool split = mode == KDA_MODE_BF16_TC && workspace != nullptr;
     if (split) {
@@ -114,7 +115,7 @@ kda_status launch_chunk(kda::ChunkArgs a, int32_t mode, const int32_t* cu_seqlen
             for (int32_t n = 0; n < a.N; ++n)
                 chunks += (cu_seqlens_host[n + 1] - cu_seqlens_host[n] + kda::kChunk - 1) / kda::kChunk;
         }
-        e = kda::launch_chunk_split(a, chunks, s);
+        e = kda::launch_chunk_split(a, chunks, overlap, s);
     } else {
         e = (mode == KDA_MODE_BF16_TC) ? kda::launch_chunk_tc(a, s) : kda::launch_chunk_fp32(a, s);
     }
@@ -223,8 +224,9 @@ kda_status kda_chunk_fwd_static(const void* q, const void* k, const void* v, int
     kda::ChunkArgs a = chunk_args(q, k, v, qkv_dtype, cu_seqlens, N, T, H, scale, qk_l2norm, out,
                                   out_dtype, initial_state, final_state, status_dev);
     a.g = g; a.beta = beta; a.gated = false;
+    // one window: the schedule the bit-for-bit tests compare the windows with
     return launch_chunk(a, KDA_MODE_BF16_TC, cu_seqlens_host, scratch, kda::kStaticScratchBytes,
-                        stream);
+                        stream, false);
 }
 
 kda_status kda_recurrent_step(const void* q, const void* k, const void* v, int32_t qkv_dtype,

@@ -146,7 +146,8 @@ constexpr uint32_t P_TM_A = 0, P_TM_W = 0, P_TM_U = 64, P_TM_COLS = 256;
 template <typename TIn, bool kGated>
 __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(ChunkArgs args,
                                                            const int32_t* __restrict__ hdr,
-                                                           unsigned char* __restrict__ records)
+                                                           unsigned char* __restrict__ records,
+                                                           int64_t unit_base, int32_t wait_primary)
 {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     const uint32_t raw_s = smem_u32(smem_raw);
@@ -160,8 +161,12 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(ChunkArgs args,
     const int ch = tid & 127, hh = tid >> 7;               // channel / token-half ownership
     const int H = args.H;
 
+    // A window launched beside the previous window's scan (programmatic
+    // dependent launch) completes only after that scan: its last CTA waits for
+    // it, so the next scan, launched after this grid, sees the state carry.
+    if (wait_primary && blockIdx.x == gridDim.x - 1 && tid == 0) grid_dependency_wait();
     const int32_t* off = hdr + kHdrOff;
-    const int64_t unit = blockIdx.x;
+    const int64_t unit = unit_base + blockIdx.x;
     const int32_t gc = (int32_t)(unit / H);
     const int h = (int)(unit % H);
     if (gc >= off[args.N]) return;
@@ -442,10 +447,22 @@ constexpr uint32_t S_TM_WS = 0, S_TM_O = 64, S_TM_P = 128, S_TM_REGION = 256, S_
 __device__ __forceinline__ void store_out(float* p, float x) { *p = x; }
 __device__ __forceinline__ void store_out(__nv_bfloat16* p, float x) { *p = __float2bfloat16_rn(x); }
 
+// The scan of the chunks whose global index lies in [g0, g1): a sequence
+// whose chunks span several windows enters each later window with the state
+// the previous one left in `carry` ([N,H,K,V] FP32, workspace).  The window
+// holding a sequence's last chunk (for an empty sequence, the last window)
+// writes its final state.
+struct ScanWindow {
+    int32_t g0, g1;
+    float* carry;
+    int32_t last;
+};
+
 template <typename TOut>
 __global__ void __launch_bounds__(SCAN_THREADS, 1) chunk_scan_kernel(ChunkArgs args,
                                                                      const int32_t* __restrict__ hdr,
-                                                                     const unsigned char* __restrict__ records)
+                                                                     const unsigned char* __restrict__ records,
+                                                                     ScanWindow win)
 {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     const uint32_t raw_s = smem_u32(smem_raw);
@@ -459,12 +476,23 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) chunk_scan_kernel(ChunkArgs a
     const int row = 32 * quad + lane;                      // TMEM lane = state row v
     const int H = args.H;
     const int n = blockIdx.x / H, h = blockIdx.x % H;
+    // the next preparation window may start on the SMs this grid leaves free
+    launch_dependents();
 
-    const int bos = args.cu_seqlens[n], eos = args.cu_seqlens[n + 1];
+    const int eos = args.cu_seqlens[n + 1];
+    int bos = args.cu_seqlens[n];
     if (bos < 0 || eos < bos || (int64_t)eos > args.T) return;   // reported by the plan
-    const int nch = (eos - bos + C - 1) / C;
+    const int nch_all = (eos - bos + C - 1) / C;
+    const int offn = hdr[kHdrOff + n];
+    const int cb = min(max(win.g0 - offn, 0), nch_all), ce = min(max(win.g1 - offn, 0), nch_all);
+    const bool writes_final = (cb < ce && ce == nch_all) || (nch_all == 0 && win.last);
+    if (cb == ce && !writes_final) return;                 // no chunk of this sequence here
+    const float* state_in = cb == 0 ? args.initial_state : win.carry;
+    float* state_out = writes_final ? args.final_state : win.carry;
+    bos += cb * C;                                         // the window's chunks, from 0
+    const int nch = ce - cb;
     const int64_t rstride = (int64_t)H * REC_BYTES;
-    const unsigned char* rec0 = records + ((int64_t)hdr[kHdrOff + n] * H + h) * REC_BYTES;
+    const unsigned char* rec0 = records + ((int64_t)(offn + cb) * H + h) * REC_BYTES;
     TOut* __restrict__ out = static_cast<TOut*>(args.out);
     // [0,1] record stages, [2] ws_done, [3] p_done, [4] delta_ready (NT),
     // [5] s_ready (NT), [6] drain after a failure, [7] o_done
@@ -475,8 +503,8 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) chunk_scan_kernel(ChunkArgs a
     // ---- the entering state (zero, or the caller's)
     float S[64];                                           // S^T[row][64 half + c]
     if (!ctrl) {
-        if (args.initial_state != nullptr) {
-            const float* s0 = args.initial_state + ((int64_t)n * H + h) * DK * DV;
+        if (state_in != nullptr) {
+            const float* s0 = state_in + ((int64_t)n * H + h) * DK * DV;
 #pragma unroll
             for (int u = 0; u < 64; ++u) S[u] = s0[(int64_t)(64 * half + u) * DV + row];
         } else {
@@ -669,8 +697,8 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) chunk_scan_kernel(ChunkArgs a
         if (fail) {
             *abort_flag = 1;
             if (tid == 0) report_status(args.status, KDA_ERR_TIMEOUT);
-        } else if (args.final_state != nullptr) {
-            float* fs = args.final_state + ((int64_t)n * H + h) * DK * DV;
+        } else if (state_out != nullptr) {
+            float* fs = state_out + ((int64_t)n * H + h) * DK * DV;
 #pragma unroll
             for (int u = 0; u < 64; ++u) fs[(int64_t)(64 * half + u) * DV + row] = S[u];
         }
@@ -682,27 +710,72 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) chunk_scan_kernel(ChunkArgs a
 
 // ---------------------------------------------------------------- launch
 template <typename TIn, bool kGated>
-cudaError_t launch_prep(const ChunkArgs& a, const int32_t* hdr, unsigned char* rec,
-                        int64_t units, cudaStream_t stream)
+cudaError_t launch_prep_typed(const ChunkArgs& a, const int32_t* hdr, unsigned char* rec,
+                              int64_t unit_base, int64_t units, bool beside_scan,
+                              cudaStream_t stream)
 {
     auto kern = chunk_prep_kernel<TIn, kGated>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)P_SMEM);
     if (e != cudaSuccess) return e;
-    kern<<<(unsigned)units, NT, P_SMEM, stream>>>(a, hdr, rec);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)units);
+    cfg.blockDim = dim3(NT);
+    cfg.dynamicSmemBytes = P_SMEM;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = beside_scan ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, a, hdr, rec, unit_base, (int32_t)(beside_scan ? 1 : 0));
 }
 
-template <typename TOut>
-cudaError_t launch_scan(const ChunkArgs& a, const int32_t* hdr, const unsigned char* rec,
-                        cudaStream_t stream)
+// Preparation of the (chunk, head) units [unit_base, unit_base + units);
+// `beside_scan`: launched to overlap the scan just before it on the stream.
+cudaError_t launch_prep(const ChunkArgs& a, const int32_t* hdr, unsigned char* rec,
+                        int64_t unit_base, int64_t units, bool beside_scan, cudaStream_t stream)
 {
-    auto kern = chunk_scan_kernel<TOut>;
+    if (units <= 0) return cudaSuccess;
+    if (a.gated)
+        return a.qkv_bf16
+                   ? launch_prep_typed<__nv_bfloat16, true>(a, hdr, rec, unit_base, units, beside_scan, stream)
+                   : launch_prep_typed<float, true>(a, hdr, rec, unit_base, units, beside_scan, stream);
+    return a.qkv_bf16
+               ? launch_prep_typed<__nv_bfloat16, false>(a, hdr, rec, unit_base, units, beside_scan, stream)
+               : launch_prep_typed<float, false>(a, hdr, rec, unit_base, units, beside_scan, stream);
+}
+
+cudaError_t launch_scan(const ChunkArgs& a, const int32_t* hdr, const unsigned char* rec,
+                        ScanWindow win, cudaStream_t stream)
+{
+    auto kern = a.out_bf16 ? chunk_scan_kernel<__nv_bfloat16> : chunk_scan_kernel<float>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)S_SMEM);
     if (e != cudaSuccess) return e;
-    kern<<<(unsigned)((int64_t)a.N * a.H), SCAN_THREADS, S_SMEM, stream>>>(a, hdr, rec);
+    kern<<<(unsigned)((int64_t)a.N * a.H), SCAN_THREADS, S_SMEM, stream>>>(a, hdr, rec, win);
     return cudaGetLastError();
+}
+
+// Overlap of preparation and scan, on the caller's stream alone.  The scan
+// keeps one CTA per (sequence, head) busy for the whole call; when those CTAs
+// leave most SMs idle (few long sequences), the chunks are cut into windows
+// and the launches go prep(0), scan(0), prep(1), scan(1), ...  Each scan
+// window lets the next preparation window start once all its CTAs are
+// resident (programmatic dependent launch), so that preparation fills the SMs
+// the scan leaves free; each scan is an ordinary launch, so it starts after
+// the preparation of its window, and that preparation's last CTA waits for
+// the previous scan.
+constexpr int kMaxWindows = 4;
+constexpr int kWindowChunks = 32;              // at least this many chunks per window
+constexpr bool kHalfLastWindow = true;         // the last window's scan runs alone: keep it short
+
+// Window w covers the global chunks [window_bound(w), window_bound(w + 1)).
+int64_t window_bound(int64_t chunks, int W, int w)
+{
+    if (w >= W) return chunks;
+    if (!kHalfLastWindow) return chunks * w / W;
+    return chunks * (2 * w) / (2 * W - 1);     // W - 1 windows of two halves, the last of one
 }
 
 // Scratch of the no-allocation entry point (kda_chunk_fwd_static): a
@@ -753,31 +826,43 @@ cudaError_t launch_chunk_plan(const int32_t* cu, int32_t N, int64_t T, int32_t* 
 
 int64_t split_chunk_bound(int32_t N, int64_t T) { return T / kChunk + N; }
 
+// Workspace: plan header, one record per chunk bound and head, then the
+// windows' state carry [N,H,K,V] FP32.
 int64_t split_workspace_bytes(int32_t N, int64_t T, int32_t H)
 {
-    return header_bytes(N) + split_chunk_bound(N, T) * H * (int64_t)REC_BYTES;
+    return header_bytes(N) + split_chunk_bound(N, T) * H * (int64_t)REC_BYTES +
+           (int64_t)N * H * DK * DV * 4;
 }
 
-cudaError_t launch_chunk_split(const ChunkArgs& a, int64_t chunks, cudaStream_t stream)
+cudaError_t launch_chunk_split(const ChunkArgs& a, int64_t chunks, bool overlap,
+                               cudaStream_t stream)
 {
     int32_t* hdr = static_cast<int32_t*>(a.workspace);
     unsigned char* rec = static_cast<unsigned char*>(a.workspace) + header_bytes(a.N);
+    float* carry = reinterpret_cast<float*>(rec + split_chunk_bound(a.N, a.T) * a.H * (int64_t)REC_BYTES);
     const int64_t units = chunks * a.H;
     if (units > INT32_MAX || (int64_t)a.N * a.H > INT32_MAX) return cudaErrorInvalidConfiguration;
     chunk_plan_kernel<<<1, 1024, 0, stream>>>(a.cu_seqlens, a.N, a.T, hdr, a.status);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    if (units > 0) {
-        if (a.gated)
-            e = a.qkv_bf16 ? launch_prep<__nv_bfloat16, true>(a, hdr, rec, units, stream)
-                           : launch_prep<float, true>(a, hdr, rec, units, stream);
-        else
-            e = a.qkv_bf16 ? launch_prep<__nv_bfloat16, false>(a, hdr, rec, units, stream)
-                           : launch_prep<float, false>(a, hdr, rec, units, stream);
+
+    const int sms = device_sm_count();
+    int W = 1;
+    if (overlap && (int64_t)a.N * a.H <= (sms > 0 ? sms : 152))
+        W = (int)std::min<int64_t>(kMaxWindows, chunks / kWindowChunks);
+    if (W <= 1) {
+        e = launch_prep(a, hdr, rec, 0, units, false, stream);
         if (e != cudaSuccess) return e;
+        return launch_scan(a, hdr, rec, ScanWindow{0, INT32_MAX, nullptr, 1}, stream);
     }
-    return a.out_bf16 ? launch_scan<__nv_bfloat16>(a, hdr, rec, stream)
-                      : launch_scan<float>(a, hdr, rec, stream);
+    for (int w = 0; w < W && e == cudaSuccess; ++w) {
+        const int32_t g0 = (int32_t)window_bound(chunks, W, w);
+        const int32_t g1 = (int32_t)window_bound(chunks, W, w + 1);
+        e = launch_prep(a, hdr, rec, (int64_t)g0 * a.H, (int64_t)(g1 - g0) * a.H, w > 0, stream);
+        const ScanWindow win{g0, w + 1 == W ? INT32_MAX : g1, carry, w + 1 == W ? 1 : 0};
+        if (e == cudaSuccess) e = launch_scan(a, hdr, rec, win, stream);
+    }
+    return e;
 }
 
 }  // namespace kda

@@ -68,7 +68,10 @@ cudaError_t launch_gate(const void* f, bool f_bf16, const float* A_log, const fl
 cudaError_t launch_chunk_fp32(const ChunkArgs& a, cudaStream_t stream);
 cudaError_t launch_chunk_tc(const ChunkArgs& a, cudaStream_t stream);
 // Two-phase path; `chunks` bounds the number of chunks over all sequences.
-cudaError_t launch_chunk_split(const ChunkArgs& a, int64_t chunks, cudaStream_t stream);
+// `overlap` lets the preparation of later chunks run beside the scan of
+// earlier ones (chunk windows; programmatic dependent launch on `stream`).
+cudaError_t launch_chunk_split(const ChunkArgs& a, int64_t chunks, bool overlap,
+                               cudaStream_t stream);
 int64_t split_chunk_bound(int32_t N, int64_t T);
 // The plan kernel: int32 header with [0] = bad-offsets flag and, from
 // [kPlanOffsets], the per-sequence chunk offsets (N + 1 of them).

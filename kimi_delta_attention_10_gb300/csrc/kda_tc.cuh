@@ -171,6 +171,19 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* m)
 }
 
 // Named barrier `id` over `nthreads` threads (whole warps).
+// Programmatic dependent launch: a grid launched with programmatic stream
+// serialisation may start once every CTA of the grid before it has signalled
+// (or exited); grid_dependency_wait() returns once that grid has completed and
+// its memory operations are visible (at once when launched without it).
+__device__ __forceinline__ void launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dependency_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 __device__ __forceinline__ void named_sync(uint32_t id, uint32_t nthreads)
 {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");

@@ -99,14 +99,15 @@ def workspace_size(lib, N, T, H, K=128, V=128, mode=0):
 
 def test_workspace_size_bound():
     """The size covers the worst case of T / 64 + N chunks (every sequence
-    adds at most one partial chunk) and a 1 KiB-aligned offsets header."""
+    adds at most one partial chunk), a 1 KiB-aligned offsets header and the
+    FP32 state carried between chunk windows."""
     lib = binding.load_library()
     rec = 74240
     for N, T, H in [(1, 16384, 64), (16, 32768, 64), (3, 65, 4), (0, 0, 1), (5000, 70000, 2)]:
         st, nbytes = workspace_size(lib, N, T, H)
         assert st == binding.KDA_OK
         hdr = -(-(4 * (N + 5)) // 1024) * 1024
-        assert nbytes == hdr + (T // 64 + N) * H * rec
+        assert nbytes == hdr + (T // 64 + N) * H * rec + N * H * 128 * 128 * 4
         # the exact chunk count of any split of T tokens into N sequences is no larger
         lens = [T // max(N, 1)] * N
         if N:
