@@ -4,11 +4,12 @@
 A step is one pass of the whole path over one batch: the decay and beta from
 their pre-activations and the chunked KDA forward with the final state, on the
 16384-token, 64-head, K=V=128 BF16 workload by default.  The default step is
-kda_gate followed by kda_chunk_fwd; --fused times one call of
-kda_chunk_fwd_gated (the gate fused into the chunk preparation) instead.  The
-BF16 tensor-core path runs in two phases through a preallocated workspace
-(plan, chunk preparation, state scan: three launches per chunk call);
---single-pass times the single-pass kernel (no workspace) instead.
+one call of kda_chunk_fwd_gated (the gate fused into the chunk preparation;
+bit for bit the same results as the two calls); --unfused times kda_gate
+followed by kda_chunk_fwd instead.  The BF16 tensor-core path runs in two
+phases through a preallocated workspace (the plan, then chunk preparation and
+state scan per chunk window); --single-pass times the single-pass kernel (no
+workspace) instead.
 Inputs are resident in HBM when the timed region starts and are larger than
 L2, so no flush is needed between steps.
 
@@ -53,15 +54,17 @@ def parse_args():
     p.add_argument("--workload", default=DEFAULT_WORKLOAD)
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--fused", action="store_true",
-                   help="time kda_chunk_fwd_gated instead of kda_gate + kda_chunk_fwd")
+    p.add_argument("--unfused", action="store_true",
+                   help="time kda_gate + kda_chunk_fwd instead of one kda_chunk_fwd_gated call")
     p.add_argument("--single-pass", action="store_true",
                    help="BF16 tensor-core path without a workspace (one kernel per call)")
     p.add_argument("--output-gate", action="store_true",
                    help="add the output gate with gated RMSNorm (kda_gated_rmsnorm) to the step")
     p.add_argument("--backward", action="store_true",
                    help="also time kda_chunk_bwd (the VJP) on the workload, after the step")
-    return p.parse_args()
+    args = p.parse_args()
+    args.fused = not args.unfused
+    return args
 
 
 def measured_peaks():
