@@ -474,7 +474,7 @@ def main():
         bwd = {"call": "kda_chunk_bwd", "steps": bsteps, "ms": bms,
                "tokens_per_s": whole_job_rate(world, T, 1, bms),
                "algorithmic_bytes": balg, "achieved_GBps": balg / bms / 1e6,
-               "launches_per_call": 4}         # plan, recurrence VJP, two norm VJPs
+               "launches_per_call": 3}         # plan, recurrence VJP, finish (sums + norm VJP)
 
     if rank == 0:
         qkv_bytes = x.q.element_size()

@@ -274,9 +274,12 @@ kda_status kda_gated_rmsnorm(const void* o, int32_t o_dtype, const void* z, int3
 /*
  * kda_chunk_bwd_workspace_size -- bytes of device scratch kda_chunk_bwd needs
  * for N sequences of T packed tokens and H heads (K = V = 128, else
- * KDA_ERR_UNSUPPORTED): the plan header, one K x V FP32 state per chunk per
- * head (the checkpoints at every chunk start) and 64 states per persistent CTA
- * (the states inside the chunk being walked backwards).
+ * KDA_ERR_UNSUPPORTED): the plan header, K x V FP32 states for the
+ * checkpoints at every 16-token segment start (4 (T / 64 + N) per head, a
+ * bound over every cu_seqlens), three FP32 copies of [T,H,K] x 3 + [T,H]
+ * (the partial row sums of three of the four 32-column slices each head is
+ * split into) and 16 state slices (K x 32 FP32) per persistent CTA, at most
+ * 1024 CTAs (the states inside the segment being walked backwards).
  */
 kda_status kda_chunk_bwd_workspace_size(int32_t N, int64_t T, int32_t H, int32_t K, int32_t V,
                                         int64_t* bytes_host);

@@ -12,38 +12,59 @@
 //   dg_t = rowsum(dS' o S'_t);  dS <- Diag(e^{g_t}) dS'
 // then dq = (dq^ - q^ (q^ . dq^)) / n for n = sqrt(|q|^2 + eps) (k alike).
 //
-// One persistent CTA (256 threads) per (sequence, head) at a time.  Thread
-// (kb, vb) = (tid / 16, tid % 16) holds the 8x8 tile rows 8 kb.., columns
-// 8 vb.. of S and of dS in registers.  Sums over V are warp-shuffle
-// transpose-reductions over the 16 lanes of a row group; sums over K go
-// through shared memory.  The state at every chunk start is kept in the
-// workspace (first, forward pass); then, chunk by chunk from the last, the
-// chunk is recomputed forward from its checkpoint (the state before each
-// token to a per-CTA scratch, u and d to shared memory) and walked backwards.
+// Every column of S (and of dS) evolves on its own: u, d, dd and du are
+// per-column, and only dq^, dk^, dg and dbeta sum over the columns.  So a
+// (sequence, head) is split over kSlices CTAs of 32 columns each; each writes
+// its partial row sums (slice 0 into the outputs, the others into the
+// workspace), and a finishing kernel adds them in slice order and applies the
+// norm VJP.
+//
+// One CTA (256 threads) per (sequence, head, slice) at a time, persistent.
+// Thread (kb, vb) = (tid / 8, tid % 8) holds rows 4 kb.. and slice columns
+// 4 vb.. of S and of dS in registers (4 x 4).  Sums over the slice's columns
+// are shuffle transpose-reductions over 8 lanes; sums over K go through
+// shared memory (two CTA barriers per token, the scratch of neighbouring
+// tokens double-buffered).  Tokens are taken in segments of 16 whose inputs
+// (q^, k^, e^g full rows; v, dO slice columns; beta) are staged in shared
+// memory with coalesced loads.  A first pass stores the state slice at every
+// segment start in the workspace; then, segment by segment from the last, the
+// segment is recomputed from its checkpoint (the state before each token to a
+// 256 KiB per-CTA scratch that stays in L2, u and d to shared memory) and
+// walked backwards, the state of the next token brought in by cp.async while
+// the current one is processed.
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <stdint.h>
 
 #include <algorithm>
+#include <cstddef>
 
 #include "kda_internal.cuh"
+#include "kda_tc.cuh"
 
 namespace kda {
 
 namespace {
 
 constexpr int NT = 256;
-constexpr int C = kChunk;
+constexpr int SEG = 16;                                  // tokens per segment
 constexpr int DK = kHeadK;
 constexpr int DV = kHeadV;
-constexpr int64_t kTileBytes = (int64_t)DK * DV * 4;     // one state, 64 KiB
-constexpr int kMaxCtas = 256;                             // persistent CTAs (scratch slots)
+constexpr int kSlices = 4;                               // CTAs per (sequence, head)
+constexpr int CW = DV / kSlices;                         // columns per slice
+constexpr int64_t kTileBytes = (int64_t)DK * CW * 4;     // one state slice, 16 KiB
+constexpr int64_t kTileF4 = kTileBytes / 16;
+constexpr int kQ = 4;                                    // float4 per thread per tile
+constexpr int kSegPerChunk = kChunk / SEG;               // checkpoint slots per plan chunk
+constexpr int kMaxCtas = 1024;                            // persistent CTAs (scratch slots)
+constexpr int kCtasPerSm = 3;
+static_assert(kQ * 4 * NT == DK * CW, "thread tiles cover the slice");
+static_assert(NT / 8 * 4 == DK && 8 * 4 == CW, "4 x 4 thread tiles");
 
 struct BwdArgs {
     const void* q;
     const void* k;
     const void* v;
-    bool qkv_bf16;
     const float* g;
     const float* beta;
     const int32_t* cu;
@@ -53,398 +74,539 @@ struct BwdArgs {
     float scale;
     int32_t l2norm;
     const void* dout;
-    bool dout_bf16;
     const float* init;      // [N,H,K,V] or nullptr
     const float* dfinal;    // [N,H,K,V] or nullptr
-    float* dq;              // holds dq^ until the norm pass
+    float* dq;              // slice 0's dq^ until the finishing kernel
     float* dk;
     float* dv;
     float* dg;
     float* dbeta;
     float* dinit;           // or nullptr
+    float* part;            // slices 1..: [kSlices-1][3][T,H,K] then [kSlices-1][T,H]
     const int32_t* hdr;     // plan header (chunk offsets)
-    float4* ckpt;           // (T/64 + N) * H states
-    float4* scratch;        // gridDim.x * 64 states
-    int32_t* status;
+    float4* ckpt;           // kSegPerChunk * (T/64 + N) * H * kSlices state slices
+    float4* scratch;        // gridDim.x * SEG state slices
+};
+
+// Shared memory of one CTA (dynamic).
+struct BwdSmem {
+    float kh[SEG][DK];        // k^ of the segment's tokens
+    float qh[SEG][DK];        // q^
+    float av[SEG][DK];        // e^g
+    float vv[SEG][CW];        // v, dO, d, u: this slice's columns
+    float dO[SEG][CW];
+    float dl[SEG][CW];
+    float uu[SEG][CW];
+    float red[2][NT / 32][CW];
+    float bc[2][CW];
+    float beta[SEG], rq[SEG], rk[SEG], pad_[SEG];
+    float4 tile[2][kQ * NT];  // the state slice before a token, double-buffered
 };
 
 __device__ __forceinline__ float ld1(const float* p, int64_t i) { return p[i]; }
 __device__ __forceinline__ float ld1(const __nv_bfloat16* p, int64_t i) { return __bfloat162float(p[i]); }
 
-template <typename T>
-__device__ __forceinline__ void ld8(const T* p, int64_t i, float (&x)[8])
+// 8 (or 4) consecutive values from global memory, 16-byte aligned for FP32
+// (8-byte for 4 BF16 values).
+__device__ __forceinline__ void ld8(const float* p, int64_t i, float (&x)[8])
 {
+    const float4 a = *reinterpret_cast<const float4*>(p + i);
+    const float4 b = *reinterpret_cast<const float4*>(p + i + 4);
+    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+}
+__device__ __forceinline__ void ld8(const __nv_bfloat16* p, int64_t i, float (&x)[8])
+{
+    const uint4 u = *reinterpret_cast<const uint4*>(p + i);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-    for (int e = 0; e < 8; ++e) x[e] = ld1(p, i + e);
+    for (int e = 0; e < 4; ++e) {
+        x[2 * e] = __uint_as_float(w[e] << 16);
+        x[2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
+    }
+}
+__device__ __forceinline__ float4 ld4(const float* p, int64_t i)
+{
+    return *reinterpret_cast<const float4*>(p + i);
+}
+__device__ __forceinline__ float4 ld4(const __nv_bfloat16* p, int64_t i)
+{
+    const uint2 u = *reinterpret_cast<const uint2*>(p + i);
+    return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u),
+                       __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
+}
+__device__ __forceinline__ void sst8(float* p, const float (&x)[8])
+{
+    reinterpret_cast<float4*>(p)[0] = make_float4(x[0], x[1], x[2], x[3]);
+    reinterpret_cast<float4*>(p)[1] = make_float4(x[4], x[5], x[6], x[7]);
+}
+__device__ __forceinline__ void f4(const float* p, float* x)
+{
+    const float4 a = *reinterpret_cast<const float4*>(p);
+    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
 }
 
-// A state tile in the workspace: float4 q (row 2 q / 2.. of the thread's tile)
-// of thread tid at (q * NT + tid): coalesced across the CTA.
-__device__ __forceinline__ void tile_store(float4* base, int tid, const float (&s)[64])
+// A state slice: float4 q (row 4 kb + q of the thread's tile) of thread tid
+// at (q * NT + tid): coalesced across the CTA, and each thread reads back only
+// what it wrote.
+__device__ __forceinline__ void tile_store(float4* base, int tid, const float (&s)[16])
 {
 #pragma unroll
-    for (int q = 0; q < 16; ++q)
+    for (int q = 0; q < kQ; ++q)
         base[q * NT + tid] = make_float4(s[4 * q], s[4 * q + 1], s[4 * q + 2], s[4 * q + 3]);
 }
-__device__ __forceinline__ void tile_load(const float4* base, int tid, float (&s)[64])
+__device__ __forceinline__ void tile_load(const float4* base, int tid, float (&s)[16])
 {
 #pragma unroll
-    for (int q = 0; q < 16; ++q) {
+    for (int q = 0; q < kQ; ++q) {
         const float4 x = base[q * NT + tid];
         s[4 * q] = x.x; s[4 * q + 1] = x.y; s[4 * q + 2] = x.z; s[4 * q + 3] = x.w;
     }
 }
-
-// Sum of x[i] over the 16 lanes of this row group; the lane ends with the sum
-// for index 4 h1 + 2 h2 + h3 (h1, h2, h3 = lane bits 3, 2, 1), as does its
-// neighbour lane ^ 1.
-__device__ __forceinline__ float vsum16(const float (&x)[8], int lane, int& idx)
+__device__ __forceinline__ void tile_fetch_async(float4* dst, const float4* src, int tid)
 {
-    const int h1 = (lane >> 3) & 1, h2 = (lane >> 2) & 1, h3 = (lane >> 1) & 1;
-    float y4[4];
 #pragma unroll
-    for (int m = 0; m < 4; ++m) {
-        const float keep = h1 ? x[4 + m] : x[m], send = h1 ? x[m] : x[4 + m];
-        y4[m] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
-    }
+    for (int q = 0; q < kQ; ++q) tc::cp_async16(dst + q * NT + tid, src + q * NT + tid, true);
+    tc::cp_async_commit();
+}
+__device__ __forceinline__ void cp_async_wait_older()
+{
+    asm volatile("cp.async.wait_group 1;" ::: "memory");
+}
+
+// Sum of x[i] over the 8 lanes of this row group (lanes with the same kb);
+// the lane ends with the sum for row index 2 h1 + h2 (h1, h2 = lane bits 2, 1),
+// as does its neighbour lane ^ 1.
+__device__ __forceinline__ float vsum8(const float (&x)[4], int lane, int& idx)
+{
+    const int h1 = (lane >> 2) & 1, h2 = (lane >> 1) & 1;
     float y2[2];
 #pragma unroll
     for (int m = 0; m < 2; ++m) {
-        const float keep = h2 ? y4[2 + m] : y4[m], send = h2 ? y4[m] : y4[2 + m];
+        const float keep = h1 ? x[2 + m] : x[m], send = h1 ? x[m] : x[2 + m];
         y2[m] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
     }
-    float y1 = (h3 ? y2[1] : y2[0]) + __shfl_xor_sync(0xffffffffu, h3 ? y2[0] : y2[1], 2);
+    float y1 = (h2 ? y2[1] : y2[0]) + __shfl_xor_sync(0xffffffffu, h2 ? y2[0] : y2[1], 2);
     y1 += __shfl_xor_sync(0xffffffffu, y1, 1);
-    idx = 4 * h1 + 2 * h2 + h3;
+    idx = 2 * h1 + h2;
     return y1;
 }
 
 template <typename TIn, typename TO>
-__global__ void __launch_bounds__(NT, 1) chunk_bwd_kernel(BwdArgs a)
+__global__ void __launch_bounds__(NT, kCtasPerSm) chunk_bwd_kernel(BwdArgs a)
 {
     extern __shared__ float4 dyn_smem[];
-    float (*dl_s)[DV] = reinterpret_cast<float (*)[DV]>(dyn_smem);   // d_t of the chunk's tokens
-    float (*u_s)[DV] = dl_s + C;                                      // u_t
-    __shared__ float red[NT / 32][DV];     // K-reduction partials
-    __shared__ float bc[DV];               // broadcast of a per-column result
-    __shared__ float rq_s[C], rk_s[C], db_s[C];
+    BwdSmem& sm = *reinterpret_cast<BwdSmem*>(dyn_smem);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int kb = tid >> 4, vb = tid & 15;
+    const int kb = tid >> 3, vb = tid & 7;
     const int H = a.H;
     const TIn* gq = static_cast<const TIn*>(a.q);
     const TIn* gk = static_cast<const TIn*>(a.k);
     const TIn* gv = static_cast<const TIn*>(a.v);
     const TO* gdo = static_cast<const TO*>(a.dout);
-    float4* scratch = a.scratch + (int64_t)blockIdx.x * C * (kTileBytes / 16);
+    float4* scratch = a.scratch + (int64_t)blockIdx.x * SEG * kTileF4;
+    const int64_t THK = a.T * H * DK, TH = a.T * H;
+    int tok = 0;                                           // parity of the K-sum buffers
 
-    // Sum over K of p[j] (this thread's 8 columns): after the call, thread
-    // j < DV (the reducer) holds column j's sum in the return value.
-    auto ksum = [&](float (&p)[8]) -> float {
+    // Sum over K of p[j] (this thread's 4 columns) into buffer `buf`: after
+    // the call, thread j < CW holds slice column j's sum in the return value.
+    auto ksum = [&](float (&p)[4], int buf) -> float {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) p[j] += __shfl_xor_sync(0xffffffffu, p[j], 16);
-        if (lane < 16) {
-#pragma unroll
-            for (int j = 0; j < 8; ++j) red[warp][8 * vb + j] = p[j];
+        for (int j = 0; j < 4; ++j) {
+            p[j] += __shfl_xor_sync(0xffffffffu, p[j], 8);
+            p[j] += __shfl_xor_sync(0xffffffffu, p[j], 16);
         }
+        if (lane < 8)
+            *reinterpret_cast<float4*>(&sm.red[buf][warp][4 * vb]) = make_float4(p[0], p[1], p[2], p[3]);
         __syncthreads();
         float s = 0.f;
-        if (tid < DV) {
+        if (tid < CW) {
 #pragma unroll
-            for (int w = 0; w < NT / 32; ++w) s += red[w][tid];
+            for (int w = 0; w < NT / 32; ++w) s += sm.red[buf][w][tid];
         }
         return s;
     };
-    // row norms of the chunk's q and k (8 tokens per warp)
-    auto chunk_norms = [&](int t0, int L, int h) {
-        for (int tl = warp; tl < L; tl += NT / 32) {
-            const int64_t base = ((int64_t)(t0 + tl) * H + h) * DK;
-            float sq = 0.f, sk = 0.f;
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float xq = ld1(gq, base + 4 * lane + e), xk = ld1(gk, base + 4 * lane + e);
-                sq += xq * xq;
-                sk += xk * xk;
-            }
-#pragma unroll
-            for (int m = 16; m > 0; m >>= 1) {
-                sq += __shfl_xor_sync(0xffffffffu, sq, m);
-                sk += __shfl_xor_sync(0xffffffffu, sk, m);
-            }
-            if (lane == 0) {
-                rq_s[tl] = a.l2norm ? 1.f / sqrtf(sq + 1e-6f) : 1.f;
-                rk_s[tl] = a.l2norm ? 1.f / sqrtf(sk + 1e-6f) : 1.f;
-                db_s[tl] = 0.f;
-            }
-        }
-        __syncthreads();
-    };
-    // One forward token: S <- S' + k^ d^T with S' = Diag(a) S.  Stores u and d
-    // of the token in u_s / dl_s row `slot` when `keep`.
-    auto fwd_token = [&](float (&S)[64], int64_t t, int h, int tl, int slot, bool keep) {
-        const int64_t rowk = (t * H + h) * DK + 8 * kb;
-        float ga[8], kn[8];
-        ld8(a.g, rowk, ga);
-        ld8(gk, rowk, kn);
-        const float rk = rk_s[tl];
-        float p[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const float ai = expf(ga[i]);
-            kn[i] *= rk;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) S[8 * i + j] *= ai;
-        }
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            float acc = 0.f;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) acc += S[8 * i + j] * kn[i];
-            p[j] = acc;
-        }
-        const float u = ksum(p);
-        if (tid < DV) {
-            const float d = a.beta[t * H + h] * (ld1(gv, (t * H + h) * DV + tid) - u);
-            bc[tid] = d;
-            if (keep) {
-                u_s[slot][tid] = u;
-                dl_s[slot][tid] = d;
-            }
-        }
-        __syncthreads();
-        float d8[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) d8[j] = bc[8 * vb + j];
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-#pragma unroll
-            for (int j = 0; j < 8; ++j) S[8 * i + j] += kn[i] * d8[j];
-        __syncthreads();                               // bc and red reused next token
-    };
 
-    const int64_t units = (int64_t)a.N * H;
+    const int64_t units = (int64_t)a.N * H * kSlices;
     for (int64_t unit = blockIdx.x; unit < units; unit += gridDim.x) {
-        const int n = (int)(unit / H), h = (int)(unit % H);
+        const int vs = (int)(unit % kSlices);
+        const int64_t nh = unit / kSlices;                 // n * H + h
+        const int n = (int)(nh / H), h = (int)(nh % H);
+        const int c0 = CW * vs;                            // first column of the slice
         const int bos = a.cu[n], eos = a.cu[n + 1];
         if (bos < 0 || eos < bos || (int64_t)eos > a.T) continue;   // reported by the plan
-        const int nch = (eos - bos + C - 1) / C;
-        float4* ck = a.ckpt + ((int64_t)a.hdr[kPlanOffsets + n] * H + h) * (kTileBytes / 16);
-        const int64_t ck_stride = (int64_t)H * (kTileBytes / 16);
+        const int nseg = (eos - bos + SEG - 1) / SEG;
+        float4* ck = a.ckpt +
+                     (((int64_t)kSegPerChunk * a.hdr[kPlanOffsets + n] * H + h) * kSlices + vs) * kTileF4;
+        const int64_t ck_stride = (int64_t)H * kSlices * kTileF4;
+        float* pq = vs == 0 ? a.dq : a.part + ((int64_t)(vs - 1) * 3 + 0) * THK;
+        float* pk = vs == 0 ? a.dk : a.part + ((int64_t)(vs - 1) * 3 + 1) * THK;
+        float* pg = vs == 0 ? a.dg : a.part + ((int64_t)(vs - 1) * 3 + 2) * THK;
+        float* pb = vs == 0 ? a.dbeta : a.part + (int64_t)(kSlices - 1) * 3 * THK + (vs - 1) * TH;
 
-        // ---- forward pass: the state at every chunk start
-        float S[64];
-        if (a.init != nullptr) {
-            const float* s0 = a.init + unit * DK * DV;
+        // The segment's inputs in shared memory: q^, k^ (normalised rows),
+        // e^g, the slice of v and (with_bwd) dO, beta; rows >= L unused.
+        auto stage = [&](int t0, int L, bool with_bwd) {
+            __syncthreads();                               // the previous segment is done
+            {
+                const int r = tid >> 4, c = 8 * (tid & 15);
+                if (r < L) {
+                    float x[8];
+                    const int64_t rowk = ((int64_t)(t0 + r) * H + h) * DK + c;
+                    ld8(gk, rowk, x);
+                    sst8(&sm.kh[r][c], x);
+                    ld8(a.g, rowk, x);
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-#pragma unroll
-                for (int j = 0; j < 8; ++j) S[8 * i + j] = s0[(8 * kb + i) * DV + 8 * vb + j];
-        } else {
-#pragma unroll
-            for (int e = 0; e < 64; ++e) S[e] = 0.f;
-        }
-        for (int c = 0; c < nch; ++c) {
-            const int t0 = bos + c * C, L = min(C, eos - t0);
-            tile_store(ck + c * ck_stride, tid, S);
-            chunk_norms(t0, L, h);
-            for (int tl = 0; tl < L; ++tl) fwd_token(S, t0 + tl, h, tl, 0, false);
-        }
-
-        // ---- backward, chunk by chunk from the last
-        float dS[64];
-        if (a.dfinal != nullptr) {
-            const float* d0 = a.dfinal + unit * DK * DV;
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-#pragma unroll
-                for (int j = 0; j < 8; ++j) dS[8 * i + j] = d0[(8 * kb + i) * DV + 8 * vb + j];
-        } else {
-#pragma unroll
-            for (int e = 0; e < 64; ++e) dS[e] = 0.f;
-        }
-        for (int c = nch - 1; c >= 0; --c) {
-            const int t0 = bos + c * C, L = min(C, eos - t0);
-            // recompute the chunk: the state before each token, u and d
-            tile_load(ck + c * ck_stride, tid, S);
-            chunk_norms(t0, L, h);
-            for (int tl = 0; tl < L; ++tl) {
-                tile_store(scratch + (int64_t)tl * (kTileBytes / 16), tid, S);
-                fwd_token(S, t0 + tl, h, tl, tl, true);
+                    for (int e = 0; e < 8; ++e) x[e] = expf(x[e]);
+                    sst8(&sm.av[r][c], x);
+                    if (with_bwd) {
+                        ld8(gq, rowk, x);
+                        sst8(&sm.qh[r][c], x);
+                    }
+                }
             }
-            // walk it backwards
+            if (tid < SEG * CW / 4) {
+                const int r = tid >> 3, c = 4 * (tid & 7);
+                if (r < L) {
+                    const int64_t rowv = ((int64_t)(t0 + r) * H + h) * DV + c0 + c;
+                    *reinterpret_cast<float4*>(&sm.vv[r][c]) = ld4(gv, rowv);
+                    if (with_bwd) *reinterpret_cast<float4*>(&sm.dO[r][c]) = ld4(gdo, rowv);
+                }
+            }
+            if (tid < SEG) sm.beta[tid] = tid < L ? a.beta[(int64_t)(t0 + tid) * H + h] : 0.f;
+            __syncthreads();
+            // row norms: warp w takes rows 2 w and 2 w + 1
+#pragma unroll
+            for (int rr = 0; rr < 2; ++rr) {
+                const int r = 2 * warp + rr;
+                if (r < L) {
+                    float sk = 0.f, sq = 0.f;
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float xk = sm.kh[r][4 * lane + e];
+                        sk += xk * xk;
+                        if (with_bwd) {
+                            const float xq = sm.qh[r][4 * lane + e];
+                            sq += xq * xq;
+                        }
+                    }
+#pragma unroll
+                    for (int m = 16; m > 0; m >>= 1) {
+                        sk += __shfl_xor_sync(0xffffffffu, sk, m);
+                        sq += __shfl_xor_sync(0xffffffffu, sq, m);
+                    }
+                    if (lane == 0) {
+                        sm.rk[r] = a.l2norm ? 1.f / sqrtf(sk + 1e-6f) : 1.f;
+                        sm.rq[r] = a.l2norm ? 1.f / sqrtf(sq + 1e-6f) : 1.f;
+                    }
+                }
+            }
+            __syncthreads();
+            {
+                const int r = tid >> 4, c = 8 * (tid & 15);
+                if (r < L) {
+                    const float nk = sm.rk[r], nq = sm.rq[r];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        sm.kh[r][c + e] *= nk;
+                        if (with_bwd) sm.qh[r][c + e] *= nq;
+                    }
+                }
+            }
+            __syncthreads();
+        };
+        // One forward token: S <- S' + k^ d^T with S' = Diag(a) S; u and d of
+        // the token to uu / dl row tl when `keep`.
+        auto fwd_token = [&](float (&S)[16], int tl, bool keep) {
+            float av4[4], kn[4], p[4];
+            f4(&sm.av[tl][4 * kb], av4);
+            f4(&sm.kh[tl][4 * kb], kn);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) S[4 * i + j] *= av4[i];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                float acc = 0.f;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) acc += S[4 * i + j] * kn[i];
+                p[j] = acc;
+            }
+            const int buf = tok++ & 1;
+            const float u = ksum(p, buf);
+            if (tid < CW) {
+                const float d = sm.beta[tl] * (sm.vv[tl][tid] - u);
+                sm.bc[buf][tid] = d;
+                if (keep) {
+                    sm.uu[tl][tid] = u;
+                    sm.dl[tl][tid] = d;
+                }
+            }
+            __syncthreads();
+            float d4[4];
+            f4(&sm.bc[buf][4 * vb], d4);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) S[4 * i + j] += kn[i] * d4[j];
+        };
+        // This thread's 4 x 4 block of a caller state [N,H,K,V] (zero if none).
+        auto load_state = [&](const float* src, float (&S)[16]) {
+            if (src == nullptr) {
+#pragma unroll
+                for (int e = 0; e < 16; ++e) S[e] = 0.f;
+                return;
+            }
+            const float* s0 = src + nh * DK * DV;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) f4(s0 + (4 * kb + i) * DV + c0 + 4 * vb, S + 4 * i);
+        };
+
+        // ---- forward pass: the state slice at every segment start
+        float S[16];
+        load_state(a.init, S);
+        for (int sg = 0; sg < nseg; ++sg) {
+            const int t0 = bos + sg * SEG, L = min(SEG, eos - t0);
+            tile_store(ck + sg * ck_stride, tid, S);
+            stage(t0, L, false);
+            for (int tl = 0; tl < L; ++tl) fwd_token(S, tl, false);
+        }
+
+        // ---- backward, segment by segment from the last
+        float dS[16];
+        load_state(a.dfinal, dS);
+        for (int sg = nseg - 1; sg >= 0; --sg) {
+            const int t0 = bos + sg * SEG, L = min(SEG, eos - t0);
+            // recompute the segment: the state before each token, u and d
+            tile_load(ck + sg * ck_stride, tid, S);
+            stage(t0, L, true);
+            for (int tl = 0; tl < L; ++tl) {
+                tile_store(scratch + (int64_t)tl * kTileF4, tid, S);
+                fwd_token(S, tl, true);
+            }
+            // walk it backwards; the state before token tl - 1 is fetched
+            // while token tl is processed
+            tile_fetch_async(sm.tile[(L - 1) & 1], scratch + (int64_t)(L - 1) * kTileF4, tid);
             for (int tl = L - 1; tl >= 0; --tl) {
                 const int64_t t = t0 + tl;
-                const int64_t rowk = (t * H + h) * DK + 8 * kb;
-                const int64_t rowv = (t * H + h) * DV + 8 * vb;
-                float Sp[64];
-                tile_load(scratch + (int64_t)tl * (kTileBytes / 16), tid, Sp);
-                float ga[8], kn[8], qn[8], dO[8], d8[8];
-                ld8(a.g, rowk, ga);
-                ld8(gk, rowk, kn);
-                ld8(gq, rowk, qn);
-                ld8(gdo, rowv, dO);
-                const float rk = rk_s[tl], rq = rq_s[tl], bt = a.beta[t * H + h];
-#pragma unroll
-                for (int j = 0; j < 8; ++j) d8[j] = dl_s[tl][8 * vb + j];
-                float av[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    av[i] = expf(ga[i]);
-                    kn[i] *= rk;
-                    qn[i] *= rq;
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) Sp[8 * i + j] *= av[i];
+                if (tl > 0) {
+                    tile_fetch_async(sm.tile[(tl - 1) & 1], scratch + (int64_t)(tl - 1) * kTileF4, tid);
+                    cp_async_wait_older();
+                } else {
+                    tc::cp_async_wait_all();
                 }
-                // o = scale S^T q^:  dS += scale q^ dO^T,  dq^ = scale S dO
-                float dqn[8], ddp[8];
+                float Sp[16];
+                tile_load(sm.tile[tl & 1], tid, Sp);
+                float av4[4], kn[4], qn[4], dO[4], d4[4];
+                f4(&sm.av[tl][4 * kb], av4);
+                f4(&sm.kh[tl][4 * kb], kn);
+                f4(&sm.qh[tl][4 * kb], qn);
+                f4(&sm.dO[tl][4 * vb], dO);
+                f4(&sm.dl[tl][4 * vb], d4);
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
+                for (int i = 0; i < 4; ++i)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) Sp[4 * i + j] *= av4[i];
+                // o = scale S^T q^:  dS += scale q^ dO^T,  dq^ = scale S dO
+                float dqn[4], ddp[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
                     float acc = 0.f;
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        acc += (Sp[8 * i + j] + kn[i] * d8[j]) * dO[j];
-                        dS[8 * i + j] += a.scale * qn[i] * dO[j];
+                    for (int j = 0; j < 4; ++j) {
+                        acc += (Sp[4 * i + j] + kn[i] * d4[j]) * dO[j];
+                        dS[4 * i + j] += a.scale * qn[i] * dO[j];
                     }
                     dqn[i] = a.scale * acc;
                 }
                 // dd = dS^T k^
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
+                for (int j = 0; j < 4; ++j) {
                     float acc = 0.f;
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) acc += dS[8 * i + j] * kn[i];
+                    for (int i = 0; i < 4; ++i) acc += dS[4 * i + j] * kn[i];
                     ddp[j] = acc;
                 }
-                const float dd = ksum(ddp);
-                if (tid < DV) {
-                    const float u = u_s[tl][tid];
-                    const float vj = ld1(gv, (t * H + h) * DV + tid);
-                    a.dv[(t * H + h) * DV + tid] = bt * dd;
-                    bc[tid] = -bt * dd;                        // du
-                    float part = dd * (vj - u);
+                const int buf = tok++ & 1;
+                const float dd = ksum(ddp, buf);
+                if (tid < CW) {                            // warp 0
+                    const float bt = sm.beta[tl];
+                    a.dv[(t * H + h) * DV + c0 + tid] = bt * dd;
+                    sm.bc[buf][tid] = -bt * dd;            // du
+                    float part = dd * (sm.vv[tl][tid] - sm.uu[tl][tid]);
 #pragma unroll
                     for (int m = 16; m > 0; m >>= 1) part += __shfl_xor_sync(0xffffffffu, part, m);
-                    if (lane == 0) atomicAdd(&db_s[tl], part);
+                    if (lane == 0) pb[t * H + h] = part;
                 }
                 __syncthreads();
-                float du[8];
-#pragma unroll
-                for (int j = 0; j < 8; ++j) du[j] = bc[8 * vb + j];
+                float du[4];
+                f4(&sm.bc[buf][4 * vb], du);
                 // dk^ = dS d + S' du;  dS' = dS + k^ du^T;  dg = rowsum(dS' o S');  dS = a dS'
-                float dkn[8], dgp[8];
+                float dkn[4], dgp[4];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
+                for (int i = 0; i < 4; ++i) {
                     float acc = 0.f, accg = 0.f;
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        acc += dS[8 * i + j] * d8[j] + Sp[8 * i + j] * du[j];
-                        const float dsp = dS[8 * i + j] + kn[i] * du[j];
-                        accg += dsp * Sp[8 * i + j];
-                        dS[8 * i + j] = av[i] * dsp;
+                    for (int j = 0; j < 4; ++j) {
+                        acc += dS[4 * i + j] * d4[j] + Sp[4 * i + j] * du[j];
+                        const float dsp = dS[4 * i + j] + kn[i] * du[j];
+                        accg += dsp * Sp[4 * i + j];
+                        dS[4 * i + j] = av4[i] * dsp;
                     }
                     dkn[i] = acc;
                     dgp[i] = accg;
                 }
                 int idx;
-                const float sq = vsum16(dqn, lane, idx);
-                const float sk = vsum16(dkn, lane, idx);
-                const float sg = vsum16(dgp, lane, idx);
+                const float sq = vsum8(dqn, lane, idx);
+                const float sk = vsum8(dkn, lane, idx);
+                const float sgd = vsum8(dgp, lane, idx);
                 if ((lane & 1) == 0) {
-                    const int64_t o = (t * H + h) * DK + 8 * kb + idx;
-                    a.dq[o] = sq;
-                    a.dk[o] = sk;
-                    a.dg[o] = sg;
+                    const int64_t o = (t * H + h) * DK + 4 * kb + idx;
+                    pq[o] = sq;
+                    pk[o] = sk;
+                    pg[o] = sgd;
                 }
-                __syncthreads();                               // bc reused next token
             }
-            for (int tl = tid; tl < L; tl += NT) a.dbeta[(int64_t)(t0 + tl) * H + h] = db_s[tl];
-            __syncthreads();
         }
         if (a.dinit != nullptr) {
-            float* d0 = a.dinit + unit * DK * DV;
+            float* d0 = a.dinit + nh * DK * DV;
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-#pragma unroll
-                for (int j = 0; j < 8; ++j) d0[(8 * kb + i) * DV + 8 * vb + j] = dS[8 * i + j];
+            for (int i = 0; i < 4; ++i)
+                *reinterpret_cast<float4*>(d0 + (4 * kb + i) * DV + c0 + 4 * vb) =
+                    make_float4(dS[4 * i], dS[4 * i + 1], dS[4 * i + 2], dS[4 * i + 3]);
         }
     }
 }
 
-// dx = (dx^ - x^ (x^ . dx^)) / n with n = sqrt(|x|^2 + eps), in place on dx
-// (which holds dx^); one warp per (token, head) row of 128.
+// The slices' partial row sums added in slice order (slice 0 already in the
+// outputs), then the norm VJP dx = (dx^ - x^ (x^ . dx^)) / n with
+// n = sqrt(|x|^2 + eps) for q and k when l2norm; one warp per (token, head) row.
 template <typename TIn>
-__global__ void __launch_bounds__(256) norm_vjp_kernel(const TIn* __restrict__ x,
-                                                       float* __restrict__ dx, int64_t rows)
+__global__ void __launch_bounds__(256) bwd_finish_kernel(const TIn* __restrict__ q,
+                                                         const TIn* __restrict__ k,
+                                                         float* __restrict__ dq,
+                                                         float* __restrict__ dk,
+                                                         float* __restrict__ dg,
+                                                         float* __restrict__ dbeta,
+                                                         const float* __restrict__ part,
+                                                         int64_t rows, int32_t l2norm)
 {
     const int lane = threadIdx.x & 31;
+    const int64_t THK = rows * DK;
     const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
     for (int64_t r = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < rows; r += nw) {
-        float xv[4], gv[4];
-        float ss = 0.f, dot = 0.f;
+        const int64_t o = r * DK + 4 * lane;
+        float4 sq = *reinterpret_cast<const float4*>(dq + o);
+        float4 sk = *reinterpret_cast<const float4*>(dk + o);
+        float4 sg = *reinterpret_cast<const float4*>(dg + o);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            xv[e] = ld1(x, r * DK + 4 * lane + e);
-            gv[e] = dx[r * DK + 4 * lane + e];
-            ss += xv[e] * xv[e];
-            dot += xv[e] * gv[e];
+        for (int s = 1; s < kSlices; ++s) {
+            const float* base = part + (int64_t)(s - 1) * 3 * THK;
+            const float4 pq = *reinterpret_cast<const float4*>(base + o);
+            const float4 pk = *reinterpret_cast<const float4*>(base + THK + o);
+            const float4 pg = *reinterpret_cast<const float4*>(base + 2 * THK + o);
+            sq.x += pq.x; sq.y += pq.y; sq.z += pq.z; sq.w += pq.w;
+            sk.x += pk.x; sk.y += pk.y; sk.z += pk.z; sk.w += pk.w;
+            sg.x += pg.x; sg.y += pg.y; sg.z += pg.z; sg.w += pg.w;
         }
-#pragma unroll
-        for (int m = 16; m > 0; m >>= 1) {
-            ss += __shfl_xor_sync(0xffffffffu, ss, m);
-            dot += __shfl_xor_sync(0xffffffffu, dot, m);
+        *reinterpret_cast<float4*>(dg + o) = sg;
+        if (lane == 0) {
+            float b = dbeta[r];
+            for (int s = 1; s < kSlices; ++s) b += part[(int64_t)(kSlices - 1) * 3 * THK + (s - 1) * rows + r];
+            dbeta[r] = b;
         }
-        const float inv = 1.f / sqrtf(ss + 1e-6f);
-        const float proj = dot * inv * inv;                 // (x^ . dx^) / n
+        auto norm_vjp = [&](const TIn* x, float4 gv4, float* out) {
+            if (!l2norm) {
+                *reinterpret_cast<float4*>(out + o) = gv4;
+                return;
+            }
+            const float gv[4] = {gv4.x, gv4.y, gv4.z, gv4.w};
+            float xv[4], ss = 0.f, dot = 0.f;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) dx[r * DK + 4 * lane + e] = (gv[e] - xv[e] * proj) * inv;
+            for (int e = 0; e < 4; ++e) {
+                xv[e] = ld1(x, o + e);
+                ss += xv[e] * xv[e];
+                dot += xv[e] * gv[e];
+            }
+#pragma unroll
+            for (int m = 16; m > 0; m >>= 1) {
+                ss += __shfl_xor_sync(0xffffffffu, ss, m);
+                dot += __shfl_xor_sync(0xffffffffu, dot, m);
+            }
+            const float inv = 1.f / sqrtf(ss + 1e-6f);
+            const float proj = dot * inv * inv;             // (x^ . dx^) / n
+            *reinterpret_cast<float4*>(out + o) =
+                make_float4((gv[0] - xv[0] * proj) * inv, (gv[1] - xv[1] * proj) * inv,
+                            (gv[2] - xv[2] * proj) * inv, (gv[3] - xv[3] * proj) * inv);
+        };
+        norm_vjp(q, sq, dq);
+        norm_vjp(k, sk, dk);
     }
 }
 
 template <typename TIn, typename TO>
 cudaError_t launch_typed(const BwdArgs& a, int grid, cudaStream_t stream)
 {
-    constexpr int smem = 2 * C * DV * 4;
+    constexpr int smem = (int)sizeof(BwdSmem);
     cudaError_t e = cudaFuncSetAttribute(chunk_bwd_kernel<TIn, TO>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     chunk_bwd_kernel<TIn, TO><<<grid, NT, smem, stream>>>(a);
     e = cudaGetLastError();
-    if (e != cudaSuccess || !a.l2norm || a.T == 0) return e;
+    if (e != cudaSuccess || a.T == 0) return e;
     const int64_t rows = a.T * a.H;
     const int sms = device_sm_count();
-    int64_t blocks = std::min<int64_t>((rows + 7) / 8, (int64_t)(sms > 0 ? sms : 152) * 8);
-    norm_vjp_kernel<TIn><<<(unsigned)blocks, 256, 0, stream>>>(static_cast<const TIn*>(a.q),
-                                                                a.dq, rows);
-    norm_vjp_kernel<TIn><<<(unsigned)blocks, 256, 0, stream>>>(static_cast<const TIn*>(a.k),
-                                                                a.dk, rows);
+    const int64_t blocks = std::min<int64_t>((rows + 7) / 8, (int64_t)(sms > 0 ? sms : 152) * 8);
+    bwd_finish_kernel<TIn><<<(unsigned)blocks, 256, 0, stream>>>(
+        static_cast<const TIn*>(a.q), static_cast<const TIn*>(a.k), a.dq, a.dk, a.dg, a.dbeta,
+        a.part, rows, a.l2norm);
     return cudaGetLastError();
+}
+
+int64_t ckpt_bytes(int32_t N, int64_t T, int32_t H)
+{
+    return kSegPerChunk * split_chunk_bound(N, T) * H * kSlices * kTileBytes;
+}
+int64_t part_bytes(int64_t T, int32_t H)
+{
+    return (int64_t)(kSlices - 1) * (3 * T * H * DK + T * H) * 4;
+}
+int64_t bwd_ctas(int32_t N, int32_t H)
+{
+    const int sms = device_sm_count();
+    return std::min<int64_t>((int64_t)N * H * kSlices,
+                             std::min<int64_t>(kMaxCtas, (int64_t)kCtasPerSm * (sms > 0 ? sms : 152)));
 }
 
 }  // namespace
 
 int64_t bwd_workspace_bytes(int32_t N, int64_t T, int32_t H)
 {
-    const int64_t ctas = std::min<int64_t>((int64_t)N * H, kMaxCtas);
-    return chunk_plan_header_bytes(N) + split_chunk_bound(N, T) * H * kTileBytes +
-           ctas * C * kTileBytes;
+    // the scratch is sized for the CTA cap, not this device's SM count
+    const int64_t ctas = std::min<int64_t>((int64_t)N * H * kSlices, kMaxCtas);
+    const int64_t part = (part_bytes(T, H) + 255) / 256 * 256;
+    return chunk_plan_header_bytes(N) + ckpt_bytes(N, T, H) + part + ctas * SEG * kTileBytes;
 }
 
 cudaError_t launch_chunk_bwd(const BwdLaunch& L, cudaStream_t stream)
 {
-    const int64_t units = (int64_t)L.N * L.H;
-    const int sms = device_sm_count();
-    const int grid = (int)std::min<int64_t>(units, std::min<int64_t>(kMaxCtas, sms > 0 ? sms : 152));
+    static_assert(sizeof(BwdSmem) * kCtasPerSm <= 227 * 1024, "shared memory budget");
+    static_assert(offsetof(BwdSmem, tile) % 16 == 0, "cp.async destinations 16-byte aligned");
+    const int64_t units = (int64_t)L.N * L.H * kSlices;
+    const int grid = (int)bwd_ctas(L.N, L.H);
     int32_t* hdr = static_cast<int32_t*>(L.workspace);
     unsigned char* ws = static_cast<unsigned char*>(L.workspace) + chunk_plan_header_bytes(L.N);
     BwdArgs a;
-    a.q = L.q; a.k = L.k; a.v = L.v; a.qkv_bf16 = L.qkv_bf16; a.g = L.g; a.beta = L.beta;
+    a.q = L.q; a.k = L.k; a.v = L.v; a.g = L.g; a.beta = L.beta;
     a.cu = L.cu; a.N = L.N; a.T = L.T; a.H = L.H; a.scale = L.scale; a.l2norm = L.l2norm;
-    a.dout = L.dout; a.dout_bf16 = L.dout_bf16; a.init = L.init; a.dfinal = L.dfinal;
+    a.dout = L.dout; a.init = L.init; a.dfinal = L.dfinal;
     a.dq = L.dq; a.dk = L.dk; a.dv = L.dv; a.dg = L.dg; a.dbeta = L.dbeta; a.dinit = L.dinit;
     a.hdr = hdr;
     a.ckpt = reinterpret_cast<float4*>(ws);
-    a.scratch = reinterpret_cast<float4*>(ws + split_chunk_bound(L.N, L.T) * L.H * kTileBytes);
-    a.status = L.status;
+    ws += ckpt_bytes(L.N, L.T, L.H);
+    a.part = reinterpret_cast<float*>(ws);
+    ws += (part_bytes(L.T, L.H) + 255) / 256 * 256;
+    a.scratch = reinterpret_cast<float4*>(ws);
     cudaError_t e = launch_chunk_plan(L.cu, L.N, L.T, hdr, L.status, stream);
     if (e != cudaSuccess || units == 0) return e;
     if (L.qkv_bf16)

@@ -299,11 +299,17 @@ def test_bwd_workspace_size(lib):
         out = ctypes.c_int64(0)
         assert lib.kda_chunk_bwd_workspace_size(N, T, H, 128, 128, ctypes.byref(out)) == 0
         return out.value
-    state = 128 * 128 * 4
-    # checkpoints: (T/64 + N) states per head; scratch: 64 states per CTA (<= 256 CTAs)
-    assert size(1, 16384, 64) - size(1, 16384 - 64, 64) == 64 * state
-    assert size(3, 100, 2) - size(3, 100, 1) == (100 // 64 + 3) * state + 3 * 64 * state
-    assert size(1, 64, 256) == size(1, 64, 257) - 2 * state      # CTAs capped at 256
+
+    def expected(N, T, H):
+        hdr = -(-(4 * (N + 5)) // 1024) * 1024
+        state = 128 * 128 * 4
+        ckpt = 4 * (T // 64 + N) * H * state            # one state per 16-token segment (bound)
+        part = 3 * (3 * T * H * 128 + T * H) * 4        # partial row sums of column slices 1..3
+        part = -(-part // 256) * 256
+        scratch = min(4 * N * H, 1024) * 16 * (128 * 32 * 4)   # 16 state slices per CTA
+        return hdr + ckpt + part + scratch
+    for N, T, H in [(1, 16384, 64), (3, 100, 2), (1, 64, 256), (1, 64, 257), (0, 0, 1), (7, 5, 3)]:
+        assert size(N, T, H) == expected(N, T, H), (N, T, H)
     out = ctypes.c_int64(0)
     assert lib.kda_chunk_bwd_workspace_size(1, 64, 1, 64, 128, ctypes.byref(out)) == \
         binding.KDA_ERR_UNSUPPORTED
