@@ -8,7 +8,8 @@ import pytest
 import torch
 
 import oracle
-from kimi_delta_attention_10_gb300 import kda_chunk_fwd, kda_chunk_fwd_static, kda_gate
+from kimi_delta_attention_10_gb300 import (kda_chunk_fwd, kda_chunk_fwd_gated, kda_chunk_fwd_static,
+                                           kda_gate)
 from kimi_delta_attention_10_gb300.inputs import make_inputs
 
 from gpu_util import device_inputs, f64, rel_l2
@@ -56,3 +57,19 @@ def test_windows_match_oracle():
     assert rel_l2(S_w.cpu().numpy(), S_ref) <= 3e-3
     # the empty sequence passes its initial state through unchanged
     assert np.array_equal(S_w[1].cpu().numpy(), S0[1].cpu().numpy())
+
+
+def test_fused_gate_in_windows_is_bitwise_gate_then_chunk():
+    """The timed configuration's shape of schedule (four chunk windows) with the
+    gate fused into the preparation, against kda_gate + kda_chunk_fwd."""
+    x = make_inputs([16384], 2, 128, 128, torch.bfloat16, 97)
+    d = device_inputs(x)
+    host = x.cu_seqlens.tolist()
+    g, beta = kda_gate(d["f"], d["A_log"], d["dt_bias"], d["b"])
+    o1, s1 = kda_chunk_fwd(d["q"], d["k"], d["v"], g, beta, d["cu_seqlens"], x.scale,
+                           mode="bf16_tc", workspace="auto", cu_seqlens_host=host)
+    o2, s2 = kda_chunk_fwd_gated(d["q"], d["k"], d["v"], d["f"], d["A_log"], d["dt_bias"],
+                                 d["b"], d["cu_seqlens"], x.scale, mode="bf16_tc",
+                                 workspace="auto", cu_seqlens_host=host)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(s1, s2)
