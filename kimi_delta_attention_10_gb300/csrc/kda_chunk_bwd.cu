@@ -20,18 +20,18 @@
 // norm VJP.
 //
 // One CTA (256 threads) per (sequence, head, slice) at a time, persistent.
-// Thread (kb, vb) = (tid / 8, tid % 8) holds rows 4 kb.. and slice columns
-// 4 vb.. of S and of dS in registers (4 x 4).  Sums over the slice's columns
-// are shuffle transpose-reductions over 8 lanes; sums over K go through
-// shared memory (two CTA barriers per token, the scratch of neighbouring
-// tokens double-buffered).  Tokens are taken in segments of 16 whose inputs
-// (q^, k^, e^g full rows; v, dO slice columns; beta) are staged in shared
-// memory with coalesced loads.  A first pass stores the state slice at every
-// segment start in the workspace; then, segment by segment from the last, the
-// segment is recomputed from its checkpoint (the state before each token to a
-// 256 KiB per-CTA scratch that stays in L2, u and d to shared memory) and
-// walked backwards, the state of the next token brought in by cp.async while
-// the current one is processed.
+// Lane l of warp w holds rows 4 l.. and slice columns 4 w.. of S and of dS in
+// registers (4 x 4): a warp owns whole columns, so the sums over K (u, dd)
+// are warp shuffles and a forward token needs no CTA barrier.  The sums over
+// the slice's columns (dq^, dk^, dg, dbeta) go through shared memory, one CTA
+// barrier per backward token (the buffers of neighbouring tokens alternate).
+// Tokens are taken in segments of 16 whose inputs (q^, k^, e^g full rows; v,
+// dO slice columns; beta) are staged in shared memory with coalesced loads.
+// A first pass stores the state slice at every segment start in the
+// workspace; then, segment by segment from the last, the segment is
+// recomputed from its checkpoint (the state before each token to a 256 KiB
+// per-CTA scratch, u and d to shared memory) and walked backwards, the state
+// before the next token loaded while the current one is processed.
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <stdint.h>
@@ -40,7 +40,6 @@
 #include <cstddef>
 
 #include "kda_internal.cuh"
-#include "kda_tc.cuh"
 
 namespace kda {
 
@@ -57,9 +56,9 @@ constexpr int64_t kTileF4 = kTileBytes / 16;
 constexpr int kQ = 4;                                    // float4 per thread per tile
 constexpr int kSegPerChunk = kChunk / SEG;               // checkpoint slots per plan chunk
 constexpr int kMaxCtas = 1024;                            // persistent CTAs (scratch slots)
-constexpr int kCtasPerSm = 3;
+constexpr int kCtasPerSm = 2;
 static_assert(kQ * 4 * NT == DK * CW, "thread tiles cover the slice");
-static_assert(NT / 8 * 4 == DK && 8 * 4 == CW, "4 x 4 thread tiles");
+static_assert(32 * 4 == DK && NT / 32 * 4 == CW, "a lane holds 4 rows, a warp 4 columns");
 
 struct BwdArgs {
     const void* q;
@@ -85,7 +84,7 @@ struct BwdArgs {
     float* part;            // slices 1..: [kSlices-1][3][T,H,K] then [kSlices-1][T,H]
     const int32_t* hdr;     // plan header (chunk offsets)
     float4* ckpt;           // kSegPerChunk * (T/64 + N) * H * kSlices state slices
-    float4* scratch;        // gridDim.x * SEG state slices
+    float4* scratch;        // gridDim.x * SEG state slices (thread-private float4s)
 };
 
 // Shared memory of one CTA (dynamic).
@@ -97,10 +96,9 @@ struct BwdSmem {
     float dO[SEG][CW];
     float dl[SEG][CW];
     float uu[SEG][CW];
-    float red[2][NT / 32][CW];
-    float bc[2][CW];
-    float beta[SEG], rq[SEG], rk[SEG], pad_[SEG];
-    float4 tile[2][kQ * NT];  // the state slice before a token, double-buffered
+    float red[2][NT / 32][3][DK];   // per-warp row partials of dq^, dk^, dg (two tokens)
+    float dbr[2][NT / 32];          // per-warp partials of dbeta
+    float beta[SEG], rq[SEG], rk[SEG];
 };
 
 __device__ __forceinline__ float ld1(const float* p, int64_t i) { return p[i]; }
@@ -110,13 +108,13 @@ __device__ __forceinline__ float ld1(const __nv_bfloat16* p, int64_t i) { return
 // (8-byte for 4 BF16 values).
 __device__ __forceinline__ void ld8(const float* p, int64_t i, float (&x)[8])
 {
-    const float4 a = *reinterpret_cast<const float4*>(p + i);
-    const float4 b = *reinterpret_cast<const float4*>(p + i + 4);
+    const float4 a = __ldcs(reinterpret_cast<const float4*>(p + i));
+    const float4 b = __ldcs(reinterpret_cast<const float4*>(p + i + 4));
     x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
 }
 __device__ __forceinline__ void ld8(const __nv_bfloat16* p, int64_t i, float (&x)[8])
 {
-    const uint4 u = *reinterpret_cast<const uint4*>(p + i);
+    const uint4 u = __ldcs(reinterpret_cast<const uint4*>(p + i));
     const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
@@ -126,11 +124,11 @@ __device__ __forceinline__ void ld8(const __nv_bfloat16* p, int64_t i, float (&x
 }
 __device__ __forceinline__ float4 ld4(const float* p, int64_t i)
 {
-    return *reinterpret_cast<const float4*>(p + i);
+    return __ldcs(reinterpret_cast<const float4*>(p + i));
 }
 __device__ __forceinline__ float4 ld4(const __nv_bfloat16* p, int64_t i)
 {
-    const uint2 u = *reinterpret_cast<const uint2*>(p + i);
+    const uint2 u = __ldcs(reinterpret_cast<const uint2*>(p + i));
     return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u),
                        __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
 }
@@ -139,56 +137,39 @@ __device__ __forceinline__ void sst8(float* p, const float (&x)[8])
     reinterpret_cast<float4*>(p)[0] = make_float4(x[0], x[1], x[2], x[3]);
     reinterpret_cast<float4*>(p)[1] = make_float4(x[4], x[5], x[6], x[7]);
 }
+// Inputs are read once and outputs written once: streaming loads and stores
+// (__ldcs / __stcs) keep them from displacing the state scratch in L2.
+// x[lane] for lane < 4 without indexing a register array.
+__device__ __forceinline__ float pick4(const float (&x)[4], int lane)
+{
+    return lane == 0 ? x[0] : lane == 1 ? x[1] : lane == 2 ? x[2] : x[3];
+}
 __device__ __forceinline__ void f4(const float* p, float* x)
 {
     const float4 a = *reinterpret_cast<const float4*>(p);
     x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
 }
 
-// A state slice: float4 q (row 4 kb + q of the thread's tile) of thread tid
-// at (q * NT + tid): coalesced across the CTA, and each thread reads back only
-// what it wrote.
-__device__ __forceinline__ void tile_store(float4* base, int tid, const float (&s)[16])
+// Sum over the warp's 32 lanes (K rows) of p[j], j < 4 (the warp's columns):
+// every lane returns all four sums.  A transpose-reduction (lanes 16 apart
+// split the columns in halves, lanes 8 apart in quarters, then a butterfly
+// over the remaining 8 lanes) leaves column 2 b4 + b3 in the lanes with
+// bits (b4, b3); four shuffles broadcast them.
+__device__ __forceinline__ void ksum_warp(const float (&p)[4], int lane, float (&out)[4])
 {
-#pragma unroll
-    for (int q = 0; q < kQ; ++q)
-        base[q * NT + tid] = make_float4(s[4 * q], s[4 * q + 1], s[4 * q + 2], s[4 * q + 3]);
-}
-__device__ __forceinline__ void tile_load(const float4* base, int tid, float (&s)[16])
-{
-#pragma unroll
-    for (int q = 0; q < kQ; ++q) {
-        const float4 x = base[q * NT + tid];
-        s[4 * q] = x.x; s[4 * q + 1] = x.y; s[4 * q + 2] = x.z; s[4 * q + 3] = x.w;
-    }
-}
-__device__ __forceinline__ void tile_fetch_async(float4* dst, const float4* src, int tid)
-{
-#pragma unroll
-    for (int q = 0; q < kQ; ++q) tc::cp_async16(dst + q * NT + tid, src + q * NT + tid, true);
-    tc::cp_async_commit();
-}
-__device__ __forceinline__ void cp_async_wait_older()
-{
-    asm volatile("cp.async.wait_group 1;" ::: "memory");
-}
-
-// Sum of x[i] over the 8 lanes of this row group (lanes with the same kb);
-// the lane ends with the sum for row index 2 h1 + h2 (h1, h2 = lane bits 2, 1),
-// as does its neighbour lane ^ 1.
-__device__ __forceinline__ float vsum8(const float (&x)[4], int lane, int& idx)
-{
-    const int h1 = (lane >> 2) & 1, h2 = (lane >> 1) & 1;
-    float y2[2];
+    const int b4 = (lane >> 4) & 1, b3 = (lane >> 3) & 1;
+    float q2[2];
 #pragma unroll
     for (int m = 0; m < 2; ++m) {
-        const float keep = h1 ? x[2 + m] : x[m], send = h1 ? x[m] : x[2 + m];
-        y2[m] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+        const float keep = b4 ? p[2 + m] : p[m], send = b4 ? p[m] : p[2 + m];
+        q2[m] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
     }
-    float y1 = (h2 ? y2[1] : y2[0]) + __shfl_xor_sync(0xffffffffu, h2 ? y2[0] : y2[1], 2);
-    y1 += __shfl_xor_sync(0xffffffffu, y1, 1);
-    idx = 2 * h1 + h2;
-    return y1;
+    float q1 = (b3 ? q2[1] : q2[0]) + __shfl_xor_sync(0xffffffffu, b3 ? q2[0] : q2[1], 8);
+    q1 += __shfl_xor_sync(0xffffffffu, q1, 4);
+    q1 += __shfl_xor_sync(0xffffffffu, q1, 2);
+    q1 += __shfl_xor_sync(0xffffffffu, q1, 1);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) out[j] = __shfl_sync(0xffffffffu, q1, 8 * j);
 }
 
 template <typename TIn, typename TO>
@@ -197,8 +178,8 @@ __global__ void __launch_bounds__(NT, kCtasPerSm) chunk_bwd_kernel(BwdArgs a)
     extern __shared__ float4 dyn_smem[];
     BwdSmem& sm = *reinterpret_cast<BwdSmem*>(dyn_smem);
 
+    // lane = row group (rows 4 lane ..), warp = column group (slice columns 4 warp ..)
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int kb = tid >> 3, vb = tid & 7;
     const int H = a.H;
     const TIn* gq = static_cast<const TIn*>(a.q);
     const TIn* gk = static_cast<const TIn*>(a.k);
@@ -206,26 +187,8 @@ __global__ void __launch_bounds__(NT, kCtasPerSm) chunk_bwd_kernel(BwdArgs a)
     const TO* gdo = static_cast<const TO*>(a.dout);
     float4* scratch = a.scratch + (int64_t)blockIdx.x * SEG * kTileF4;
     const int64_t THK = a.T * H * DK, TH = a.T * H;
-    int tok = 0;                                           // parity of the K-sum buffers
-
-    // Sum over K of p[j] (this thread's 4 columns) into buffer `buf`: after
-    // the call, thread j < CW holds slice column j's sum in the return value.
-    auto ksum = [&](float (&p)[4], int buf) -> float {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            p[j] += __shfl_xor_sync(0xffffffffu, p[j], 8);
-            p[j] += __shfl_xor_sync(0xffffffffu, p[j], 16);
-        }
-        if (lane < 8)
-            *reinterpret_cast<float4*>(&sm.red[buf][warp][4 * vb]) = make_float4(p[0], p[1], p[2], p[3]);
-        __syncthreads();
-        float s = 0.f;
-        if (tid < CW) {
-#pragma unroll
-            for (int w = 0; w < NT / 32; ++w) s += sm.red[buf][w][tid];
-        }
-        return s;
-    };
+    const int tofs = warp * kQ * 32 + lane;                // this thread's float4 q of a tile: tofs + 32 q
+    int tok = 0;                                           // parity of the row-sum buffers
 
     const int64_t units = (int64_t)a.N * H * kSlices;
     for (int64_t unit = blockIdx.x; unit < units; unit += gridDim.x) {
@@ -233,6 +196,7 @@ __global__ void __launch_bounds__(NT, kCtasPerSm) chunk_bwd_kernel(BwdArgs a)
         const int64_t nh = unit / kSlices;                 // n * H + h
         const int n = (int)(nh / H), h = (int)(nh % H);
         const int c0 = CW * vs;                            // first column of the slice
+        const int cw = 4 * warp;                           // the warp's first column in the slice
         const int bos = a.cu[n], eos = a.cu[n + 1];
         if (bos < 0 || eos < bos || (int64_t)eos > a.T) continue;   // reported by the plan
         const int nseg = (eos - bos + SEG - 1) / SEG;
@@ -316,11 +280,12 @@ __global__ void __launch_bounds__(NT, kCtasPerSm) chunk_bwd_kernel(BwdArgs a)
             __syncthreads();
         };
         // One forward token: S <- S' + k^ d^T with S' = Diag(a) S; u and d of
-        // the token to uu / dl row tl when `keep`.
+        // the token to uu / dl row tl when `keep`.  Warp-local: no barrier.
         auto fwd_token = [&](float (&S)[16], int tl, bool keep) {
-            float av4[4], kn[4], p[4];
-            f4(&sm.av[tl][4 * kb], av4);
-            f4(&sm.kh[tl][4 * kb], kn);
+            float av4[4], kn[4], p[4], u[4], vv4[4];
+            f4(&sm.av[tl][4 * lane], av4);
+            f4(&sm.kh[tl][4 * lane], kn);
+            f4(&sm.vv[tl][cw], vv4);
 #pragma unroll
             for (int i = 0; i < 4; ++i)
 #pragma unroll
@@ -332,19 +297,15 @@ __global__ void __launch_bounds__(NT, kCtasPerSm) chunk_bwd_kernel(BwdArgs a)
                 for (int i = 0; i < 4; ++i) acc += S[4 * i + j] * kn[i];
                 p[j] = acc;
             }
-            const int buf = tok++ & 1;
-            const float u = ksum(p, buf);
-            if (tid < CW) {
-                const float d = sm.beta[tl] * (sm.vv[tl][tid] - u);
-                sm.bc[buf][tid] = d;
-                if (keep) {
-                    sm.uu[tl][tid] = u;
-                    sm.dl[tl][tid] = d;
-                }
-            }
-            __syncthreads();
+            ksum_warp(p, lane, u);
+            const float bt = sm.beta[tl];
             float d4[4];
-            f4(&sm.bc[buf][4 * vb], d4);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) d4[j] = bt * (vv4[j] - u[j]);
+            if (keep && lane < 4) {
+                sm.uu[tl][cw + lane] = pick4(u, lane);
+                sm.dl[tl][cw + lane] = pick4(d4, lane);
+            }
 #pragma unroll
             for (int i = 0; i < 4; ++i)
 #pragma unroll
@@ -359,7 +320,19 @@ __global__ void __launch_bounds__(NT, kCtasPerSm) chunk_bwd_kernel(BwdArgs a)
             }
             const float* s0 = src + nh * DK * DV;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) f4(s0 + (4 * kb + i) * DV + c0 + 4 * vb, S + 4 * i);
+            for (int i = 0; i < 4; ++i) f4(s0 + (4 * lane + i) * DV + c0 + cw, S + 4 * i);
+        };
+        auto tstore = [&](float4* base, const float (&s)[16]) {
+#pragma unroll
+            for (int q = 0; q < kQ; ++q)
+                base[tofs + 32 * q] = make_float4(s[4 * q], s[4 * q + 1], s[4 * q + 2], s[4 * q + 3]);
+        };
+        auto tload = [&](const float4* base, float (&s)[16]) {
+#pragma unroll
+            for (int q = 0; q < kQ; ++q) {
+                const float4 x = base[tofs + 32 * q];
+                s[4 * q] = x.x; s[4 * q + 1] = x.y; s[4 * q + 2] = x.z; s[4 * q + 3] = x.w;
+            }
         };
 
         // ---- forward pass: the state slice at every segment start
@@ -367,7 +340,7 @@ __global__ void __launch_bounds__(NT, kCtasPerSm) chunk_bwd_kernel(BwdArgs a)
         load_state(a.init, S);
         for (int sg = 0; sg < nseg; ++sg) {
             const int t0 = bos + sg * SEG, L = min(SEG, eos - t0);
-            tile_store(ck + sg * ck_stride, tid, S);
+            tstore(ck + sg * ck_stride, S);
             stage(t0, L, false);
             for (int tl = 0; tl < L; ++tl) fwd_token(S, tl, false);
         }
@@ -378,37 +351,38 @@ __global__ void __launch_bounds__(NT, kCtasPerSm) chunk_bwd_kernel(BwdArgs a)
         for (int sg = nseg - 1; sg >= 0; --sg) {
             const int t0 = bos + sg * SEG, L = min(SEG, eos - t0);
             // recompute the segment: the state before each token, u and d
-            tile_load(ck + sg * ck_stride, tid, S);
+            tload(ck + sg * ck_stride, S);
             stage(t0, L, true);
             for (int tl = 0; tl < L; ++tl) {
-                tile_store(scratch + (int64_t)tl * kTileF4, tid, S);
+                tstore(scratch + (int64_t)tl * kTileF4, S);
                 fwd_token(S, tl, true);
             }
-            // walk it backwards; the state before token tl - 1 is fetched
-            // while token tl is processed
-            tile_fetch_async(sm.tile[(L - 1) & 1], scratch + (int64_t)(L - 1) * kTileF4, tid);
+            __syncthreads();                               // u and d of every column in place
+            // walk it backwards; the state before token tl - 1 is loaded while
+            // token tl is processed (each thread reads back what it wrote)
+            float Snext[16];
+            tload(scratch + (int64_t)(L - 1) * kTileF4, Snext);
             for (int tl = L - 1; tl >= 0; --tl) {
                 const int64_t t = t0 + tl;
-                if (tl > 0) {
-                    tile_fetch_async(sm.tile[(tl - 1) & 1], scratch + (int64_t)(tl - 1) * kTileF4, tid);
-                    cp_async_wait_older();
-                } else {
-                    tc::cp_async_wait_all();
-                }
                 float Sp[16];
-                tile_load(sm.tile[tl & 1], tid, Sp);
-                float av4[4], kn[4], qn[4], dO[4], d4[4];
-                f4(&sm.av[tl][4 * kb], av4);
-                f4(&sm.kh[tl][4 * kb], kn);
-                f4(&sm.qh[tl][4 * kb], qn);
-                f4(&sm.dO[tl][4 * vb], dO);
-                f4(&sm.dl[tl][4 * vb], d4);
+#pragma unroll
+                for (int e = 0; e < 16; ++e) Sp[e] = Snext[e];
+                if (tl > 0) tload(scratch + (int64_t)(tl - 1) * kTileF4, Snext);
+                float av4[4], kn[4], qn[4], dO[4], d4[4], vv4[4], uu4[4];
+                f4(&sm.av[tl][4 * lane], av4);
+                f4(&sm.kh[tl][4 * lane], kn);
+                f4(&sm.qh[tl][4 * lane], qn);
+                f4(&sm.dO[tl][cw], dO);
+                f4(&sm.dl[tl][cw], d4);
+                f4(&sm.vv[tl][cw], vv4);
+                f4(&sm.uu[tl][cw], uu4);
+                const float bt = sm.beta[tl];
 #pragma unroll
                 for (int i = 0; i < 4; ++i)
 #pragma unroll
                     for (int j = 0; j < 4; ++j) Sp[4 * i + j] *= av4[i];
                 // o = scale S^T q^:  dS += scale q^ dO^T,  dq^ = scale S dO
-                float dqn[4], ddp[4];
+                float dqn[4], ddp[4], dd[4];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     float acc = 0.f;
@@ -419,7 +393,7 @@ __global__ void __launch_bounds__(NT, kCtasPerSm) chunk_bwd_kernel(BwdArgs a)
                     }
                     dqn[i] = a.scale * acc;
                 }
-                // dd = dS^T k^
+                // dd = dS^T k^ (over all K rows: the warp)
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     float acc = 0.f;
@@ -427,20 +401,14 @@ __global__ void __launch_bounds__(NT, kCtasPerSm) chunk_bwd_kernel(BwdArgs a)
                     for (int i = 0; i < 4; ++i) acc += dS[4 * i + j] * kn[i];
                     ddp[j] = acc;
                 }
-                const int buf = tok++ & 1;
-                const float dd = ksum(ddp, buf);
-                if (tid < CW) {                            // warp 0
-                    const float bt = sm.beta[tl];
-                    a.dv[(t * H + h) * DV + c0 + tid] = bt * dd;
-                    sm.bc[buf][tid] = -bt * dd;            // du
-                    float part = dd * (sm.vv[tl][tid] - sm.uu[tl][tid]);
+                ksum_warp(ddp, lane, dd);
+                float du[4], dbw = 0.f;
 #pragma unroll
-                    for (int m = 16; m > 0; m >>= 1) part += __shfl_xor_sync(0xffffffffu, part, m);
-                    if (lane == 0) pb[t * H + h] = part;
+                for (int j = 0; j < 4; ++j) {
+                    du[j] = -bt * dd[j];
+                    dbw += dd[j] * (vv4[j] - uu4[j]);
                 }
-                __syncthreads();
-                float du[4];
-                f4(&sm.bc[buf][4 * vb], du);
+                if (lane < 4) __stcs(&a.dv[(t * H + h) * DV + c0 + cw + lane], bt * pick4(dd, lane));
                 // dk^ = dS d + S' du;  dS' = dS + k^ du^T;  dg = rowsum(dS' o S');  dS = a dS'
                 float dkn[4], dgp[4];
 #pragma unroll
@@ -456,15 +424,27 @@ __global__ void __launch_bounds__(NT, kCtasPerSm) chunk_bwd_kernel(BwdArgs a)
                     dkn[i] = acc;
                     dgp[i] = accg;
                 }
-                int idx;
-                const float sq = vsum8(dqn, lane, idx);
-                const float sk = vsum8(dkn, lane, idx);
-                const float sgd = vsum8(dgp, lane, idx);
-                if ((lane & 1) == 0) {
-                    const int64_t o = (t * H + h) * DK + 4 * kb + idx;
-                    pq[o] = sq;
-                    pk[o] = sk;
-                    pg[o] = sgd;
+                // the warp's row partials (its 4 columns) to shared memory; the
+                // sums over the slice's 8 warps after one barrier
+                const int buf = tok++ & 1;
+                *reinterpret_cast<float4*>(&sm.red[buf][warp][0][4 * lane]) = make_float4(dqn[0], dqn[1], dqn[2], dqn[3]);
+                *reinterpret_cast<float4*>(&sm.red[buf][warp][1][4 * lane]) = make_float4(dkn[0], dkn[1], dkn[2], dkn[3]);
+                *reinterpret_cast<float4*>(&sm.red[buf][warp][2][4 * lane]) = make_float4(dgp[0], dgp[1], dgp[2], dgp[3]);
+                if (lane == 0) sm.dbr[buf][warp] = dbw;
+                __syncthreads();
+                for (int o = tid; o < 3 * DK; o += NT) {
+                    const int qv = o / DK, r = o % DK;
+                    float acc = 0.f;
+#pragma unroll
+                    for (int w = 0; w < NT / 32; ++w) acc += sm.red[buf][w][qv][r];
+                    float* dst = qv == 0 ? pq : (qv == 1 ? pk : pg);
+                    __stcs(&dst[(t * H + h) * DK + r], acc);
+                }
+                if (tid == 0) {
+                    float acc = 0.f;
+#pragma unroll
+                    for (int w = 0; w < NT / 32; ++w) acc += sm.dbr[buf][w];
+                    pb[t * H + h] = acc;
                 }
             }
         }
@@ -472,7 +452,7 @@ __global__ void __launch_bounds__(NT, kCtasPerSm) chunk_bwd_kernel(BwdArgs a)
             float* d0 = a.dinit + nh * DK * DV;
 #pragma unroll
             for (int i = 0; i < 4; ++i)
-                *reinterpret_cast<float4*>(d0 + (4 * kb + i) * DV + c0 + 4 * vb) =
+                *reinterpret_cast<float4*>(d0 + (4 * lane + i) * DV + c0 + cw) =
                     make_float4(dS[4 * i], dS[4 * i + 1], dS[4 * i + 2], dS[4 * i + 3]);
         }
     }
@@ -591,7 +571,7 @@ int64_t bwd_workspace_bytes(int32_t N, int64_t T, int32_t H)
 cudaError_t launch_chunk_bwd(const BwdLaunch& L, cudaStream_t stream)
 {
     static_assert(sizeof(BwdSmem) * kCtasPerSm <= 227 * 1024, "shared memory budget");
-    static_assert(offsetof(BwdSmem, tile) % 16 == 0, "cp.async destinations 16-byte aligned");
+    static_assert(offsetof(BwdSmem, red) % 16 == 0, "16-byte shared stores");
     const int64_t units = (int64_t)L.N * L.H * kSlices;
     const int grid = (int)bwd_ctas(L.N, L.H);
     int32_t* hdr = static_cast<int32_t*>(L.workspace);
