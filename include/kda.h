@@ -308,8 +308,9 @@ kda_status kda_chunk_bwd_workspace_size(int32_t N, int64_t T, int32_t H, int32_t
  * No output may alias an input.  workspace: device, 16-byte aligned, at least
  * kda_chunk_bwd_workspace_size bytes, owned by the caller, contents on entry
  * irrelevant; calls sharing one workspace must be ordered on one stream.
- * FP32 arithmetic throughout (the forward is recomputed from the per-chunk
- * checkpoints, so its rounding matches fp32_exact's token order, not BF16_TC).
+ * FP32 arithmetic throughout: the forward is recomputed token by token from
+ * checkpoints of the state every 16 tokens, so the gradients are those of the
+ * exact recurrence (either forward mode's output approximates it).
  * Errors as kda_chunk_fwd; offsets outside [0, T] seen on the device set
  * KDA_ERR_DEVICE_ARG in status_dev and leave those sequences' outputs unwritten.
  */
