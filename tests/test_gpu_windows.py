@@ -41,6 +41,7 @@ def _both(lens, H, seed, init, host_mirror):
     ([3000, 0, 1200], 2, True, True),       # a sequence across both windows, an empty one
     ([16384], 2, False, True),              # eight windows
     ([2100, 2100], 3, True, False),         # windows from the chunk bound (no host mirror)
+    ([5000, 1, 6000, 0, 3000], 3, True, True),   # four windows, sequences across several
 ])
 def test_windows_are_bitwise_one_window(lens, H, init, host_mirror):
     _, _, (o_w, S_w), (o_1, S_1) = _both(lens, H, 91 + H, init, host_mirror)
