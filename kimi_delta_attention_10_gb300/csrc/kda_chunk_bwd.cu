@@ -26,7 +26,8 @@
 // the slice's columns (dq^, dk^, dg, dbeta) go through shared memory, one CTA
 // barrier per backward token (the buffers of neighbouring tokens alternate).
 // Tokens are taken in segments of 16 whose inputs (q^, k^, e^g full rows; v,
-// dO slice columns; beta) are staged in shared memory with coalesced loads.
+// dO slice columns; beta) are staged in shared memory; the raw rows of the
+// next segment arrive by cp.async while the current one is processed.
 // A first pass stores the state slice at every segment start in the
 // workspace; then, segment by segment from the last, the segment is
 // recomputed from its checkpoint (the state before each token to a 256 KiB
@@ -40,6 +41,7 @@
 #include <cstddef>
 
 #include "kda_internal.cuh"
+#include "kda_tc.cuh"
 
 namespace kda {
 
@@ -99,46 +101,26 @@ struct BwdSmem {
     float red[2][NT / 32][3][DK];   // per-warp row partials of dq^, dk^, dg (two tokens)
     float dbr[2][NT / 32];          // per-warp partials of dbeta
     float beta[SEG], rq[SEG], rk[SEG];
+    // the next segment's raw input rows, brought in by cp.async while the
+    // current segment is processed (sized for FP32 inputs)
+    unsigned char raw_q[SEG * DK * 4];
+    unsigned char raw_k[SEG * DK * 4];
+    unsigned char raw_g[SEG * DK * 4];
+    unsigned char raw_v[SEG * CW * 4];
+    unsigned char raw_do[SEG * CW * 4];
+    float raw_beta[SEG];
 };
 
 __device__ __forceinline__ float ld1(const float* p, int64_t i) { return p[i]; }
 __device__ __forceinline__ float ld1(const __nv_bfloat16* p, int64_t i) { return __bfloat162float(p[i]); }
 
-// 8 (or 4) consecutive values from global memory, 16-byte aligned for FP32
-// (8-byte for 4 BF16 values).
-__device__ __forceinline__ void ld8(const float* p, int64_t i, float (&x)[8])
-{
-    const float4 a = __ldcs(reinterpret_cast<const float4*>(p + i));
-    const float4 b = __ldcs(reinterpret_cast<const float4*>(p + i + 4));
-    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
-}
-__device__ __forceinline__ void ld8(const __nv_bfloat16* p, int64_t i, float (&x)[8])
-{
-    const uint4 u = __ldcs(reinterpret_cast<const uint4*>(p + i));
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        x[2 * e] = __uint_as_float(w[e] << 16);
-        x[2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
-    }
-}
-__device__ __forceinline__ float4 ld4(const float* p, int64_t i)
-{
-    return __ldcs(reinterpret_cast<const float4*>(p + i));
-}
-__device__ __forceinline__ float4 ld4(const __nv_bfloat16* p, int64_t i)
-{
-    const uint2 u = __ldcs(reinterpret_cast<const uint2*>(p + i));
-    return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u),
-                       __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
-}
 __device__ __forceinline__ void sst8(float* p, const float (&x)[8])
 {
     reinterpret_cast<float4*>(p)[0] = make_float4(x[0], x[1], x[2], x[3]);
     reinterpret_cast<float4*>(p)[1] = make_float4(x[4], x[5], x[6], x[7]);
 }
-// Inputs are read once and outputs written once: streaming loads and stores
-// (__ldcs / __stcs) keep them from displacing the state scratch in L2.
+// Outputs are written once: streaming stores (__stcs) keep them from
+// displacing the state scratch in L2.
 // x[lane] for lane < 4 without indexing a register array.
 __device__ __forceinline__ float pick4(const float (&x)[4], int lane)
 {
@@ -148,6 +130,39 @@ __device__ __forceinline__ void f4(const float* p, float* x)
 {
     const float4 a = *reinterpret_cast<const float4*>(p);
     x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+}
+
+// 8 (or 4) values of a raw staged row at element c, as float.
+__device__ __forceinline__ void raw8(const unsigned char* row, int c, const float*, float (&x)[8])
+{
+    const float4 a = *reinterpret_cast<const float4*>(row + 4 * c);
+    const float4 b = *reinterpret_cast<const float4*>(row + 4 * c + 16);
+    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+}
+__device__ __forceinline__ void raw8(const unsigned char* row, int c, const __nv_bfloat16*, float (&x)[8])
+{
+    const uint4 u = *reinterpret_cast<const uint4*>(row + 2 * c);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        x[2 * e] = __uint_as_float(w[e] << 16);
+        x[2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
+    }
+}
+__device__ __forceinline__ float4 raw4(const unsigned char* row, int c, const float*)
+{
+    return *reinterpret_cast<const float4*>(row + 4 * c);
+}
+__device__ __forceinline__ float4 raw4(const unsigned char* row, int c, const __nv_bfloat16*)
+{
+    const uint2 u = *reinterpret_cast<const uint2*>(row + 2 * c);
+    return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u),
+                       __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
+}
+__device__ __forceinline__ void cp_async4(void* dst, const void* src)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(tc::smem_u32(dst)), "l"(src)
+                 : "memory");
 }
 
 // Sum over the warp's 32 lanes (K rows) of p[j], j < 4 (the warp's columns):
@@ -208,23 +223,65 @@ __global__ void __launch_bounds__(NT, kCtasPerSm) chunk_bwd_kernel(BwdArgs a)
         float* pg = vs == 0 ? a.dg : a.part + ((int64_t)(vs - 1) * 3 + 2) * THK;
         float* pb = vs == 0 ? a.dbeta : a.part + (int64_t)(kSlices - 1) * 3 * THK + (vs - 1) * TH;
 
-        // The segment's inputs in shared memory: q^, k^ (normalised rows),
+        // The segment's raw input rows (k, g, v, beta and, with_bwd, q and dO)
+        // into the raw buffers by cp.async; rows >= L are not loaded.
+        auto issue = [&](int t0, int L, bool with_bwd) {
+            constexpr int kRow = DK * (int)sizeof(TIn), kCpr = kRow / 16;     // q, k rows
+            constexpr int vRow = CW * (int)sizeof(TIn), vCpr = vRow / 16;     // v slice rows
+            constexpr int oRow = CW * (int)sizeof(TO), oCpr = oRow / 16;      // dO slice rows
+            for (int e = tid; e < SEG * kCpr; e += NT) {
+                const int r = e / kCpr, pc = e % kCpr;
+                if (r < L) {
+                    const int64_t row = ((int64_t)(t0 + r) * H + h) * DK;
+                    tc::cp_async16(sm.raw_k + r * kRow + 16 * pc,
+                                   reinterpret_cast<const unsigned char*>(gk + row) + 16 * pc, true);
+                    if (with_bwd)
+                        tc::cp_async16(sm.raw_q + r * kRow + 16 * pc,
+                                       reinterpret_cast<const unsigned char*>(gq + row) + 16 * pc, true);
+                }
+            }
+            for (int e = tid; e < SEG * 32; e += NT) {                           // g: 512-byte rows
+                const int r = e >> 5, pc = e & 31;
+                if (r < L)
+                    tc::cp_async16(sm.raw_g + r * 512 + 16 * pc,
+                                   a.g + ((int64_t)(t0 + r) * H + h) * DK + 4 * pc, true);
+            }
+            for (int e = tid; e < SEG * vCpr; e += NT) {
+                const int r = e / vCpr, pc = e % vCpr;
+                if (r < L)
+                    tc::cp_async16(sm.raw_v + r * vRow + 16 * pc,
+                                   reinterpret_cast<const unsigned char*>(
+                                       gv + ((int64_t)(t0 + r) * H + h) * DV + c0) + 16 * pc, true);
+            }
+            if (with_bwd) {
+                for (int e = tid; e < SEG * oCpr; e += NT) {
+                    const int r = e / oCpr, pc = e % oCpr;
+                    if (r < L)
+                        tc::cp_async16(sm.raw_do + r * oRow + 16 * pc,
+                                       reinterpret_cast<const unsigned char*>(
+                                           gdo + ((int64_t)(t0 + r) * H + h) * DV + c0) + 16 * pc, true);
+                }
+            }
+            if (tid < L) cp_async4(&sm.raw_beta[tid], a.beta + (int64_t)(t0 + tid) * H + h);
+            tc::cp_async_commit();
+        };
+        // The issued segment in the working arrays: q^, k^ (normalised rows),
         // e^g, the slice of v and (with_bwd) dO, beta; rows >= L unused.
-        auto stage = [&](int t0, int L, bool with_bwd) {
-            __syncthreads();                               // the previous segment is done
+        auto finish = [&](int L, bool with_bwd) {
+            tc::cp_async_wait_all();
+            __syncthreads();                               // the raw rows landed; the previous segment is done
             {
                 const int r = tid >> 4, c = 8 * (tid & 15);
                 if (r < L) {
                     float x[8];
-                    const int64_t rowk = ((int64_t)(t0 + r) * H + h) * DK + c;
-                    ld8(gk, rowk, x);
+                    raw8(sm.raw_k + r * DK * (int)sizeof(TIn), c, gk, x);
                     sst8(&sm.kh[r][c], x);
-                    ld8(a.g, rowk, x);
+                    raw8(sm.raw_g + r * DK * 4, c, a.g, x);
 #pragma unroll
                     for (int e = 0; e < 8; ++e) x[e] = expf(x[e]);
                     sst8(&sm.av[r][c], x);
                     if (with_bwd) {
-                        ld8(gq, rowk, x);
+                        raw8(sm.raw_q + r * DK * (int)sizeof(TIn), c, gq, x);
                         sst8(&sm.qh[r][c], x);
                     }
                 }
@@ -232,12 +289,12 @@ __global__ void __launch_bounds__(NT, kCtasPerSm) chunk_bwd_kernel(BwdArgs a)
             if (tid < SEG * CW / 4) {
                 const int r = tid >> 3, c = 4 * (tid & 7);
                 if (r < L) {
-                    const int64_t rowv = ((int64_t)(t0 + r) * H + h) * DV + c0 + c;
-                    *reinterpret_cast<float4*>(&sm.vv[r][c]) = ld4(gv, rowv);
-                    if (with_bwd) *reinterpret_cast<float4*>(&sm.dO[r][c]) = ld4(gdo, rowv);
+                    *reinterpret_cast<float4*>(&sm.vv[r][c]) = raw4(sm.raw_v + r * CW * (int)sizeof(TIn), c, gv);
+                    if (with_bwd)
+                        *reinterpret_cast<float4*>(&sm.dO[r][c]) = raw4(sm.raw_do + r * CW * (int)sizeof(TO), c, gdo);
                 }
             }
-            if (tid < SEG) sm.beta[tid] = tid < L ? a.beta[(int64_t)(t0 + tid) * H + h] : 0.f;
+            if (tid < SEG) sm.beta[tid] = tid < L ? sm.raw_beta[tid] : 0.f;
             __syncthreads();
             // row norms: warp w takes rows 2 w and 2 w + 1
 #pragma unroll
@@ -277,7 +334,7 @@ __global__ void __launch_bounds__(NT, kCtasPerSm) chunk_bwd_kernel(BwdArgs a)
                     }
                 }
             }
-            __syncthreads();
+            __syncthreads();                               // working arrays ready; raw buffers free
         };
         // One forward token: S <- S' + k^ d^T with S' = Diag(a) S; u and d of
         // the token to uu / dl row tl when `keep`.  Warp-local: no barrier.
@@ -338,21 +395,26 @@ __global__ void __launch_bounds__(NT, kCtasPerSm) chunk_bwd_kernel(BwdArgs a)
         // ---- forward pass: the state slice at every segment start
         float S[16];
         load_state(a.init, S);
+        auto seg_len = [&](int sg) { return min(SEG, eos - (bos + sg * SEG)); };
+        if (nseg > 0) issue(bos, seg_len(0), false);
         for (int sg = 0; sg < nseg; ++sg) {
-            const int t0 = bos + sg * SEG, L = min(SEG, eos - t0);
+            const int L = seg_len(sg);
             tstore(ck + sg * ck_stride, S);
-            stage(t0, L, false);
+            finish(L, false);
+            if (sg + 1 < nseg) issue(bos + (sg + 1) * SEG, seg_len(sg + 1), false);
             for (int tl = 0; tl < L; ++tl) fwd_token(S, tl, false);
         }
 
         // ---- backward, segment by segment from the last
         float dS[16];
         load_state(a.dfinal, dS);
+        if (nseg > 0) issue(bos + (nseg - 1) * SEG, seg_len(nseg - 1), true);
         for (int sg = nseg - 1; sg >= 0; --sg) {
-            const int t0 = bos + sg * SEG, L = min(SEG, eos - t0);
+            const int t0 = bos + sg * SEG, L = seg_len(sg);
             // recompute the segment: the state before each token, u and d
             tload(ck + sg * ck_stride, S);
-            stage(t0, L, true);
+            finish(L, true);
+            if (sg > 0) issue(bos + (sg - 1) * SEG, seg_len(sg - 1), true);
             for (int tl = 0; tl < L; ++tl) {
                 tstore(scratch + (int64_t)tl * kTileF4, S);
                 fwd_token(S, tl, true);
