@@ -301,15 +301,14 @@ __global__ void __launch_bounds__(NT, kCtasPerSm) chunk_bwd_kernel(BwdArgs a)
             for (int rr = 0; rr < 2; ++rr) {
                 const int r = 2 * warp + rr;
                 if (r < L) {
-                    float sk = 0.f, sq = 0.f;
+                    float sk = 0.f, sq = 0.f, x4[4];
+                    f4(&sm.kh[r][4 * lane], x4);
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float xk = sm.kh[r][4 * lane + e];
-                        sk += xk * xk;
-                        if (with_bwd) {
-                            const float xq = sm.qh[r][4 * lane + e];
-                            sq += xq * xq;
-                        }
+                    for (int e = 0; e < 4; ++e) sk += x4[e] * x4[e];
+                    if (with_bwd) {
+                        f4(&sm.qh[r][4 * lane], x4);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) sq += x4[e] * x4[e];
                     }
 #pragma unroll
                     for (int m = 16; m > 0; m >>= 1) {
@@ -326,11 +325,19 @@ __global__ void __launch_bounds__(NT, kCtasPerSm) chunk_bwd_kernel(BwdArgs a)
             {
                 const int r = tid >> 4, c = 8 * (tid & 15);
                 if (r < L) {
+                    float x[8];
                     const float nk = sm.rk[r], nq = sm.rq[r];
+                    f4(&sm.kh[r][c], x);
+                    f4(&sm.kh[r][c + 4], x + 4);
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        sm.kh[r][c + e] *= nk;
-                        if (with_bwd) sm.qh[r][c + e] *= nq;
+                    for (int e = 0; e < 8; ++e) x[e] *= nk;
+                    sst8(&sm.kh[r][c], x);
+                    if (with_bwd) {
+                        f4(&sm.qh[r][c], x);
+                        f4(&sm.qh[r][c + 4], x + 4);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) x[e] *= nq;
+                        sst8(&sm.qh[r][c], x);
                     }
                 }
             }
