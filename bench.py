@@ -505,7 +505,9 @@ def main():
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-                "dtype": "f32" if mode == "fp32_exact" else "bf16", "data": "synthetic",
+                # the arithmetic type: FP16 tensor-core operands (formed from the
+                # BF16 inputs) with FP32 accumulation and an FP32 state, or FP32
+                "dtype": "f32" if mode == "fp32_exact" else "f16/f32", "data": "synthetic",
                 "config": cfg, "roofline": roof,
                 "kernels": {f"{kname}_ms": statistics.mean(chunk_ms),
                             f"{kname}_p50_ms": statistics.median(chunk_ms),
