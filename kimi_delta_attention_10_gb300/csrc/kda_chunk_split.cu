@@ -16,7 +16,10 @@
 // The scan (chunk_scan_kernel: one CTA per (sequence, head)) then walks the
 // chunks in order with the state on chip, bringing each record in by one bulk
 // copy, double-buffered, while it works on the one before.  A plan kernel
-// first turns cu_seqlens into per-sequence chunk offsets.
+// first turns cu_seqlens into per-sequence chunk offsets.  When the scan CTAs
+// alone would leave SMs idle, the chunks are cut into windows so that the
+// preparation of later chunks runs beside the scan of earlier ones (see
+// launch_chunk_split).
 //
 // Record of one unit (bytes), in this order:
 //   W       fp16 [128 c][64 i]  (MN-major B of [W S]^T = S^T W^T)
