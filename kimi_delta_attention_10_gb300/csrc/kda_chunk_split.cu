@@ -61,10 +61,14 @@ static_assert(REC_BYTES % 16 == 0 && REC_BYTES < (1u << 20), "bulk copy size");
 
 // Workspace header: int32 [0] = 1 when the plan found offsets outside [0, T]
 // (those sequences get no chunks and are skipped), int32 [4 .. 4 + N] = chunk
-// offsets (chunks of sequences 0 .. n-1).
+// offsets (chunks of sequences 0 .. n-1), then int32 [5 + N .. 5 + 2N) = the
+// order in which the scan takes the sequences: longest first (LPT), so that
+// short sequences fill the tail of a packed batch (input order above
+// kLptMaxSeqs sequences).
 constexpr int kHdrOff = 4;
+constexpr int kLptMaxSeqs = 1024;
 
-int64_t header_bytes(int32_t N) { return ((int64_t)(kHdrOff + N + 1) * 4 + 1023) / 1024 * 1024; }
+int64_t header_bytes(int32_t N) { return ((int64_t)(kHdrOff + 2 * N + 1) * 4 + 1023) / 1024 * 1024; }
 
 // ---------------------------------------------------------------- plan
 __global__ void __launch_bounds__(1024) chunk_plan_kernel(const int32_t* __restrict__ cu, int32_t N,
@@ -117,6 +121,27 @@ __global__ void __launch_bounds__(1024) chunk_plan_kernel(const int32_t* __restr
     if (tid == 0) {
         hdr[0] = bad;
         if (bad) report_status(status, KDA_ERR_DEVICE_ARG);
+    }
+    // scan order: rank of each sequence by length, longest first, ties by index
+    int32_t* order = hdr + kHdrOff + N + 1;
+    if (N <= kLptMaxSeqs) {
+        __shared__ int32_t len[kLptMaxSeqs];
+        if (tid < N) {
+            const int32_t bos = cu[tid], eos = cu[tid + 1];
+            len[tid] = (bos < 0 || eos < bos || (int64_t)eos > T) ? 0 : eos - bos;
+        }
+        __syncthreads();
+        if (tid < N) {
+            const int32_t mine = len[tid];
+            int32_t rank = 0;
+            for (int32_t m = 0; m < N; ++m) {
+                const int32_t other = len[m];
+                rank += (other > mine) || (other == mine && m < tid);
+            }
+            order[rank] = tid;
+        }
+    } else {
+        for (int32_t n = tid; n < N; n += 1024) order[n] = n;
     }
 }
 
@@ -478,7 +503,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) chunk_scan_kernel(ChunkArgs a
     const int quad = warp & 3, half = (warp >> 2) & 1;
     const int row = 32 * quad + lane;                      // TMEM lane = state row v
     const int H = args.H;
-    const int n = blockIdx.x / H, h = blockIdx.x % H;
+    const int n = hdr[kHdrOff + args.N + 1 + blockIdx.x / H], h = blockIdx.x % H;
     // the next preparation window may start on the SMs this grid leaves free
     launch_dependents();
 

@@ -106,7 +106,7 @@ def test_workspace_size_bound():
     for N, T, H in [(1, 16384, 64), (16, 32768, 64), (3, 65, 4), (0, 0, 1), (5000, 70000, 2)]:
         st, nbytes = workspace_size(lib, N, T, H)
         assert st == binding.KDA_OK
-        hdr = -(-(4 * (N + 5)) // 1024) * 1024
+        hdr = -(-(4 * (2 * N + 5)) // 1024) * 1024      # flag, N + 1 offsets, N scan order
         assert nbytes == hdr + (T // 64 + N) * H * rec + N * H * 128 * 128 * 4
         # the exact chunk count of any split of T tokens into N sequences is no larger
         lens = [T // max(N, 1)] * N
@@ -301,7 +301,7 @@ def test_bwd_workspace_size(lib):
         return out.value
 
     def expected(N, T, H):
-        hdr = -(-(4 * (N + 5)) // 1024) * 1024
+        hdr = -(-(4 * (2 * N + 5)) // 1024) * 1024
         state = 128 * 128 * 4
         ckpt = 4 * (T // 64 + N) * H * state            # one state per 16-token segment (bound)
         part = 3 * (3 * T * H * 128 + T * H) * 4        # partial row sums of column slices 1..3
