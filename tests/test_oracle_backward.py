@@ -75,3 +75,35 @@ def test_each_planted_mistake_fails_finite_differences(mutation):
     c, cu, dO, dST = _case(13)
     ok, _ = _fd_check(c, cu, dO, dST, True, mutation=mutation)
     assert not ok
+
+
+# ---- a second algorithm: the chunked (WY) VJP must equal the token VJP
+
+from oracle.chunked_backward import backward_chunked  # noqa: E402
+
+
+def _both(c, cu, dO, dST, l2norm, C, mutation="none"):
+    a = backward(c["q"], c["k"], c["v"], c["g"], c["beta"], cu, 0.7, dO, dS_final=dST,
+                 initial_state=c["S0"], l2norm=l2norm, mutation=mutation)
+    b = backward_chunked(c["q"], c["k"], c["v"], c["g"], c["beta"], cu, 0.7, dO, dS_final=dST,
+                         initial_state=c["S0"], l2norm=l2norm, C=C)
+    return [np.linalg.norm(x - y) / max(np.linalg.norm(y), 1e-300) for x, y in zip(a, b)]
+
+
+@pytest.mark.parametrize("C", [1, 3, 16, 64])
+@pytest.mark.parametrize("l2norm,init", [(True, True), (False, False)])
+def test_chunked_vjp_equals_token_vjp(C, l2norm, init):
+    c, cu, dO, dST = _case(21 + C, lens=(9, 0, 17, 40), H=2, K=6, V=5, init=init)
+    assert max(_both(c, cu, dO, dST, l2norm, C)) < 1e-12
+
+
+def test_chunked_vjp_equals_token_vjp_full_width():
+    """K = V = 128 (the library's shape), two packed sequences across chunk edges."""
+    c, cu, dO, dST = _case(22, lens=(130, 37), H=1, K=128, V=128)
+    assert max(_both(c, cu, dO, dST, True, 64)) < 1e-12
+
+
+@pytest.mark.parametrize("mutation", [m for m in MUTATIONS if m != "none"])
+def test_each_planted_mistake_disagrees_with_the_chunked_vjp(mutation):
+    c, cu, dO, dST = _case(23, lens=(9, 17), H=2, K=6, V=5)
+    assert max(_both(c, cu, dO, dST, True, 4, mutation=mutation)) > 1e-6
