@@ -305,7 +305,8 @@ kda_status kda_chunk_bwd_workspace_size(int32_t N, int64_t T, int32_t H, int32_t
  * Outputs, all F32 and written in full (every token of every sequence):
  *   dq, dk [T,H,K], dv [T,H,V], dg [T,H,K], dbeta [T,H];
  *   dinitial_state [N,H,K,V] or NULL (not computed).
- * No output may alias an input.  workspace: device, 16-byte aligned, at least
+ * No output may alias an input or another output (the same base pointer is
+ * rejected with KDA_ERR_INVALID_ARG).  workspace: device, 16-byte aligned, at least
  * kda_chunk_bwd_workspace_size bytes, owned by the caller, contents on entry
  * irrelevant; calls sharing one workspace must be ordered on one stream.
  * FP32 arithmetic throughout: the forward is recomputed token by token from

@@ -304,6 +304,16 @@ kda_status kda_chunk_bwd(const void* q, const void* k, const void* v, int32_t qk
     for (const void* p : ptrs)
         if (p && !aligned16(p)) return KDA_ERR_ALIGNMENT;
     if (N > 0 && workspace_bytes < kda::bwd_workspace_bytes(N, T, H)) return KDA_ERR_INVALID_ARG;
+    // no output may be an input or another output (checked on the base pointers)
+    const void* outs[] = {dq, dk, dv, dg, dbeta, dinitial_state};
+    const void* ins[] = {q, k, v, g, beta, dout, initial_state, dfinal_state, cu_seqlens, workspace};
+    for (int i = 0; i < 6; ++i) {
+        if (!outs[i]) continue;
+        for (const void* p : ins)
+            if (p == outs[i]) return KDA_ERR_INVALID_ARG;
+        for (int j = i + 1; j < 6; ++j)
+            if (outs[j] == outs[i]) return KDA_ERR_INVALID_ARG;
+    }
     if (N == 0) return KDA_OK;
     kda::BwdLaunch a = {};
     a.q = q; a.k = k; a.v = v; a.qkv_bf16 = qkv_dtype == KDA_BF16; a.g = g; a.beta = beta;

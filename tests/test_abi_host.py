@@ -259,9 +259,11 @@ def test_gated_rmsnorm_rejects_bad_arguments(lib, kw, expect):
 
 
 def bwd(lib, **kw):
-    a = dict(q=P, k=P, v=P, qkv=1, g=P, beta=P, cu=P, host=None, N=1, T=100, H=2, K=128, V=128,
-             scale=0.1, l2=1, dout=P, ddt=1, init=None, dfin=None, dq=P, dk=P, dv=P, dg=P, db=P,
-             dinit=None, ws=P, wsb=1 << 40, status=None)
+    ptr = lambda i: P + 0x1000 * i                 # distinct, 16-byte aligned, never dereferenced
+    a = dict(q=ptr(0), k=ptr(1), v=ptr(2), qkv=1, g=ptr(3), beta=ptr(4), cu=ptr(5), host=None,
+             N=1, T=100, H=2, K=128, V=128, scale=0.1, l2=1, dout=ptr(6), ddt=1, init=None,
+             dfin=None, dq=ptr(7), dk=ptr(8), dv=ptr(9), dg=ptr(10), db=ptr(11), dinit=None,
+             ws=ptr(12), wsb=1 << 40, status=None)
     a.update(kw)
     host = a["host"]
     hp = None
@@ -289,6 +291,9 @@ def bwd(lib, **kw):
     (dict(l2=2), binding.KDA_ERR_INVALID_ARG),
     (dict(N=0, T=0, ws=None, q=None, k=None, v=None, dout=None, dq=None, dk=None, dv=None,
           dg=None, db=None), binding.KDA_OK),
+    (dict(dq=P), binding.KDA_ERR_INVALID_ARG),                       # output is the q input
+    (dict(dg=P + 0x8000), binding.KDA_ERR_INVALID_ARG),              # two outputs (dk, dg) alias
+    (dict(dinit=P + 0xC000), binding.KDA_ERR_INVALID_ARG),           # output is the workspace
 ])
 def test_chunk_bwd_rejects_bad_arguments(lib, kw, expect):
     assert bwd(lib, **kw) == expect
