@@ -50,12 +50,15 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     """Compile every csrc/*.cu in parallel and link the shared library."""
     if not force and up_to_date():
         return LIB_PATH
-    os.makedirs(BUILD_DIR, exist_ok=True)
+    # objects in a directory of this process's own, the library replaced
+    # atomically: concurrent builders (one per rank) never clobber each other
+    obj_dir = os.path.join(BUILD_DIR, f"p{os.getpid()}")
+    os.makedirs(obj_dir, exist_ok=True)
     cc = nvcc()
     inc = ["-I", INCLUDE, "-I", CSRC]
 
     def compile_one(src):
-        obj = os.path.join(BUILD_DIR, os.path.basename(src) + ".o")
+        obj = os.path.join(obj_dir, os.path.basename(src) + ".o")
         cmd = [cc, *ARCH, *NVCC_FLAGS, *extra_flags, *inc, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -73,6 +76,7 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     if r.returncode != 0:
         raise RuntimeError(f"nvcc link failed:\n{r.stdout}{r.stderr}")
     os.replace(tmp, LIB_PATH)
+    shutil.rmtree(obj_dir, ignore_errors=True)
     return LIB_PATH
 
 
