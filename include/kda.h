@@ -17,8 +17,11 @@
  *   - Every array argument is a DEVICE pointer unless its name ends in
  *     `_host`.  Arrays are dense, row-major, in the layout given per argument,
  *     owned by the caller, and must stay valid until the stream reaches the
- *     launched work.  The library allocates no device memory and keeps no
- *     mutable global state; calls on different streams are independent.
+ *     launched work.  The library allocates no device memory.  Its only
+ *     mutable global state is the static scratch of kda_chunk_fwd_static
+ *     (calls of that entry point share it; see there) and the process-wide
+ *     test switch of kda_test_set_fault; calls of every other entry point on
+ *     different streams are independent.
  *   - Every device pointer must be 16-byte aligned (KDA_ERR_ALIGNMENT).
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
  *     default stream).  The library never synchronises.
@@ -50,16 +53,22 @@ typedef enum {
     KDA_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed             */
     KDA_ERR_TIMEOUT = 5,       /* device: a bounded wait gave up (status word)     */
     KDA_ERR_DEVICE_ARG = 6,    /* device: offsets outside [0, T] (status word)     */
-    KDA_ERR_TOO_LARGE = 7      /* kda_chunk_fwd_static: over its static scratch    */
+    KDA_ERR_TOO_LARGE = 7,     /* kda_chunk_fwd_static: over its static scratch    */
+    KDA_ERR_RANGE = 8          /* device: a non-finite output value (status word)  */
 } kda_status;
 
 typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype;
 
 typedef enum {
-    /* 16-bit tensor-core operands (FP16: v, and q and k when qk_l2norm = 0,
-     * must lie within its range, |x| < 65504) with FP32 accumulation and an
-     * FP32 state; output rel-L2 error against the FP64 recurrence is held
-     * below 3e-3. */
+    /* 16-bit tensor-core operands with FP32 accumulation and an FP32 state;
+     * output rel-L2 error against the FP64 recurrence is held below 3e-3.
+     * The operands are FP16, so v (and q and k when qk_l2norm = 0), and the
+     * state and the chunk's intermediates built from them, must stay within
+     * FP16's range, |x| < 65504.  Out-of-range values become infinities that
+     * reach the output; every kernel of this mode checks the values it
+     * stores (output rows and final states) and writes KDA_ERR_RANGE to
+     * *status_dev when one is not finite, so an overflow is never silent
+     * (inputs that hold NaN or infinity are reported the same way). */
     KDA_MODE_BF16_TC = 0,
     /* FP32 arithmetic throughout (IEEE FP32, no TF32), output rel-L2 error
      * below 1e-5 with F32 output.  This is the counterpart of the pages'
@@ -210,12 +219,21 @@ kda_status kda_chunk_fwd_gated(const void* q, const void* k, const void* v, int3
  *
  * The scratch is one file-scope device array of 64 MiB in the library, so
  * the call allocates nothing; every GPU that loads the library holds those
- * 64 MiB until the process exits, and they keep the last call's contents.  A problem whose kda_chunk_workspace_size(...)
- * exceeds 64 MiB is rejected with KDA_ERR_TOO_LARGE before anything is
- * launched (for H = 64: T / 64 + N must not exceed 14).
+ * 64 MiB until the process exits, and they keep the last call's contents.
+ * A problem whose kda_chunk_workspace_size(...) exceeds 64 MiB is rejected
+ * with KDA_ERR_TOO_LARGE before anything is launched.  That bound counts
+ * (T / 64 + N) * H records of 74240 bytes plus N * H * 64 KiB of state
+ * carry, so for H = 64 and N = 1, T / 64 + N may be at most 13 (T <= 768
+ * tokens), and every further sequence costs one more record per head and
+ * 4 MiB of carry.
  * The first call on a device does set-up (it looks up the array's device
  * address, which may load the library's device code), so make it before any
- * stream capture.  Every call on a device uses the same scratch: calls that
+ * stream capture.  The address is remembered per device for the life of the
+ * process: after cudaDeviceReset (or any reset of the primary context) the
+ * remembered address is stale and this entry point must not be called
+ * again in that process.  `stream` must belong to the current device
+ * (KDA_ERR_INVALID_ARG otherwise).  Every call on a device uses the same
+ * scratch: calls that
  * overlap in time (on different streams, or from different host threads
  * without ordering) race on it and give undefined results.  Nothing in the
  * scratch needs to start at zero.  The result equals kda_chunk_fwd with mode
@@ -326,6 +344,30 @@ kda_status kda_chunk_bwd(const void* q, const void* k, const void* v, int32_t qk
                          float* dinitial_state, void* workspace, int64_t workspace_bytes,
                          int32_t* status_dev, kda_stream_t stream);
 
+/*
+ * kda_test_set_fault -- TEST HOOK, not for production use (no page
+ * counterpart).  Lets a test make a bounded device wait run out without
+ * faulting the GPU: while it is set, CTA 0 of every launch of the named
+ * kernel withholds one mbarrier arrival, its wait gives up after about one
+ * second, the kernel writes KDA_ERR_TIMEOUT to *status_dev, lets its copies
+ * and MMAs in flight finish, releases its tensor memory and returns; the
+ * results of that launch are undefined.
+ *   where = KDA_TEST_FAULT_NONE (0)         off (the default)
+ *           KDA_TEST_FAULT_SCAN (1)         state scan of the two-phase path
+ *                                           (an epilogue arrival is withheld)
+ *           KDA_TEST_FAULT_PREP (2)         chunk preparation of the two-phase
+ *                                           path (its first MMA group and the
+ *                                           commit that signals it are withheld)
+ *           KDA_TEST_FAULT_SINGLE_PASS (3)  the single-pass kernel (likewise)
+ * The setting is process-wide and read at each launch; other values return
+ * KDA_ERR_INVALID_ARG.
+ */
+#define KDA_TEST_FAULT_NONE 0
+#define KDA_TEST_FAULT_SCAN 1
+#define KDA_TEST_FAULT_PREP 2
+#define KDA_TEST_FAULT_SINGLE_PASS 3
+kda_status kda_test_set_fault(int32_t where);
+
 /* Static text for a kda_status value ("unknown status" otherwise). */
 const char* kda_status_string(int32_t status);
 
@@ -333,7 +375,8 @@ const char* kda_status_string(int32_t status);
  * state argument of kda_chunk_fwd; kda_chunk_fwd_gated; kda_recurrent_step.
  * 3: workspace arguments; kda_chunk_workspace_size.  Later additions that
  * change no existing signature keep the number: kda_chunk_fwd_static,
- * kda_gated_rmsnorm, kda_chunk_bwd_workspace_size, kda_chunk_bwd). */
+ * kda_gated_rmsnorm, kda_chunk_bwd_workspace_size, kda_chunk_bwd,
+ * KDA_ERR_RANGE, kda_test_set_fault). */
 int32_t kda_abi_version(void);
 
 #ifdef __cplusplus

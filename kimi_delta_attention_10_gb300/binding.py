@@ -23,6 +23,13 @@ KDA_ERR_CUDA = 4
 KDA_ERR_TIMEOUT = 5
 KDA_ERR_DEVICE_ARG = 6
 KDA_ERR_TOO_LARGE = 7
+KDA_ERR_RANGE = 8
+
+# kda_test_set_fault values (test hook)
+KDA_TEST_FAULT_NONE = 0
+KDA_TEST_FAULT_SCAN = 1
+KDA_TEST_FAULT_PREP = 2
+KDA_TEST_FAULT_SINGLE_PASS = 3
 
 KDA_F32 = 0
 KDA_BF16 = 1
@@ -35,7 +42,8 @@ MODES = {"bf16_tc": KDA_MODE_BF16_TC, "fp32_exact": KDA_MODE_FP32_EXACT}
 # Every symbol include/kda.h declares.
 EXPORTS = ("kda_gate", "kda_chunk_workspace_size", "kda_chunk_fwd", "kda_chunk_fwd_gated",
            "kda_chunk_fwd_static", "kda_recurrent_step", "kda_gated_rmsnorm",
-           "kda_chunk_bwd_workspace_size", "kda_chunk_bwd", "kda_status_string", "kda_abi_version")
+           "kda_chunk_bwd_workspace_size", "kda_chunk_bwd", "kda_test_set_fault",
+           "kda_status_string", "kda_abi_version")
 
 _lock = threading.Lock()
 _lib = None
@@ -92,6 +100,8 @@ def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
                                       ctypes.c_float, i32, vp, i32, vp, vp, vp, vp, vp, vp, vp,
                                       vp, vp, i64, vp, vp]
         lib.kda_chunk_bwd.restype = i32
+        lib.kda_test_set_fault.argtypes = [i32]
+        lib.kda_test_set_fault.restype = i32
         lib.kda_status_string.argtypes = [i32]
         lib.kda_status_string.restype = ctypes.c_char_p
         lib.kda_abi_version.argtypes = []
@@ -102,6 +112,14 @@ def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
 
 def status_string(status: int) -> str:
     return load_library().kda_status_string(int(status)).decode()
+
+
+def test_set_fault(where: int) -> None:
+    """Test hook: make CTA 0 of the named kernel lose one arrival so that its
+    bounded wait gives up (KDA_TEST_FAULT_*; KDA_TEST_FAULT_NONE turns it off)."""
+    st = load_library().kda_test_set_fault(int(where))
+    if st != KDA_OK:
+        raise KDAError(st, "kda_test_set_fault")
 
 
 def _dtype_code(t: torch.Tensor) -> int:

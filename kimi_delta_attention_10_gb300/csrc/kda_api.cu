@@ -3,6 +3,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "kda.h"
 #include "kda_internal.cuh"
 
@@ -11,9 +13,14 @@ namespace {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool valid_dtype(int32_t d) { return d == KDA_F32 || d == KDA_BF16; }
 
+// kda_test_set_fault's setting, read by every chunk-forward launch.
+std::atomic<int32_t> g_test_fault{KDA_TEST_FAULT_NONE};
+
 }  // namespace
 
 namespace kda {
+
+int32_t test_fault() { return g_test_fault.load(std::memory_order_relaxed); }
 
 int device_sm_count()
 {
@@ -41,6 +48,8 @@ const char* kda_status_string(int32_t s)
         case KDA_ERR_DEVICE_ARG: return "device saw offsets outside [0, T]";
         case KDA_ERR_TOO_LARGE:
             return "problem needs more than the 64 MiB static scratch of kda_chunk_fwd_static";
+        case KDA_ERR_RANGE:
+            return "device stored a non-finite value (an input or an FP16 operand out of range)";
         default: return "unknown status";
     }
 }
@@ -133,6 +142,7 @@ kda::ChunkArgs chunk_args(const void* q, const void* k, const void* v, int32_t q
     a.out = out; a.final_state = final_state; a.status = status_dev;
     a.qkv_bf16 = qkv_dtype == KDA_BF16; a.out_bf16 = out_dtype == KDA_BF16;
     a.initial_state = initial_state;
+    a.fault = kda::test_fault();
     return a;
 }
 
@@ -219,6 +229,14 @@ kda_status kda_chunk_fwd_static(const void* q, const void* k, const void* v, int
     if ((g && !aligned16(g)) || (beta && !aligned16(beta))) return KDA_ERR_ALIGNMENT;
     if (kda::split_workspace_bytes(N, T, H) > kda::kStaticScratchBytes) return KDA_ERR_TOO_LARGE;
     if (N == 0) return KDA_OK;
+    {
+        // the scratch address is the current device's: the stream must be on it
+        int cur = 0, sdev = 0;
+        if (cudaGetDevice(&cur) != cudaSuccess) return KDA_ERR_CUDA;
+        if (cudaStreamGetDevice(reinterpret_cast<cudaStream_t>(stream), &sdev) != cudaSuccess)
+            return KDA_ERR_CUDA;
+        if (sdev != cur) return KDA_ERR_INVALID_ARG;
+    }
     void* scratch = nullptr;
     if (kda::static_scratch(&scratch) != cudaSuccess) return KDA_ERR_CUDA;
     kda::ChunkArgs a = chunk_args(q, k, v, qkv_dtype, cu_seqlens, N, T, H, scale, qk_l2norm, out,
@@ -324,6 +342,14 @@ kda_status kda_chunk_bwd(const void* q, const void* k, const void* v, int32_t qk
     a.workspace = workspace; a.status = status_dev;
     cudaError_t e = kda::launch_chunk_bwd(a, reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+kda_status kda_test_set_fault(int32_t where)
+{
+    if (where < KDA_TEST_FAULT_NONE || where > KDA_TEST_FAULT_SINGLE_PASS)
+        return KDA_ERR_INVALID_ARG;
+    g_test_fault.store(where, std::memory_order_relaxed);
+    return KDA_OK;
 }
 
 }  // extern "C"

@@ -48,7 +48,6 @@ using namespace tc;
 using namespace chunk_ops;
 
 constexpr int DV = kHeadV;
-constexpr uint32_t kWaitIters = 1u << 22;   // polls before a wait gives up
 
 constexpr uint32_t REC_W = 0;
 constexpr uint32_t REC_QP = 16384;
@@ -164,7 +163,7 @@ constexpr uint32_t P_RK = P_RQ + 256;  // 1/|k_t|
 constexpr uint32_t P_DQK = P_RK + 256; // q^_t . k^_t
 constexpr uint32_t P_BETA = P_DQK + 256;
 constexpr uint32_t P_TOT = P_BETA + 256;   // half-chunk decay fp32 [2][128]
-constexpr uint32_t P_BAR = P_TOT + 1024;   // 4 mbarriers + TMEM slot
+constexpr uint32_t P_BAR = P_TOT + 1024;   // 5 mbarriers + TMEM slot
 constexpr uint32_t P_SMEM = P_BAR + 64 + 1024;
 static_assert(P_TF + C * LDA * 4 <= P_XT, "A_kk and T fit below X'^T");
 static_assert(P_PAIR + 49152 <= P_XT, "pair-sum operands fit below X'^T");
@@ -221,8 +220,11 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(ChunkArgs args,
     float* dqk = reinterpret_cast<float*>(sm + P_DQK);
     float* sbeta = reinterpret_cast<float*>(sm + P_BETA);
     float* tot = reinterpret_cast<float*>(sm + P_TOT);
-    uint64_t* bar = reinterpret_cast<uint64_t*>(sm + P_BAR);   // [0..2] pair rounds, [3] W/U
+    // [0..2] pair rounds, [3] W/U, [4] drain after a failure
+    uint64_t* bar = reinterpret_cast<uint64_t*>(sm + P_BAR);
     uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + P_BAR + 48);
+    // test hook: CTA 0 withholds its first MMA group and the commit that signals it
+    const bool withhold = args.fault == KDA_TEST_FAULT_PREP && blockIdx.x == 0;
 
     const TIn* __restrict__ gq = static_cast<const TIn*>(args.q);
     const TIn* __restrict__ gk = static_cast<const TIn*>(args.k);
@@ -293,7 +295,7 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(ChunkArgs args,
         tmem_relinquish();
     }
     if (tid == 0) {
-        for (int b = 0; b < 4; ++b) mbar_init(&bar[b], 1);
+        for (int b = 0; b < 5; ++b) mbar_init(&bar[b], 1);
         fence_mbar_init();
     }
     cp_async_wait_all();
@@ -337,13 +339,12 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(ChunkArgs args,
     // ---- 4: pair sums, three rounds through one operand buffer; the
     // per-channel rows and the zeroing of A_qk's upper part run beside the MMAs
     bool failed = false;
-    int last_bar = -1;
     constexpr uint32_t id_pairs = idesc(kFmtF16, 128, 64, true, true);
     auto issue_round = [&](int rnd) {
         fence_async_smem();
         fence_before_sync();
         __syncthreads();
-        if (tid == 0) {
+        if (tid == 0 && !(withhold && rnd == 0)) {
             fence_after_sync();
 #pragma unroll
             for (int s = 0; s < 8; ++s)
@@ -351,10 +352,9 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(ChunkArgs args,
                         desc_mnmajor64(sb + P_PAIR + 32768, s), id_pairs, s > 0);
             commit(&bar[rnd]);
         }
-        last_bar = rnd;
     };
     auto wait_bar = [&](int b) -> bool {
-        const bool ok = mbar_wait(&bar[b], 0, kWaitIters);
+        const bool ok = mbar_wait(&bar[b], 0);
         return __syncthreads_or(!ok) == 0;
     };
     float vv[32];
@@ -412,7 +412,6 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(ChunkArgs args,
                         id, s > 0);
             commit(&bar[3]);
         }
-        last_bar = 3;
         {
             // A_qk tile to the record while the MMAs run (32 bytes per thread)
             const uint4* src = reinterpret_cast<const uint4*>(sm + P_AQK);
@@ -433,10 +432,11 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(ChunkArgs args,
         }
     } while (false);
 
-    if (failed) {
-        if (tid == 0) report_status(args.status, KDA_ERR_TIMEOUT);
-        // let the MMAs still in flight finish before the TMEM is released
-        for (int b = 0; b <= last_bar; ++b) mbar_wait(&bar[b], 0, kWaitIters);
+    if (failed && tid == 0) {
+        report_status(args.status, KDA_ERR_TIMEOUT);
+        // every MMA this thread issued finishes before the TMEM is released
+        commit(&bar[4]);
+        mbar_wait(&bar[4], 0);
     }
     fence_before_sync();
     __syncthreads();
@@ -562,9 +562,13 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) chunk_scan_kernel(ChunkArgs a
 
     // A bounded wait that also gives up once the other role has.
     auto wait_or_abort = [&](uint64_t* m, uint32_t parity) -> bool {
-        for (uint32_t i = 0; i < kWaitIters; ++i) {
-            if (mbar_try_wait(m, parity)) return true;
-            if ((i & 255u) == 255u && *abort_flag) return false;
+        if (mbar_try_wait(m, parity)) return true;
+        const uint64_t t0 = globaltimer_ns();
+        for (uint32_t i = 0; i < kMaxTimerChecks; ++i) {
+            for (uint32_t j = 0; j < kPollsPerCheck; ++j)
+                if (mbar_try_wait(m, parity)) return true;
+            if (*abort_flag) return false;
+            if (globaltimer_ns() - t0 > kWaitLimitNs) break;
         }
         *abort_flag = 1;
         return false;
@@ -625,15 +629,18 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) chunk_scan_kernel(ChunkArgs a
                 // let the MMAs and copies in flight finish before the CTA leaves
                 if (any_mma) {
                     commit(&bar[6]);
-                    mbar_wait(&bar[6], 0, kWaitIters);
+                    mbar_wait(&bar[6], 0);
                 }
-                for (int cc = c; cc < issued; ++cc) mbar_wait(&bar[cc & 1], (cc >> 1) & 1, kWaitIters);
+                for (int cc = c; cc < issued; ++cc) mbar_wait(&bar[cc & 1], (cc >> 1) & 1);
             }
         }
     } else {
         // out rows of chunk cc = scale O (o: this thread's 32 tokens of its V
         // column, read from TMEM), stored straight from registers: each store
-        // instruction writes 32 consecutive V values of one token.
+        // instruction writes 32 consecutive V values of one token.  `nan_acc`
+        // gathers x * 0 over every stored value: it turns NaN once one of them
+        // is infinite or NaN (an FP16 operand out of range, or a bad input).
+        float nan_acc = 0.f;
         auto store_chunk_out = [&](int cc, const float (&o)[32]) {
             const int tc = bos + cc * C, Lc = min(C, eos - tc);
             const int64_t ostride = (int64_t)H * DV;
@@ -641,10 +648,16 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) chunk_scan_kernel(ChunkArgs a
             const int nrows = min(32, Lc - 32 * half);
 #pragma unroll
             for (int u = 0; u < 32; ++u) {
-                if (u < nrows) store_out(op, args.scale * o[u]);
+                if (u < nrows) {
+                    const float y = args.scale * o[u];
+                    nan_acc = fmaf(y, 0.f, nan_acc);
+                    store_out(op, y);
+                }
                 op += ostride;
             }
         };
+        // test hook: CTA 0 withholds its first delta_ready arrival
+        const bool withhold = args.fault == KDA_TEST_FAULT_SCAN && blockIdx.x == 0;
         bool fail = false;
         for (int c = 0; c < nch; ++c) {
             const uint32_t R = tlane + S_TM_REGION * (c & 1);
@@ -680,7 +693,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) chunk_scan_kernel(ChunkArgs a
             }
             fence_async_smem();
             fence_before_sync();
-            mbar_arrive(&bar[4]);
+            if (!(withhold && c == 0)) mbar_arrive(&bar[4]);
             {
                 const bool ok = wait_or_abort(&bar[3], c & 1);
                 if (named_sync_or(kEpiBar, NT, !ok)) { fail = true; break; }
@@ -728,8 +741,12 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) chunk_scan_kernel(ChunkArgs a
         } else if (state_out != nullptr) {
             float* fs = state_out + ((int64_t)n * H + h) * DK * DV;
 #pragma unroll
-            for (int u = 0; u < 64; ++u) fs[(int64_t)(64 * half + u) * DV + row] = S[u];
+            for (int u = 0; u < 64; ++u) {
+                nan_acc = fmaf(S[u], 0.f, nan_acc);
+                fs[(int64_t)(64 * half + u) * DV + row] = S[u];
+            }
         }
+        if (nan_acc != nan_acc) report_status(args.status, KDA_ERR_RANGE);
     }
     fence_before_sync();
     __syncthreads();

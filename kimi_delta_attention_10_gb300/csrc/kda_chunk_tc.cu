@@ -47,7 +47,6 @@ using namespace tc;
 using namespace chunk_ops;
 
 constexpr int DV = kHeadV;    // 128
-constexpr uint32_t kWaitIters = 1u << 22;   // polls before a wait gives up
 
 // Shared memory map (bytes from a 1024-aligned base).
 constexpr uint32_t OFF_ST = 0;          // S^T fp16 K-major [128 v][128 c]            32 KiB
@@ -71,7 +70,7 @@ constexpr uint32_t OFF_DQK = OFF_RK + 256;            // q^_t . k^_t       fp32 
 constexpr uint32_t OFF_BETA = OFF_DQK + 256;          // beta              fp32 [64]
 constexpr uint32_t OFF_DEC = OFF_BETA + 256;          // e^{G_last}        fp32 [128]
 constexpr uint32_t OFF_TOT = OFF_DEC + 512;           // half-chunk decay  fp32 [2][128]
-constexpr uint32_t OFF_BAR = OFF_TOT + 1024;          // 5 mbarriers + TMEM slot
+constexpr uint32_t OFF_BAR = OFF_TOT + 1024;          // 6 mbarriers + TMEM slot
 constexpr uint32_t SMEM_USED = OFF_BAR + 64;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;     // + alignment slack
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
@@ -109,7 +108,8 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(ChunkArgs args)
     float* sbeta = reinterpret_cast<float*>(sm + OFF_BETA);
     float* dec = reinterpret_cast<float*>(sm + OFF_DEC);
     float* tot = reinterpret_cast<float*>(sm + OFF_TOT);
-    // [0..2] pair-sum rounds, [3] Delta, [4] output/state update
+    // [0..2] pair-sum rounds, [3] Delta, [4] output/state update, [5] drain
+    // after a failure
     uint64_t* bar = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
     uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + OFF_BAR + 56);
 
@@ -168,7 +168,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(ChunkArgs args)
         tmem_relinquish();
     }
     if (tid == 0) {
-        for (int b = 0; b < 5; ++b) mbar_init(&bar[b], 1);
+        for (int b = 0; b < 6; ++b) mbar_init(&bar[b], 1);
         fence_mbar_init();
     }
     fence_async_smem();
@@ -179,8 +179,11 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(ChunkArgs args)
     const uint32_t tlane = tmem + ((uint32_t)(32 * quad) << 16);
 
     bool failed = false;
-    int last_bar = -1;
     uint32_t phase = 0;                                    // every barrier completes once per chunk
+    // test hook: CTA 0 withholds its first MMA group and the commit that signals it
+    const bool withhold = args.fault == KDA_TEST_FAULT_SINGLE_PASS && blockIdx.x == 0;
+    // gathers x * 0 over every stored value: NaN once one is infinite or NaN
+    float nan_acc = 0.f;
 
     // 16-bit inputs: each staging region receives the next chunk by cp.async as
     // soon as its last reader in this chunk is done.  FP32 inputs are converted
@@ -314,7 +317,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(ChunkArgs args)
             fence_async_smem();
             fence_before_sync();
             __syncthreads();
-            if (tid == 0) {
+            if (tid == 0 && !(withhold && rnd == 0)) {
                 fence_after_sync();
 #pragma unroll
                 for (int s = 0; s < 8; ++s)
@@ -324,8 +327,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(ChunkArgs args)
             }
         };
         auto wait_round = [&](int rnd) -> bool {
-            last_bar = rnd;
-            const bool ok = mbar_wait(&bar[rnd], phase, kWaitIters);
+            const bool ok = mbar_wait(&bar[rnd], phase);
             return __syncthreads_or(!ok) == 0;
         };
         level32_operands(sm + OFF_AOP, ch, hh, a, kh, qh);
@@ -411,9 +413,8 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(ChunkArgs args)
                 mma_f16(tmem + TM_XS, desc_kmajor(sb + OFF_SQ, 128, s), desc_kmajor(sb + OFF_TP, 64, s), id, s > 0);
             commit(&bar[3]);
         }
-        last_bar = 3;
         {
-            const bool ok = mbar_wait(&bar[3], phase, kWaitIters);
+            const bool ok = mbar_wait(&bar[3], phase);
             if (__syncthreads_or(!ok)) { failed = true; break; }
         }
         if (more) { async_rows16(OFF_SQ, gq, t0 + C); cp_async_commit(); }
@@ -442,9 +443,8 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(ChunkArgs args)
                 mma_f16(tmem + TM_P, desc_kmajor(sb + OFF_XT, 128, s), desc_kmajor(sb + OFF_KT, 128, s), idp, s > 0);
             commit(&bar[4]);
         }
-        last_bar = 4;
         {
-            const bool ok = mbar_wait(&bar[4], phase, kWaitIters);
+            const bool ok = mbar_wait(&bar[4], phase);
             if (__syncthreads_or(!ok)) { failed = true; break; }
         }
         fence_after_sync();
@@ -457,7 +457,11 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(ChunkArgs args)
             const int nrows = min(32, L - 32 * half);
 #pragma unroll
             for (int u = 0; u < 32; ++u) {
-                if (u < nrows) store_out(op, args.scale * o[u]);
+                if (u < nrows) {
+                    const float y = args.scale * o[u];
+                    nan_acc = fmaf(y, 0.f, nan_acc);
+                    store_out(op, y);
+                }
                 op += ostride;
             }
             float p[32];
@@ -485,15 +489,21 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(ChunkArgs args)
 
     if (kPrefetch) cp_async_wait_all();
     if (failed) {
-        if (tid == 0) report_status(args.status, KDA_ERR_TIMEOUT);
-        // let the MMAs still in flight finish before the TMEM is released
-        for (int b = 0; b <= 4; ++b)
-            if (b <= last_bar) mbar_wait(&bar[b], phase, kWaitIters);
+        if (tid == 0) {
+            report_status(args.status, KDA_ERR_TIMEOUT);
+            // every MMA this thread issued finishes before the TMEM is released
+            commit(&bar[5]);
+            mbar_wait(&bar[5], 0);
+        }
     } else if (args.final_state != nullptr) {
         float* fs = args.final_state + ((int64_t)n * H + h) * DK * DV;
 #pragma unroll
-        for (int u = 0; u < 64; ++u) fs[(int64_t)(64 * half + u) * DV + row] = S[u];
+        for (int u = 0; u < 64; ++u) {
+            nan_acc = fmaf(S[u], 0.f, nan_acc);
+            fs[(int64_t)(64 * half + u) * DV + row] = S[u];
+        }
     }
+    if (nan_acc != nan_acc) report_status(args.status, KDA_ERR_RANGE);
     fence_before_sync();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, TM_COLS);

@@ -42,7 +42,13 @@ struct ChunkArgs {
     // Two-phase tensor-core path: caller-provided scratch of at least
     // split_workspace_bytes(N, T, H) bytes (nullptr: single-pass kernel).
     void* workspace;
+    // Test hook (kda_test_set_fault): a KDA_TEST_FAULT_* value; the named
+    // kernel's CTA 0 withholds one arrival so that its bounded wait gives up.
+    int32_t fault;
 };
+
+// The current test-hook setting (0 unless a test set one).
+int32_t test_fault();
 
 struct StepArgs {
     const void* q;

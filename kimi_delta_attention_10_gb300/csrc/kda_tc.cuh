@@ -1,6 +1,6 @@
 // Blackwell (sm_103a) tensor-core primitives: tcgen05 MMA with operands in
-// shared memory and accumulators in tensor memory (TMEM), mbarrier waits with
-// an iteration bound, and the 128-byte-swizzled shared-memory tile layout the
+// shared memory and accumulators in tensor memory (TMEM), mbarrier waits
+// bounded in time, and the 128-byte-swizzled shared-memory tile layout the
 // MMA descriptors describe.  Inline PTX only.
 #pragma once
 
@@ -148,11 +148,35 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* m, uint32_t parity)
         : "memory");
     return ok != 0;
 }
-// Waits for phase `parity` to complete; gives up after `max_iter` polls.
-__device__ __forceinline__ bool mbar_wait(uint64_t* m, uint32_t parity, uint32_t max_iter)
+// Nanoseconds on the GPU's global timer.
+__device__ __forceinline__ uint64_t globaltimer_ns()
 {
-    for (uint32_t i = 0; i < max_iter; ++i)
-        if (mbar_try_wait(m, parity)) return true;
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// How long a bounded wait polls before it gives up.  Every wait in these
+// kernels is for work of the same CTA (an MMA group, a bulk copy, the other
+// warps of the CTA), which takes microseconds; a second means an arrival was
+// lost, and the kernel then reports KDA_ERR_TIMEOUT and returns.
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
+// Polls between two reads of the timer, and the most reads of it per wait (a
+// second bound on the loop that does not depend on the timer).
+constexpr uint32_t kPollsPerCheck = 64;
+constexpr uint32_t kMaxTimerChecks = 1u << 20;
+
+// Waits for phase `parity` to complete; false after about `limit_ns`.
+__device__ __forceinline__ bool mbar_wait(uint64_t* m, uint32_t parity,
+                                          uint64_t limit_ns = kWaitLimitNs)
+{
+    if (mbar_try_wait(m, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t i = 0; i < kMaxTimerChecks; ++i) {
+        for (uint32_t j = 0; j < kPollsPerCheck; ++j)
+            if (mbar_try_wait(m, parity)) return true;
+        if (globaltimer_ns() - t0 > limit_ns) return false;
+    }
     return false;
 }
 

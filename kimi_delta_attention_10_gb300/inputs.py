@@ -162,3 +162,80 @@ def make_cotangents(T: int, N: int, H: int, K: int, V: int, seed: int,
     dfinal = torch.randn(N, H, K, V, generator=gen, dtype=torch.float32)
     init = torch.randn(N, H, K, V, generator=gen, dtype=torch.float32) * 0.5
     return dout, dfinal, init
+
+
+# Regimes in which the state carried from chunk to chunk dominates the output
+# (the workloads above forget within a few tokens: mean g is about -4 per token).
+STATE_REGIMES = ("alog_0.01", "alog_0.05", "g_slow", "g_zero_beta_small", "g_zero",
+                 "beta_zero", "beta_one_direction", "zero_qk_rows", "initial_state")
+
+
+@dataclass
+class RegimeInputs:
+    """One input set of a state regime.
+
+    ``x`` holds q, k, v and the gate pre-activations.  When ``g`` and ``beta``
+    are given ([T,H,K] and [T,H] FP32), they are the decay and write strength
+    fed to the chunk forward directly, and the pre-activations are unused;
+    otherwise both sides form them from the pre-activations.  ``initial_state``
+    is [N,H,K,V] FP32 or None (zero)."""
+    x: KDAInputs
+    g: Optional[torch.Tensor] = None
+    beta: Optional[torch.Tensor] = None
+    initial_state: Optional[torch.Tensor] = None
+
+
+def state_regime_inputs(regime: str, seqlens: List[int], H: int = 4,
+                        qkv_dtype: torch.dtype = torch.bfloat16, seed: int = 0) -> RegimeInputs:
+    """Seeded draws of one state regime (q, k, v, f, b as in ``make_inputs``,
+    then the regime's own draws from a second generator seeded 1000 + seed):
+
+    alog_0.01, alog_0.05  exp(A_log) = 0.01 or 0.05 for every head: slow decay
+                          through the gate (g about -0.007 or -0.035 per token)
+    g_slow                g ~ U(-0.05, 0) per element, beta ~ U(0, 1)
+    g_zero_beta_small     g = 0, beta = 1e-3 (the linear-attention limit)
+    g_zero                g = 0, beta ~ U(0, 1) (delta rule without decay)
+    beta_zero             g ~ U(-0.05, 0), beta = 0 (nothing is ever written)
+    beta_one_direction    g ~ U(-0.05, 0), beta = 1, every key of a head along
+                          one direction u_h ~ N(0, I) with an N(0, 1) length
+                          (the delta rule overwrites)
+    zero_qk_rows          exp(A_log) = 0.05, q rows t % 7 == 3 and k rows
+                          t % 5 == 1 set to zero
+    initial_state         exp(A_log) = 0.05, initial state ~ N(0, 0.3^2)
+    """
+    K = V = 128
+    x = make_inputs(seqlens, H, K, V, qkv_dtype, seed)
+    gen = torch.Generator().manual_seed(1000 + seed)
+    T, N = x.T, x.N
+    r = RegimeInputs(x=x)
+    slow_g = lambda: -0.05 * torch.rand(T, H, K, generator=gen, dtype=torch.float32)
+    if regime in ("alog_0.01", "alog_0.05"):
+        x.A_log = torch.full((H,), math.log(float(regime.split("_")[1])), dtype=torch.float32)
+    elif regime == "g_slow":
+        r.g = slow_g()
+        r.beta = torch.rand(T, H, generator=gen, dtype=torch.float32)
+    elif regime == "g_zero_beta_small":
+        r.g = torch.zeros(T, H, K)
+        r.beta = torch.full((T, H), 1e-3, dtype=torch.float32)
+    elif regime == "g_zero":
+        r.g = torch.zeros(T, H, K)
+        r.beta = torch.rand(T, H, generator=gen, dtype=torch.float32)
+    elif regime == "beta_zero":
+        r.g = slow_g()
+        r.beta = torch.zeros(T, H)
+    elif regime == "beta_one_direction":
+        r.g = slow_g()
+        r.beta = torch.ones(T, H)
+        u = torch.randn(H, K, generator=gen, dtype=torch.float32)
+        length = torch.randn(T, H, 1, generator=gen, dtype=torch.float32)
+        x.k = (length * u).to(qkv_dtype)
+    elif regime == "zero_qk_rows":
+        x.A_log = torch.full((H,), math.log(0.05), dtype=torch.float32)
+        x.q[3::7] = 0
+        x.k[1::5] = 0
+    elif regime == "initial_state":
+        x.A_log = torch.full((H,), math.log(0.05), dtype=torch.float32)
+        r.initial_state = 0.3 * torch.randn(N, H, K, V, generator=gen, dtype=torch.float32)
+    else:
+        raise KeyError(regime)
+    return r

@@ -37,7 +37,7 @@ def test_library_exports_every_declared_symbol(lib):
 def test_abi_version_and_status_strings(lib):
     assert lib.kda_abi_version() == 3
     assert binding.status_string(0) == "ok"
-    for s in range(1, 8):
+    for s in range(1, 9):
         assert binding.status_string(s) not in ("ok", "unknown status")
     assert binding.status_string(99) == "unknown status"
 
@@ -217,6 +217,20 @@ def static(lib, **kw):
 ])
 def test_chunk_fwd_static_rejects_bad_arguments(lib, kw, expect):
     assert static(lib, **kw) == expect
+
+
+def test_static_scratch_limit_at_64_heads_one_sequence(lib):
+    """H = 64, N = 1: T / 64 + N = 13 fits the 64 MiB scratch (12 full chunks,
+    768 tokens), 14 does not (the bound adds 64 x 64 KiB of state carry)."""
+    assert static(lib, T=64 * 12, N=1, H=64) != binding.KDA_ERR_TOO_LARGE
+    assert static(lib, T=64 * 13, N=1, H=64) == binding.KDA_ERR_TOO_LARGE
+    assert workspace_size(lib, 1, 64 * 12, 64)[1] <= (64 << 20) < workspace_size(lib, 1, 64 * 13, 64)[1]
+
+
+def test_test_fault_hook_rejects_unknown_values(lib):
+    assert lib.kda_test_set_fault(4) == binding.KDA_ERR_INVALID_ARG
+    assert lib.kda_test_set_fault(-1) == binding.KDA_ERR_INVALID_ARG
+    assert lib.kda_test_set_fault(binding.KDA_TEST_FAULT_NONE) == binding.KDA_OK
 
 
 def test_static_scratch_limit_is_the_workspace_bound(lib):
