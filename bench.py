@@ -62,6 +62,9 @@ def parse_args():
                    help="add the output gate with gated RMSNorm (kda_gated_rmsnorm) to the step")
     p.add_argument("--backward", action="store_true",
                    help="also time kda_chunk_bwd (the VJP) on the workload, after the step")
+    p.add_argument("--f-dtype", choices=["auto", "bf16", "f32"], default="auto",
+                   help="dtype of the gate pre-activation f (auto: the workload's activation "
+                        "dtype, i.e. BF16 beside BF16 q/k/v)")
     args = p.parse_args()
     args.fused = not args.unfused
     return args
@@ -153,10 +156,11 @@ class ClockSampler:
                 "reasons": sorted(reasons)}
 
 
-def algorithmic_bytes(T, H, K, V, N, qkv_bytes, out_bytes):
-    """Compulsory HBM bytes of one kda_chunk_fwd launch: read q, k, v, g (FP32),
-    beta (FP32); write out and the FP32 final state."""
-    per_token_head = (2 * K + V) * qkv_bytes + 4 * K + 4 + V * out_bytes
+def algorithmic_bytes(T, H, K, V, N, qkv_bytes, out_bytes, gate_bytes_per_elem=4):
+    """Compulsory HBM bytes of one chunk call: read q, k, v, the decay input
+    (FP32 g for kda_chunk_fwd; f in its dtype for kda_chunk_fwd_gated), the
+    FP32 beta or its FP32 logits; write out and the FP32 final state."""
+    per_token_head = (2 * K + V) * qkv_bytes + gate_bytes_per_elem * K + 4 + V * out_bytes
     return T * H * per_token_head + N * H * K * V * 4
 
 
@@ -177,8 +181,8 @@ def chunk_windows(N, H, chunks, sms):
     return 1
 
 
-def gate_bytes(T, H, K):
-    return T * H * K * (4 + 4) + T * H * (4 + 4)
+def gate_bytes(T, H, K, f_bytes=4):
+    return T * H * K * (f_bytes + 4) + T * H * (4 + 4)
 
 
 def max_over_ranks(x: float, device) -> float:
@@ -298,6 +302,9 @@ def main():
     x = workload_inputs(w)
     T, H, K, V, N = x.T, w.H, w.K, w.V, x.N
     out_dtype = torch.float32 if mode == "fp32_exact" else x.v.dtype
+    f_dtype = {"bf16": torch.bfloat16, "f32": torch.float32}.get(
+        args.f_dtype, torch.bfloat16 if x.v.dtype == torch.bfloat16 else torch.float32)
+    x.f = x.f.to(f_dtype)             # the gate projection's output, in its dtype
     d = {n: getattr(x, n).to(dev) for n in ("q", "k", "v", "f", "A_log", "dt_bias", "b",
                                             "cu_seqlens")}
     cu_host = x.cu_seqlens.tolist()
@@ -479,7 +486,8 @@ def main():
     if rank == 0:
         qkv_bytes = x.q.element_size()
         out_bytes = out.element_size()
-        alg = algorithmic_bytes(T, H, K, V, N, qkv_bytes, out_bytes)
+        alg = algorithmic_bytes(T, H, K, V, N, qkv_bytes, out_bytes,
+                                x.f.element_size() if args.fused else 4)
         avg_chunk_s = statistics.mean(chunk_ms) * 1e-3
         peak, peak_src = measured_peaks()
         achieved = alg / avg_chunk_s / 1e9
@@ -500,6 +508,7 @@ def main():
         cfg["T"], cfg["N"] = T, N
         cfg["step"] = "kda_gate + kda_chunk_fwd" if (not args.fused) else "kda_chunk_fwd_gated"
         cfg["chunk_path"] = variant
+        cfg["f_dtype"] = str(x.f.dtype).replace("torch.", "")
         value = whole_job_rate(world, T, args.steps, ms)
         chunk_tps = T / avg_chunk_s
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
@@ -526,7 +535,8 @@ def main():
             cfg["step"] += " + kda_gated_rmsnorm"
         if (not args.fused):
             line["kernels"]["kda_gate_ms"] = statistics.mean(gate_ms)
-            line["kernels"]["kda_gate_GBps"] = gate_bytes(T, H, K) / statistics.mean(gate_ms) / 1e6
+            line["kernels"]["kda_gate_GBps"] = (gate_bytes(T, H, K, x.f.element_size()) /
+                                                statistics.mean(gate_ms) / 1e6)
         if bwd is not None:
             peak_b, _ = measured_peaks()
             bwd["frac_of_hbm_peak"] = bwd["achieved_GBps"] / peak_b

@@ -191,9 +191,12 @@ kda_status kda_chunk_fwd(const void* q, const void* k, const void* v, int32_t qk
  * choice), without writing g or beta
  * to memory.  The pages compute the gate outside the chunk kernel ("GLM-5.3-
  * Flash F6.2: KDA correctness and FLA sequence parallelism", fused-gate
- * commit); fusing it here removes that launch and its round trip of g.
+ * commit, with FP32 A_log/dt_bias); fusing it here removes that launch and
+ * its round trip of g, and with f in BF16 (the activation dtype of the gate
+ * projection that produces it) the call reads 256 bytes of f per token and
+ * head instead of the 512 bytes of an FP32 g.
  *
- *   f       [T, H, K]  F32 (KDA_ERR_UNSUPPORTED otherwise)
+ *   f       [T, H, K]  F32 or BF16 (f_dtype)
  *   A_log   [H] F32, dt_bias [H, K] F32
  *   b       [T, H]     F32 or BF16 (b_dtype)
  * Every other argument as kda_chunk_fwd.

@@ -114,7 +114,7 @@ def status_string(status: int) -> str:
     return load_library().kda_status_string(int(status)).decode()
 
 
-def test_set_fault(where: int) -> None:
+def set_test_fault(where: int) -> None:
     """Test hook: make CTA 0 of the named kernel lose one arrival so that its
     bounded wait gives up (KDA_TEST_FAULT_*; KDA_TEST_FAULT_NONE turns it off)."""
     st = load_library().kda_test_set_fault(int(where))

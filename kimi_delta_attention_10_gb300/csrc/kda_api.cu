@@ -196,7 +196,6 @@ kda_status kda_chunk_fwd_gated(const void* q, const void* k, const void* v, int3
                                 status_dev);
     if (st != KDA_OK) return st;
     if (!valid_dtype(f_dtype) || !valid_dtype(b_dtype)) return KDA_ERR_INVALID_ARG;
-    if (f_dtype != KDA_F32) return KDA_ERR_UNSUPPORTED;
     if (!A_log || !dt_bias) return KDA_ERR_INVALID_ARG;
     if (T > 0 && (!f || !b)) return KDA_ERR_INVALID_ARG;
     const void* ptrs[] = {f, A_log, dt_bias, b};
@@ -205,7 +204,8 @@ kda_status kda_chunk_fwd_gated(const void* q, const void* k, const void* v, int3
     kda::ChunkArgs a = chunk_args(q, k, v, qkv_dtype, cu_seqlens, N, T, H, scale, qk_l2norm, out,
                                   out_dtype, initial_state, final_state, status_dev);
     a.gated = true;
-    a.f = static_cast<const float*>(f);
+    a.f = f;
+    a.f_bf16 = f_dtype == KDA_BF16;
     a.A_log = A_log;
     a.dt_bias = dt_bias;
     a.b = b;

@@ -71,7 +71,7 @@ __device__ __forceinline__ float warp_sum(float x)
 __device__ __forceinline__ void store_out(float* p, float x) { *p = x; }
 __device__ __forceinline__ void store_out(__nv_bfloat16* p, float x) { *p = __float2bfloat16_rn(x); }
 
-template <typename TIn, typename TOut, bool kGated>
+template <typename TIn, typename TOut, int kGate>
 __global__ void __launch_bounds__(NT, 1) chunk_fp32_kernel(ChunkArgs args)
 {
     extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -103,7 +103,10 @@ __global__ void __launch_bounds__(NT, 1) chunk_fp32_kernel(ChunkArgs args)
     } else {
         for (int i = tid; i < DK * BV; i += NT) sm.s[i / BV][i % BV] = 0.f;
     }
-    const float* __restrict__ graw = kGated ? args.f : g;
+    constexpr bool kGated = kGate != kGateG;
+    using TG = typename GateSrc<kGate>::T;                 // element of g or f
+    const TG* __restrict__ graw =
+        kGated ? static_cast<const TG*>(args.f) : reinterpret_cast<const TG*>(g);
     const float lamneg = kGated ? -expf(args.A_log[h]) : 0.f;
 
     for (int t0 = bos; t0 < eos; t0 += C) {
@@ -118,8 +121,8 @@ __global__ void __launch_bounds__(NT, 1) chunk_fp32_kernel(ChunkArgs args)
                 const int64_t off = ((int64_t)(t0 + r) * H + h) * DK + c;
                 qv = load_as_float(q + off);
                 kv = load_as_float(k + off);
-                av = expf(kGated ? gate_decay(graw[off], args.dt_bias[(int64_t)h * DK + c], lamneg)
-                                 : graw[off]);
+                const float gin = load_as_float(graw + off);
+                av = expf(kGated ? gate_decay(gin, args.dt_bias[(int64_t)h * DK + c], lamneg) : gin);
             }
             sm.q[r][c] = qv;
             sm.k[r][c] = kv;
@@ -315,34 +318,38 @@ __global__ void __launch_bounds__(NT, 1) chunk_fp32_kernel(ChunkArgs args)
     }
 }
 
-template <typename TIn, typename TOut, bool kGated>
+template <typename TIn, typename TOut, int kGate>
 cudaError_t launch_typed(const ChunkArgs& a, cudaStream_t stream)
 {
     const size_t smem = sizeof(Smem);
-    cudaError_t e = cudaFuncSetAttribute(chunk_fp32_kernel<TIn, TOut, kGated>,
+    cudaError_t e = cudaFuncSetAttribute(chunk_fp32_kernel<TIn, TOut, kGate>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const int64_t units = (int64_t)a.N * a.H * NVS;
     if (units > INT32_MAX) return cudaErrorInvalidConfiguration;
-    chunk_fp32_kernel<TIn, TOut, kGated><<<(unsigned)units, NT, smem, stream>>>(a);
+    chunk_fp32_kernel<TIn, TOut, kGate><<<(unsigned)units, NT, smem, stream>>>(a);
     return cudaGetLastError();
 }
 
-template <bool kGated>
+template <int kGate>
 cudaError_t launch_gated(const ChunkArgs& a, cudaStream_t stream)
 {
     if (a.qkv_bf16)
-        return a.out_bf16 ? launch_typed<__nv_bfloat16, __nv_bfloat16, kGated>(a, stream)
-                          : launch_typed<__nv_bfloat16, float, kGated>(a, stream);
-    return a.out_bf16 ? launch_typed<float, __nv_bfloat16, kGated>(a, stream)
-                      : launch_typed<float, float, kGated>(a, stream);
+        return a.out_bf16 ? launch_typed<__nv_bfloat16, __nv_bfloat16, kGate>(a, stream)
+                          : launch_typed<__nv_bfloat16, float, kGate>(a, stream);
+    return a.out_bf16 ? launch_typed<float, __nv_bfloat16, kGate>(a, stream)
+                      : launch_typed<float, float, kGate>(a, stream);
 }
 
 }  // namespace
 
 cudaError_t launch_chunk_fp32(const ChunkArgs& a, cudaStream_t stream)
 {
-    return a.gated ? launch_gated<true>(a, stream) : launch_gated<false>(a, stream);
+    switch (gate_in(a)) {
+        case kGateF32: return launch_gated<kGateF32>(a, stream);
+        case kGateBF16: return launch_gated<kGateBF16>(a, stream);
+        default: return launch_gated<kGateG>(a, stream);
+    }
 }
 
 }  // namespace kda

@@ -170,7 +170,7 @@ static_assert(P_PAIR + 49152 <= P_XT, "pair-sum operands fit below X'^T");
 static_assert(2 * (P_SMEM + 1024) <= 233472, "two preparation CTAs per SM");
 constexpr uint32_t P_TM_A = 0, P_TM_W = 0, P_TM_U = 64, P_TM_COLS = 256;
 
-template <typename TIn, bool kGated>
+template <typename TIn, int kGate>
 __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(ChunkArgs args,
                                                            const int32_t* __restrict__ hdr,
                                                            unsigned char* __restrict__ records,
@@ -214,7 +214,9 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(ChunkArgs args,
     const uint16_t* sq = reinterpret_cast<const uint16_t*>(sm + P_SQ);
     const uint16_t* sk = reinterpret_cast<const uint16_t*>(sm + P_SK);
     const uint16_t* sv = reinterpret_cast<const uint16_t*>(sm + P_SV);
-    const float* sg = reinterpret_cast<const float*>(sm + P_SG);
+    constexpr bool kGated = kGate != kGateG;
+    using TG = typename GateSrc<kGate>::T;                 // element of g or f
+    const TG* sg = reinterpret_cast<const TG*>(sm + P_SG);
     float* rq = reinterpret_cast<float*>(sm + P_RQ);
     float* rk = reinterpret_cast<float*>(sm + P_RK);
     float* dqk = reinterpret_cast<float*>(sm + P_DQK);
@@ -229,7 +231,8 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(ChunkArgs args,
     const TIn* __restrict__ gq = static_cast<const TIn*>(args.q);
     const TIn* __restrict__ gk = static_cast<const TIn*>(args.k);
     const TIn* __restrict__ gv = static_cast<const TIn*>(args.v);
-    const float* __restrict__ graw = kGated ? args.f : args.g;
+    const TG* __restrict__ graw =
+        kGated ? static_cast<const TG*>(args.f) : reinterpret_cast<const TG*>(args.g);
     using ST = Stage<TIn>;
 
     // ---- 1: the chunk in staging (rows >= L zero, decay 1)
@@ -264,11 +267,13 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(ChunkArgs args,
         rows_via_regs(gk, P_SK);
         rows_via_regs(gv, P_SV);
     }
+    constexpr int GP = DK * (int)sizeof(TG) / 16;           // 16-byte pieces per g/f row
 #pragma unroll
-    for (int u = 0; u < C * 32 / NT; ++u) {
-        const int e = tid + u * NT, r = e >> 5, pc = e & 31;
+    for (int u = 0; u < C * GP / NT; ++u) {
+        const int e = tid + u * NT, r = e / GP, pc = e % GP;
         const bool ok = r < L;
-        cp_async16(sm + P_SG + e * 16, graw + ((int64_t)(t0 + (ok ? r : 0)) * H + h) * DK + pc * 4,
+        cp_async16(sm + P_SG + e * 16,
+                   graw + ((int64_t)(t0 + (ok ? r : 0)) * H + h) * DK + pc * (16 / (int)sizeof(TG)),
                    ok);
     }
     cp_async_commit();
@@ -323,7 +328,7 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(ChunkArgs args,
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const int u = 4 * u4 + e, t = 32 * hh + u;
-                const float gv_ = sg[t * DK + ch];
+                const float gv_ = load_as_float(sg + t * DK + ch);
                 a[u] = __expf(kGated ? (t < L ? gate_decay(gv_, dtb, lamneg) : 0.f) : gv_);
                 kh[u] = ST::to_f32(sk[t * DK + ch]) * nkv[e];
                 qh[u] = ST::to_f32(sq[t * DK + ch]) * nqv[e];
@@ -562,7 +567,8 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) chunk_scan_kernel(ChunkArgs a
 
     // A bounded wait that also gives up once the other role has.
     auto wait_or_abort = [&](uint64_t* m, uint32_t parity) -> bool {
-        if (mbar_try_wait(m, parity)) return true;
+        for (uint32_t j = 0; j < kPollsPerCheck; ++j)
+            if (mbar_try_wait(m, parity)) return true;
         const uint64_t t0 = globaltimer_ns();
         for (uint32_t i = 0; i < kMaxTimerChecks; ++i) {
             for (uint32_t j = 0; j < kPollsPerCheck; ++j)
@@ -754,12 +760,12 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) chunk_scan_kernel(ChunkArgs a
 }
 
 // ---------------------------------------------------------------- launch
-template <typename TIn, bool kGated>
+template <typename TIn, int kGate>
 cudaError_t launch_prep_typed(const ChunkArgs& a, const int32_t* hdr, unsigned char* rec,
                               int64_t unit_base, int64_t units, bool beside_scan,
                               cudaStream_t stream)
 {
-    auto kern = chunk_prep_kernel<TIn, kGated>;
+    auto kern = chunk_prep_kernel<TIn, kGate>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)P_SMEM);
     if (e != cudaSuccess) return e;
@@ -782,13 +788,16 @@ cudaError_t launch_prep(const ChunkArgs& a, const int32_t* hdr, unsigned char* r
                         int64_t unit_base, int64_t units, bool beside_scan, cudaStream_t stream)
 {
     if (units <= 0) return cudaSuccess;
-    if (a.gated)
-        return a.qkv_bf16
-                   ? launch_prep_typed<__nv_bfloat16, true>(a, hdr, rec, unit_base, units, beside_scan, stream)
-                   : launch_prep_typed<float, true>(a, hdr, rec, unit_base, units, beside_scan, stream);
-    return a.qkv_bf16
-               ? launch_prep_typed<__nv_bfloat16, false>(a, hdr, rec, unit_base, units, beside_scan, stream)
-               : launch_prep_typed<float, false>(a, hdr, rec, unit_base, units, beside_scan, stream);
+#define KDA_PREP(TIN, GATE) launch_prep_typed<TIN, GATE>(a, hdr, rec, unit_base, units, beside_scan, stream)
+    switch (gate_in(a)) {
+        case kGateF32:
+            return a.qkv_bf16 ? KDA_PREP(__nv_bfloat16, kGateF32) : KDA_PREP(float, kGateF32);
+        case kGateBF16:
+            return a.qkv_bf16 ? KDA_PREP(__nv_bfloat16, kGateBF16) : KDA_PREP(float, kGateBF16);
+        default:
+            return a.qkv_bf16 ? KDA_PREP(__nv_bfloat16, kGateG) : KDA_PREP(float, kGateG);
+    }
+#undef KDA_PREP
 }
 
 cudaError_t launch_scan(const ChunkArgs& a, const int32_t* hdr, const unsigned char* rec,

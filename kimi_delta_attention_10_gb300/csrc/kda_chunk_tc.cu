@@ -87,7 +87,7 @@ constexpr uint32_t TM_COLS = 512;
 __device__ __forceinline__ void store_out(float* p, float x) { *p = x; }
 __device__ __forceinline__ void store_out(__nv_bfloat16* p, float x) { *p = __float2bfloat16_rn(x); }
 
-template <typename TIn, typename TOut, bool kGated>
+template <typename TIn, typename TOut, int kGate>
 __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(ChunkArgs args)
 {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -101,7 +101,10 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(ChunkArgs args)
     const uint16_t* sk = reinterpret_cast<const uint16_t*>(sm + OFF_SK);
     const uint16_t* sq = reinterpret_cast<const uint16_t*>(sm + OFF_SQ);
     const uint16_t* sv = reinterpret_cast<const uint16_t*>(sm + OFF_SV);
-    const float* sg = reinterpret_cast<const float*>(sm + OFF_SG);
+    constexpr bool kGated = kGate != kGateG;
+    using TG = typename GateSrc<kGate>::T;                 // element of g or f
+    constexpr int GP = DK * (int)sizeof(TG) / 16;           // 16-byte pieces per g/f row
+    const TG* sg = reinterpret_cast<const TG*>(sm + OFF_SG);
     float* rq = reinterpret_cast<float*>(sm + OFF_RQ);
     float* rk = reinterpret_cast<float*>(sm + OFF_RK);
     float* dqk = reinterpret_cast<float*>(sm + OFF_DQK);
@@ -137,7 +140,8 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(ChunkArgs args)
     constexpr bool kPrefetch = sizeof(TIn) == 2;
 
     // fused gate: g and beta formed from f, A_log, dt_bias and b (as kda_gate does)
-    const float* __restrict__ graw = kGated ? args.f : args.g;
+    const TG* __restrict__ graw =
+        kGated ? static_cast<const TG*>(args.f) : reinterpret_cast<const TG*>(args.g);
     float lamneg = 0.f, dtb = 0.f;
     if (kGated) {
         lamneg = -expf(args.A_log[h]);
@@ -201,10 +205,10 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(ChunkArgs args)
     auto async_g = [&](int tc) {
         const int Lc = min(C, eos - tc);
 #pragma unroll
-        for (int u = 0; u < C * 32 / NT; ++u) {
-            const int e = tid + u * NT, r = e >> 5, pc = e & 31;
+        for (int u = 0; u < C * GP / NT; ++u) {
+            const int e = tid + u * NT, r = e / GP, pc = e % GP;
             const bool ok = r < Lc;
-            const float* src = graw + ((int64_t)(tc + (ok ? r : 0)) * H + h) * DK + pc * 4;
+            const TG* src = graw + ((int64_t)(tc + (ok ? r : 0)) * H + h) * DK + pc * (16 / (int)sizeof(TG));
             cp_async16(sm + OFF_SG + e * 16, src, ok);
         }
     };
@@ -255,17 +259,17 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(ChunkArgs args)
             rows_via_regs(gq, OFF_SQ);
             rows_via_regs(gk, OFF_SK);
             rows_via_regs(gv, OFF_SV);
-            uint4 xg[8];
+            uint4 xg[C * GP / NT];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int e = tid + u * NT, r = e / 32, pc = e % 32;
+            for (int u = 0; u < C * GP / NT; ++u) {
+                const int e = tid + u * NT, r = e / GP, pc = e % GP;
                 xg[u] = (r < L) ? __ldg(reinterpret_cast<const uint4*>(
                                       graw + ((int64_t)(t0 + r) * H + h) * DK) + pc)
                                 : make_uint4(0, 0, 0, 0);
             }
             load_beta(t0);
 #pragma unroll
-            for (int u = 0; u < 8; ++u) reinterpret_cast<uint4*>(sm + OFF_SG)[tid + u * NT] = xg[u];
+            for (int u = 0; u < C * GP / NT; ++u) reinterpret_cast<uint4*>(sm + OFF_SG)[tid + u * NT] = xg[u];
         }
         if (tid < C) sbeta[tid] = xb;
         __syncthreads();
@@ -289,7 +293,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(ChunkArgs args)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const int u = 4 * u4 + e, t = 32 * hh + u;
-                    const float gv = sg[t * DK + ch];
+                    const float gv = load_as_float(sg + t * DK + ch);
                     // rows past the sequence end hold 0: decay 1 in both forms
                     a[u] = __expf(kGated ? (t < L ? gate_decay(gv, dtb, lamneg) : 0.f) : gv);
                     kh[u] = ST::to_f32(sk[t * DK + ch]) * nkv[e];
@@ -509,34 +513,38 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(ChunkArgs args)
     if (warp == 0) tmem_dealloc(tmem, TM_COLS);
 }
 
-template <typename TIn, typename TOut, bool kGated>
+template <typename TIn, typename TOut, int kGate>
 cudaError_t launch_typed(const ChunkArgs& a, cudaStream_t stream)
 {
-    cudaError_t e = cudaFuncSetAttribute(chunk_tc_kernel<TIn, TOut, kGated>,
+    cudaError_t e = cudaFuncSetAttribute(chunk_tc_kernel<TIn, TOut, kGate>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;
     const int64_t units = (int64_t)a.N * a.H;
     if (units > INT32_MAX) return cudaErrorInvalidConfiguration;
-    chunk_tc_kernel<TIn, TOut, kGated><<<(unsigned)units, NT, SMEM_BYTES, stream>>>(a);
+    chunk_tc_kernel<TIn, TOut, kGate><<<(unsigned)units, NT, SMEM_BYTES, stream>>>(a);
     return cudaGetLastError();
 }
 
-template <bool kGated>
+template <int kGate>
 cudaError_t launch_gated(const ChunkArgs& a, cudaStream_t stream)
 {
     if (a.qkv_bf16)
-        return a.out_bf16 ? launch_typed<__nv_bfloat16, __nv_bfloat16, kGated>(a, stream)
-                          : launch_typed<__nv_bfloat16, float, kGated>(a, stream);
-    return a.out_bf16 ? launch_typed<float, __nv_bfloat16, kGated>(a, stream)
-                      : launch_typed<float, float, kGated>(a, stream);
+        return a.out_bf16 ? launch_typed<__nv_bfloat16, __nv_bfloat16, kGate>(a, stream)
+                          : launch_typed<__nv_bfloat16, float, kGate>(a, stream);
+    return a.out_bf16 ? launch_typed<float, __nv_bfloat16, kGate>(a, stream)
+                      : launch_typed<float, float, kGate>(a, stream);
 }
 
 }  // namespace
 
 cudaError_t launch_chunk_tc(const ChunkArgs& a, cudaStream_t stream)
 {
-    return a.gated ? launch_gated<true>(a, stream) : launch_gated<false>(a, stream);
+    switch (gate_in(a)) {
+        case kGateF32: return launch_gated<kGateF32>(a, stream);
+        case kGateBF16: return launch_gated<kGateBF16>(a, stream);
+        default: return launch_gated<kGateG>(a, stream);
+    }
 }
 
 }  // namespace kda

@@ -34,7 +34,8 @@ struct ChunkArgs {
     // Gate fused into the prologue (kda_chunk_fwd_gated): g and beta are then
     // formed from f, A_log, dt_bias and b, and the g/beta pointers are unused.
     bool gated;
-    const float* f;
+    const void* f;                // [T,H,K] F32 or BF16 (f_bf16)
+    bool f_bf16;
     const float* A_log;
     const float* dt_bias;
     const void* b;
@@ -49,6 +50,15 @@ struct ChunkArgs {
 
 // The current test-hook setting (0 unless a test set one).
 int32_t test_fault();
+
+// Where a chunk kernel's decay comes from: g given (kda_chunk_fwd), or formed
+// from the gate's pre-activation f read as F32 or as BF16 (kda_chunk_fwd_gated).
+enum GateIn : int { kGateG = 0, kGateF32 = 1, kGateBF16 = 2 };
+template <int kGate> struct GateSrc { using T = float; };
+template <> struct GateSrc<kGateBF16> { using T = __nv_bfloat16; };
+
+// The decay input of a launch: the pointer and the GateIn value it needs.
+inline int gate_in(const ChunkArgs& a) { return !a.gated ? kGateG : a.f_bf16 ? kGateBF16 : kGateF32; }
 
 struct StepArgs {
     const void* q;

@@ -166,11 +166,14 @@ constexpr uint64_t kWaitLimitNs = 1000000000ull;
 constexpr uint32_t kPollsPerCheck = 64;
 constexpr uint32_t kMaxTimerChecks = 1u << 20;
 
-// Waits for phase `parity` to complete; false after about `limit_ns`.
+// Waits for phase `parity` to complete; false after about `limit_ns`.  The
+// first batch of polls reads no timer: ordinary waits end there, and the
+// timer read stays off the kernels' critical paths.
 __device__ __forceinline__ bool mbar_wait(uint64_t* m, uint32_t parity,
                                           uint64_t limit_ns = kWaitLimitNs)
 {
-    if (mbar_try_wait(m, parity)) return true;
+    for (uint32_t j = 0; j < kPollsPerCheck; ++j)
+        if (mbar_try_wait(m, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t i = 0; i < kMaxTimerChecks; ++i) {
         for (uint32_t j = 0; j < kPollsPerCheck; ++j)

@@ -164,8 +164,8 @@ def gated(lib, **kw):
 
 
 @pytest.mark.parametrize("kw,expect", [
-    (dict(fdt=1), binding.KDA_ERR_UNSUPPORTED),        # BF16 f is not supported
     (dict(fdt=4), binding.KDA_ERR_INVALID_ARG),
+    (dict(fdt=1, f=MIS), binding.KDA_ERR_ALIGNMENT),   # BF16 f accepted, checked like F32
     (dict(bdt=4), binding.KDA_ERR_INVALID_ARG),
     (dict(A=None), binding.KDA_ERR_INVALID_ARG),
     (dict(f=None), binding.KDA_ERR_INVALID_ARG),

@@ -48,6 +48,39 @@ def test_gated_matches_oracle(mode):
     assert rel_l2(S.cpu().double().numpy(), S_ref) <= tol(mode)
 
 
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("lens", [[1, 64, 0, 130], [8192]])
+def test_gated_bf16_f_equals_gate_then_chunk_bitwise(lens, mode):
+    """f in BF16 (the gate projection's activation dtype): the fused call reads
+    it as the gate does, so the bits equal kda_gate on the same BF16 f followed
+    by kda_chunk_fwd; 8192 tokens run the two-phase path in four windows."""
+    x = _small(lens, H=2, seed=23)
+    x.f = x.f.to(torch.bfloat16)
+    d = device_inputs(x)
+    g, beta = kda_gate(d["f"], d["A_log"], d["dt_bias"], d["b"])
+    o1, s1 = kda_chunk_fwd(d["q"], d["k"], d["v"], g, beta, d["cu_seqlens"], x.scale,
+                           out_dtype=OUT_DTYPE[mode], **path_kw(mode))
+    o2, s2 = kda_chunk_fwd_gated(d["q"], d["k"], d["v"], d["f"], d["A_log"], d["dt_bias"],
+                                 d["b"], d["cu_seqlens"], x.scale, out_dtype=OUT_DTYPE[mode],
+                                 **path_kw(mode))
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(s1, s2)
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_gated_bf16_f_matches_oracle(mode):
+    """BF16 f against the FP64 oracle fed the same BF16 values, upcast."""
+    x = workload_inputs("single_2048_bf16")
+    x.f = x.f.to(torch.bfloat16)
+    d = device_inputs(x)
+    out, S = kda_chunk_fwd_gated(d["q"], d["k"], d["v"], d["f"], d["A_log"], d["dt_bias"],
+                                 d["b"], d["cu_seqlens"], x.scale, out_dtype=OUT_DTYPE[mode],
+                                 cu_seqlens_host=x.cu_seqlens.tolist(), **path_kw(mode))
+    o_ref, S_ref, _, _ = oracle_pipeline(x)
+    assert rel_l2(out.cpu().double().numpy(), o_ref) <= tol(mode)
+    assert rel_l2(S.cpu().double().numpy(), S_ref) <= tol(mode)
+
+
 def test_gated_bf16_beta_logits():
     x = _small([70, 33], seed=22)
     x.b = x.b.to(torch.bfloat16)

@@ -14,7 +14,7 @@ import torch
 from kimi_delta_attention_10_gb300 import kda_chunk_fwd, kda_gate
 from kimi_delta_attention_10_gb300.binding import (KDA_ERR_TIMEOUT, KDA_TEST_FAULT_NONE,
                                                    KDA_TEST_FAULT_PREP, KDA_TEST_FAULT_SCAN,
-                                                   KDA_TEST_FAULT_SINGLE_PASS, test_set_fault)
+                                                   KDA_TEST_FAULT_SINGLE_PASS, set_test_fault)
 from kimi_delta_attention_10_gb300.inputs import make_inputs
 
 from gpu_util import device_inputs
@@ -40,11 +40,11 @@ def test_lost_arrival_times_out_and_the_next_call_is_clean(where, workspace):
     g, beta = kda_gate(d["f"], d["A_log"], d["dt_bias"], d["b"])
     o_ref, S_ref, st = _call(d, g, beta, x, workspace)
     assert st == 0
-    test_set_fault(where)
+    set_test_fault(where)
     try:
         _, _, st_fault = _call(d, g, beta, x, workspace)
     finally:
-        test_set_fault(KDA_TEST_FAULT_NONE)
+        set_test_fault(KDA_TEST_FAULT_NONE)
     assert st_fault == KDA_ERR_TIMEOUT
     o2, S2, st2 = _call(d, g, beta, x, workspace)
     assert st2 == 0
