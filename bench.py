@@ -62,6 +62,9 @@ def parse_args():
                    help="add the output gate with gated RMSNorm (kda_gated_rmsnorm) to the step")
     p.add_argument("--backward", action="store_true",
                    help="also time kda_chunk_bwd (the VJP) on the workload, after the step")
+    p.add_argument("--all-workloads", action="store_true",
+                   help="one line per workload: the step captured in a CUDA graph, 50 timed "
+                        "replays after 10 warm-ups (p50 and max), beside the oracle")
     p.add_argument("--f-dtype", choices=["auto", "bf16", "f32"], default="auto",
                    help="dtype of the gate pre-activation f (auto: the workload's activation "
                         "dtype, i.e. BF16 beside BF16 q/k/v)")
@@ -272,10 +275,101 @@ def cpu_baseline(x, w, budget_heads=8):
                       f"all {x.T} tokens ({dt:.2f} s wall); value scaled to whole tokens"}
 
 
+def run_all_workloads(args):
+    """Every workload: the default step (kda_chunk_fwd_gated, two-phase with a
+    preallocated workspace, f in the activation dtype) captured in a CUDA graph
+    and replayed, 10 warm-ups then 50 replays each timed with CUDA events, the
+    method the pages time the chunk forward with ("Add opt-in FP32 KDA chunk
+    computation", section Validation); the FP64 oracle is timed beside it on a
+    bounded sample of the same workload."""
+    import numpy as np
+    import torch
+    import oracle
+    import __graft_entry__
+    __graft_entry__.build()
+    from kimi_delta_attention_10_gb300 import chunk_workspace_size, kda_chunk_fwd_gated
+    from kimi_delta_attention_10_gb300.inputs import WORKLOADS, workload_inputs
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    peak, peak_src = measured_peaks()
+    mode = args.mode or "bf16_tc"
+    for w in WORKLOADS:
+        x = workload_inputs(w)
+        T, H, K, V, N = x.T, w.H, w.K, w.V, x.N
+        x.f = x.f.to(x.v.dtype)
+        d = {n: getattr(x, n).to(dev) for n in ("q", "k", "v", "f", "A_log", "dt_bias", "b",
+                                                "cu_seqlens")}
+        out_dtype = torch.float32 if mode == "fp32_exact" else x.v.dtype
+        out = torch.empty(T, H, V, dtype=out_dtype, device=dev)
+        fs = torch.empty(N, H, K, V, device=dev)
+        ws = (torch.empty(chunk_workspace_size(N, T, H, K, V), dtype=torch.uint8, device=dev)
+              if mode == "bf16_tc" else None)
+        cu_host = x.cu_seqlens.tolist()
+
+        def call():
+            kda_chunk_fwd_gated(d["q"], d["k"], d["v"], d["f"], d["A_log"], d["dt_bias"], d["b"],
+                                d["cu_seqlens"], x.scale, mode=mode, out=out, final_state=fs,
+                                cu_seqlens_host=cu_host, workspace=ws)
+
+        s = torch.cuda.Stream(dev)
+        s.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(s):
+            call()                                   # eager once (set-up outside capture)
+        torch.cuda.synchronize(dev)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=s):
+            call()
+        for _ in range(10):
+            graph.replay()
+        torch.cuda.synchronize(dev)
+        times = []
+        for _ in range(50):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+            graph.replay()
+            e1.record()
+            e1.synchronize()
+            times.append(e0.elapsed_time(e1))
+        p50, mx = statistics.median(times), max(times)
+        alg = algorithmic_bytes(T, H, K, V, N, x.q.element_size(), out.element_size(),
+                                x.f.element_size())
+        # the oracle on a bounded sample: whole sequences of the first heads
+        hs = list(range(min(H, max(1, (1 << 17) // max(T, 1)))))
+        f64 = lambda t: t.float().numpy().astype(np.float64)
+        t0 = time.perf_counter()
+        oracle.reference(f64(x.q[:, hs]), f64(x.k[:, hs]), f64(x.v[:, hs]), f64(x.f[:, hs]),
+                         f64(x.A_log[hs]), f64(x.dt_bias[hs]), f64(x.b[:, hs]),
+                         x.cu_seqlens.numpy(), x.scale)
+        ot = time.perf_counter() - t0
+        cfg = workload_config(w, mode)
+        cfg["T"], cfg["N"], cfg["f_dtype"] = T, N, str(x.f.dtype).replace("torch.", "")
+        cfg["l2"] = ("inputs larger than L2" if alg > 129e6 else
+                     "inputs fit in L2 (replays run warm, as the pages' timings do)")
+        line = {"metric": METRIC, "workload": w.name, "timing": "CUDA graph replay, 50 samples "
+                "after 10 warm-ups, CUDA events", "p50_ms": p50, "max_ms": mx,
+                "tokens_per_s": T / (p50 * 1e-3), "unit": UNIT,
+                "roofline": {"bound": "hbm", "algorithmic_bytes": alg,
+                             "achieved": alg / (p50 * 1e-3) / 1e9, "peak": peak, "unit": "GB/s",
+                             "frac": alg / (p50 * 1e-3) / 1e9 / peak,
+                             "peak_source": f"{peak_src} hbm_gbs"},
+                "oracle": {"tokens_per_s": T * len(hs) / H / ot, "seconds": ot,
+                           "cores": oracle.default_threads(),
+                           "sample": f"heads 0-{len(hs) - 1} of {H}, all {T} tokens"},
+                "config": cfg}
+        print(json.dumps(line), flush=True)
+        del graph, ws, out, fs, d
+        torch.cuda.empty_cache()
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
         run_reference(args)
+        return
+    if args.all_workloads:
+        run_all_workloads(args)
         return
 
     import torch
