@@ -186,10 +186,14 @@ kda_status kda_chunk_fwd(const void* q, const void* k, const void* v, int32_t qk
  *
  * Takes the gate's inputs instead of g and beta and forms, per element,
  *   g = -exp(A_log[h]) * softplus(f + dt_bias[h,c]),  beta = sigmoid(b)
- * exactly as kda_gate does (same FP32 arithmetic, so the result equals
- * kda_gate followed by kda_chunk_fwd bit for bit, given the same workspace
- * choice), without writing g or beta
- * to memory.  The pages compute the gate outside the chunk kernel ("GLM-5.3-
+ * without writing g or beta to memory.  KDA_MODE_FP32_EXACT uses kda_gate's
+ * FP32 arithmetic, so its result equals kda_gate followed by kda_chunk_fwd
+ * bit for bit.  KDA_MODE_BF16_TC needs only e^g, which it forms directly as
+ * (1 + e^(f + dt_bias))^(-exp(A_log)) with the hardware exp2/log2
+ * approximations (relative error below 1e-5, against the 2^-11 rounding of
+ * its FP16 operands), so its result agrees with kda_gate + kda_chunk_fwd
+ * within the mode's tolerance but not bit for bit.
+ * The pages compute the gate outside the chunk kernel ("GLM-5.3-
  * Flash F6.2: KDA correctness and FLA sequence parallelism", fused-gate
  * commit, with FP32 A_log/dt_bias); fusing it here removes that launch and
  * its round trip of g, and with f in BF16 (the activation dtype of the gate

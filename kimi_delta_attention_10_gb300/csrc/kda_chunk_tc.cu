@@ -282,8 +282,9 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(ChunkArgs args)
         // ---- 3: per channel (thread ch, tokens 32 hh .. 32 hh + 31)
         float a[32], kh[32], qh[32];
         {
-            // e^g by the hardware exponential (relative error ~1e-6, far below the
-            // FP16 operands' rounding); the norms as broadcast 16-byte loads
+            // e^g by the hardware exponential, or straight from the gate's input by
+            // gate_exp_fast (relative error below 1e-5 either way, far below the FP16
+            // operands' rounding); the norms as broadcast 16-byte loads
             const float4* rq4 = reinterpret_cast<const float4*>(rq) + 8 * hh;
             const float4* rk4 = reinterpret_cast<const float4*>(rk) + 8 * hh;
 #pragma unroll
@@ -295,7 +296,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(ChunkArgs args)
                     const int u = 4 * u4 + e, t = 32 * hh + u;
                     const float gv = load_as_float(sg + t * DK + ch);
                     // rows past the sequence end hold 0: decay 1 in both forms
-                    a[u] = __expf(kGated ? (t < L ? gate_decay(gv, dtb, lamneg) : 0.f) : gv);
+                    a[u] = kGated ? (t < L ? gate_exp_fast(gv, dtb, lamneg) : 1.f) : __expf(gv);
                     kh[u] = ST::to_f32(sk[t * DK + ch]) * nkv[e];
                     qh[u] = ST::to_f32(sq[t * DK + ch]) * nqv[e];
                 }

@@ -20,10 +20,27 @@ def _small(lens, H=4, seed=0, dtype=torch.bfloat16):
     return make_inputs(lens, H, 128, 128, dtype, seed)
 
 
+# Fused against unfused on the tensor-core paths: they differ only by the fused
+# prologue's e^g (relative 1e-5 against kda_gate's exp(g)), which flips a few
+# FP16 operand and BF16 output roundings; both stay within 3e-3 of the oracle.
+FUSED_VS_UNFUSED_TC = 2e-3
+
+
+def assert_fused_matches_unfused(mode, o1, s1, o2, s2):
+    """Bit for bit in FP32-exact mode (the gate's own arithmetic); within
+    FUSED_VS_UNFUSED_TC on the tensor-core paths (the fast e^g)."""
+    if mode == "fp32_exact":
+        assert torch.equal(o1, o2) and torch.equal(s1, s2)
+    else:
+        f = lambda t: t.float().cpu().double().numpy()
+        assert rel_l2(f(o2), f(o1)) <= FUSED_VS_UNFUSED_TC
+        assert rel_l2(f(s2), f(s1)) <= FUSED_VS_UNFUSED_TC
+
+
 @pytest.mark.parametrize("mode", MODES)
 @pytest.mark.parametrize("case", ["packed_37_28_f32", "single_129_bf16", "edges"])
-def test_gated_equals_gate_then_chunk_bitwise(case, mode):
-    """The fused prologue uses the gate's exact FP32 arithmetic."""
+def test_gated_equals_gate_then_chunk(case, mode):
+    """FP32-exact: the fused prologue uses the gate's exact FP32 arithmetic."""
     x = _small([1, 64, 0, 130], seed=21) if case == "edges" else workload_inputs(case)
     d = device_inputs(x)
     g, beta = kda_gate(d["f"], d["A_log"], d["dt_bias"], d["b"])
@@ -33,7 +50,7 @@ def test_gated_equals_gate_then_chunk_bitwise(case, mode):
                                  d["b"], d["cu_seqlens"], x.scale, out_dtype=OUT_DTYPE[mode],
                                  **path_kw(mode))
     torch.cuda.synchronize()
-    assert torch.equal(o1, o2) and torch.equal(s1, s2)
+    assert_fused_matches_unfused(mode, o1, s1, o2, s2)
 
 
 @pytest.mark.parametrize("mode", MODES)
@@ -50,10 +67,11 @@ def test_gated_matches_oracle(mode):
 
 @pytest.mark.parametrize("mode", MODES)
 @pytest.mark.parametrize("lens", [[1, 64, 0, 130], [8192]])
-def test_gated_bf16_f_equals_gate_then_chunk_bitwise(lens, mode):
+def test_gated_bf16_f_equals_gate_then_chunk(lens, mode):
     """f in BF16 (the gate projection's activation dtype): the fused call reads
-    it as the gate does, so the bits equal kda_gate on the same BF16 f followed
-    by kda_chunk_fwd; 8192 tokens run the two-phase path in four windows."""
+    it as kda_gate does (FP32-exact: the same bits as kda_gate on the same BF16
+    f followed by kda_chunk_fwd); 8192 tokens run the two-phase path in four
+    windows."""
     x = _small(lens, H=2, seed=23)
     x.f = x.f.to(torch.bfloat16)
     d = device_inputs(x)
@@ -64,7 +82,7 @@ def test_gated_bf16_f_equals_gate_then_chunk_bitwise(lens, mode):
                                  d["b"], d["cu_seqlens"], x.scale, out_dtype=OUT_DTYPE[mode],
                                  **path_kw(mode))
     torch.cuda.synchronize()
-    assert torch.equal(o1, o2) and torch.equal(s1, s2)
+    assert_fused_matches_unfused(mode, o1, s1, o2, s2)
 
 
 @pytest.mark.parametrize("mode", MODES)
