@@ -121,7 +121,7 @@ kda_status kda_gate(const void* f, int32_t f_dtype, const float* A_log, const fl
  * for bit those of one window.
  *
  * The size is a bound that holds for every cu_seqlens with these N and T:
- * a 1 KiB-aligned header of 2 N + 5 int32, (T / 64 + N) * H records of 74240
+ * a 1 KiB-aligned header of 2 N + 9 int32, (T / 64 + N) * H records of 74240
  * bytes, and N * H * K * V FP32 (the state carried between windows).
  * Arguments as kda_chunk_fwd; *bytes_host is host memory.
  */

@@ -63,11 +63,18 @@ static_assert(REC_BYTES % 16 == 0 && REC_BYTES < (1u << 20), "bulk copy size");
 // offsets (chunks of sequences 0 .. n-1), then int32 [5 + N .. 5 + 2N) = the
 // order in which the scan takes the sequences: longest first (LPT), so that
 // short sequences fill the tail of a packed batch (input order above
-// kLptMaxSeqs sequences).
+// kLptMaxSeqs sequences), then int32 [5 + 2N .. 5 + 2N + kMaxWindows) = the
+// unit counters the preparation CTAs of each chunk window take work from
+// (zeroed by the plan).
 constexpr int kHdrOff = 4;
 constexpr int kLptMaxSeqs = 1024;
+constexpr int kMaxWindows = 4;
 
-int64_t header_bytes(int32_t N) { return ((int64_t)(kHdrOff + 2 * N + 1) * 4 + 1023) / 1024 * 1024; }
+int64_t header_bytes(int32_t N)
+{
+    return ((int64_t)(kHdrOff + 2 * N + 1 + kMaxWindows) * 4 + 1023) / 1024 * 1024;
+}
+__host__ __device__ int32_t* window_counters(int32_t* hdr, int32_t N) { return hdr + kHdrOff + 2 * N + 1; }
 
 // ---------------------------------------------------------------- plan
 __global__ void __launch_bounds__(1024) chunk_plan_kernel(const int32_t* __restrict__ cu, int32_t N,
@@ -121,6 +128,7 @@ __global__ void __launch_bounds__(1024) chunk_plan_kernel(const int32_t* __restr
         hdr[0] = bad;
         if (bad) report_status(status, KDA_ERR_DEVICE_ARG);
     }
+    if (tid < kMaxWindows) window_counters(hdr, N)[tid] = 0;
     // scan order: rank of each sequence by length, longest first, ties by index
     int32_t* order = hdr + kHdrOff + N + 1;
     if (N <= kLptMaxSeqs) {
@@ -170,11 +178,26 @@ static_assert(P_PAIR + 49152 <= P_XT, "pair-sum operands fit below X'^T");
 static_assert(2 * (P_SMEM + 1024) <= 233472, "two preparation CTAs per SM");
 constexpr uint32_t P_TM_A = 0, P_TM_W = 0, P_TM_U = 64, P_TM_COLS = 256;
 
+// Where one (chunk, head) unit lies in the packed input.
+struct UnitLoc {
+    bool valid;
+    int h, t0, L;
+    int64_t unit;
+};
+
+// Persistent: each CTA takes units in order from the window's counter (so CTAs
+// that start late, on SMs a scan frees, find the work already shared out) and
+// keeps its tensor memory and barriers across them.  The next unit's 16-bit
+// inputs are staged while the current one finishes: q, k (and f in BF16) as
+// soon as the inverse has freed their region, v (and an FP32 g or f) once the
+// W/U MMAs have read X'^T and V^T.
 template <typename TIn, int kGate>
 __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(ChunkArgs args,
                                                            const int32_t* __restrict__ hdr,
                                                            unsigned char* __restrict__ records,
-                                                           int64_t unit_base, int32_t wait_primary)
+                                                           int64_t unit_base, int64_t units,
+                                                           int32_t* __restrict__ ctr,
+                                                           int32_t wait_primary)
 {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     const uint32_t raw_s = smem_u32(smem_raw);
@@ -193,21 +216,6 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(ChunkArgs args,
     // it, so the next scan, launched after this grid, sees the state carry.
     if (wait_primary && blockIdx.x == gridDim.x - 1 && tid == 0) grid_dependency_wait();
     const int32_t* off = hdr + kHdrOff;
-    const int64_t unit = unit_base + blockIdx.x;
-    const int32_t gc = (int32_t)(unit / H);
-    const int h = (int)(unit % H);
-    if (gc >= off[args.N]) return;
-    int lo = 0, hi = args.N - 1;                           // last n with off[n] <= gc
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (off[mid] <= gc) lo = mid;
-        else hi = mid - 1;
-    }
-    const int n = lo;
-    const int bos = args.cu_seqlens[n], eos = args.cu_seqlens[n + 1];
-    const int t0 = bos + (gc - off[n]) * C;
-    const int L = min(C, eos - t0);
-    unsigned char* rec = records + unit * REC_BYTES;
 
     float (*akk)[LDA] = reinterpret_cast<float (*)[LDA]>(sm + P_AKK);
     float (*Tf)[LDA] = reinterpret_cast<float (*)[LDA]>(sm + P_TF);
@@ -225,6 +233,7 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(ChunkArgs args,
     // [0..2] pair rounds, [3] W/U, [4] drain after a failure
     uint64_t* bar = reinterpret_cast<uint64_t*>(sm + P_BAR);
     uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + P_BAR + 48);
+    int64_t* s_next = reinterpret_cast<int64_t*>(sm + P_BAR + 56);
     // test hook: CTA 0 withholds its first MMA group and the commit that signals it
     const bool withhold = args.fault == KDA_TEST_FAULT_PREP && blockIdx.x == 0;
 
@@ -234,67 +243,69 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(ChunkArgs args,
     const TG* __restrict__ graw =
         kGated ? static_cast<const TG*>(args.f) : reinterpret_cast<const TG*>(args.g);
     using ST = Stage<TIn>;
+    constexpr bool k16 = sizeof(TIn) == 2;                 // 16-bit inputs: staged by cp.async
+    constexpr bool kGEarly = sizeof(TG) == 2;              // a BF16 f fits beside q and k
+    constexpr int GP = DK * (int)sizeof(TG) / 16;          // 16-byte pieces per g/f row
 
-    // ---- 1: the chunk in staging (rows >= L zero, decay 1)
-    if constexpr (sizeof(TIn) == 2) {
-#pragma unroll
-        for (int u = 0; u < C * 16 / NT; ++u) {
-            const int e = tid + u * NT, r = e >> 4, pc = e & 15;
-            const bool ok = r < L;
-            const int64_t src = ((int64_t)(t0 + (ok ? r : 0)) * H + h) * DK + pc * 8;
-            cp_async16(sm + P_SQ + r * 256 + pc * 16, gq + src, ok);
-            cp_async16(sm + P_SK + r * 256 + pc * 16, gk + src, ok);
-            cp_async16(sm + P_SV + r * 256 + pc * 16, gv + src, ok);
+    // the next unit of this window, from its counter (tid 0; read after a barrier)
+    auto grab = [&]() {
+        const int64_t c = atomicAdd(ctr, 1);
+        *s_next = c < units ? unit_base + c : -1;
+    };
+    auto locate = [&](int64_t unit) -> UnitLoc {
+        UnitLoc u{false, 0, 0, 0, unit};
+        if (unit < 0) return u;
+        const int32_t gc = (int32_t)(unit / H);
+        if (gc >= off[args.N]) return u;                   // past the chunks of the offsets
+        int lo = 0, hi = args.N - 1;                       // last n with off[n] <= gc
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (off[mid] <= gc) lo = mid;
+            else hi = mid - 1;
         }
-    } else {
-        using LD = Loader<TIn>;
-        constexpr int P = LD::kPieces;
-        auto rows_via_regs = [&](const TIn* base, uint32_t so) {
-            uint4 x[C * P / NT];
+        const int bos = args.cu_seqlens[lo], eos = args.cu_seqlens[lo + 1];
+        u.valid = true;
+        u.h = (int)(unit % H);
+        u.t0 = bos + (gc - off[lo]) * C;
+        u.L = min(C, eos - u.t0);
+        return u;
+    };
+    auto stage16 = [&](uint32_t so, const TIn* base, const UnitLoc& u) {
 #pragma unroll
-            for (int u = 0; u < C * P / NT; ++u) {
-                const int e = tid + u * NT, r = e / P, pc = e % P;
-                x[u] = (r < L) ? LD::load(base + ((int64_t)(t0 + r) * H + h) * DK, pc)
-                               : make_uint4(0, 0, 0, 0);
-            }
-#pragma unroll
-            for (int u = 0; u < C * P / NT; ++u) {
-                const int e = tid + u * NT;
-                LD::store(sm + so, e / P, e % P, x[u]);
-            }
-        };
-        rows_via_regs(gq, P_SQ);
-        rows_via_regs(gk, P_SK);
-        rows_via_regs(gv, P_SV);
-    }
-    constexpr int GP = DK * (int)sizeof(TG) / 16;           // 16-byte pieces per g/f row
-#pragma unroll
-    for (int u = 0; u < C * GP / NT; ++u) {
-        const int e = tid + u * NT, r = e / GP, pc = e % GP;
-        const bool ok = r < L;
-        cp_async16(sm + P_SG + e * 16,
-                   graw + ((int64_t)(t0 + (ok ? r : 0)) * H + h) * DK + pc * (16 / (int)sizeof(TG)),
-                   ok);
-    }
-    cp_async_commit();
-    float lamneg = 0.f, dtb = 0.f;
-    if (kGated) {
-        lamneg = -expf(args.A_log[h]);
-        dtb = args.dt_bias[(int64_t)h * DK + ch];
-    }
-    if (tid < C) {
-        float xb = 0.f;
-        if (tid < L) {
-            const int64_t i = (int64_t)(t0 + tid) * H + h;
-            if (kGated)
-                xb = gate_sigmoid(args.b_bf16
-                                      ? __bfloat162float(static_cast<const __nv_bfloat16*>(args.b)[i])
-                                      : static_cast<const float*>(args.b)[i]);
-            else
-                xb = args.beta[i];
+        for (int k = 0; k < C * 16 / NT; ++k) {
+            const int e = tid + k * NT, r = e >> 4, pc = e & 15;
+            const bool ok = r < u.L;
+            const int64_t src = ((int64_t)(u.t0 + (ok ? r : 0)) * H + u.h) * DK + pc * 8;
+            cp_async16(sm + so + r * 256 + pc * 16, base + src, ok);
         }
-        sbeta[tid] = xb;
-    }
+    };
+    auto stage_g = [&](const UnitLoc& u) {
+#pragma unroll
+        for (int k = 0; k < C * GP / NT; ++k) {
+            const int e = tid + k * NT, r = e / GP, pc = e % GP;
+            const bool ok = r < u.L;
+            cp_async16(sm + P_SG + e * 16,
+                       graw + ((int64_t)(u.t0 + (ok ? r : 0)) * H + u.h) * DK +
+                           pc * (16 / (int)sizeof(TG)),
+                       ok);
+        }
+    };
+    // q, k (and a BF16 f): their region is free once the inverse is done
+    auto stage_early = [&](const UnitLoc& u) {
+        if constexpr (k16) {
+            stage16(P_SQ, gq, u);
+            stage16(P_SK, gk, u);
+        }
+        if constexpr (kGEarly) stage_g(u);
+        cp_async_commit();
+    };
+    // v (and an FP32 g or f): free once the W/U MMAs have read X'^T and V^T
+    auto stage_late = [&](const UnitLoc& u) {
+        if constexpr (k16) stage16(P_SV, gv, u);
+        if constexpr (!kGEarly) stage_g(u);
+        cp_async_commit();
+    };
+
     if (warp == 0) {
         tmem_alloc(tslot, P_TM_COLS);
         tmem_relinquish();
@@ -302,49 +313,21 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(ChunkArgs args,
     if (tid == 0) {
         for (int b = 0; b < 5; ++b) mbar_init(&bar[b], 1);
         fence_mbar_init();
+        grab();
     }
-    cp_async_wait_all();
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
     const uint32_t tmem = *tslot;
     const uint32_t tlane = tmem + ((uint32_t)(32 * quad) << 16);
 
-    // ---- 2: row norms and q^ . k^
-    chunk_norms<TIn>(sm + P_SQ, sm + P_SK, rq, rk, dqk, args.l2norm != 0, tid);
-    __syncthreads();
-
-    // ---- 3: per channel (thread ch, tokens 32 hh .. 32 hh + 31)
-    float a[32], kh[32], qh[32];
-    {
-        // e^g by the hardware exponential, or straight from the gate's input by
-        // gate_exp_fast (relative error below 1e-5 either way, far below the FP16
-        // operands' rounding); the norms as broadcast 16-byte loads
-        const float4* rq4 = reinterpret_cast<const float4*>(rq) + 8 * hh;
-        const float4* rk4 = reinterpret_cast<const float4*>(rk) + 8 * hh;
-#pragma unroll
-        for (int u4 = 0; u4 < 8; ++u4) {
-            const float4 nq = rq4[u4], nk = rk4[u4];
-            const float nqv[4] = {nq.x, nq.y, nq.z, nq.w}, nkv[4] = {nk.x, nk.y, nk.z, nk.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int u = 4 * u4 + e, t = 32 * hh + u;
-                const float gv_ = load_as_float(sg + t * DK + ch);
-                a[u] = kGated ? (t < L ? gate_exp_fast(gv_, dtb, lamneg) : 1.f) : __expf(gv_);
-                kh[u] = ST::to_f32(sk[t * DK + ch]) * nkv[e];
-                qh[u] = ST::to_f32(sq[t * DK + ch]) * nqv[e];
-            }
-        }
-        float p = 1.f;
-#pragma unroll
-        for (int u = 0; u < 32; ++u) p *= a[u];
-        tot[hh * DK + ch] = p;
+    UnitLoc cur = locate(*s_next);
+    if (cur.valid) {
+        stage_early(cur);
+        stage_late(cur);
     }
-    __syncthreads();
-
-    // ---- 4: pair sums, three rounds through one operand buffer; the
-    // per-channel rows and the zeroing of A_qk's upper part run beside the MMAs
     bool failed = false;
+    uint32_t ph = 0;                                       // each barrier completes once per unit
     constexpr uint32_t id_pairs = idesc(kFmtF16, 128, 64, true, true);
     auto issue_round = [&](int rnd) {
         fence_async_smem();
@@ -360,11 +343,92 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(ChunkArgs args,
         }
     };
     auto wait_bar = [&](int b) -> bool {
-        const bool ok = mbar_wait(&bar[b], 0);
+        const bool ok = mbar_wait(&bar[b], ph);
         return __syncthreads_or(!ok) == 0;
     };
-    float vv[32];
-    do {
+
+    while (cur.valid) {
+        const int h = cur.h, t0 = cur.t0, L = cur.L;
+        unsigned char* rec = records + cur.unit * REC_BYTES;
+
+        // ---- 1: the chunk in staging (rows >= L zero, decay 1)
+        if constexpr (!k16) {
+            using LD = Loader<TIn>;
+            constexpr int P = LD::kPieces;
+            auto rows_via_regs = [&](const TIn* base, uint32_t so) {
+                uint4 x[C * P / NT];
+#pragma unroll
+                for (int u = 0; u < C * P / NT; ++u) {
+                    const int e = tid + u * NT, r = e / P, pc = e % P;
+                    x[u] = (r < L) ? LD::load(base + ((int64_t)(t0 + r) * H + h) * DK, pc)
+                                   : make_uint4(0, 0, 0, 0);
+                }
+#pragma unroll
+                for (int u = 0; u < C * P / NT; ++u) {
+                    const int e = tid + u * NT;
+                    LD::store(sm + so, e / P, e % P, x[u]);
+                }
+            };
+            rows_via_regs(gq, P_SQ);
+            rows_via_regs(gk, P_SK);
+            rows_via_regs(gv, P_SV);
+        }
+        float lamneg = 0.f, dtb = 0.f;
+        if (kGated) {
+            lamneg = -expf(args.A_log[h]);
+            dtb = args.dt_bias[(int64_t)h * DK + ch];
+        }
+        if (tid < C) {
+            float xb = 0.f;
+            if (tid < L) {
+                const int64_t i = (int64_t)(t0 + tid) * H + h;
+                if (kGated)
+                    xb = gate_sigmoid(args.b_bf16
+                                          ? __bfloat162float(static_cast<const __nv_bfloat16*>(args.b)[i])
+                                          : static_cast<const float*>(args.b)[i]);
+                else
+                    xb = args.beta[i];
+            }
+            sbeta[tid] = xb;
+        }
+        cp_async_wait_all();
+        __syncthreads();
+
+        // ---- 2: row norms and q^ . k^
+        chunk_norms<TIn>(sm + P_SQ, sm + P_SK, rq, rk, dqk, args.l2norm != 0, tid);
+        __syncthreads();
+
+        // ---- 3: per channel (thread ch, tokens 32 hh .. 32 hh + 31)
+        float a[32], kh[32], qh[32];
+        {
+            // e^g by the hardware exponential, or straight from the gate's input by
+            // gate_exp_fast (relative error below 1e-5 either way, far below the FP16
+            // operands' rounding); the norms as broadcast 16-byte loads
+            const float4* rq4 = reinterpret_cast<const float4*>(rq) + 8 * hh;
+            const float4* rk4 = reinterpret_cast<const float4*>(rk) + 8 * hh;
+#pragma unroll
+            for (int u4 = 0; u4 < 8; ++u4) {
+                const float4 nq = rq4[u4], nk = rk4[u4];
+                const float nqv[4] = {nq.x, nq.y, nq.z, nq.w}, nkv[4] = {nk.x, nk.y, nk.z, nk.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int u = 4 * u4 + e, t = 32 * hh + u;
+                    const float gv_ = load_as_float(sg + t * DK + ch);
+                    a[u] = kGated ? (t < L ? gate_exp_fast(gv_, dtb, lamneg) : 1.f) : __expf(gv_);
+                    kh[u] = ST::to_f32(sk[t * DK + ch]) * nkv[e];
+                    qh[u] = ST::to_f32(sq[t * DK + ch]) * nqv[e];
+                }
+            }
+            float p = 1.f;
+#pragma unroll
+            for (int u = 0; u < 32; ++u) p *= a[u];
+            tot[hh * DK + ch] = p;
+        }
+        __syncthreads();
+
+        // ---- 4: pair sums, three rounds through one operand buffer; the
+        // per-channel rows and the zeroing of A_qk's upper part run beside the MMAs
+        float vv[32];
         level32_operands(sm + P_PAIR, ch, hh, a, kh, qh);
         level_operands<16>(sm + P_PAIR, ch, hh, 64, 32, a, kh, qh);
         issue_round(0);
@@ -393,7 +457,8 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(ChunkArgs args,
         for (int q = 0; q < 4; ++q) st8(sm + P_SV, 0, ch, 32 * hh + 8 * q, vv + 8 * q);
         fence_after_sync();
 
-        // ---- 5: A_kk (fp32) and A_qk (fp16) from TMEM
+        // ---- 5: A_kk (fp32) and A_qk (fp16) from TMEM; the next unit's number
+        if (tid == 0) grab();
         extract_pairs(sm + P_AQK, &akk[0][0], sbeta, dqk, tlane, P_TM_A, tid, warp, lane);
         fence_before_sync();
         __syncthreads();
@@ -403,6 +468,8 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(ChunkArgs args,
         fence_async_smem();
         fence_before_sync();
         __syncthreads();
+        const UnitLoc nxt = locate(*s_next);
+        if (nxt.valid) stage_early(nxt);                   // into the dead q, k, f, A_kk, T
 
         // ---- 7: W^T = X'^T T'^T, U^T = V^T T'^T
         if (tid == 0) {
@@ -427,6 +494,7 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(ChunkArgs args,
         }
         if (!wait_bar(3)) { failed = true; break; }
         fence_after_sync();
+        if (nxt.valid) stage_late(nxt);                    // into the read X'^T, V^T
         {
             float w[32];
             tmem_ld32(tlane + P_TM_W + 32 * half, w);
@@ -436,7 +504,9 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(ChunkArgs args,
 #pragma unroll
             for (int q = 0; q < 4; ++q) st8(rec + REC_U, 0, row, 32 * half + 8 * q, w + 8 * q);
         }
-    } while (false);
+        cur = nxt;
+        ph ^= 1u;
+    }
 
     if (failed && tid == 0) {
         report_status(args.status, KDA_ERR_TIMEOUT);
@@ -444,6 +514,7 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(ChunkArgs args,
         commit(&bar[4]);
         mbar_wait(&bar[4], 0);
     }
+    cp_async_wait_all();                                   // staging of a next unit, if any
     fence_before_sync();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, P_TM_COLS);
@@ -763,15 +834,17 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) chunk_scan_kernel(ChunkArgs a
 // ---------------------------------------------------------------- launch
 template <typename TIn, int kGate>
 cudaError_t launch_prep_typed(const ChunkArgs& a, const int32_t* hdr, unsigned char* rec,
-                              int64_t unit_base, int64_t units, bool beside_scan,
+                              int64_t unit_base, int64_t units, int32_t* ctr, bool beside_scan,
                               cudaStream_t stream)
 {
     auto kern = chunk_prep_kernel<TIn, kGate>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)P_SMEM);
     if (e != cudaSuccess) return e;
+    const int sms = device_sm_count();
+    const int64_t ctas = std::min<int64_t>(units, 2 * (int64_t)(sms > 0 ? sms : 152));
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)units);
+    cfg.gridDim = dim3((unsigned)ctas);
     cfg.blockDim = dim3(NT);
     cfg.dynamicSmemBytes = P_SMEM;
     cfg.stream = stream;
@@ -780,16 +853,20 @@ cudaError_t launch_prep_typed(const ChunkArgs& a, const int32_t* hdr, unsigned c
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = beside_scan ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, kern, a, hdr, rec, unit_base, (int32_t)(beside_scan ? 1 : 0));
+    return cudaLaunchKernelEx(&cfg, kern, a, hdr, rec, unit_base, units, ctr,
+                              (int32_t)(beside_scan ? 1 : 0));
 }
 
-// Preparation of the (chunk, head) units [unit_base, unit_base + units);
-// `beside_scan`: launched to overlap the scan just before it on the stream.
+// Preparation of the (chunk, head) units [unit_base, unit_base + units), taken
+// from the counter `ctr` (zero at launch); `beside_scan`: launched to overlap
+// the scan just before it on the stream.
 cudaError_t launch_prep(const ChunkArgs& a, const int32_t* hdr, unsigned char* rec,
-                        int64_t unit_base, int64_t units, bool beside_scan, cudaStream_t stream)
+                        int64_t unit_base, int64_t units, int32_t* ctr, bool beside_scan,
+                        cudaStream_t stream)
 {
     if (units <= 0) return cudaSuccess;
-#define KDA_PREP(TIN, GATE) launch_prep_typed<TIN, GATE>(a, hdr, rec, unit_base, units, beside_scan, stream)
+#define KDA_PREP(TIN, GATE) \
+    launch_prep_typed<TIN, GATE>(a, hdr, rec, unit_base, units, ctr, beside_scan, stream)
     switch (gate_in(a)) {
         case kGateF32:
             return a.qkv_bf16 ? KDA_PREP(__nv_bfloat16, kGateF32) : KDA_PREP(float, kGateF32);
@@ -821,7 +898,6 @@ cudaError_t launch_scan(const ChunkArgs& a, const int32_t* hdr, const unsigned c
 // the scan leaves free; each scan is an ordinary launch, so it starts after
 // the preparation of its window, and that preparation's last CTA waits for
 // the previous scan.
-constexpr int kMaxWindows = 4;
 constexpr int kWindowChunks = 32;              // at least this many chunks per window
 constexpr bool kHalfLastWindow = true;         // the last window's scan runs alone: keep it short
 
@@ -905,15 +981,17 @@ cudaError_t launch_chunk_split(const ChunkArgs& a, int64_t chunks, bool overlap,
     int W = 1;
     if (overlap && (int64_t)a.N * a.H <= (sms > 0 ? sms : 152))
         W = (int)std::min<int64_t>(kMaxWindows, chunks / kWindowChunks);
+    int32_t* ctr = window_counters(hdr, a.N);
     if (W <= 1) {
-        e = launch_prep(a, hdr, rec, 0, units, false, stream);
+        e = launch_prep(a, hdr, rec, 0, units, ctr, false, stream);
         if (e != cudaSuccess) return e;
         return launch_scan(a, hdr, rec, ScanWindow{0, INT32_MAX, nullptr, 1}, stream);
     }
     for (int w = 0; w < W && e == cudaSuccess; ++w) {
         const int32_t g0 = (int32_t)window_bound(chunks, W, w);
         const int32_t g1 = (int32_t)window_bound(chunks, W, w + 1);
-        e = launch_prep(a, hdr, rec, (int64_t)g0 * a.H, (int64_t)(g1 - g0) * a.H, w > 0, stream);
+        e = launch_prep(a, hdr, rec, (int64_t)g0 * a.H, (int64_t)(g1 - g0) * a.H, ctr + w, w > 0,
+                        stream);
         const ScanWindow win{g0, w + 1 == W ? INT32_MAX : g1, carry, w + 1 == W ? 1 : 0};
         if (e == cudaSuccess) e = launch_scan(a, hdr, rec, win, stream);
     }
