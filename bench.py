@@ -59,7 +59,9 @@ def parse_args():
     p.add_argument("--single-pass", action="store_true",
                    help="BF16 tensor-core path without a workspace (one kernel per call)")
     p.add_argument("--output-gate", action="store_true",
-                   help="add the output gate with gated RMSNorm (kda_gated_rmsnorm) to the step")
+                   help="add the output gate with gated RMSNorm to the step: fused into the "
+                        "forward's output store (kda_chunk_fwd_gated_norm), or with --unfused "
+                        "a separate kda_gated_rmsnorm")
     p.add_argument("--backward", action="store_true",
                    help="also time kda_chunk_bwd (the VJP) on the workload, after the step")
     p.add_argument("--all-workloads", action="store_true",
@@ -387,7 +389,8 @@ def main():
     __graft_entry__.build()
     from kimi_delta_attention_10_gb300 import (chunk_bwd_workspace_size, chunk_workspace_size,
                                                kda_chunk_bwd, kda_chunk_fwd, kda_chunk_fwd_gated,
-                                               kda_gate, kda_gated_rmsnorm)
+                                               kda_chunk_fwd_gated_norm, kda_gate,
+                                               kda_gated_rmsnorm)
     from kimi_delta_attention_10_gb300.inputs import WORKLOAD_BY_NAME, workload_inputs
 
     mode = args.mode or "bf16_tc"
@@ -426,16 +429,21 @@ def main():
         if (not args.fused):
             kda_chunk_fwd(d["q"], d["k"], d["v"], g, beta, d["cu_seqlens"], x.scale, mode=mode,
                           out=out, final_state=fs, cu_seqlens_host=cu_host, workspace=ws)
+        elif args.output_gate:
+            kda_chunk_fwd_gated_norm(d["q"], d["k"], d["v"], d["f"], d["A_log"], d["dt_bias"],
+                                     d["b"], d["cu_seqlens"], zg, wg, x.scale, eps=1e-6,
+                                     mode=mode, out=yg, final_state=fs, cu_seqlens_host=cu_host,
+                                     workspace=ws)
         else:
             kda_chunk_fwd_gated(d["q"], d["k"], d["v"], d["f"], d["A_log"], d["dt_bias"],
                                 d["b"], d["cu_seqlens"], x.scale, mode=mode, out=out,
                                 final_state=fs, cu_seqlens_host=cu_host, workspace=ws)
         if ev is not None:
             ev[2].record(stream)
-        if args.output_gate:
+        if args.output_gate and not args.fused:
             kda_gated_rmsnorm(out, zg, wg, eps=1e-6, out=yg)
-            if ev is not None:
-                ev[3].record(stream)
+        if ev is not None:
+            ev[3].record(stream)
 
     def barrier():
         if world > 1:
@@ -505,12 +513,18 @@ def main():
                 kda_chunk_fwd(db["q"], db["k"], db["v"], g, beta, db["cu_seqlens"], x.scale,
                               mode=mode, out=outs[b], final_state=fss[b],
                               cu_seqlens_host=cu_host, workspace=ws)
+            elif args.output_gate:
+                kda_chunk_fwd_gated_norm(db["q"], db["k"], db["v"], db["f"], db["A_log"],
+                                         db["dt_bias"], db["b"], db["cu_seqlens"], zg, wg,
+                                         x.scale, eps=1e-6, mode=mode, out=outs[b],
+                                         final_state=fss[b], cu_seqlens_host=cu_host,
+                                         workspace=ws)
             else:
                 kda_chunk_fwd_gated(db["q"], db["k"], db["v"], db["f"], db["A_log"],
                                     db["dt_bias"], db["b"], db["cu_seqlens"], x.scale, mode=mode,
                                     out=outs[b], final_state=fss[b], cu_seqlens_host=cu_host,
                                     workspace=ws)
-            if args.output_gate:                   # y in place of o: the step's result
+            if args.output_gate and not args.fused:    # y in place of o: the step's result
                 kda_gated_rmsnorm(outs[b], zg, wg, eps=1e-6, out=outs[b])
             ev_comp[b].record(stream)
 
@@ -582,10 +596,13 @@ def main():
         out_bytes = out.element_size()
         alg = algorithmic_bytes(T, H, K, V, N, qkv_bytes, out_bytes,
                                 x.f.element_size() if args.fused else 4)
+        if args.output_gate and args.fused:       # the fused gate also reads z
+            alg += T * H * V * zg.element_size()
         avg_chunk_s = statistics.mean(chunk_ms) * 1e-3
         peak, peak_src = measured_peaks()
         achieved = alg / avg_chunk_s / 1e9
-        kname = "kda_chunk_fwd" if (not args.fused) else "kda_chunk_fwd_gated"
+        kname = ("kda_chunk_fwd" if not args.fused else
+                 "kda_chunk_fwd_gated_norm" if args.output_gate else "kda_chunk_fwd_gated")
         variant = "two_phase" if two_phase else ("single_pass" if mode == "bf16_tc" else mode)
         kernel_key = f"{kname}:{variant}:{w.name}"
         windows = chunk_windows(N, H, sum(-(-L // 64) for L in x.seqlens),
@@ -621,12 +638,14 @@ def main():
                 "gpu_launches": ((0 if args.fused else 1) +
                                  (1 + 2 * windows if two_phase else 1)) * args.steps,
                 "clocks": clk, "e2e": e2e}
-        if args.output_gate:
+        if args.output_gate and not args.fused:
             og_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
             line["kernels"]["kda_gated_rmsnorm_ms"] = og_ms
             line["kernels"]["kda_gated_rmsnorm_GBps"] = T * H * V * 3 * out.element_size() / og_ms / 1e6
             line["gpu_launches"] += args.steps
             cfg["step"] += " + kda_gated_rmsnorm"
+        elif args.output_gate:
+            cfg["step"] = "kda_chunk_fwd_gated_norm (output gate fused into the scan)"
         if (not args.fused):
             line["kernels"]["kda_gate_ms"] = statistics.mean(gate_ms)
             line["kernels"]["kda_gate_GBps"] = (gate_bytes(T, H, K, x.f.element_size()) /

@@ -216,6 +216,45 @@ kda_status kda_chunk_fwd_gated(const void* q, const void* k, const void* v, int3
                                int32_t* status_dev, kda_stream_t stream);
 
 /*
+ * kda_chunk_fwd_gated_norm -- kda_chunk_fwd_gated followed by the output gate
+ * with gated RMSNorm (kda_gated_rmsnorm), in one call:
+ *
+ *   out[t, h, v] = o[t, h, v] / sqrt(mean_v' o[t, h, v']^2 + eps) * weight[v]
+ *                  * sigmoid(z[t, h, v])
+ *
+ * where o is kda_chunk_fwd_gated's output.  The pages name the low-rank output
+ * gate (g_a_proj -> g_b_proj) and the gated-norm wrapper that follow the core
+ * ("GLM-5.3-Flash F6.2: KDA correctness and FLA sequence parallelism", module
+ * and FLA-SP commits).  In KDA_MODE_BF16_TC with a workspace and BF16 z the
+ * gate is applied in the state scan's output store: each chunk's o rows are
+ * normalised from their FP32 values in registers and never reach memory, so
+ * the call reads z once and writes the gated output once instead of writing
+ * o, reading it back and writing y.  Any other mode, workspace choice or z
+ * dtype runs kda_chunk_fwd_gated into `out` and then kda_gated_rmsnorm on it
+ * in place (two launches, the same result up to the rounding of o to
+ * out_dtype).
+ *
+ *   z       [T, H, V]  F32 or BF16 (z_dtype)   output-gate pre-activation; must
+ *                                              not be `out`
+ *   weight  [V]        F32                     per-channel weight shared by heads
+ *   eps     >= 0
+ *   out     [T, H, V]  out_dtype               the gated output
+ * Every other argument as kda_chunk_fwd_gated.  In KDA_MODE_BF16_TC a
+ * non-finite stored value sets KDA_ERR_RANGE as for kda_chunk_fwd.
+ */
+kda_status kda_chunk_fwd_gated_norm(const void* q, const void* k, const void* v, int32_t qkv_dtype,
+                                    const void* f, int32_t f_dtype, const float* A_log,
+                                    const float* dt_bias, const void* b, int32_t b_dtype,
+                                    const int32_t* cu_seqlens, const int32_t* cu_seqlens_host,
+                                    int32_t N, int64_t T, int32_t H, int32_t K, int32_t V,
+                                    float scale, int32_t qk_l2norm, int32_t mode,
+                                    const void* z, int32_t z_dtype, const float* weight,
+                                    float eps, void* out, int32_t out_dtype,
+                                    const float* initial_state, float* final_state,
+                                    void* workspace, int64_t workspace_bytes,
+                                    int32_t* status_dev, kda_stream_t stream);
+
+/*
  * kda_chunk_fwd_static -- kda_chunk_fwd in KDA_MODE_BF16_TC, two-phase, with
  * the library's own scratch instead of a caller workspace.  The pages have no
  * counterpart: this is an interface for callers that cannot allocate device
@@ -383,7 +422,7 @@ const char* kda_status_string(int32_t status);
  * 3: workspace arguments; kda_chunk_workspace_size.  Later additions that
  * change no existing signature keep the number: kda_chunk_fwd_static,
  * kda_gated_rmsnorm, kda_chunk_bwd_workspace_size, kda_chunk_bwd,
- * KDA_ERR_RANGE, kda_test_set_fault). */
+ * KDA_ERR_RANGE, kda_test_set_fault, kda_chunk_fwd_gated_norm). */
 int32_t kda_abi_version(void);
 
 #ifdef __cplusplus

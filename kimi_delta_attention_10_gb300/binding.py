@@ -41,6 +41,7 @@ MODES = {"bf16_tc": KDA_MODE_BF16_TC, "fp32_exact": KDA_MODE_FP32_EXACT}
 
 # Every symbol include/kda.h declares.
 EXPORTS = ("kda_gate", "kda_chunk_workspace_size", "kda_chunk_fwd", "kda_chunk_fwd_gated",
+           "kda_chunk_fwd_gated_norm",
            "kda_chunk_fwd_static", "kda_recurrent_step", "kda_gated_rmsnorm",
            "kda_chunk_bwd_workspace_size", "kda_chunk_bwd", "kda_test_set_fault",
            "kda_status_string", "kda_abi_version")
@@ -85,6 +86,11 @@ def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
                                             i32, i64, i32, i32, i32, ctypes.c_float, i32, i32,
                                             vp, i32, vp, vp, vp, i64, vp, vp]
         lib.kda_chunk_fwd_gated.restype = i32
+        lib.kda_chunk_fwd_gated_norm.argtypes = [vp, vp, vp, i32, vp, i32, vp, vp, vp, i32, vp,
+                                                 vp, i32, i64, i32, i32, i32, ctypes.c_float, i32,
+                                                 i32, vp, i32, vp, ctypes.c_float, vp, i32, vp, vp,
+                                                 vp, i64, vp, vp]
+        lib.kda_chunk_fwd_gated_norm.restype = i32
         lib.kda_chunk_fwd_static.argtypes = [vp, vp, vp, i32, vp, vp, vp, vp, i32, i64, i32, i32,
                                              i32, ctypes.c_float, i32, vp, i32, vp, vp, vp, vp]
         lib.kda_chunk_fwd_static.restype = i32
@@ -275,6 +281,44 @@ def kda_chunk_fwd_gated(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, f: to
         _stream_handle(stream, q.device))
     if st != KDA_OK:
         raise KDAError(st, "kda_chunk_fwd_gated")
+    return out, final_state
+
+
+def kda_chunk_fwd_gated_norm(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, f: torch.Tensor,
+                             A_log: torch.Tensor, dt_bias: torch.Tensor, b: torch.Tensor,
+                             cu_seqlens: torch.Tensor, z: torch.Tensor, weight: torch.Tensor,
+                             scale: Optional[float] = None, eps: float = 1e-6,
+                             mode: str = "bf16_tc", out: Optional[torch.Tensor] = None,
+                             out_dtype: Optional[torch.dtype] = None,
+                             output_final_state: bool = True,
+                             final_state: Optional[torch.Tensor] = None,
+                             initial_state: Optional[torch.Tensor] = None,
+                             cu_seqlens_host: Optional[Sequence[int]] = None,
+                             qk_l2norm: bool = True, status: Optional[torch.Tensor] = None,
+                             stream: Optional[torch.cuda.Stream] = None, workspace="auto"):
+    """kda_chunk_fwd_gated with the output gate and gated RMSNorm applied to its
+    output (z [T,H,V] gate pre-activation, weight [V]); returns (y, final_state)."""
+    lib = load_library()
+    T, H, K = q.shape
+    V = v.shape[2]
+    N = cu_seqlens.numel() - 1
+    if scale is None:
+        scale = K ** -0.5
+    out, final_state = _chunk_outputs(q, v, cu_seqlens, out, out_dtype, output_final_state,
+                                      final_state)
+    keep, host = _host_offsets(cu_seqlens_host)
+    ws, ws_bytes, ws_keep = _workspace(workspace, mode, N, T, H, K, V, q.device)
+    st = lib.kda_chunk_fwd_gated_norm(
+        _dev_ptr(q, "q"), _dev_ptr(k, "k"), _dev_ptr(v, "v"), _dtype_code(q),
+        _dev_ptr(f, "f"), _dtype_code(f), _dev_ptr(A_log, "A_log"), _dev_ptr(dt_bias, "dt_bias"),
+        _dev_ptr(b, "b"), _dtype_code(b), _dev_ptr(cu_seqlens, "cu_seqlens"), host,
+        N, T, H, K, V, float(scale), 1 if qk_l2norm else 0, MODES[mode],
+        _dev_ptr(z, "z"), _dtype_code(z), _dev_ptr(weight, "weight"), float(eps),
+        _dev_ptr(out, "out"), _dtype_code(out), _dev_ptr(initial_state, "initial_state"),
+        _dev_ptr(final_state, "final_state"), ws, ws_bytes, _dev_ptr(status, "status"),
+        _stream_handle(stream, q.device))
+    if st != KDA_OK:
+        raise KDAError(st, "kda_chunk_fwd_gated_norm")
     return out, final_state
 
 

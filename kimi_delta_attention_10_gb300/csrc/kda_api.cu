@@ -213,6 +213,55 @@ kda_status kda_chunk_fwd_gated(const void* q, const void* k, const void* v, int3
     return launch_chunk(a, mode, cu_seqlens_host, workspace, workspace_bytes, stream);
 }
 
+kda_status kda_chunk_fwd_gated_norm(const void* q, const void* k, const void* v, int32_t qkv_dtype,
+                                    const void* f, int32_t f_dtype, const float* A_log,
+                                    const float* dt_bias, const void* b, int32_t b_dtype,
+                                    const int32_t* cu_seqlens, const int32_t* cu_seqlens_host,
+                                    int32_t N, int64_t T, int32_t H, int32_t K, int32_t V,
+                                    float scale, int32_t qk_l2norm, int32_t mode,
+                                    const void* z, int32_t z_dtype, const float* weight,
+                                    float eps, void* out, int32_t out_dtype,
+                                    const float* initial_state, float* final_state,
+                                    void* workspace, int64_t workspace_bytes,
+                                    int32_t* status_dev, kda_stream_t stream)
+{
+    kda_status st = check_chunk(q, k, v, qkv_dtype, cu_seqlens, cu_seqlens_host, N, T, H, K, V,
+                                qk_l2norm, mode, out, out_dtype, initial_state, final_state,
+                                status_dev);
+    if (st != KDA_OK) return st;
+    if (!valid_dtype(f_dtype) || !valid_dtype(b_dtype) || !valid_dtype(z_dtype))
+        return KDA_ERR_INVALID_ARG;
+    if (!A_log || !dt_bias || !weight || !(eps >= 0.f)) return KDA_ERR_INVALID_ARG;
+    if (T > 0 && (!f || !b || !z)) return KDA_ERR_INVALID_ARG;
+    if (z != nullptr && z == out) return KDA_ERR_INVALID_ARG;
+    const void* ptrs[] = {f, A_log, dt_bias, b, z, weight};
+    for (const void* p : ptrs)
+        if (p && !aligned16(p)) return KDA_ERR_ALIGNMENT;
+    kda::ChunkArgs a = chunk_args(q, k, v, qkv_dtype, cu_seqlens, N, T, H, scale, qk_l2norm, out,
+                                  out_dtype, initial_state, final_state, status_dev);
+    a.gated = true;
+    a.f = f;
+    a.f_bf16 = f_dtype == KDA_BF16;
+    a.A_log = A_log;
+    a.dt_bias = dt_bias;
+    a.b = b;
+    a.b_bf16 = b_dtype == KDA_BF16;
+    if (mode == KDA_MODE_BF16_TC && workspace != nullptr && z_dtype == KDA_BF16) {
+        // fused: the scan stores y in place of o
+        a.out_norm = true;
+        a.z = static_cast<const __nv_bfloat16*>(z);
+        a.norm_w = weight;
+        a.norm_eps = eps;
+        return launch_chunk(a, mode, cu_seqlens_host, workspace, workspace_bytes, stream);
+    }
+    st = launch_chunk(a, mode, cu_seqlens_host, workspace, workspace_bytes, stream);
+    if (st != KDA_OK || N == 0 || T == 0) return st;
+    cudaError_t e = kda::launch_gated_rmsnorm(out, out_dtype == KDA_BF16, z, z_dtype == KDA_BF16,
+                                              weight, T * H, eps, out, out_dtype == KDA_BF16,
+                                              reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
 kda_status kda_chunk_fwd_static(const void* q, const void* k, const void* v, int32_t qkv_dtype,
                                 const float* g, const float* beta,
                                 const int32_t* cu_seqlens, const int32_t* cu_seqlens_host,

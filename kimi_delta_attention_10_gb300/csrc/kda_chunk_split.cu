@@ -544,6 +544,12 @@ constexpr uint32_t S_STG = 49152;             // two record stages
 constexpr uint32_t S_STG_STRIDE = 74752;      // REC_BYTES rounded up to 1024
 constexpr uint32_t S_BAR = S_STG + 2 * S_STG_STRIDE;   // 8 mbarriers, TMEM slot, abort flag
 constexpr uint32_t S_SMEM = S_BAR + 128 + 1024;
+// With the output gate fused (kNorm): the chunk's z rows (BF16 [64 t][128 v])
+// and the per-warp partial sums of squares ([2 halves][4 quads][32 tokens]).
+constexpr uint32_t S_Z = S_BAR + 1024;
+constexpr uint32_t S_RED = S_Z + 16384;
+constexpr uint32_t S_SMEM_NORM = S_RED + 1024 + 1024;
+static_assert(S_SMEM_NORM <= 232448, "shared memory budget with the output gate");
 static_assert(S_STG_STRIDE >= REC_BYTES && S_STG_STRIDE % 1024 == 0, "stage alignment");
 static_assert(S_SMEM <= 232448, "shared memory budget");
 // TMEM region of one parity: [W S]^T, O^T (on top of [Q' S]^T), P^T.
@@ -563,7 +569,24 @@ struct ScanWindow {
     int32_t last;
 };
 
-template <typename TOut>
+// Sum over the 32 lanes of a warp of each of 32 values, scattered: lane l
+// returns the sum of every lane's v[l] (five halving steps, 31 shuffles).
+__device__ __forceinline__ float warp_reduce_scatter32(float (&v)[32], int lane)
+{
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) {
+        const bool upper = (lane & off) != 0;
+#pragma unroll
+        for (int k = 0; k < off; ++k) {
+            const float send = upper ? v[k] : v[k + off];
+            const float keep = upper ? v[k + off] : v[k];
+            v[k] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+        }
+    }
+    return v[0];
+}
+
+template <typename TOut, bool kNorm>
 __global__ void __launch_bounds__(SCAN_THREADS, 1) chunk_scan_kernel(ChunkArgs args,
                                                                      const int32_t* __restrict__ hdr,
                                                                      const unsigned char* __restrict__ records,
@@ -724,15 +747,55 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) chunk_scan_kernel(ChunkArgs a
             const int64_t ostride = (int64_t)H * DV;
             TOut* op = out + ((int64_t)(tc + 32 * half) * H + h) * DV + row;
             const int nrows = min(32, Lc - 32 * half);
+            float y[32];
+#pragma unroll
+            for (int u = 0; u < 32; ++u) y[u] = args.scale * o[u];
+            if constexpr (kNorm) {
+                // y = o / sqrt(mean_v o^2 + eps) * w[v] * sigmoid(z): the sum of
+                // squares of token 32 half + u over v is spread over the 128
+                // threads of this half (lanes of four warps); each warp sums its
+                // 32 v values per token (lane u ends with token u), the four
+                // warps' sums meet in shared memory, and each lane's 1/rms goes
+                // back to the lanes by shuffles.
+                float sq[32];
+#pragma unroll
+                for (int u = 0; u < 32; ++u) sq[u] = y[u] * y[u];
+                float* red = reinterpret_cast<float*>(sm + S_RED);
+                red[(half * 4 + quad) * 32 + lane] = warp_reduce_scatter32(sq, lane);
+                cp_async_wait_all();                   // this chunk's z rows
+                named_sync(kEpiBar, NT);
+                const float ss = red[(half * 4) * 32 + lane] + red[(half * 4 + 1) * 32 + lane] +
+                                 red[(half * 4 + 2) * 32 + lane] + red[(half * 4 + 3) * 32 + lane];
+                const float rstd = rsqrtf(ss * (1.f / DV) + args.norm_eps);
+                const float wv = args.norm_w[row];
+                const __nv_bfloat16* zt = reinterpret_cast<const __nv_bfloat16*>(sm + S_Z);
+#pragma unroll
+                for (int u = 0; u < 32; ++u) {
+                    const float zv = __bfloat162float(zt[(32 * half + u) * DV + row]);
+                    const float gate = __fdividef(1.f, 1.f + __expf(-zv));
+                    y[u] *= __shfl_sync(0xffffffffu, rstd, u) * wv * gate;
+                }
+            }
 #pragma unroll
             for (int u = 0; u < 32; ++u) {
                 if (u < nrows) {
-                    const float y = args.scale * o[u];
-                    nan_acc = fmaf(y, 0.f, nan_acc);
-                    store_out(op, y);
+                    nan_acc = fmaf(y[u], 0.f, nan_acc);
+                    store_out(op, y[u]);
                 }
                 op += ostride;
             }
+        };
+        // the z rows of chunk cc into the tile (rows past the sequence end zero)
+        auto stage_z = [&](int cc) {
+            const int tc = bos + cc * C, Lc = min(C, eos - tc);
+#pragma unroll
+            for (int k = 0; k < C * 16 / NT; ++k) {
+                const int e = tid + k * NT, r = e >> 4, pc = e & 15;
+                const bool ok = r < Lc;
+                cp_async16(sm + S_Z + r * 256 + pc * 16,
+                           args.z + ((int64_t)(tc + (ok ? r : 0)) * H + h) * DV + pc * 8, ok);
+            }
+            cp_async_commit();
         };
         // test hook: CTA 0 withholds its first delta_ready arrival
         const bool withhold = args.fault == KDA_TEST_FAULT_SCAN && blockIdx.x == 0;
@@ -752,6 +815,8 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) chunk_scan_kernel(ChunkArgs a
                 }
                 if (named_sync_or(kEpiBar, NT, !ok)) { fail = true; break; }
             }
+            // every epilogue thread is past chunk c - 1's outputs: its z tile is free
+            if constexpr (kNorm) stage_z(c);
             fence_after_sync();
             {
                 // Delta^T[v][i] = U^T[v][i] - [W S]^T[v][i], fp16 K-major
@@ -826,6 +891,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) chunk_scan_kernel(ChunkArgs a
         }
         if (nan_acc != nan_acc) report_status(args.status, KDA_ERR_RANGE);
     }
+    if constexpr (kNorm) cp_async_wait_all();
     fence_before_sync();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, S_TM_COLS);
@@ -881,11 +947,15 @@ cudaError_t launch_prep(const ChunkArgs& a, const int32_t* hdr, unsigned char* r
 cudaError_t launch_scan(const ChunkArgs& a, const int32_t* hdr, const unsigned char* rec,
                         ScanWindow win, cudaStream_t stream)
 {
-    auto kern = a.out_bf16 ? chunk_scan_kernel<__nv_bfloat16> : chunk_scan_kernel<float>;
+    auto kern = a.out_norm ? (a.out_bf16 ? chunk_scan_kernel<__nv_bfloat16, true>
+                                         : chunk_scan_kernel<float, true>)
+                           : (a.out_bf16 ? chunk_scan_kernel<__nv_bfloat16, false>
+                                         : chunk_scan_kernel<float, false>);
+    const uint32_t smem = a.out_norm ? S_SMEM_NORM : S_SMEM;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)S_SMEM);
+                                         (int)smem);
     if (e != cudaSuccess) return e;
-    kern<<<(unsigned)((int64_t)a.N * a.H), SCAN_THREADS, S_SMEM, stream>>>(a, hdr, rec, win);
+    kern<<<(unsigned)((int64_t)a.N * a.H), SCAN_THREADS, smem, stream>>>(a, hdr, rec, win);
     return cudaGetLastError();
 }
 

@@ -43,6 +43,14 @@ struct ChunkArgs {
     // Two-phase tensor-core path: caller-provided scratch of at least
     // split_workspace_bytes(N, T, H) bytes (nullptr: single-pass kernel).
     void* workspace;
+    // Output gate fused into the scan's output store (kda_chunk_fwd_gated_norm,
+    // two-phase path, BF16 z): out receives
+    //   y = o / sqrt(mean_v o^2 + norm_eps) * norm_w[v] * sigmoid(z)
+    // instead of o.
+    bool out_norm;
+    const __nv_bfloat16* z;       // [T,H,V]
+    const float* norm_w;          // [V]
+    float norm_eps;
     // Test hook (kda_test_set_fault): a KDA_TEST_FAULT_* value; the named
     // kernel's CTA 0 withholds one arrival so that its bounded wait gives up.
     int32_t fault;
