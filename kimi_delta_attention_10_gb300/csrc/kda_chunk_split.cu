@@ -171,8 +171,8 @@ constexpr uint32_t P_RK = P_RQ + 256;  // 1/|k_t|
 constexpr uint32_t P_DQK = P_RK + 256; // q^_t . k^_t
 constexpr uint32_t P_BETA = P_DQK + 256;
 constexpr uint32_t P_TOT = P_BETA + 256;   // half-chunk decay fp32 [2][128]
-constexpr uint32_t P_BAR = P_TOT + 1024;   // 5 mbarriers + TMEM slot
-constexpr uint32_t P_SMEM = P_BAR + 64 + 1024;
+constexpr uint32_t P_BAR = P_TOT + 1024;   // 5 mbarriers, TMEM slot, the next unit
+constexpr uint32_t P_SMEM = P_BAR + 128 + 1024;
 static_assert(P_TF + C * LDA * 4 <= P_XT, "A_kk and T fit below X'^T");
 static_assert(P_PAIR + 49152 <= P_XT, "pair-sum operands fit below X'^T");
 static_assert(2 * (P_SMEM + 1024) <= 233472, "two preparation CTAs per SM");
@@ -180,9 +180,8 @@ constexpr uint32_t P_TM_A = 0, P_TM_W = 0, P_TM_U = 64, P_TM_COLS = 256;
 
 // Where one (chunk, head) unit lies in the packed input.
 struct UnitLoc {
-    bool valid;
-    int h, t0, L;
     int64_t unit;
+    int32_t valid, h, t0, L;
 };
 
 // Persistent: each CTA takes units in order from the window's counter (so CTAs
@@ -233,7 +232,7 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(ChunkArgs args,
     // [0..2] pair rounds, [3] W/U, [4] drain after a failure
     uint64_t* bar = reinterpret_cast<uint64_t*>(sm + P_BAR);
     uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + P_BAR + 48);
-    int64_t* s_next = reinterpret_cast<int64_t*>(sm + P_BAR + 56);
+    UnitLoc* s_next = reinterpret_cast<UnitLoc*>(sm + P_BAR + 64);
     // test hook: CTA 0 withholds its first MMA group and the commit that signals it
     const bool withhold = args.fault == KDA_TEST_FAULT_PREP && blockIdx.x == 0;
 
@@ -247,28 +246,27 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(ChunkArgs args,
     constexpr bool kGEarly = sizeof(TG) == 2;              // a BF16 f fits beside q and k
     constexpr int GP = DK * (int)sizeof(TG) / 16;          // 16-byte pieces per g/f row
 
-    // the next unit of this window, from its counter (tid 0; read after a barrier)
-    auto grab = [&]() {
+    // The next unit of this window, taken from its counter and located in the
+    // packed input by one thread (its dependent loads of the offsets run while
+    // the other warps work); the rest read it after a barrier.
+    auto grab_locate = [&]() {
         const int64_t c = atomicAdd(ctr, 1);
-        *s_next = c < units ? unit_base + c : -1;
-    };
-    auto locate = [&](int64_t unit) -> UnitLoc {
-        UnitLoc u{false, 0, 0, 0, unit};
-        if (unit < 0) return u;
-        const int32_t gc = (int32_t)(unit / H);
-        if (gc >= off[args.N]) return u;                   // past the chunks of the offsets
-        int lo = 0, hi = args.N - 1;                       // last n with off[n] <= gc
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (off[mid] <= gc) lo = mid;
-            else hi = mid - 1;
+        UnitLoc u{unit_base + c, 0, 0, 0, 0};
+        const int32_t gc = (int32_t)(u.unit / H);
+        if (c < units && gc < off[args.N]) {               // else past the window or the chunks
+            int lo = 0, hi = args.N - 1;                   // last n with off[n] <= gc
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (off[mid] <= gc) lo = mid;
+                else hi = mid - 1;
+            }
+            const int bos = args.cu_seqlens[lo], eos = args.cu_seqlens[lo + 1];
+            u.valid = 1;
+            u.h = (int)(u.unit % H);
+            u.t0 = bos + (gc - off[lo]) * C;
+            u.L = min(C, eos - u.t0);
         }
-        const int bos = args.cu_seqlens[lo], eos = args.cu_seqlens[lo + 1];
-        u.valid = true;
-        u.h = (int)(unit % H);
-        u.t0 = bos + (gc - off[lo]) * C;
-        u.L = min(C, eos - u.t0);
-        return u;
+        *s_next = u;
     };
     auto stage16 = [&](uint32_t so, const TIn* base, const UnitLoc& u) {
 #pragma unroll
@@ -313,7 +311,7 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(ChunkArgs args,
     if (tid == 0) {
         for (int b = 0; b < 5; ++b) mbar_init(&bar[b], 1);
         fence_mbar_init();
-        grab();
+        grab_locate();
     }
     fence_before_sync();
     __syncthreads();
@@ -321,7 +319,7 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(ChunkArgs args,
     const uint32_t tmem = *tslot;
     const uint32_t tlane = tmem + ((uint32_t)(32 * quad) << 16);
 
-    UnitLoc cur = locate(*s_next);
+    UnitLoc cur = *s_next;
     if (cur.valid) {
         stage_early(cur);
         stage_late(cur);
@@ -457,18 +455,19 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(ChunkArgs args,
         for (int q = 0; q < 4; ++q) st8(sm + P_SV, 0, ch, 32 * hh + 8 * q, vv + 8 * q);
         fence_after_sync();
 
-        // ---- 5: A_kk (fp32) and A_qk (fp16) from TMEM; the next unit's number
-        if (tid == 0) grab();
+        // ---- 5: A_kk (fp32) and A_qk (fp16) from TMEM
         extract_pairs(sm + P_AQK, &akk[0][0], sbeta, dqk, tlane, P_TM_A, tid, warp, lane);
         fence_before_sync();
         __syncthreads();
 
-        // ---- 6: T' = (I + A_kk)^-1 diag(beta)
+        // ---- 6: T' = (I + A_kk)^-1 diag(beta); a warp that sits out the
+        // inverse's first phase takes and locates the next unit meanwhile
+        if (tid == 4 * 32) grab_locate();
         chunk_inverse(akk, Tf, sbeta, sm + P_TP, tid, warp, lane);
         fence_async_smem();
         fence_before_sync();
         __syncthreads();
-        const UnitLoc nxt = locate(*s_next);
+        const UnitLoc nxt = *s_next;
         if (nxt.valid) stage_early(nxt);                   // into the dead q, k, f, A_kk, T
 
         // ---- 7: W^T = X'^T T'^T, U^T = V^T T'^T
