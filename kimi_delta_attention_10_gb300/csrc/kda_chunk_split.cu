@@ -232,7 +232,8 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(ChunkArgs args,
     // [0..2] pair rounds, [3] W/U, [4] drain after a failure
     uint64_t* bar = reinterpret_cast<uint64_t*>(sm + P_BAR);
     uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + P_BAR + 48);
-    UnitLoc* s_next = reinterpret_cast<UnitLoc*>(sm + P_BAR + 64);
+    // [0] the CTA's first unit, [1] the unit after the current one
+    UnitLoc* s_loc = reinterpret_cast<UnitLoc*>(sm + P_BAR + 64);
     // test hook: CTA 0 withholds its first MMA group and the commit that signals it
     const bool withhold = args.fault == KDA_TEST_FAULT_PREP && blockIdx.x == 0;
 
@@ -248,8 +249,9 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(ChunkArgs args,
 
     // The next unit of this window, taken from its counter and located in the
     // packed input by one thread (its dependent loads of the offsets run while
-    // the other warps work); the rest read it after a barrier.
-    auto grab_locate = [&]() {
+    // the CTA waits for the current unit's staging); the rest read it after a
+    // barrier.
+    auto grab_locate = [&](UnitLoc* slot) {
         const int64_t c = atomicAdd(ctr, 1);
         UnitLoc u{unit_base + c, 0, 0, 0, 0};
         const int32_t gc = (int32_t)(u.unit / H);
@@ -266,7 +268,7 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(ChunkArgs args,
             u.t0 = bos + (gc - off[lo]) * C;
             u.L = min(C, eos - u.t0);
         }
-        *s_next = u;
+        *slot = u;
     };
     auto stage16 = [&](uint32_t so, const TIn* base, const UnitLoc& u) {
 #pragma unroll
@@ -311,7 +313,7 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(ChunkArgs args,
     if (tid == 0) {
         for (int b = 0; b < 5; ++b) mbar_init(&bar[b], 1);
         fence_mbar_init();
-        grab_locate();
+        grab_locate(&s_loc[0]);
     }
     fence_before_sync();
     __syncthreads();
@@ -319,7 +321,7 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(ChunkArgs args,
     const uint32_t tmem = *tslot;
     const uint32_t tlane = tmem + ((uint32_t)(32 * quad) << 16);
 
-    UnitLoc cur = *s_next;
+    UnitLoc cur = s_loc[0];
     if (cur.valid) {
         stage_early(cur);
         stage_late(cur);
@@ -389,6 +391,7 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(ChunkArgs args,
             }
             sbeta[tid] = xb;
         }
+        if (tid == 4 * 32) grab_locate(&s_loc[1]);          // read after the inverse
         cp_async_wait_all();
         __syncthreads();
 
@@ -460,14 +463,12 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(ChunkArgs args,
         fence_before_sync();
         __syncthreads();
 
-        // ---- 6: T' = (I + A_kk)^-1 diag(beta); a warp that sits out the
-        // inverse's first phase takes and locates the next unit meanwhile
-        if (tid == 4 * 32) grab_locate();
+        // ---- 6: T' = (I + A_kk)^-1 diag(beta)
         chunk_inverse(akk, Tf, sbeta, sm + P_TP, tid, warp, lane);
         fence_async_smem();
         fence_before_sync();
         __syncthreads();
-        const UnitLoc nxt = *s_next;
+        const UnitLoc nxt = s_loc[1];
         if (nxt.valid) stage_early(nxt);                   // into the dead q, k, f, A_kk, T
 
         // ---- 7: W^T = X'^T T'^T, U^T = V^T T'^T
