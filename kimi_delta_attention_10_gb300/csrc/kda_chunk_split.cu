@@ -897,6 +897,312 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) chunk_scan_kernel(ChunkArgs a
     if (warp == 0) tmem_dealloc(tmem, S_TM_COLS);
 }
 
+// 32 consecutive output values of one row (16-byte stores; the row piece is
+// 64-byte aligned for BF16 and 128-byte aligned for FP32).
+__device__ __forceinline__ void store_row32(float* p, const float (&o)[32])
+{
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+        reinterpret_cast<float4*>(p)[q] = make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+}
+__device__ __forceinline__ void store_row32(__nv_bfloat16* p, const float (&o)[32])
+{
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        uint4 w;
+        uint32_t* wp = reinterpret_cast<uint32_t*>(&w);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const __nv_bfloat162 b2 = __floats2bfloat162_rn(o[8 * q + 2 * e], o[8 * q + 2 * e + 1]);
+            wp[e] = *reinterpret_cast<const uint32_t*>(&b2);
+        }
+        reinterpret_cast<uint4*>(p)[q] = w;
+    }
+}
+
+// ---------------------------------------------------------------- scan, V in halves
+// The recurrence is separable in the columns of the state (every column of S
+// evolves with the same W, Q', K'', A_qk and decay, and only its own column of
+// U), so each (sequence, head) is scanned by two CTAs, one per half of V (64
+// columns each).  Per chunk c, in TMEM region R = 128 (c & 1):
+//   control:  D1 = [W; Q'] S_v (8 MMAs, M = 128: rows 0..63 W S, 64..127 Q' S),
+//             commit d1_done
+//   epilogue (warps of lanes 0..63): Delta = U_v - W S_v -> shared (fp16),
+//             arrive delta_ready
+//   control:  P = K''^T Delta (4 MMAs) into R + 64, commit p_done; then
+//             D1 += [any; A_qk] Delta (4 MMAs; its rows 0..63 are dead), commit
+//             o_done
+//   epilogue (all warps): S_v <- Diag(d) S_v + P and its fp16 copy, arrive
+//             s_ready; then the warps of lanes 64..127 read O once o_done has
+//             come, arrive o_read and store the chunk's outputs
+// so the state's chain per chunk is D1 -> Delta -> P -> S, with half the
+// columns of the full-width scan per CTA; the control warp waits for o_read of
+// chunk c - 2 before it writes region (c & 1) again.
+constexpr int VH = 64;                        // state columns per CTA
+constexpr uint32_t V_ST = 0;                  // S_v fp16 MN-major [128 c][64 v]
+constexpr uint32_t V_DT = 16384;              // Delta fp16 MN-major [64 i][64 v]
+constexpr uint32_t V_STG = 24576;             // two record stages
+constexpr uint32_t V_BAR = V_STG + 2 * S_STG_STRIDE;   // 9 mbarriers, TMEM slot, abort flag
+constexpr uint32_t V_SMEM = V_BAR + 128 + 1024;
+static_assert(V_SMEM <= 232448, "shared memory budget of the V-half scan");
+constexpr uint32_t V_TM_D1 = 0, V_TM_P = 64, V_TM_REGION = 128, V_TM_COLS = 256;
+constexpr uint32_t kDeltaBar = 2;             // named barrier of the four Delta warps
+
+template <typename TOut>
+__global__ void __launch_bounds__(SCAN_THREADS, 1) chunk_scan_vh_kernel(ChunkArgs args,
+                                                                        const int32_t* __restrict__ hdr,
+                                                                        const unsigned char* __restrict__ records,
+                                                                        ScanWindow win)
+{
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    const uint32_t raw_s = smem_u32(smem_raw);
+    const uint32_t pad = (1024u - (raw_s & 1023u)) & 1023u;
+    unsigned char* sm = smem_raw + pad;
+    const uint32_t sb = raw_s + pad;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const bool ctrl = warp == NT / 32;
+    const int quad = warp & 3, half = (warp >> 2) & 1;
+    const int row = 32 * quad + lane;                      // TMEM lane
+    const bool dwarp = quad < 2;                           // lanes 0..63: W S rows -> Delta
+    const int H = args.H;
+    const int vh = blockIdx.x & 1;                         // this CTA's half of V
+    const int hb = blockIdx.x >> 1;
+    const int n = hdr[kHdrOff + args.N + 1 + hb / H], h = hb % H;
+    launch_dependents();
+
+    const int eos = args.cu_seqlens[n + 1];
+    int bos = args.cu_seqlens[n];
+    if (bos < 0 || eos < bos || (int64_t)eos > args.T) return;   // reported by the plan
+    const int nch_all = (eos - bos + C - 1) / C;
+    const int offn = hdr[kHdrOff + n];
+    const int cb = min(max(win.g0 - offn, 0), nch_all), ce = min(max(win.g1 - offn, 0), nch_all);
+    const bool writes_final = (cb < ce && ce == nch_all) || (nch_all == 0 && win.last);
+    if (cb == ce && !writes_final) return;
+    const float* state_in = cb == 0 ? args.initial_state : win.carry;
+    float* state_out = writes_final ? args.final_state : win.carry;
+    bos += cb * C;
+    const int nch = ce - cb;
+    const int64_t rstride = (int64_t)H * REC_BYTES;
+    const unsigned char* rec0 = records + ((int64_t)(offn + cb) * H + h) * REC_BYTES;
+    TOut* __restrict__ out = static_cast<TOut*>(args.out);
+    const int v0 = VH * vh + 32 * half;                    // this thread's first column of V
+    // [0,1] record stages, [2] d1_done, [3] p_done, [4] delta_ready (128),
+    // [5] s_ready (NT), [6] drain after a failure, [7] o_done, [8] o_read (128)
+    uint64_t* bar = reinterpret_cast<uint64_t*>(sm + V_BAR);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + V_BAR + 80);
+    volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(sm + V_BAR + 84);
+
+    // ---- the entering state: S[c][v0 .. v0 + 31] of state row c = this thread's lane
+    float S[32];
+    if (!ctrl) {
+        if (state_in != nullptr) {
+            const float4* s0 = reinterpret_cast<const float4*>(
+                state_in + (((int64_t)n * H + h) * DK + row) * DV + v0);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const float4 x = s0[q];
+                S[4 * q] = x.x; S[4 * q + 1] = x.y; S[4 * q + 2] = x.z; S[4 * q + 3] = x.w;
+            }
+        } else {
+#pragma unroll
+            for (int u = 0; u < 32; ++u) S[u] = 0.f;
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) st8(sm + V_ST, 0, row, 32 * half + 8 * q, S + 8 * q);
+    }
+    if (warp == 0) {
+        tmem_alloc(tslot, V_TM_COLS);
+        tmem_relinquish();
+    }
+    if (tid == 0) {
+        for (int b = 0; b < 9; ++b)
+            mbar_init(&bar[b], (b == 4 || b == 8) ? NT / 2 : b == 5 ? NT : 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    fence_async_smem();
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tmem = *tslot;
+    const uint32_t tlane = tmem + ((uint32_t)(32 * quad) << 16);
+
+    auto wait_or_abort = [&](uint64_t* m, uint32_t parity) -> bool {
+        for (uint32_t j = 0; j < kPollsPerCheck; ++j)
+            if (mbar_try_wait(m, parity)) return true;
+        const uint64_t t0 = globaltimer_ns();
+        for (uint32_t i = 0; i < kMaxTimerChecks; ++i) {
+            for (uint32_t j = 0; j < kPollsPerCheck; ++j)
+                if (mbar_try_wait(m, parity)) return true;
+            if (*abort_flag) return false;
+            if (globaltimer_ns() - t0 > kWaitLimitNs) break;
+        }
+        *abort_flag = 1;
+        return false;
+    };
+
+    if (ctrl) {
+        if (lane == 0) {
+            auto issue_load = [&](int c) {
+                unsigned char* stage = sm + V_STG + (c & 1) * S_STG_STRIDE;
+                mbar_arrive_expect_tx(&bar[c & 1], REC_BYTES);
+                bulk_g2s(stage, rec0 + c * rstride, REC_BYTES, &bar[c & 1]);
+            };
+            for (int c = 0; c < min(2, nch); ++c) issue_load(c);
+            for (int c = 2; c < min(kL2Ahead, nch); ++c) bulk_prefetch_l2(rec0 + c * rstride, REC_BYTES);
+            int issued = min(2, nch), c = 0;
+            bool fail = false, any_mma = false;
+            constexpr uint32_t id_d1 = idesc(kFmtF16, 128, VH, true, true);
+            constexpr uint32_t id_pv = idesc(kFmtF16, 128, VH, false, true);
+            for (; c < nch; ++c) {
+                const uint32_t R = tmem + V_TM_REGION * (c & 1);
+                const uint32_t sst = sb + V_STG + (c & 1) * S_STG_STRIDE;
+                if (!wait_or_abort(&bar[c & 1], (c >> 1) & 1)) { fail = true; break; }
+                // chunk c - 1's state is current; chunk c - 2's O has left region (c & 1)
+                if (c > 0 && !wait_or_abort(&bar[5], (c - 1) & 1)) { fail = true; break; }
+                if (c > 1 && !wait_or_abort(&bar[8], (c - 2) & 1)) { fail = true; break; }
+                fence_after_sync();
+#pragma unroll
+                for (int s = 0; s < 8; ++s)
+                    mma_f16(R + V_TM_D1, desc_mnmajor128(sst + REC_W, 16384, s),
+                            desc_mnmajor64(sb + V_ST, s), id_d1, s > 0);
+                commit(&bar[2]);
+                any_mma = true;
+                if (c > 0 && c + 1 < nch) {
+                    issue_load(c + 1);
+                    issued = c + 2;
+                }
+                if (c + kL2Ahead < nch) bulk_prefetch_l2(rec0 + (c + kL2Ahead) * rstride, REC_BYTES);
+                if (!wait_or_abort(&bar[4], c & 1)) { fail = true; break; }
+                fence_after_sync();
+#pragma unroll
+                for (int s = 0; s < 4; ++s)
+                    mma_f16(R + V_TM_P, desc_kmajor(sst + REC_KT, 128, s),
+                            desc_mnmajor64(sb + V_DT, s), id_pv, s > 0);
+                commit(&bar[3]);
+                // rows 0..63 of this A operand are the 8 KiB before A_qk in the
+                // record (finite FP16 values of U^T); they add into the dead W S rows
+#pragma unroll
+                for (int s = 0; s < 4; ++s)
+                    mma_f16(R + V_TM_D1, desc_kmajor(sst + REC_AQK - 8192, 128, s),
+                            desc_mnmajor64(sb + V_DT, s), id_pv, 1);
+                commit(&bar[7]);
+            }
+            if (fail) {
+                *abort_flag = 1;
+                report_status(args.status, KDA_ERR_TIMEOUT);
+                if (any_mma) {
+                    commit(&bar[6]);
+                    mbar_wait(&bar[6], 0);
+                }
+                for (int cc = c; cc < issued; ++cc) mbar_wait(&bar[cc & 1], (cc >> 1) & 1);
+            }
+        }
+    } else {
+        float nan_acc = 0.f;
+        // test hook: CTA 0 withholds its first delta_ready arrival
+        const bool withhold = args.fault == KDA_TEST_FAULT_SCAN && blockIdx.x == 0;
+        bool fail = false;
+        for (int c = 0; c < nch; ++c) {
+            const uint32_t R = tlane + V_TM_REGION * (c & 1);
+            unsigned char* stage = sm + V_STG + (c & 1) * S_STG_STRIDE;
+            __half2 u2[16];                                // U[i][v0 .. v0 + 31] (Delta warps)
+            {
+                // (an O warp that gave up on the previous chunk carries `fail` here)
+                const bool ok = !fail && wait_or_abort(&bar[c & 1], (c >> 1) & 1);
+                if (named_sync_or(kEpiBar, NT, !ok)) { fail = true; break; }
+            }
+            if (dwarp) {
+                // U from the record's U^T [v][i] tile, read down a column while D1 runs
+                const unsigned char* up = stage + REC_U;
+#pragma unroll
+                for (int u = 0; u < 16; ++u) {
+                    const __half lo = *reinterpret_cast<const __half*>(up + sw128(v0 + 2 * u, 2 * row));
+                    const __half hi = *reinterpret_cast<const __half*>(up + sw128(v0 + 2 * u + 1, 2 * row));
+                    u2[u] = __halves2half2(lo, hi);
+                }
+                bool ok = wait_or_abort(&bar[2], c & 1);
+                if (named_sync_or(kDeltaBar, NT / 2, !ok)) {
+                    fail = true;                           // the others see the abort flag
+                } else {
+                    fence_after_sync();
+                    // Delta[i][v] = U[i][v] - (W S)[i][v], fp16 MN-major
+                    float ws[32], dl[32];
+                    tmem_ld32(R + V_TM_D1 + 32 * half, ws);
+#pragma unroll
+                    for (int u = 0; u < 16; ++u) {
+                        const float2 uf = __half22float2(u2[u]);
+                        dl[2 * u] = uf.x - ws[2 * u];
+                        dl[2 * u + 1] = uf.y - ws[2 * u + 1];
+                    }
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) st8(sm + V_DT, 0, row, 32 * half + 8 * q, dl + 8 * q);
+                    fence_async_smem();
+                    fence_before_sync();
+                    if (!(withhold && c == 0)) mbar_arrive(&bar[4]);
+                }
+            }
+            {
+                const bool ok = !fail && wait_or_abort(&bar[3], c & 1);
+                if (named_sync_or(kEpiBar, NT, !ok)) { fail = true; break; }
+            }
+            fence_after_sync();
+            {
+                // S_v <- Diag(d) S_v + P;  fp16 copy of S_v for the next chunk
+                const float dc = reinterpret_cast<const float*>(stage + REC_DEC)[row];
+                float p[32];
+                tmem_ld32(R + V_TM_P + 32 * half, p);
+#pragma unroll
+                for (int u = 0; u < 32; ++u) S[u] = fmaf(S[u], dc, p[u]);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) st8(sm + V_ST, 0, row, 32 * half + 8 * q, S + 8 * q);
+            }
+            fence_async_smem();
+            fence_before_sync();
+            mbar_arrive(&bar[5]);
+            if (!dwarp) {
+                // O rows (token i = row - 64) leave TMEM, then go out from registers
+                const bool ok = wait_or_abort(&bar[7], c & 1);
+                float o[32];
+                if (ok) {
+                    fence_after_sync();
+                    tmem_ld32(R + V_TM_D1 + 32 * half, o);
+                    fence_before_sync();
+                    mbar_arrive(&bar[8]);
+                    const int i = row - 64, t = bos + c * C + i;
+                    if (t < eos) {
+                        TOut* op = out + ((int64_t)t * H + h) * DV + v0;
+#pragma unroll
+                        for (int u = 0; u < 32; ++u) {
+                            o[u] *= args.scale;
+                            nan_acc = fmaf(o[u], 0.f, nan_acc);
+                        }
+                        store_row32(op, o);
+                    }
+                } else {
+                    fail = true;                           // seen at the next chunk's barrier
+                }
+            }
+        }
+        if (fail) {
+            *abort_flag = 1;
+            if (tid == 0) report_status(args.status, KDA_ERR_TIMEOUT);
+        } else if (state_out != nullptr) {
+            float4* fs = reinterpret_cast<float4*>(state_out + (((int64_t)n * H + h) * DK + row) * DV + v0);
+#pragma unroll
+            for (int u = 0; u < 32; ++u) nan_acc = fmaf(S[u], 0.f, nan_acc);
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                fs[q] = make_float4(S[4 * q], S[4 * q + 1], S[4 * q + 2], S[4 * q + 3]);
+        }
+        if (nan_acc != nan_acc) report_status(args.status, KDA_ERR_RANGE);
+    }
+    fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, V_TM_COLS);
+}
+
 // ---------------------------------------------------------------- launch
 template <typename TIn, int kGate>
 cudaError_t launch_prep_typed(const ChunkArgs& a, const int32_t* hdr, unsigned char* rec,
@@ -947,6 +1253,17 @@ cudaError_t launch_prep(const ChunkArgs& a, const int32_t* hdr, unsigned char* r
 cudaError_t launch_scan(const ChunkArgs& a, const int32_t* hdr, const unsigned char* rec,
                         ScanWindow win, cudaStream_t stream)
 {
+    if (!a.out_norm) {
+        // plain output: two CTAs per (sequence, head), one per half of V
+        auto kv = a.out_bf16 ? chunk_scan_vh_kernel<__nv_bfloat16> : chunk_scan_vh_kernel<float>;
+        cudaError_t e = cudaFuncSetAttribute(kv, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)V_SMEM);
+        if (e != cudaSuccess) return e;
+        kv<<<(unsigned)(2 * (int64_t)a.N * a.H), SCAN_THREADS, V_SMEM, stream>>>(a, hdr, rec, win);
+        return cudaGetLastError();
+    }
+    // the output gate fused into the output store needs whole rows of V: one
+    // CTA per (sequence, head)
     auto kern = a.out_norm ? (a.out_bf16 ? chunk_scan_kernel<__nv_bfloat16, true>
                                          : chunk_scan_kernel<float, true>)
                            : (a.out_bf16 ? chunk_scan_kernel<__nv_bfloat16, false>
@@ -1048,8 +1365,9 @@ cudaError_t launch_chunk_split(const ChunkArgs& a, int64_t chunks, bool overlap,
     if (e != cudaSuccess) return e;
 
     const int sms = device_sm_count();
+    const int64_t scan_ctas = (a.out_norm ? 1 : 2) * (int64_t)a.N * a.H;
     int W = 1;
-    if (overlap && (int64_t)a.N * a.H <= (sms > 0 ? sms : 152))
+    if (overlap && scan_ctas <= (sms > 0 ? sms : 152))
         W = (int)std::min<int64_t>(kMaxWindows, chunks / kWindowChunks);
     int32_t* ctr = window_counters(hdr, a.N);
     if (W <= 1) {
