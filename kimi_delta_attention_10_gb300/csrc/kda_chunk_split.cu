@@ -936,13 +936,17 @@ __device__ __forceinline__ void store_row32(__nv_bfloat16* p, const float (&o)[3
 //             s_ready; then the warps of lanes 64..127 read O once o_done has
 //             come, arrive o_read and store the chunk's outputs
 // so the state's chain per chunk is D1 -> Delta -> P -> S, with half the
-// columns of the full-width scan per CTA; the control warp waits for o_read of
-// chunk c - 2 before it writes region (c & 1) again.
+// columns of the full-width scan per CTA.  The control warp waits for o_read
+// of chunk c - 2 before it writes region (c & 1) again, and for o_done of
+// chunk c - 1 before it refills that chunk's record stage.  o_read has one
+// barrier per chunk parity: the O warps may have finished chunk c - 1 as well
+// when the control asks about chunk c - 2, and a single barrier two phases
+// ahead of its waiter would make the parity wait ambiguous.
 constexpr int VH = 64;                        // state columns per CTA
 constexpr uint32_t V_ST = 0;                  // S_v fp16 MN-major [128 c][64 v]
 constexpr uint32_t V_DT = 16384;              // Delta fp16 MN-major [64 i][64 v]
 constexpr uint32_t V_STG = 24576;             // two record stages
-constexpr uint32_t V_BAR = V_STG + 2 * S_STG_STRIDE;   // 9 mbarriers, TMEM slot, abort flag
+constexpr uint32_t V_BAR = V_STG + 2 * S_STG_STRIDE;   // 10 mbarriers, TMEM slot, abort flag
 constexpr uint32_t V_SMEM = V_BAR + 128 + 1024;
 static_assert(V_SMEM <= 232448, "shared memory budget of the V-half scan");
 constexpr uint32_t V_TM_D1 = 0, V_TM_P = 64, V_TM_REGION = 128, V_TM_COLS = 256;
@@ -988,7 +992,8 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) chunk_scan_vh_kernel(ChunkArg
     TOut* __restrict__ out = static_cast<TOut*>(args.out);
     const int v0 = VH * vh + 32 * half;                    // this thread's first column of V
     // [0,1] record stages, [2] d1_done, [3] p_done, [4] delta_ready (128),
-    // [5] s_ready (NT), [6] drain after a failure, [7] o_done, [8] o_read (128)
+    // [5] s_ready (NT), [6] drain after a failure, [7] o_done, [8,9] o_read of
+    // even and odd chunks (128)
     uint64_t* bar = reinterpret_cast<uint64_t*>(sm + V_BAR);
     uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + V_BAR + 80);
     volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(sm + V_BAR + 84);
@@ -1016,8 +1021,8 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) chunk_scan_vh_kernel(ChunkArg
         tmem_relinquish();
     }
     if (tid == 0) {
-        for (int b = 0; b < 9; ++b)
-            mbar_init(&bar[b], (b == 4 || b == 8) ? NT / 2 : b == 5 ? NT : 1);
+        for (int b = 0; b < 10; ++b)
+            mbar_init(&bar[b], (b == 4 || b >= 8) ? NT / 2 : b == 5 ? NT : 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -1061,7 +1066,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) chunk_scan_vh_kernel(ChunkArg
                 if (!wait_or_abort(&bar[c & 1], (c >> 1) & 1)) { fail = true; break; }
                 // chunk c - 1's state is current; chunk c - 2's O has left region (c & 1)
                 if (c > 0 && !wait_or_abort(&bar[5], (c - 1) & 1)) { fail = true; break; }
-                if (c > 1 && !wait_or_abort(&bar[8], (c - 2) & 1)) { fail = true; break; }
+                if (c > 1 && !wait_or_abort(&bar[8 + (c & 1)], ((c - 2) >> 1) & 1)) { fail = true; break; }
                 fence_after_sync();
 #pragma unroll
                 for (int s = 0; s < 8; ++s)
@@ -1070,6 +1075,9 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) chunk_scan_vh_kernel(ChunkArg
                 commit(&bar[2]);
                 any_mma = true;
                 if (c > 0 && c + 1 < nch) {
+                    // stage (c + 1) & 1 held chunk c - 1, whose last MMA group
+                    // (A_qk Delta, signalled by o_done) must be done reading it
+                    if (!wait_or_abort(&bar[7], (c - 1) & 1)) { fail = true; break; }
                     issue_load(c + 1);
                     issued = c + 2;
                 }
@@ -1169,7 +1177,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) chunk_scan_vh_kernel(ChunkArg
                     fence_after_sync();
                     tmem_ld32(R + V_TM_D1 + 32 * half, o);
                     fence_before_sync();
-                    mbar_arrive(&bar[8]);
+                    mbar_arrive(&bar[8 + (c & 1)]);
                     const int i = row - 64, t = bos + c * C + i;
                     if (t < eos) {
                         TOut* op = out + ((int64_t)t * H + h) * DV + v0;
