@@ -177,13 +177,11 @@ def backward_bytes(T, H, K, V, N, qkv_bytes, dout_bytes):
     return T * H * per_token_head + 2 * N * H * K * V * 4
 
 
-def chunk_windows(N, H, chunks, sms, scan_ctas_per_head=2):
+def chunk_windows(N, H, chunks, sms):
     """Chunk windows of one two-phase kda_chunk_fwd call: min(4, chunks // 32)
-    when the scan's CTAs (two per (sequence, head), one per half of V; one with
-    the output gate fused) number at most the SM count (the rule in
-    kda_chunk_split.cu), else one.  The call launches the plan, then one
-    preparation and one scan per window."""
-    if scan_ctas_per_head * N * H <= sms:
+    when N * H <= the SM count (the rule in kda_chunk_split.cu), else one.
+    The call launches the plan, then one preparation and one scan per window."""
+    if N * H <= sms:
         return max(1, min(4, chunks // 32))
     return 1
 
@@ -608,8 +606,7 @@ def main():
         variant = "two_phase" if two_phase else ("single_pass" if mode == "bf16_tc" else mode)
         kernel_key = f"{kname}:{variant}:{w.name}"
         windows = chunk_windows(N, H, sum(-(-L // 64) for L in x.seqlens),
-                                torch.cuda.get_device_properties(dev).multi_processor_count,
-                                1 if (args.output_gate and args.fused) else 2)
+                                torch.cuda.get_device_properties(dev).multi_processor_count)
         what = {"two_phase": f"two-phase call: plan, then chunk preparation and state scan "
                              f"in {windows} chunk window(s)",
                 "single_pass": "single-pass kernel"}.get(variant, "FP32-exact kernel")

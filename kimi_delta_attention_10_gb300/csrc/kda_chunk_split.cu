@@ -1259,9 +1259,9 @@ cudaError_t launch_prep(const ChunkArgs& a, const int32_t* hdr, unsigned char* r
 }
 
 cudaError_t launch_scan(const ChunkArgs& a, const int32_t* hdr, const unsigned char* rec,
-                        ScanWindow win, cudaStream_t stream)
+                        ScanWindow win, bool halves, cudaStream_t stream)
 {
-    if (!a.out_norm) {
+    if (halves) {
         // plain output: two CTAs per (sequence, head), one per half of V
         auto kv = a.out_bf16 ? chunk_scan_vh_kernel<__nv_bfloat16> : chunk_scan_vh_kernel<float>;
         cudaError_t e = cudaFuncSetAttribute(kv, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1372,16 +1372,22 @@ cudaError_t launch_chunk_split(const ChunkArgs& a, int64_t chunks, bool overlap,
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
 
-    const int sms = device_sm_count();
-    const int64_t scan_ctas = (a.out_norm ? 1 : 2) * (int64_t)a.N * a.H;
-    int W = 1;
-    if (overlap && scan_ctas <= (sms > 0 ? sms : 152))
-        W = (int)std::min<int64_t>(kMaxWindows, chunks / kWindowChunks);
+    const int sms = device_sm_count() > 0 ? device_sm_count() : 152;
+    const int64_t heads = (int64_t)a.N * a.H;
+    const int64_t W_shape = heads <= sms ? std::min<int64_t>(kMaxWindows, chunks / kWindowChunks) : 1;
+    const int W = overlap ? (int)std::max<int64_t>(W_shape, 1) : 1;
+    // The scan in V halves shortens the state's chain but streams the records
+    // twice as fast and holds twice the SMs: it pays only for problems too
+    // short for windows whose CTAs fit the GPU at once.  Windowed problems keep
+    // the full-width scan (so that the preparation beside it keeps more SMs),
+    // also when run in one window (kda_chunk_fwd_static): the choice depends on
+    // the problem's shape alone, so both entry points give the same bits.
+    const bool halves = !a.out_norm && W_shape <= 1 && 2 * heads <= sms;
     int32_t* ctr = window_counters(hdr, a.N);
     if (W <= 1) {
         e = launch_prep(a, hdr, rec, 0, units, ctr, false, stream);
         if (e != cudaSuccess) return e;
-        return launch_scan(a, hdr, rec, ScanWindow{0, INT32_MAX, nullptr, 1}, stream);
+        return launch_scan(a, hdr, rec, ScanWindow{0, INT32_MAX, nullptr, 1}, halves, stream);
     }
     for (int w = 0; w < W && e == cudaSuccess; ++w) {
         const int32_t g0 = (int32_t)window_bound(chunks, W, w);
@@ -1389,7 +1395,7 @@ cudaError_t launch_chunk_split(const ChunkArgs& a, int64_t chunks, bool overlap,
         e = launch_prep(a, hdr, rec, (int64_t)g0 * a.H, (int64_t)(g1 - g0) * a.H, ctr + w, w > 0,
                         stream);
         const ScanWindow win{g0, w + 1 == W ? INT32_MAX : g1, carry, w + 1 == W ? 1 : 0};
-        if (e == cudaSuccess) e = launch_scan(a, hdr, rec, win, stream);
+        if (e == cudaSuccess) e = launch_scan(a, hdr, rec, win, halves, stream);
     }
     return e;
 }

@@ -81,22 +81,18 @@ def test_chunk_windows_rule():
     assert bench.chunk_windows(1, 64, 32, 152) == 1           # 2048 tokens: one window
     assert bench.chunk_windows(16, 64, 520, 152) == 1         # 1024 scan CTAs fill the GPU
     assert bench.chunk_windows(1, 2, 66, 152) == 2
-    assert bench.chunk_windows(1, 76, 256, 152) == 4          # 152 V-half scan CTAs
-    assert bench.chunk_windows(1, 77, 256, 152) == 1
-    assert bench.chunk_windows(1, 77, 256, 152, scan_ctas_per_head=1) == 4
 
 
 def test_chunk_windows_mirror_matches_the_library_constants():
     """bench.chunk_windows restates the window rule of kda_chunk_split.cu
-    (min(kMaxWindows, chunks / kWindowChunks) when the scan's CTAs, two per
-    (sequence, head) or one with the output gate fused, fit the SM count)."""
+    (min(kMaxWindows, chunks / kWindowChunks) when N * H <= the SM count)."""
     import re
     src = open(os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
                             "kimi_delta_attention_10_gb300", "csrc", "kda_chunk_split.cu")).read()
     max_w = int(re.search(r"constexpr int kMaxWindows = (\d+);", src).group(1))
     per_w = int(re.search(r"constexpr int kWindowChunks = (\d+);", src).group(1))
-    assert "const int64_t scan_ctas = (a.out_norm ? 1 : 2) * (int64_t)a.N * a.H;" in src
-    assert "overlap && scan_ctas <= (sms > 0 ? sms : 152)" in src
+    assert ("const int64_t W_shape = heads <= sms ? std::min<int64_t>(kMaxWindows, chunks / "
+            "kWindowChunks) : 1;") in src
     for chunks in (0, 31, 32, 63, 64, 100, 256, 10000):
         assert bench.chunk_windows(1, 64, chunks, 152) == max(1, min(max_w, chunks // per_w))
     assert bench.chunk_windows(3, 64, 10000, 152) == 1

@@ -31,11 +31,18 @@ def _call(d, g, beta, x, workspace):
     return out.clone(), S.clone(), int(status[0])
 
 
-@pytest.mark.parametrize("where,workspace", [(KDA_TEST_FAULT_SCAN, "auto"),
-                                             (KDA_TEST_FAULT_PREP, "auto"),
-                                             (KDA_TEST_FAULT_SINGLE_PASS, None)])
-def test_lost_arrival_times_out_and_the_next_call_is_clean(where, workspace):
-    x = make_inputs([300, 77], 2, 128, 128, torch.bfloat16, 71)
+# (fault, workspace, lengths, heads): the short problem runs the scan in V
+# halves, the 8192-token one the full-width scan in four chunk windows (its CTA
+# 0 gives up once per window)
+CASES = [(KDA_TEST_FAULT_SCAN, "auto", [300, 77], 2),
+         (KDA_TEST_FAULT_SCAN, "auto", [8192], 1),
+         (KDA_TEST_FAULT_PREP, "auto", [300, 77], 2),
+         (KDA_TEST_FAULT_SINGLE_PASS, None, [300, 77], 2)]
+
+
+@pytest.mark.parametrize("where,workspace,lens,H", CASES)
+def test_lost_arrival_times_out_and_the_next_call_is_clean(where, workspace, lens, H):
+    x = make_inputs(lens, H, 128, 128, torch.bfloat16, 71)
     d = device_inputs(x)
     g, beta = kda_gate(d["f"], d["A_log"], d["dt_bias"], d["b"])
     o_ref, S_ref, st = _call(d, g, beta, x, workspace)
