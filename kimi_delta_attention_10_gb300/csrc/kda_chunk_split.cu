@@ -171,7 +171,7 @@ constexpr uint32_t P_RK = P_RQ + 256;  // 1/|k_t|
 constexpr uint32_t P_DQK = P_RK + 256; // q^_t . k^_t
 constexpr uint32_t P_BETA = P_DQK + 256;
 constexpr uint32_t P_TOT = P_BETA + 256;   // half-chunk decay fp32 [2][128]
-constexpr uint32_t P_BAR = P_TOT + 1024;   // 5 mbarriers, TMEM slot, the next unit
+constexpr uint32_t P_BAR = P_TOT + 1024;   // 8 mbarriers, TMEM slot, the next units
 constexpr uint32_t P_SMEM = P_BAR + 128 + 1024;
 static_assert(P_TF + C * LDA * 4 <= P_XT, "A_kk and T fit below X'^T");
 static_assert(P_PAIR + 49152 <= P_XT, "pair-sum operands fit below X'^T");
@@ -229,11 +229,12 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(ChunkArgs args,
     float* dqk = reinterpret_cast<float*>(sm + P_DQK);
     float* sbeta = reinterpret_cast<float*>(sm + P_BETA);
     float* tot = reinterpret_cast<float*>(sm + P_TOT);
-    // [0..2] pair rounds, [3] W/U, [4] drain after a failure
+    // [0..2] pair rounds, [3] W/U, [4] drain after a failure, [5..7] the
+    // operands of pair round 0..2 written (every thread arrives)
     uint64_t* bar = reinterpret_cast<uint64_t*>(sm + P_BAR);
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + P_BAR + 48);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + P_BAR + 64);
     // [0] the CTA's first unit, [1] the unit after the current one
-    UnitLoc* s_loc = reinterpret_cast<UnitLoc*>(sm + P_BAR + 64);
+    UnitLoc* s_loc = reinterpret_cast<UnitLoc*>(sm + P_BAR + 80);
     // test hook: CTA 0 withholds its first MMA group and the commit that signals it
     const bool withhold = args.fault == KDA_TEST_FAULT_PREP && blockIdx.x == 0;
 
@@ -311,7 +312,7 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(ChunkArgs args,
         tmem_relinquish();
     }
     if (tid == 0) {
-        for (int b = 0; b < 5; ++b) mbar_init(&bar[b], 1);
+        for (int b = 0; b < 8; ++b) mbar_init(&bar[b], b >= 5 ? NT : 1);
         fence_mbar_init();
         grab_locate(&s_loc[0]);
     }
@@ -329,22 +330,35 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(ChunkArgs args,
     bool failed = false;
     uint32_t ph = 0;                                       // each barrier completes once per unit
     constexpr uint32_t id_pairs = idesc(kFmtF16, 128, 64, true, true);
+    // A pair round: every thread arrives once its operand rows are written, and
+    // only the issuing thread waits for the arrivals; the others go on at once.
     auto issue_round = [&](int rnd) {
         fence_async_smem();
         fence_before_sync();
-        __syncthreads();
+        mbar_arrive(&bar[5 + rnd]);
         if (tid == 0 && !(withhold && rnd == 0)) {
-            fence_after_sync();
+            if (!mbar_wait(&bar[5 + rnd], ph)) {
+                failed = true;                             // no commit: the others time out too
+            } else {
+                fence_after_sync();
 #pragma unroll
-            for (int s = 0; s < 8; ++s)
-                mma_f16(tmem + P_TM_A + 64 * rnd, desc_mnmajor128(sb + P_PAIR, 16384, s),
-                        desc_mnmajor64(sb + P_PAIR + 32768, s), id_pairs, s > 0);
-            commit(&bar[rnd]);
+                for (int s = 0; s < 8; ++s)
+                    mma_f16(tmem + P_TM_A + 64 * rnd, desc_mnmajor128(sb + P_PAIR, 16384, s),
+                            desc_mnmajor64(sb + P_PAIR + 32768, s), id_pairs, s > 0);
+                commit(&bar[rnd]);
+            }
         }
+    };
+    // Each thread waits for a round's MMAs before it overwrites their operands;
+    // a wait that gives up is only recorded here, and the CTA decides together
+    // at the next barrier (a lone thread leaving early would desert the CTA's
+    // later barriers).
+    auto wait_round = [&](int b) {
+        if (!mbar_wait(&bar[b], ph)) failed = true;
     };
     auto wait_bar = [&](int b) -> bool {
         const bool ok = mbar_wait(&bar[b], ph);
-        return __syncthreads_or(!ok) == 0;
+        return __syncthreads_or(failed || !ok) == 0;
     };
 
     while (cur.valid) {
@@ -440,17 +454,17 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(ChunkArgs args,
             if (hh == 0) reinterpret_cast<float*>(rec + REC_DEC)[ch] = tot[ch] * tot[DK + ch];
             channel_rows(sm + P_XT, rec + REC_QP, rec + REC_KT, ch, hh, before, after, a, kh, qh);
         }
-        if (!wait_bar(0)) { failed = true; break; }
+        wait_round(0);
         level_operands<8>(sm + P_PAIR, ch, hh, 0, 0, a, kh, qh);
         level_operands<4>(sm + P_PAIR, ch, hh, 64, 32, a, kh, qh);
         issue_round(1);
         aqk_zero_upper(sm + P_AQK, tid);
-        if (!wait_bar(1)) { failed = true; break; }
+        wait_round(1);
         level_operands<2>(sm + P_PAIR, ch, hh, 0, 0, a, kh, qh);
         level_operands<1>(sm + P_PAIR, ch, hh, 64, 32, a, kh, qh);
         issue_round(2);
         // v column of this thread, read before the barrier that precedes the
-        // in-place V^T writes
+        // in-place V^T writes (which also settles any wait that gave up)
 #pragma unroll
         for (int u = 0; u < 32; ++u) vv[u] = ST::to_f32(sv[(32 * hh + u) * DV + ch]);
         if (!wait_bar(2)) { failed = true; break; }
