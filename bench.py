@@ -67,9 +67,10 @@ def parse_args():
     p.add_argument("--all-workloads", action="store_true",
                    help="one line per workload: the step captured in a CUDA graph, 50 timed "
                         "replays after 10 warm-ups (p50 and max), beside the oracle")
-    p.add_argument("--f-dtype", choices=["auto", "bf16", "f32"], default="auto",
-                   help="dtype of the gate pre-activation f (auto: the workload's activation "
-                        "dtype, i.e. BF16 beside BF16 q/k/v)")
+    p.add_argument("--f-dtype", choices=["f32", "bf16"], default="f32",
+                   help="dtype of the gate pre-activation f: FP32 (the workloads' FP32 decay "
+                        "input, 512 bytes per token-head like an FP32 g) or BF16 (the gate "
+                        "projection's activation dtype, 256 bytes)")
     args = p.parse_args()
     args.fused = not args.unfused
     return args
@@ -299,7 +300,7 @@ def run_all_workloads(args):
     for w in WORKLOADS:
         x = workload_inputs(w)
         T, H, K, V, N = x.T, w.H, w.K, w.V, x.N
-        x.f = x.f.to(x.v.dtype)
+        x.f = x.f.to(torch.bfloat16 if args.f_dtype == "bf16" else torch.float32)
         d = {n: getattr(x, n).to(dev) for n in ("q", "k", "v", "f", "A_log", "dt_bias", "b",
                                                 "cu_seqlens")}
         out_dtype = torch.float32 if mode == "fp32_exact" else x.v.dtype
@@ -399,9 +400,7 @@ def main():
     x = workload_inputs(w)
     T, H, K, V, N = x.T, w.H, w.K, w.V, x.N
     out_dtype = torch.float32 if mode == "fp32_exact" else x.v.dtype
-    f_dtype = {"bf16": torch.bfloat16, "f32": torch.float32}.get(
-        args.f_dtype, torch.bfloat16 if x.v.dtype == torch.bfloat16 else torch.float32)
-    x.f = x.f.to(f_dtype)             # the gate projection's output, in its dtype
+    x.f = x.f.to(torch.bfloat16 if args.f_dtype == "bf16" else torch.float32)
     d = {n: getattr(x, n).to(dev) for n in ("q", "k", "v", "f", "A_log", "dt_bias", "b",
                                             "cu_seqlens")}
     cu_host = x.cu_seqlens.tolist()
