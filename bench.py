@@ -6,10 +6,10 @@ their pre-activations and the chunked KDA forward with the final state, on the
 16384-token, 64-head, K=V=128 BF16 workload by default.  The default step is
 one call of kda_chunk_fwd_gated (the gate fused into the chunk preparation;
 bit for bit the same results as the two calls); --unfused times kda_gate
-followed by kda_chunk_fwd instead.  The BF16 tensor-core path runs in two
-phases through a preallocated workspace (the plan, then chunk preparation and
-state scan per chunk window); --single-pass times the single-pass kernel (no
-workspace) instead.
+followed by kda_chunk_fwd instead.  Both modes run in two phases through a
+preallocated workspace (the plan, then chunk preparation and state scan; the
+BF16 tensor-core path per chunk window); --single-pass times the mode's
+single-pass kernel (no workspace) instead.
 Inputs are resident in HBM when the timed region starts and are larger than
 L2, so no flush is needed between steps.
 
@@ -306,8 +306,8 @@ def run_all_workloads(args):
         out_dtype = torch.float32 if mode == "fp32_exact" else x.v.dtype
         out = torch.empty(T, H, V, dtype=out_dtype, device=dev)
         fs = torch.empty(N, H, K, V, device=dev)
-        ws = (torch.empty(chunk_workspace_size(N, T, H, K, V), dtype=torch.uint8, device=dev)
-              if mode == "bf16_tc" else None)
+        ws = (torch.empty(chunk_workspace_size(N, T, H, K, V, mode=mode), dtype=torch.uint8,
+                          device=dev) if not args.single_pass else None)
         cu_host = x.cu_seqlens.tolist()
 
         def call():
@@ -395,7 +395,7 @@ def main():
     from kimi_delta_attention_10_gb300.inputs import WORKLOAD_BY_NAME, workload_inputs
 
     mode = args.mode or "bf16_tc"
-    two_phase = mode == "bf16_tc" and not args.single_pass
+    two_phase = not args.single_pass
     w = WORKLOAD_BY_NAME[args.workload]
     x = workload_inputs(w)
     T, H, K, V, N = x.T, w.H, w.K, w.V, x.N
@@ -408,8 +408,8 @@ def main():
     beta = torch.empty(T, H, device=dev)
     out = torch.empty(T, H, V, dtype=out_dtype, device=dev)
     fs = torch.empty(N, H, K, V, device=dev)
-    ws = (torch.empty(chunk_workspace_size(N, T, H, K, V), dtype=torch.uint8, device=dev)
-          if two_phase else None)
+    ws = (torch.empty(chunk_workspace_size(N, T, H, K, V, mode=mode), dtype=torch.uint8,
+                      device=dev) if two_phase else None)
     stream = torch.cuda.current_stream(dev)
     if args.output_gate:
         # synthetic output-gate pre-activation and weight (the module's g_b_proj output)
@@ -602,13 +602,17 @@ def main():
         achieved = alg / avg_chunk_s / 1e9
         kname = ("kda_chunk_fwd" if not args.fused else
                  "kda_chunk_fwd_gated_norm" if args.output_gate else "kda_chunk_fwd_gated")
-        variant = "two_phase" if two_phase else ("single_pass" if mode == "bf16_tc" else mode)
+        variant = (("two_phase" if two_phase else "single_pass") if mode == "bf16_tc" else
+                   ("fp32_two_phase" if two_phase else "fp32_exact"))
         kernel_key = f"{kname}:{variant}:{w.name}"
-        windows = chunk_windows(N, H, sum(-(-L // 64) for L in x.seqlens),
-                                torch.cuda.get_device_properties(dev).multi_processor_count)
+        windows = (chunk_windows(N, H, sum(-(-L // 64) for L in x.seqlens),
+                                 torch.cuda.get_device_properties(dev).multi_processor_count)
+                   if mode == "bf16_tc" else 1)
         what = {"two_phase": f"two-phase call: plan, then chunk preparation and state scan "
                              f"in {windows} chunk window(s)",
-                "single_pass": "single-pass kernel"}.get(variant, "FP32-exact kernel")
+                "single_pass": "single-pass kernel",
+                "fp32_two_phase": "two-phase FP32 call: plan, chunk preparation, state scan "
+                                  "in V halves"}.get(variant, "FP32-exact single-pass kernel")
         roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "traffic": kernel_traffic(kernel_key),
                 "kernel": f"{kname} ({mode}, {what})", "peak_source": f"{peak_src} hbm_gbs",

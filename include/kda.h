@@ -111,7 +111,12 @@ kda_status kda_gate(const void* f, int32_t f_dtype, const float* A_log, const fl
  * state through the chunks ("Add opt-in FP32 KDA chunk computation", section
  * Problem: the chunk solve and the carried state).  Without one it runs a
  * single pass per (sequence, head) that does all of a chunk's work in order.
- * KDA_MODE_FP32_EXACT uses no workspace (*bytes_host = 0).
+ * KDA_MODE_FP32_EXACT splits the same way on CUDA cores in FP32: with a
+ * workspace of at least this size every (chunk, head) is prepared in parallel
+ * (Q', K'', A_qk, the decay factors and W, U in FP32), then two CTAs per
+ * (sequence, head), one per half of V, carry the state.  The arithmetic per
+ * element is that of the single-pass FP32 kernel up to summation order, so
+ * both meet the same tolerance; the two need not agree bit for bit.
  *
  * When N * H is at most the GPU's SM count (the scan then leaves SMs idle)
  * and there are at least 64 chunks, the chunks are cut into up to 4 windows
@@ -121,8 +126,10 @@ kda_status kda_gate(const void* f, int32_t f_dtype, const float* A_log, const fl
  * for bit those of one window.
  *
  * The size is a bound that holds for every cu_seqlens with these N and T:
- * a 1 KiB-aligned header of 2 N + 9 int32, (T / 64 + N) * H records of 74240
- * bytes, and N * H * K * V FP32 (the state carried between windows).
+ * a 1 KiB-aligned header of 2 N + 9 int32, then for KDA_MODE_BF16_TC
+ * (T / 64 + N) * H records of 74240 bytes and N * H * K * V FP32 (the state
+ * carried between windows), for KDA_MODE_FP32_EXACT (T / 64 + N) * H records
+ * of 147968 bytes.
  * Arguments as kda_chunk_fwd; *bytes_host is host memory.
  */
 kda_status kda_chunk_workspace_size(int32_t N, int64_t T, int32_t H, int32_t K, int32_t V,
@@ -168,7 +175,10 @@ kda_status kda_chunk_workspace_size(int32_t N, int64_t T, int32_t H, int32_t K, 
  *              KDA_ERR_INVALID_ARG); its contents are overwritten and mean
  *              nothing after the call.  Calls that share one workspace must be
  *              ordered (same stream, or synchronised): the library does not
- *              guard it.  Ignored by KDA_MODE_FP32_EXACT.
+ *              guard it.  KDA_MODE_FP32_EXACT runs in two phases when
+ *              workspace_bytes >= kda_chunk_workspace_size(...) for that mode
+ *              (16-byte aligned, else KDA_ERR_ALIGNMENT) and in its single-pass
+ *              kernel otherwise (a smaller workspace is not used).
  *   status_dev one device int32 or NULL; the kernel writes a kda_status there
  *              only on a device-detected error (the caller zeroes it).
  */

@@ -183,7 +183,7 @@ def _chunk_outputs(q, v, cu_seqlens, out, out_dtype, output_final_state, final_s
 
 def chunk_workspace_size(N: int, T: int, H: int, K: int = 128, V: int = 128,
                          mode: str = "bf16_tc") -> int:
-    """Bytes of workspace the two-phase chunk path needs (0 for fp32_exact)."""
+    """Bytes of workspace the mode's two-phase chunk path needs."""
     out = ctypes.c_int64(0)
     st = load_library().kda_chunk_workspace_size(N, T, H, K, V, MODES[mode], ctypes.byref(out))
     if st != KDA_OK:
@@ -193,9 +193,9 @@ def chunk_workspace_size(N: int, T: int, H: int, K: int = 128, V: int = 128,
 
 def _workspace(workspace, mode, N, T, H, K, V, device):
     """(pointer, bytes) for the call: None -> no workspace (single-pass
-    kernel); "auto" -> a fresh buffer of the required size for bf16_tc; a
-    tensor -> its storage."""
-    if workspace is None or mode != "bf16_tc":
+    kernel); "auto" -> a fresh buffer of the size the mode's two-phase path
+    needs; a tensor -> its storage."""
+    if workspace is None:
         return None, 0, None
     if isinstance(workspace, str):
         if workspace != "auto":

@@ -103,7 +103,7 @@ kda_status check_chunk(const void* q, const void* k, const void* v, int32_t qkv_
     return KDA_OK;
 }
 
-// Workspace checks (BF16_TC only) and dispatch.
+// Workspace checks and dispatch.
 kda_status launch_chunk(kda::ChunkArgs a, int32_t mode, const int32_t* cu_seqlens_host,
                         void* workspace, int64_t workspace_bytes, kda_stream_t stream,
                         bool overlap = true)
@@ -113,10 +113,15 @@ kda_status launch_chunk(kda::ChunkArgs a, int32_t mode, const int32_t* cu_seqlen
         if (!aligned16(workspace)) return KDA_ERR_ALIGNMENT;
         if (workspace_bytes < kda::split_workspace_bytes(a.N, a.T, a.H)) return KDA_ERR_INVALID_ARG;
     }
+    // FP32-exact mode runs in two phases when its workspace fits, else in the
+    // single-pass kernel (a smaller workspace is not used)
+    const bool split32 = mode == KDA_MODE_FP32_EXACT && workspace != nullptr &&
+                         workspace_bytes >= kda::fp32_split_workspace_bytes(a.N, a.T, a.H);
+    if (split32 && !aligned16(workspace)) return KDA_ERR_ALIGNMENT;
     if (a.N == 0) return KDA_OK;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e;
-    if (split) {
+    if (split || split32) {
         a.workspace = workspace;
         int64_t chunks = kda::split_chunk_bound(a.N, a.T);
         if (cu_seqlens_host) {            // exact count: no idle preparation CTAs
@@ -124,7 +129,8 @@ kda_status launch_chunk(kda::ChunkArgs a, int32_t mode, const int32_t* cu_seqlen
             for (int32_t n = 0; n < a.N; ++n)
                 chunks += (cu_seqlens_host[n + 1] - cu_seqlens_host[n] + kda::kChunk - 1) / kda::kChunk;
         }
-        e = kda::launch_chunk_split(a, chunks, overlap, s);
+        e = split ? kda::launch_chunk_split(a, chunks, overlap, s)
+                  : kda::launch_chunk_fp32_split(a, chunks, s);
     } else {
         e = (mode == KDA_MODE_BF16_TC) ? kda::launch_chunk_tc(a, s) : kda::launch_chunk_fp32(a, s);
     }
@@ -156,7 +162,8 @@ kda_status kda_chunk_workspace_size(int32_t N, int64_t T, int32_t H, int32_t K, 
     if (mode != KDA_MODE_BF16_TC && mode != KDA_MODE_FP32_EXACT) return KDA_ERR_INVALID_ARG;
     if (T > INT32_MAX) return KDA_ERR_UNSUPPORTED;
     if (K != kda::kHeadK || V != kda::kHeadV) return KDA_ERR_UNSUPPORTED;
-    *bytes_host = mode == KDA_MODE_BF16_TC ? kda::split_workspace_bytes(N, T, H) : 0;
+    *bytes_host = mode == KDA_MODE_BF16_TC ? kda::split_workspace_bytes(N, T, H)
+                                           : kda::fp32_split_workspace_bytes(N, T, H);
     return KDA_OK;
 }
 

@@ -374,10 +374,11 @@ __device__ __forceinline__ float f4(const float4& v, int e)
 }
 
 // Rows of A_kk and T are read 4 columns at a time (16-byte loads along k);
-// every accumulation keeps its k order.
-__device__ __forceinline__ void chunk_inverse(float (*akk)[LDA], float (*Tf)[LDA],
-                                              const float* sbeta, unsigned char* tp, int tid,
-                                              int warp, int lane)
+// every accumulation keeps its k order.  chunk_inverse_f32 leaves T in Tf
+// (FP32, unit diagonal; its upper blocks hold scratch and must be read as 0)
+// and ends with a CTA barrier.
+__device__ __forceinline__ void chunk_inverse_f32(float (*akk)[LDA], float (*Tf)[LDA], int tid,
+                                                  int warp, int lane)
 {
     if (warp < NB && lane < SB) {
         const int b = warp * SB, m = lane;
@@ -469,6 +470,13 @@ __device__ __forceinline__ void chunk_inverse(float (*akk)[LDA], float (*Tf)[LDA
         *reinterpret_cast<float2*>(&Tf[32 + r2 + 1][c2]) = make_float2(-t10, -t11);
     }
     __syncthreads();
+}
+
+__device__ __forceinline__ void chunk_inverse(float (*akk)[LDA], float (*Tf)[LDA],
+                                              const float* sbeta, unsigned char* tp, int tid,
+                                              int warp, int lane)
+{
+    chunk_inverse_f32(akk, Tf, tid, warp, lane);
     // T'[i][j] = T[i][j] beta_j (j <= i), row i, 8 columns per store
 #pragma unroll
     for (int u = 0; u < 2; ++u) {

@@ -59,7 +59,10 @@ constexpr uint32_t REC_BYTES = 74240;
 static_assert(REC_BYTES % 16 == 0 && REC_BYTES < (1u << 20), "bulk copy size");
 
 // Workspace header: int32 [0] = 1 when the plan found offsets outside [0, T]
-// (those sequences get no chunks and are skipped), int32 [4 .. 4 + N] = chunk
+// or out of order (those sequences get no chunks and are skipped; the chunks
+// of the others can then add up past the T / 64 + N records the workspace
+// holds, and the scans skip every sequence whose records would lie past
+// that bound), int32 [4 .. 4 + N] = chunk
 // offsets (chunks of sequences 0 .. n-1), then int32 [5 + N .. 5 + 2N) = the
 // order in which the scan takes the sequences: longest first (LPT), so that
 // short sequences fill the tail of a packed batch (input order above
@@ -626,6 +629,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) chunk_scan_kernel(ChunkArgs a
     if (bos < 0 || eos < bos || (int64_t)eos > args.T) return;   // reported by the plan
     const int nch_all = (eos - bos + C - 1) / C;
     const int offn = hdr[kHdrOff + n];
+    if (offn + nch_all > split_chunk_bound(args.N, args.T)) return;   // bad offsets elsewhere
     const int cb = min(max(win.g0 - offn, 0), nch_all), ce = min(max(win.g1 - offn, 0), nch_all);
     const bool writes_final = (cb < ce && ce == nch_all) || (nch_all == 0 && win.last);
     if (cb == ce && !writes_final) return;                 // no chunk of this sequence here
@@ -994,6 +998,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) chunk_scan_vh_kernel(ChunkArg
     if (bos < 0 || eos < bos || (int64_t)eos > args.T) return;   // reported by the plan
     const int nch_all = (eos - bos + C - 1) / C;
     const int offn = hdr[kHdrOff + n];
+    if (offn + nch_all > split_chunk_bound(args.N, args.T)) return;   // bad offsets elsewhere
     const int cb = min(max(win.g0 - offn, 0), nch_all), ce = min(max(win.g1 - offn, 0), nch_all);
     const bool writes_final = (cb < ce && ce == nch_all) || (nch_all == 0 && win.last);
     if (cb == ce && !writes_final) return;
@@ -1364,7 +1369,6 @@ cudaError_t launch_chunk_plan(const int32_t* cu, int32_t N, int64_t T, int32_t* 
     return cudaGetLastError();
 }
 
-int64_t split_chunk_bound(int32_t N, int64_t T) { return T / kChunk + N; }
 
 // Workspace: plan header, one record per chunk bound and head, then the
 // windows' state carry [N,H,K,V] FP32.

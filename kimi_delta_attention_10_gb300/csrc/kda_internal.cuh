@@ -96,7 +96,8 @@ cudaError_t launch_chunk_tc(const ChunkArgs& a, cudaStream_t stream);
 // earlier ones (chunk windows; programmatic dependent launch on `stream`).
 cudaError_t launch_chunk_split(const ChunkArgs& a, int64_t chunks, bool overlap,
                                cudaStream_t stream);
-int64_t split_chunk_bound(int32_t N, int64_t T);
+// Chunks of N packed sequences of T tokens in all, at most.
+__host__ __device__ inline int64_t split_chunk_bound(int32_t N, int64_t T) { return T / kChunk + N; }
 // The plan kernel: int32 header with [0] = bad-offsets flag and, from
 // [kPlanOffsets], the per-sequence chunk offsets (N + 1 of them).
 constexpr int kPlanOffsets = 4;
@@ -104,6 +105,10 @@ int64_t chunk_plan_header_bytes(int32_t N);
 cudaError_t launch_chunk_plan(const int32_t* cu, int32_t N, int64_t T, int32_t* hdr,
                               int32_t* status, cudaStream_t stream);
 int64_t split_workspace_bytes(int32_t N, int64_t T, int32_t H);
+// FP32-exact mode in two phases (kda_chunk_fp32_split.cu): plan header and one
+// FP32 record per (chunk bound, head).
+int64_t fp32_split_workspace_bytes(int32_t N, int64_t T, int32_t H);
+cudaError_t launch_chunk_fp32_split(const ChunkArgs& a, int64_t chunks, cudaStream_t stream);
 // The static scratch of kda_chunk_fwd_static and its size; static_scratch()
 // returns its address on the current device (looked up once per device).
 constexpr int64_t kStaticScratchBytes = 64ll << 20;

@@ -11,12 +11,13 @@ from kimi_delta_attention_10_gb300.inputs import KDAInputs
 # Output tolerances (rel-L2 against the FP64 oracle), per mode.
 TOL = {"fp32_exact": 1e-5, "bf16_tc": 3e-3}
 
-# The library's chunk paths: (mode, workspace).  bf16_tc with a workspace is
-# the two-phase path (prepare every chunk, then scan); without one, the
+# The library's chunk paths: (mode, workspace).  With a workspace each mode
+# runs in two phases (prepare every chunk, then scan); without one, in its
 # single-pass kernel.
-PATHS = {"fp32_exact": ("fp32_exact", None), "bf16_tc": ("bf16_tc", "auto"),
-         "bf16_tc_1pass": ("bf16_tc", None)}
-OUT_DTYPE = {"fp32_exact": torch.float32, "bf16_tc": None, "bf16_tc_1pass": None}
+PATHS = {"fp32_exact": ("fp32_exact", None), "fp32_exact_2p": ("fp32_exact", "auto"),
+         "bf16_tc": ("bf16_tc", "auto"), "bf16_tc_1pass": ("bf16_tc", None)}
+OUT_DTYPE = {"fp32_exact": torch.float32, "fp32_exact_2p": torch.float32, "bf16_tc": None,
+             "bf16_tc_1pass": None}
 
 
 def path_kw(path: str) -> dict:

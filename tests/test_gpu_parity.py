@@ -62,7 +62,7 @@ def test_gate_extremes_and_bf16_inputs():
         assert np.max(np.abs(beta.cpu().double().numpy() - b_ref) / b_ref) < 2e-6
 
 
-MODES = list(PATHS)     # fp32_exact, bf16_tc (two-phase), bf16_tc_1pass (single-pass)
+MODES = list(PATHS)     # FP32-exact and BF16 tensor-core, each single-pass and two-phase
 
 
 @pytest.mark.parametrize("mode", MODES)
