@@ -59,6 +59,12 @@ struct PrepSmem {
     float aqk[C][LDQ];
     float t4[C / S4][DK];  // decay over each 4-token sub-block
     float blk[NB][DK];     // decay over each 16-token block
+    // the decay over the sub-blocks between two others of a block, by block:
+    // [I][0] = 1, [I][1] = t4 of sub-block 1, [I][2] = of 2, [I][3] = of 1 and 2
+    float mid4[NB][4][DK];
+    float mid16[4][DK];    // likewise over the blocks between two others
+    float pre16[NB][DK];   // the decay over the blocks before block I
+    float post16[NB][DK];  // over the blocks after it
     float beta[C];
 };
 
@@ -333,47 +339,37 @@ __global__ void __launch_bounds__(NT, 1) fp32_prep_kernel(ChunkArgs args,
             bt *= p;
         }
         sm.blk[I][c] = bt;
+        const float t1 = sm.t4[I * (SB / S4) + 1][c], t2 = sm.t4[I * (SB / S4) + 2][c];
+        sm.mid4[I][0][c] = 1.f;
+        sm.mid4[I][1][c] = t1;
+        sm.mid4[I][2][c] = t2;
+        sm.mid4[I][3][c] = t1 * t2;
     }
     __syncthreads();
 
     // ---- 4. pairs in different sub-blocks of one 16-token block: 24 tiles of
-    // 4 x 4, 8 lanes per tile, each with 16 channels (4 runs of 4, 32 apart)
+    // 4 x 4, eight lanes per tile (a quarter warp, so that the lanes of a tile
+    // read the same Kb4 rows at once), each lane one row of A_kk or of A_qk
     if (tid < 24 * 8) {
-        const int tile = tid >> 3, sl = tid & 7;
-        const int I = tile / 6, pr = tile % 6;
+        const int tile = tid >> 3, I = tile / 6, pr = tile % 6;
         const int sa = pr == 0 ? 1 : (pr < 3 ? 2 : 3);      // (sa, sb): (1,0) (2,0) (2,1)
         const int sb = pr == 0 ? 0 : (pr < 3 ? pr - 1 : pr - 3);   //   (3,0) (3,1) (3,2)
-        const int ri = I * SB + sa * S4, rj = I * SB + sb * S4;
-        float val[32];
+        const int i = I * SB + sa * S4 + ((tid >> 1) & 3), rj = I * SB + sb * S4;
+        const bool qk = tid & 1;
+        const float* x = qk ? &sm.q[i][0] : &sm.k[i][0];
+        // sub-blocks strictly between: none, 1, 2 or 1 and 2
+        const float* midp = &sm.mid4[I][sa - sb == 1 ? 0 : (sa - sb == 3 ? 3 : sb + 1)][0];
+        float acc[S4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+        for (int c = 0; c < DK; c += 4) {
+            const float4 mid = ld4s(midp + c);
+            const float4 xv = ld4s(x + c);
 #pragma unroll
-        for (int x = 0; x < 32; ++x) val[x] = 0.f;
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-            const int c = sl * 4 + 32 * cc;
-            float4 mid = make_float4(1.f, 1.f, 1.f, 1.f);
-            for (int M = sb + 1; M < sa; ++M) mid = mul4(mid, ld4s(&sm.t4[I * (SB / S4) + M][c]));
-            float4 kb[S4], kf[S4], qf[S4];
-#pragma unroll
-            for (int u = 0; u < S4; ++u) {
-                kb[u] = mul4(ld4s(&sm.a[rj + u][c]), mid);
-                kf[u] = ld4s(&sm.k[ri + u][c]);
-                qf[u] = ld4s(&sm.q[ri + u][c]);
-            }
-#pragma unroll
-            for (int i = 0; i < S4; ++i)
-#pragma unroll
-                for (int j = 0; j < S4; ++j) {
-                    val[i * 4 + j] = dot4(kf[i], kb[j], val[i * 4 + j]);
-                    val[16 + i * 4 + j] = dot4(qf[i], kb[j], val[16 + i * 4 + j]);
-                }
+            for (int u = 0; u < S4; ++u) acc[u] = dot4(xv, mul4(ld4s(&sm.a[rj + u][c]), mid), acc[u]);
         }
-        ReduceScatter<32, 4>::run(val, lane);
-        const int e0 = 4 * (lane & 7);                       // entries e0 .. e0+3: one row
-        const int i = ri + ((e0 & 15) >> 2);
-        if (e0 < 16)
-            st4s(&sm.akk[i][rj], scale4(make_float4(val[0], val[1], val[2], val[3]), sm.beta[i]));
-        else
-            st4s(&sm.aqk[i][rj], make_float4(val[0], val[1], val[2], val[3]));
+        const float s = qk ? 1.f : sm.beta[i];
+        st4s(qk ? &sm.aqk[i][rj] : &sm.akk[i][rj],
+             make_float4(s * acc[0], s * acc[1], s * acc[2], s * acc[3]));
     }
     __syncthreads();
 
@@ -385,6 +381,24 @@ __global__ void __launch_bounds__(NT, 1) fp32_prep_kernel(ChunkArgs args,
         float t[SB / S4];
 #pragma unroll
         for (int s = 0; s < SB / S4; ++s) t[s] = sm.t4[I * (SB / S4) + s][c];
+        if (ii == 0) {
+            const float b0 = sm.blk[0][c], b1 = sm.blk[1][c], b2 = sm.blk[2][c], b3 = sm.blk[3][c];
+            if (tid < 128) {
+                sm.mid16[0][c] = 1.f;
+                sm.mid16[1][c] = b1;
+                sm.pre16[0][c] = 1.f;
+                sm.pre16[1][c] = b0;
+                sm.pre16[2][c] = b0 * b1;
+                sm.pre16[3][c] = b0 * b1 * b2;
+            } else {
+                sm.mid16[2][c] = b2;
+                sm.mid16[3][c] = b1 * b2;
+                sm.post16[0][c] = b1 * b2 * b3;
+                sm.post16[1][c] = b2 * b3;
+                sm.post16[2][c] = b3;
+                sm.post16[3][c] = 1.f;
+            }
+        }
         const float pre[4] = {1.f, t[0], t[0] * t[1], t[0] * t[1] * t[2]};
         const float post[4] = {t[1] * t[2] * t[3], t[2] * t[3], t[3], 1.f};
 #pragma unroll
@@ -400,12 +414,16 @@ __global__ void __launch_bounds__(NT, 1) fp32_prep_kernel(ChunkArgs args,
     __syncthreads();
 
     // ---- 6. pairs in different 16-token blocks: one warp per block pair, each
-    // lane a 2 x 4 tile of A_kk and of A_qk over all 128 channels
+    // lane a 2 x 4 tile of A_kk and of A_qk over all 128 channels (rows r and
+    // r + 8: the eight lanes of a quarter warp read eight consecutive rows and
+    // one set of Kb16 rows)
     if (tid < 6 * 32) {
         const int pr = tid >> 5, lt = tid & 31;
         const int I = pr == 0 ? 1 : (pr < 3 ? 2 : 3);        // (I, J): (1,0) (2,0) (2,1)
         const int J = pr == 0 ? 0 : (pr < 3 ? pr - 1 : pr - 3);   //   (3,0) (3,1) (3,2)
-        const int i0 = I * SB + (lt >> 2) * 2, j0 = J * SB + (lt & 3) * 4;
+        const int ib = I * SB + (lt & 7), j0 = J * SB + (lt >> 3) * 4;
+        // blocks strictly between: none, 1, 2 or 1 and 2
+        const float* midp = &sm.mid16[I - J == 1 ? 0 : (I - J == 3 ? 3 : J + 1)][0];
         float skk[2][4], sqk[2][4];
 #pragma unroll
         for (int r = 0; r < 2; ++r)
@@ -413,14 +431,13 @@ __global__ void __launch_bounds__(NT, 1) fp32_prep_kernel(ChunkArgs args,
             for (int x = 0; x < 4; ++x) { skk[r][x] = 0.f; sqk[r][x] = 0.f; }
 #pragma unroll 2
         for (int c = 0; c < DK; c += 4) {
-            float4 mid = make_float4(1.f, 1.f, 1.f, 1.f);
-            for (int M = J + 1; M < I; ++M) mid = mul4(mid, ld4s(&sm.blk[M][c]));
+            const float4 mid = ld4s(midp + c);
             float4 kb[4];
 #pragma unroll
             for (int u = 0; u < 4; ++u) kb[u] = mul4(ld4s(&sm.a[j0 + u][c]), mid);
 #pragma unroll
             for (int r = 0; r < 2; ++r) {
-                const float4 kf = ld4s(&sm.k[i0 + r][c]), qf = ld4s(&sm.q[i0 + r][c]);
+                const float4 kf = ld4s(&sm.k[ib + 8 * r][c]), qf = ld4s(&sm.q[ib + 8 * r][c]);
 #pragma unroll
                 for (int x = 0; x < 4; ++x) {
                     skk[r][x] = dot4(kf, kb[x], skk[r][x]);
@@ -430,10 +447,10 @@ __global__ void __launch_bounds__(NT, 1) fp32_prep_kernel(ChunkArgs args,
         }
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
-            const float b = sm.beta[i0 + r];
-            st4s(&sm.akk[i0 + r][j0],
+            const float b = sm.beta[ib + 8 * r];
+            st4s(&sm.akk[ib + 8 * r][j0],
                  make_float4(b * skk[r][0], b * skk[r][1], b * skk[r][2], b * skk[r][3]));
-            st4s(&sm.aqk[i0 + r][j0], make_float4(sqk[r][0], sqk[r][1], sqk[r][2], sqk[r][3]));
+            st4s(&sm.aqk[ib + 8 * r][j0], make_float4(sqk[r][0], sqk[r][1], sqk[r][2], sqk[r][3]));
         }
     }
     __syncthreads();
@@ -444,9 +461,7 @@ __global__ void __launch_bounds__(NT, 1) fp32_prep_kernel(ChunkArgs args,
 #pragma unroll 2
     for (int m = 0; m < C * DK / 4 / NT; ++m) {
         const int e = tid + NT * m, r = e >> 5, c = (e & 31) * 4, I = r / SB;
-        float4 pre = make_float4(1.f, 1.f, 1.f, 1.f), post = pre;
-        for (int M = 0; M < I; ++M) pre = mul4(pre, ld4s(&sm.blk[M][c]));
-        for (int M = I + 1; M < NB; ++M) post = mul4(post, ld4s(&sm.blk[M][c]));
+        const float4 pre = ld4s(&sm.pre16[I][c]), post = ld4s(&sm.post16[I][c]);
         const float b = sm.beta[r];
         st4s(&sm.k[r][c], scale4(mul4(ld4s(&sm.k[r][c]), pre), b));
         st4s(rec + R_QP / 4 + r * DK + c, mul4(ld4s(&sm.q[r][c]), pre));
@@ -462,10 +477,7 @@ __global__ void __launch_bounds__(NT, 1) fp32_prep_kernel(ChunkArgs args,
     }
     if (tid < DK / 4) {
         const int c = tid * 4;
-        float4 d = ld4s(&sm.blk[0][c]);
-#pragma unroll
-        for (int M = 1; M < NB; ++M) d = mul4(d, ld4s(&sm.blk[M][c]));
-        st4s(rec + R_DEC / 4 + c, d);
+        st4s(rec + R_DEC / 4 + c, mul4(ld4s(&sm.pre16[NB - 1][c]), ld4s(&sm.blk[NB - 1][c])));
     }
     __syncthreads();
 
@@ -487,21 +499,35 @@ __global__ void __launch_bounds__(NT, 1) fp32_prep_kernel(ChunkArgs args,
             for (int r = 0; r < 4; ++r)
 #pragma unroll
                 for (int x = 0; x < 8; ++x) w[r][x] = 0.f;
-            for (int kk = 0; kk <= i0; kk += 4) {
+            for (int kk = 0; kk < i0; kk += 4) {           // the full blocks left of the diagonal
                 float4 t4[4];
 #pragma unroll
                 for (int r = 0; r < 4; ++r) t4[r] = ld4s(&sm.tf[i0 + r][kk]);
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const int kx = kk + e;
-                    const float4 xa = ld4s(&src[kx][c0]), xb = ld4s(&src[kx][c0 + 4]);
+                    const float4 xa = ld4s(&src[kk + e][c0]), xb = ld4s(&src[kk + e][c0 + 4]);
                     const float xs[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
 #pragma unroll
                     for (int r = 0; r < 4; ++r) {
-                        // T is lower triangular with a unit diagonal: entries above it
-                        // (scratch of the merges) count as zero
-                        const int ir = i0 + r;
-                        const float t = kx < ir ? f4at(t4[r], e) : (kx == ir ? 1.f : 0.f);
+                        const float t = f4at(t4[r], e);
+#pragma unroll
+                        for (int x = 0; x < 8; ++x) w[r][x] = fmaf(t, xs[x], w[r][x]);
+                    }
+                }
+            }
+            {
+                // the diagonal block: T is lower triangular with a unit diagonal,
+                // and its entries above the diagonal (scratch of the merges) count as 0
+                float4 t4[4];
+#pragma unroll
+                for (int r = 0; r < 4; ++r) t4[r] = ld4s(&sm.tf[i0 + r][i0]);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float4 xa = ld4s(&src[i0 + e][c0]), xb = ld4s(&src[i0 + e][c0 + 4]);
+                    const float xs[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
+#pragma unroll
+                    for (int r = e; r < 4; ++r) {
+                        const float t = r == e ? 1.f : f4at(t4[r], e);
 #pragma unroll
                         for (int x = 0; x < 8; ++x) w[r][x] = fmaf(t, xs[x], w[r][x]);
                     }
