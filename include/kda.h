@@ -70,10 +70,16 @@ typedef enum {
      * *status_dev when one is not finite, so an overflow is never silent
      * (inputs that hold NaN or infinity are reported the same way). */
     KDA_MODE_BF16_TC = 0,
-    /* FP32 arithmetic throughout (IEEE FP32, no TF32), output rel-L2 error
-     * below 1e-5 with F32 output.  This is the counterpart of the pages'
-     * opt-in FP32 chunk intermediates ("Add opt-in FP32 KDA chunk
-     * computation", section Change), without their TF32 caveat. */
+    /* FP32-exact: output rel-L2 error below 1e-5 with F32 output.  This is
+     * the counterpart of the pages' opt-in FP32 chunk intermediates ("Add
+     * opt-in FP32 KDA chunk computation", section Change), without their
+     * TF32 caveat.  Without a workspace every product is an IEEE FP32 fused
+     * multiply-add on CUDA cores.  With one (two phases, see
+     * kda_chunk_workspace_size) the chunk preparation is IEEE FP32 on CUDA
+     * cores and the state scan's products run on the tensor cores with each
+     * FP32 operand held as a pair of FP16 values scaled by a power of two
+     * (about 22 significant bits; three MMAs with FP32 accumulation per
+     * product), so it keeps FP32's range: no FP16 limit applies. */
     KDA_MODE_FP32_EXACT = 1
 } kda_mode;
 
@@ -111,12 +117,13 @@ kda_status kda_gate(const void* f, int32_t f_dtype, const float* A_log, const fl
  * state through the chunks ("Add opt-in FP32 KDA chunk computation", section
  * Problem: the chunk solve and the carried state).  Without one it runs a
  * single pass per (sequence, head) that does all of a chunk's work in order.
- * KDA_MODE_FP32_EXACT splits the same way on CUDA cores in FP32: with a
- * workspace of at least this size every (chunk, head) is prepared in parallel
- * (Q', K'', A_qk, the decay factors and W, U in FP32), then two CTAs per
- * (sequence, head), one per half of V, carry the state.  The arithmetic per
- * element is that of the single-pass FP32 kernel up to summation order, so
- * both meet the same tolerance; the two need not agree bit for bit.
+ * KDA_MODE_FP32_EXACT splits the same way: with a workspace of at least
+ * this size every (chunk, head) is prepared in parallel in IEEE FP32 on CUDA
+ * cores (Q', K'', A_qk, the decay factors and W, U), then two CTAs per
+ * (sequence, head), one per half of V, carry the FP32 state with the scan's
+ * products on the tensor cores as scaled FP16 pairs (see KDA_MODE_FP32_EXACT).
+ * It meets the same tolerance as the single-pass FP32 kernel; the two need
+ * not agree bit for bit.
  *
  * When N * H is at most the GPU's SM count (the scan then leaves SMs idle)
  * and there are at least 64 chunks, the chunks are cut into up to 4 windows
@@ -129,7 +136,7 @@ kda_status kda_gate(const void* f, int32_t f_dtype, const float* A_log, const fl
  * a 1 KiB-aligned header of 2 N + 9 int32, then for KDA_MODE_BF16_TC
  * (T / 64 + N) * H records of 74240 bytes and N * H * K * V FP32 (the state
  * carried between windows), for KDA_MODE_FP32_EXACT (T / 64 + N) * H records
- * of 147968 bytes.
+ * of 148224 bytes.
  * Arguments as kda_chunk_fwd; *bytes_host is host memory.
  */
 kda_status kda_chunk_workspace_size(int32_t N, int64_t T, int32_t H, int32_t K, int32_t V,

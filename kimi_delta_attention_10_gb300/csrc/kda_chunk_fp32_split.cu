@@ -1,20 +1,31 @@
-// FP32-exact chunked KDA forward in two phases, on CUDA cores (IEEE FP32).
+// FP32-exact chunked KDA forward in two phases.
 //
 // The same split as the tensor-core two-phase path ("Add opt-in FP32 KDA chunk
 // computation", sections Problem and Change: the chunk solve and the carried
 // state, kept in FP32 here):
-//   prepare (every (chunk, head) at once, one CTA each):
+//   prepare (every (chunk, head) at once, one CTA each, IEEE FP32 on CUDA
+//   cores):
 //     A_kk, A_qk (pair sums with decay factors built from 4- and 16-token
 //     sub-blocks, each a product of factors <= 1, so that nothing overflows),
 //     T = (I + A_kk)^-1 (16x16 blocks and their merges), W = T X with
 //     X = beta k^ o e^G, U = T (beta v), Q' = q^ o e^G,
-//     K'' = k^ o e^{G_last - G}, d = e^{G_last}   ->  one FP32 record
-//   scan (one CTA per (sequence, head, half of V), chunks in order):
+//     K'' = k^ o e^{G_last - G}, d = e^{G_last}   ->  one record
+//   scan (one CTA per (sequence, head, half of V), chunks in order, tcgen05):
 //     Delta = U - W S,  O = scale [Q' S + A_qk Delta],  S <- Diag(d) S + K''^T Delta
-// Every product is an FP32 fused multiply-add on CUDA cores, so the mode keeps
-// its FP32 accuracy (no TF32 or FP16 operands).
+// The scan's products run on the tensor cores with each FP32 operand x held
+// as a pair of FP16 values, x ~ (hi + lo) / s: hi = fp16(x s) and
+// lo = fp16(x s - hi) carry about 22 significant bits, and
+// x y ~ (hi_x hi_y + hi_x lo_y + lo_x hi_y) / (s_x s_y), three MMAs with FP32
+// accumulation, the dropped lo_x lo_y term below 2^-22 of the product.  The
+// scales s are powers of two (exact): per row of W (whose magnitude follows
+// T), per chunk for the state and for Delta (they follow v and beta, so a
+// fixed scale would either overflow FP16 or leave small states in its
+// subnormals), and 1 for Q', K'' and A_qk (|x| <= 1: unit q^, k^ and decays
+// <= 1).  The state itself, U, d, Delta = U - W S and the state update are
+// FP32 on CUDA cores.
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <stdint.h>
 
 #include "kda_internal.cuh"
@@ -37,17 +48,57 @@ constexpr int LDK = DK + 4;      // FP32 rows of 128 (16-byte aligned, shifted b
 constexpr int LDT = chunk_ops::LDA;   // 68: A_kk and T for the blocked inverse
 constexpr int LDQ = C + 4;       // A_qk
 
-// Record of one unit (FP32, row-major; bytes).
-constexpr uint32_t R_W = 0;            // W   [64 i][128 c]
-constexpr uint32_t R_QP = 32768;       // Q'  [64 i][128 c]
-constexpr uint32_t R_U = 65536;        // U   [64 i][128 v]
-constexpr uint32_t R_KT = 98304;       // K'' [64 i][128 c]
-constexpr uint32_t R_AQK = 131072;     // A_qk [64 i][64 j] (upper part 0)
-constexpr uint32_t R_DEC = 147456;     // d [128]
-constexpr uint32_t R_BYTES = 147968;
-// the scan brings a record in as two bulk copies: [W, Q', U] and [K'', A_qk, d]
-constexpr uint32_t R_EARLY = R_KT, R_LATE = R_BYTES - R_KT;
-static_assert(R_BYTES % 16 == 0 && R_EARLY % 16 == 0, "bulk copy sizes");
+// Record of one unit (bytes).  FP16 pairs (hi, lo) are two tiles of the
+// same 128-byte-swizzled layout, lo 32 KiB (W, Q'), 16 KiB (K'') or 8 KiB
+// (A_qk) after hi.  The scan brings the early part in before [W; Q'] S and
+// the late part before K''^T Delta.
+constexpr uint32_t R_WQ = 0;           // [W; Q'] K-major [128 rows][128 c]: rows 0..63 W s_i, 64..127 Q'
+constexpr uint32_t R_WQ_LO = 32768;
+constexpr uint32_t R_WINV = 65536;     // 1 / s_i of W row i, FP32 [64]
+constexpr uint32_t R_U = 65792;        // U FP32 [2 halves of V][64 i][64 v], 16-byte piece p of row i at p ^ (i & 7)
+constexpr uint32_t R_LATE = R_U + 32768;
+constexpr uint32_t L_KT = 0;           // K''^T MN-major [64 i][128 c] (two 64-channel groups of 8 KiB)
+constexpr uint32_t L_KT_LO = 16384;
+constexpr uint32_t L_AQK = 32768;      // A_qk K-major [64 i][64 j] (zero above the diagonal)
+constexpr uint32_t L_AQK_LO = 40960;
+constexpr uint32_t L_DEC = 49152;      // d FP32 [128]
+constexpr uint32_t R_LATE_BYTES = L_DEC + 512;
+constexpr uint32_t R_BYTES = R_LATE + R_LATE_BYTES;
+constexpr uint32_t R_UHALF = 16384;
+static_assert(R_BYTES % 16 == 0 && R_LATE % 16 == 0 && R_U % 16 == 0, "bulk copy sizes");
+
+// x s as an FP16 pair: hi = fp16(x s), lo = fp16(x s - hi), eight values at
+// MN (or K) indices m .. m + 7 of row `row` of a swizzled tile pair (lo at
+// hi + lo_off, 64-element groups `gbytes` apart), in shared or global memory.
+__device__ __forceinline__ void st8_pair(unsigned char* tile, uint32_t lo_off, uint32_t gbytes,
+                                         int row, int m, const float* x, float s)
+{
+    uint32_t h[4], l[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const float y0 = x[2 * e] * s, y1 = x[2 * e + 1] * s;
+        const __half2 hh = __floats2half2_rn(y0, y1);
+        const float2 hf = __half22float2(hh);
+        const __half2 ll = __floats2half2_rn(y0 - hf.x, y1 - hf.y);
+        h[e] = *reinterpret_cast<const uint32_t*>(&hh);
+        l[e] = *reinterpret_cast<const uint32_t*>(&ll);
+    }
+    const uint32_t o = (m >> 6) * gbytes + tc::sw128(row, (m & 63) * 2);
+    *reinterpret_cast<uint4*>(tile + o) = make_uint4(h[0], h[1], h[2], h[3]);
+    *reinterpret_cast<uint4*>(tile + lo_off + o) = make_uint4(l[0], l[1], l[2], l[3]);
+}
+
+// The power of two s = 2^(14 - e) for a maximum magnitude mx < 2^e, and 1/s:
+// every |x| <= mx then has |x s| < 2^14, inside FP16's range with room for
+// the rounding of hi.  The exponent is kept within +-100 (mx of zero, or
+// beyond FP32's range).
+__device__ __forceinline__ void pow2_scale(float mx, float& s, float& inv)
+{
+    const int e = (int)((__float_as_uint(mx) >> 23) & 0xffu) - 126;
+    const int k = max(-100, min(100, 14 - e));
+    s = __uint_as_float((uint32_t)(127 + k) << 23);
+    inv = __uint_as_float((uint32_t)(127 - k) << 23);
+}
 
 struct PrepSmem {
     float q[C][LDK];       // q^ -> Qf4 -> Qf16 (then Q' goes to the record)
@@ -174,7 +225,7 @@ __global__ void __launch_bounds__(NT, 1) fp32_prep_kernel(ChunkArgs args,
     const int bos = args.cu_seqlens[lo], eos = args.cu_seqlens[lo + 1];
     const int t0 = bos + (gc - off[lo]) * C;
     const int L = min(C, eos - t0);
-    float* rec = reinterpret_cast<float*>(records + unit * (int64_t)R_BYTES);
+    unsigned char* recb = records + unit * (int64_t)R_BYTES;
 
     const TIn* __restrict__ q = static_cast<const TIn*>(args.q);
     const TIn* __restrict__ k = static_cast<const TIn*>(args.k);
@@ -455,29 +506,42 @@ __global__ void __launch_bounds__(NT, 1) fp32_prep_kernel(ChunkArgs args,
     }
     __syncthreads();
 
-    // ---- 7. X = beta k^ o e^G (in place of Kf16), Q' = q^ o e^G and
-    // K'' = k^ o e^{G_last - G} to the record, beta v; then A_qk (zero above
-    // the diagonal) and d = e^{G_last}
+    // ---- 7. X = beta k^ o e^G (in place of Kf16) and beta v; Q' = q^ o e^G
+    // (rows 64.. of the [W; Q'] operand), K'' = k^ o e^{G_last - G} and A_qk
+    // (zero above the diagonal) to the record as FP16 pairs (|x| <= 1, scale
+    // 1); d = e^{G_last}
 #pragma unroll 2
-    for (int m = 0; m < C * DK / 4 / NT; ++m) {
-        const int e = tid + NT * m, r = e >> 5, c = (e & 31) * 4, I = r / SB;
-        const float4 pre = ld4s(&sm.pre16[I][c]), post = ld4s(&sm.post16[I][c]);
+    for (int m = 0; m < C * DK / 8 / NT; ++m) {
+        const int e = tid + NT * m, r = e >> 4, c = (e & 15) * 8, I = r / SB;
         const float b = sm.beta[r];
-        st4s(&sm.k[r][c], scale4(mul4(ld4s(&sm.k[r][c]), pre), b));
-        st4s(rec + R_QP / 4 + r * DK + c, mul4(ld4s(&sm.q[r][c]), pre));
-        st4s(rec + R_KT / 4 + r * DK + c, mul4(ld4s(&sm.a[r][c]), post));
-        st4s(&sm.v[r][c], scale4(ld4s(&sm.v[r][c]), b));
+        float qv[8], kv[8];
+#pragma unroll
+        for (int hx = 0; hx < 2; ++hx) {
+            const int cx = c + 4 * hx;
+            const float4 pre = ld4s(&sm.pre16[I][cx]), post = ld4s(&sm.post16[I][cx]);
+            st4s(&sm.k[r][cx], scale4(mul4(ld4s(&sm.k[r][cx]), pre), b));
+            st4s(&sm.v[r][cx], scale4(ld4s(&sm.v[r][cx]), b));
+            const float4 q4 = mul4(ld4s(&sm.q[r][cx]), pre), k4 = mul4(ld4s(&sm.a[r][cx]), post);
+            qv[4 * hx] = q4.x; qv[4 * hx + 1] = q4.y; qv[4 * hx + 2] = q4.z; qv[4 * hx + 3] = q4.w;
+            kv[4 * hx] = k4.x; kv[4 * hx + 1] = k4.y; kv[4 * hx + 2] = k4.z; kv[4 * hx + 3] = k4.w;
+        }
+        st8_pair(recb + R_WQ, R_WQ_LO - R_WQ, 16384, 64 + r, c, qv, 1.f);
+        st8_pair(recb + R_LATE + L_KT, L_KT_LO - L_KT, 8192, r, c, kv, 1.f);
     }
 #pragma unroll
-    for (int m = 0; m < C * C / 4 / NT; ++m) {
-        const int e = tid + NT * m, r = e >> 4, j = (e & 15) * 4;
-        const float4 x = ld4s(&sm.aqk[r][j]);
-        st4s(rec + R_AQK / 4 + r * C + j, make_float4(j <= r ? x.x : 0.f, j + 1 <= r ? x.y : 0.f,
-                                                     j + 2 <= r ? x.z : 0.f, j + 3 <= r ? x.w : 0.f));
+    for (int m = 0; m < C * C / 8 / NT; ++m) {
+        const int e = tid + NT * m, r = e >> 3, j = (e & 7) * 8;
+        const float4 x0 = ld4s(&sm.aqk[r][j]), x1 = ld4s(&sm.aqk[r][j + 4]);
+        const float x[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+        float y[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) y[u] = j + u <= r ? x[u] : 0.f;
+        st8_pair(recb + R_LATE + L_AQK, L_AQK_LO - L_AQK, 0, r, j, y, 1.f);
     }
     if (tid < DK / 4) {
         const int c = tid * 4;
-        st4s(rec + R_DEC / 4 + c, mul4(ld4s(&sm.pre16[NB - 1][c]), ld4s(&sm.blk[NB - 1][c])));
+        st4s(reinterpret_cast<float*>(recb + R_LATE + L_DEC) + c,
+             mul4(ld4s(&sm.pre16[NB - 1][c]), ld4s(&sm.blk[NB - 1][c])));
     }
     __syncthreads();
 
@@ -490,7 +554,6 @@ __global__ void __launch_bounds__(NT, 1) fp32_prep_kernel(ChunkArgs args,
     {
         const int tt = tid & 127, gp = tt >> 4, c0 = (tt & 15) * 8;
         const float (*src)[LDK] = tid < 128 ? sm.k : sm.v;
-        float* dst = rec + (tid < 128 ? R_W : R_U) / 4;
 #pragma unroll 1
         for (int pass = 0; pass < 2; ++pass) {
             const int i0 = 4 * (pass ? 15 - gp : gp);
@@ -533,50 +596,121 @@ __global__ void __launch_bounds__(NT, 1) fp32_prep_kernel(ChunkArgs args,
                     }
                 }
             }
+            if (tid < 128) {
+                // W rows as FP16 pairs, row i scaled by s_i from the row's largest
+                // magnitude (over the 16 lanes of a half warp that hold the row)
 #pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                st4s(dst + (i0 + r) * DK + c0, make_float4(w[r][0], w[r][1], w[r][2], w[r][3]));
-                st4s(dst + (i0 + r) * DK + c0 + 4, make_float4(w[r][4], w[r][5], w[r][6], w[r][7]));
+                for (int r = 0; r < 4; ++r) {
+                    float mx = 0.f;
+#pragma unroll
+                    for (int x = 0; x < 8; ++x) mx = fmaxf(mx, fabsf(w[r][x]));
+#pragma unroll
+                    for (int o = 8; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+                    float sc, inv;
+                    pow2_scale(mx, sc, inv);
+                    st8_pair(recb + R_WQ, R_WQ_LO - R_WQ, 16384, i0 + r, c0, w[r], sc);
+                    if ((tt & 15) == 0) reinterpret_cast<float*>(recb + R_WINV)[i0 + r] = inv;
+                }
+            } else {
+                // U rows in FP32, V halves apart, 16-byte pieces swizzled by row
+                unsigned char* uh = recb + R_U + (c0 >> 6) * R_UHALF;
+                const int p0 = (c0 & 63) >> 2;
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    const int i = i0 + r;
+                    st4s(reinterpret_cast<float*>(uh + i * 256 + ((p0 ^ (i & 7)) << 4)),
+                         make_float4(w[r][0], w[r][1], w[r][2], w[r][3]));
+                    st4s(reinterpret_cast<float*>(uh + i * 256 + (((p0 + 1) ^ (i & 7)) << 4)),
+                         make_float4(w[r][4], w[r][5], w[r][6], w[r][7]));
+                }
             }
         }
     }
 }
 
 // ---------------------------------------------------------------- scan
-// One CTA per (sequence, head, half of V).  Shared memory holds one record
-// (brought in as two bulk copies), the state slice S[c][v] (128 x 64 FP32)
-// and Delta (64 x 64).  Per chunk:
-//   A: Delta = U - W S and Q S (a 4 x 4 tile of each per thread), then the early
-//      part of the next record (W, Q', U) is requested into the freed space;
-//   B: O = scale (Q S + A_qk Delta), stored; C: S <- Diag(d) S + K''^T Delta
-//      (an 8 x 4 tile per thread); then the late part of the next record.
+// One CTA per (sequence, head, half of V): eight epilogue warps and one
+// control warp whose lane 0 issues the bulk copies and the MMAs.  Epilogue
+// thread (quad q = warp & 3, half hf = warp >> 2, lane l) owns TMEM lane
+// row = 32 q + l and columns 32 hf .. 32 hf + 31 of this CTA's 64: the FP32
+// state S[row][v] for those columns lives in its registers.  Per chunk c, in
+// TMEM region R = 256 (c & 1):
+//   control:  D1 = [W s; Q'] (S sS) (24 MMAs, M = 128, K = 128 channels: rows
+//             0..63 W S, 64..127 Q' S), commit d1_done
+//   Delta warps (lanes 0..63): Delta = U - D1 / (s_i sS); its largest
+//             magnitude over the four warps gives sD; Delta sD as FP16 pairs
+//             to shared memory; arrive delta_ready
+//   control:  the next chunk's early part may come; P = K''^T (Delta sD) and
+//             O2 = [any; A_qk] (Delta sD) (12 MMAs each, K = 64 tokens; rows
+//             0..63 of O2's A operand are the 8 KiB before A_qk, finite
+//             values whose products land in rows that are never read)
+//   all warps: S <- Diag(d) S + P / sD; the new state's largest magnitude over
+//             the eight warps gives the next sS; S sS as FP16 pairs; arrive
+//             s_ready
+//   O warps (lanes 64..127): O = D1 / sS + O2 / sD once o_done has come,
+//             arrive o_read, store the chunk's output rows
+// The record comes in two parts, each into one region of shared memory: the
+// early part once the Delta warps have read U (D1's MMAs are complete by
+// then), the late part once chunk c - 1's P, O2 and Diag(d) S are done.
 constexpr int VH = 64;
-constexpr int LDS = VH + 4;
-constexpr uint32_t F_REC = 0;
-constexpr uint32_t F_S = 148480;                        // after the record, 1 KiB aligned
-constexpr uint32_t F_D = F_S + DK * LDS * 4;            // Delta [64][68]
-constexpr uint32_t F_BAR = F_D + C * LDS * 4;           // 2 mbarriers
-constexpr uint32_t F_SMEM = F_BAR + 64;
-static_assert(F_S >= R_BYTES && F_SMEM <= 232448, "FP32 scan shared memory");
+constexpr int SCAN_THREADS = NT + 32;
+constexpr int kL2Ahead = 4;                   // records prefetched into L2 this many chunks ahead
+constexpr uint32_t kEpiBar = 1;               // named barrier of the 256 epilogue threads
+constexpr uint32_t kDeltaBar = 2;             // named barrier of the four Delta warps
+constexpr uint32_t F_E = 0;                   // early part: [W; Q'] pairs, 1/s_i
+constexpr uint32_t F_U = R_U;                 //             U of this half of V [64 i][64 v]
+constexpr uint32_t F_L = 82944;               // late part (1 KiB aligned)
+constexpr uint32_t F_S = F_L + 50176;         // S sS pair: MN-major [128 c][64 v] fp16, lo 16 KiB after
+constexpr uint32_t F_D = F_S + 32768;         // Delta sD pair: MN-major [64 i][64 v], lo 8 KiB after
+constexpr uint32_t F_BAR = F_D + 16384;       // 10 mbarriers, TMEM slot, abort flag, maxima, 1/sD
+constexpr uint32_t F_SMEM = F_BAR + 256 + 1024;
+static_assert(F_U + R_UHALF <= F_L && F_L % 1024 == 0 && F_L + R_LATE_BYTES <= F_S, "scan regions");
+static_assert(F_S % 1024 == 0 && F_D % 1024 == 0 && F_SMEM <= 232448, "FP32 scan shared memory");
+constexpr uint32_t F_TM_D1 = 0, F_TM_P = 64, F_TM_O2 = 128, F_TM_REGION = 256, F_TM_COLS = 512;
+
+__device__ __forceinline__ void store_row32(float* p, const float (&o)[32])
+{
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+        reinterpret_cast<float4*>(p)[q] = make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+}
+__device__ __forceinline__ void store_row32(__nv_bfloat16* p, const float (&o)[32])
+{
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const __nv_bfloat162 b2 = __floats2bfloat162_rn(o[8 * q + 2 * e], o[8 * q + 2 * e + 1]);
+            w[e] = *reinterpret_cast<const uint32_t*>(&b2);
+        }
+        reinterpret_cast<uint4*>(p)[q] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+
+__device__ __forceinline__ float warp_max(float x)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+    return x;
+}
 
 template <typename TOut>
-__global__ void __launch_bounds__(NT, 1) fp32_scan_kernel(ChunkArgs args,
-                                                          const int32_t* __restrict__ hdr,
-                                                          const unsigned char* __restrict__ records)
+__global__ void __launch_bounds__(SCAN_THREADS, 1) fp32_scan_kernel(ChunkArgs args,
+                                                                    const int32_t* __restrict__ hdr,
+                                                                    const unsigned char* __restrict__ records)
 {
-    extern __shared__ __align__(16) unsigned char smem_raw[];
-    unsigned char* sm = smem_raw;
-    const float* rw = reinterpret_cast<const float*>(sm + F_REC + R_W);
-    const float* rq = reinterpret_cast<const float*>(sm + F_REC + R_QP);
-    const float* ru = reinterpret_cast<const float*>(sm + F_REC + R_U);
-    const float* rk = reinterpret_cast<const float*>(sm + F_REC + R_KT);
-    const float* ra = reinterpret_cast<const float*>(sm + F_REC + R_AQK);
-    const float* rd = reinterpret_cast<const float*>(sm + F_REC + R_DEC);
-    float (*S)[LDS] = reinterpret_cast<float (*)[LDS]>(sm + F_S);
-    float (*D)[LDS] = reinterpret_cast<float (*)[LDS]>(sm + F_D);
-    uint64_t* bar = reinterpret_cast<uint64_t*>(sm + F_BAR);   // [0] early part, [1] late part
+    extern __shared__ __align__(16) unsigned char smem_raw[];   // aligned to 1 KiB below
+    const uint32_t raw_s = smem_u32(smem_raw);
+    const uint32_t pad = (1024u - (raw_s & 1023u)) & 1023u;
+    unsigned char* sm = smem_raw + pad;
+    const uint32_t sb = raw_s + pad;
 
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const bool ctrl = warp == NT / 32;
+    const int quad = warp & 3, half = (warp >> 2) & 1;
+    const int row = 32 * quad + lane;                      // TMEM lane
+    const bool dwarp = quad < 2;                           // lanes 0..63: W S rows -> Delta
     const int H = args.H;
     const int vh = blockIdx.x & 1, hb = blockIdx.x >> 1;
     const int n = hdr[kPlanOffsets + args.N + 1 + hb / H], h = hb % H;
@@ -584,166 +718,300 @@ __global__ void __launch_bounds__(NT, 1) fp32_scan_kernel(ChunkArgs args,
     if (bos < 0 || eos < bos || (int64_t)eos > args.T) return;   // reported by the plan
     const int nch = (eos - bos + C - 1) / C;
     if (hdr[kPlanOffsets + n] + nch > split_chunk_bound(args.N, args.T)) return;   // bad offsets elsewhere
-    const int v0 = VH * vh;
     const unsigned char* rec0 =
         records + ((int64_t)hdr[kPlanOffsets + n] * H + h) * (int64_t)R_BYTES;
     const int64_t rstride = (int64_t)H * R_BYTES;
     TOut* __restrict__ out = static_cast<TOut*>(args.out);
+    const int v0 = VH * vh + 32 * half;                    // this thread's first column of V
+    // [0] early part, [1] late part, [2] d1_done, [3] p_done, [4] delta_ready
+    // (128), [5] s_ready (NT), [6] drain after a failure, [7] o_done, [8,9]
+    // o_read of even and odd chunks (128)
+    uint64_t* bar = reinterpret_cast<uint64_t*>(sm + F_BAR);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + F_BAR + 80);
+    volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(sm + F_BAR + 84);
+    float* smax = reinterpret_cast<float*>(sm + F_BAR + 96);      // [2][8]: state maxima by warp
+    float* dmax = reinterpret_cast<float*>(sm + F_BAR + 160);     // [2][4]: Delta maxima by warp
+    float* dinv = reinterpret_cast<float*>(sm + F_BAR + 192);     // [2]: 1/sD by chunk parity
 
-    // the entering state slice
-    for (int e = tid; e < DK * VH; e += NT) {
-        const int c = e / VH, m = e % VH;
-        S[c][m] = args.initial_state != nullptr
-                      ? args.initial_state[(((int64_t)n * H + h) * DK + c) * DV + v0 + m]
-                      : 0.f;
+    // The largest |x| over the 256 epilogue threads (exchange `k`, parity-alternating slots).
+    auto epi_max = [&](float mx, int k) -> float {
+        mx = warp_max(mx);
+        float* slot = smax + 8 * (k & 1);
+        if (lane == 0) slot[warp] = mx;
+        named_sync(kEpiBar, NT);
+        const float4 a = reinterpret_cast<const float4*>(slot)[0], b = reinterpret_cast<const float4*>(slot)[1];
+        return fmaxf(fmaxf(fmaxf(a.x, a.y), fmaxf(a.z, a.w)), fmaxf(fmaxf(b.x, b.y), fmaxf(b.z, b.w)));
+    };
+
+    // ---- the entering state: S[row][v0 .. v0 + 31], and its scaled pair
+    float S[32];
+    float s_S = 1.f, inv_S = 1.f;                          // scale of the state's copy
+    if (!ctrl) {
+        if (args.initial_state != nullptr) {
+            const float4* s0 = reinterpret_cast<const float4*>(
+                args.initial_state + (((int64_t)n * H + h) * DK + row) * DV + v0);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const float4 x = s0[q];
+                S[4 * q] = x.x; S[4 * q + 1] = x.y; S[4 * q + 2] = x.z; S[4 * q + 3] = x.w;
+            }
+        } else {
+#pragma unroll
+            for (int u = 0; u < 32; ++u) S[u] = 0.f;
+        }
+        float mx = 0.f;
+#pragma unroll
+        for (int u = 0; u < 32; ++u) mx = fmaxf(mx, fabsf(S[u]));
+        pow2_scale(epi_max(mx, 1), s_S, inv_S);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) st8_pair(sm + F_S, 16384, 0, row, 32 * half + 8 * q, S + 8 * q, s_S);
+    }
+    if (warp == 0) {
+        tmem_alloc(tslot, F_TM_COLS);
+        tmem_relinquish();
     }
     if (tid == 0) {
-        mbar_init(&bar[0], 1);
-        mbar_init(&bar[1], 1);
+        for (int b = 0; b < 10; ++b)
+            mbar_init(&bar[b], (b == 4 || b >= 8) ? NT / 2 : b == 5 ? NT : 1);
+        *abort_flag = 0;
         fence_mbar_init();
-        if (nch > 0) {
-            mbar_arrive_expect_tx(&bar[0], R_EARLY);
-            bulk_g2s(sm + F_REC, rec0, R_EARLY, &bar[0]);
-            mbar_arrive_expect_tx(&bar[1], R_LATE);
-            bulk_g2s(sm + F_REC + R_KT, rec0 + R_KT, R_LATE, &bar[1]);
-        }
     }
+    fence_async_smem();
+    fence_before_sync();
     __syncthreads();
+    fence_after_sync();
+    const uint32_t tmem = *tslot;
+    const uint32_t tlane = tmem + ((uint32_t)(32 * quad) << 16);
 
-    // tiles: A and B use rows i0 .. i0 + 3 and columns m0 .. m0 + 3; C uses
-    // state rows c0 .. c0 + 7 and columns m0 .. m0 + 3
-    const int i0 = (tid >> 4) * 4, m0 = (tid & 15) * 4;
-    const int c0 = (tid >> 4) * 8;
-    int fail_cc = -1;                                      // chunk whose record did not arrive
-    for (int cc = 0; cc < nch; ++cc) {
-        const uint32_t par = cc & 1;
-        const bool more = cc + 1 < nch;
-        const unsigned char* recn = rec0 + (cc + 1) * rstride;
-        if (more && tid == 0) bulk_prefetch_l2(recn, R_BYTES);
-        {
-            const bool ok = mbar_wait(&bar[0], par) && mbar_wait(&bar[1], par);
-            if (__syncthreads_or(!ok)) { fail_cc = cc; break; }
+    auto wait_or_abort = [&](uint64_t* m, uint32_t parity) -> bool {
+        for (uint32_t j = 0; j < kPollsPerCheck; ++j)
+            if (mbar_try_wait(m, parity)) return true;
+        const uint64_t t0 = globaltimer_ns();
+        for (uint32_t i = 0; i < kMaxTimerChecks; ++i) {
+            for (uint32_t j = 0; j < kPollsPerCheck; ++j)
+                if (mbar_try_wait(m, parity)) return true;
+            if (*abort_flag) return false;
+            if (globaltimer_ns() - t0 > kWaitLimitNs) break;
         }
-        // ---- A: W S and Q' S (K = 128)
-        float ws[4][4], qs[4][4];
-#pragma unroll
-        for (int r = 0; r < 4; ++r)
-#pragma unroll
-            for (int x = 0; x < 4; ++x) { ws[r][x] = 0.f; qs[r][x] = 0.f; }
-        for (int c = 0; c < DK; c += 4) {
-            float4 w4[4], q4[4];
-#pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                w4[r] = ld4s(rw + (i0 + r) * DK + c);
-                q4[r] = ld4s(rq + (i0 + r) * DK + c);
+        *abort_flag = 1;
+        return false;
+    };
+
+    if (ctrl) {
+        if (lane == 0) {
+            auto issue_early = [&](int c) {
+                const unsigned char* r = rec0 + c * rstride;
+                mbar_arrive_expect_tx(&bar[0], R_U + R_UHALF);
+                bulk_g2s(sm + F_E, r, R_U, &bar[0]);
+                bulk_g2s(sm + F_U, r + R_U + vh * R_UHALF, R_UHALF, &bar[0]);
+            };
+            auto issue_late = [&](int c) {
+                mbar_arrive_expect_tx(&bar[1], R_LATE_BYTES);
+                bulk_g2s(sm + F_L, rec0 + c * rstride + R_LATE, R_LATE_BYTES, &bar[1]);
+            };
+            // copies issued and copies waited for (at most one of each part in flight)
+            int e_issued = 0, l_issued = 0, e_done = 0, l_done = 0, c = 0;
+            if (nch > 0) {
+                issue_early(0);
+                issue_late(0);
+                e_issued = l_issued = 1;
             }
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float4 s4 = ld4s(&S[c + e][m0]);
-                const float sv[4] = {s4.x, s4.y, s4.z, s4.w};
-#pragma unroll
-                for (int r = 0; r < 4; ++r) {
-                    const float wv = f4at(w4[r], e), qv = f4at(q4[r], e);
-#pragma unroll
-                    for (int x = 0; x < 4; ++x) {
-                        ws[r][x] = fmaf(wv, sv[x], ws[r][x]);
-                        qs[r][x] = fmaf(qv, sv[x], qs[r][x]);
+            for (int cc = 1; cc < min(kL2Ahead, nch); ++cc) bulk_prefetch_l2(rec0 + cc * rstride, R_BYTES);
+            bool fail = false, any_mma = false;
+            constexpr uint32_t id_d1 = idesc(kFmtF16, 128, VH, false, true);
+            constexpr uint32_t id_p = idesc(kFmtF16, 128, VH, true, true);
+            constexpr uint32_t id_o = idesc(kFmtF16, 128, VH, false, true);
+            for (; c < nch; ++c) {
+                const uint32_t R = tmem + F_TM_REGION * (c & 1);
+                if (c > 0) {
+                    // chunk c - 1's state is current, and its P, O2 and d are done
+                    // with the late region
+                    if (!wait_or_abort(&bar[5], (c - 1) & 1) || !wait_or_abort(&bar[7], (c - 1) & 1)) {
+                        fail = true;
+                        break;
                     }
+                    issue_late(c);
+                    ++l_issued;
+                }
+                // chunk c - 2's O has left region (c & 1)
+                if (c > 1 && !wait_or_abort(&bar[8 + (c & 1)], ((c - 2) >> 1) & 1)) { fail = true; break; }
+                if (!wait_or_abort(&bar[0], c & 1)) { fail = true; break; }
+                ++e_done;
+                fence_after_sync();
+#pragma unroll
+                for (int s = 0; s < 8; ++s) {
+                    const uint64_t ah = desc_kmajor(sb + F_E + R_WQ, 128, s);
+                    const uint64_t al = desc_kmajor(sb + F_E + R_WQ_LO, 128, s);
+                    const uint64_t bh = desc_mnmajor64(sb + F_S, s), bl = desc_mnmajor64(sb + F_S + 16384, s);
+                    mma_f16(R + F_TM_D1, ah, bh, id_d1, s > 0);
+                    mma_f16(R + F_TM_D1, ah, bl, id_d1, 1);
+                    mma_f16(R + F_TM_D1, al, bh, id_d1, 1);
+                }
+                commit(&bar[2]);
+                any_mma = true;
+                if (c + kL2Ahead < nch) bulk_prefetch_l2(rec0 + (c + kL2Ahead) * rstride, R_BYTES);
+                if (!wait_or_abort(&bar[4], c & 1)) { fail = true; break; }
+                // D1's MMAs are complete (the Delta warps waited for them) and U is read
+                if (c + 1 < nch) {
+                    issue_early(c + 1);
+                    ++e_issued;
+                }
+                if (!wait_or_abort(&bar[1], c & 1)) { fail = true; break; }
+                ++l_done;
+                fence_after_sync();
+#pragma unroll
+                for (int s = 0; s < 4; ++s) {
+                    const uint64_t ah = desc_mnmajor128(sb + F_L + L_KT, 8192, s);
+                    const uint64_t al = desc_mnmajor128(sb + F_L + L_KT_LO, 8192, s);
+                    const uint64_t bh = desc_mnmajor64(sb + F_D, s), bl = desc_mnmajor64(sb + F_D + 8192, s);
+                    mma_f16(R + F_TM_P, ah, bh, id_p, s > 0);
+                    mma_f16(R + F_TM_P, ah, bl, id_p, 1);
+                    mma_f16(R + F_TM_P, al, bh, id_p, 1);
+                }
+                commit(&bar[3]);
+#pragma unroll
+                for (int s = 0; s < 4; ++s) {
+                    const uint64_t ah = desc_kmajor(sb + F_L + L_AQK - 8192, 128, s);
+                    const uint64_t al = desc_kmajor(sb + F_L + L_AQK_LO - 8192, 128, s);
+                    const uint64_t bh = desc_mnmajor64(sb + F_D, s), bl = desc_mnmajor64(sb + F_D + 8192, s);
+                    mma_f16(R + F_TM_O2, ah, bh, id_o, s > 0);
+                    mma_f16(R + F_TM_O2, ah, bl, id_o, 1);
+                    mma_f16(R + F_TM_O2, al, bh, id_o, 1);
+                }
+                commit(&bar[7]);
+            }
+            if (fail) {
+                *abort_flag = 1;
+                report_status(args.status, KDA_ERR_TIMEOUT);
+                // the MMAs and copies in flight finish before the CTA leaves
+                if (any_mma) {
+                    commit(&bar[6]);
+                    mbar_wait(&bar[6], 0);
+                }
+                if (e_issued > e_done) mbar_wait(&bar[0], (e_issued - 1) & 1);
+                if (l_issued > l_done) mbar_wait(&bar[1], (l_issued - 1) & 1);
+            }
+        }
+    } else {
+        float nan_acc = 0.f;
+        // test hook: CTA 0 withholds its first delta_ready arrival
+        const bool withhold = args.fault == KDA_TEST_FAULT_SCAN && blockIdx.x == 0;
+        bool fail = false;
+        const float* winv = reinterpret_cast<const float*>(sm + F_E + R_WINV);
+        const float* dec = reinterpret_cast<const float*>(sm + F_L + L_DEC);
+        for (int c = 0; c < nch; ++c) {
+            const uint32_t R = tlane + F_TM_REGION * (c & 1);
+            {
+                // (an O warp that gave up on the previous chunk carries `fail` here)
+                const bool ok = !fail && (!dwarp || wait_or_abort(&bar[0], c & 1));
+                if (named_sync_or(kEpiBar, NT, !ok)) { fail = true; break; }
+            }
+            if (dwarp) {
+                // U[i][v0 .. v0 + 31] (i = row), read while D1 runs
+                float u[32];
+                const unsigned char* up = sm + F_U + row * 256;
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const int p = 8 * half + q;
+                    const float4 x = *reinterpret_cast<const float4*>(up + ((p ^ (row & 7)) << 4));
+                    u[4 * q] = x.x; u[4 * q + 1] = x.y; u[4 * q + 2] = x.z; u[4 * q + 3] = x.w;
+                }
+                const float wsc = winv[row] * inv_S;
+                const bool ok = wait_or_abort(&bar[2], c & 1);
+                if (named_sync_or(kDeltaBar, NT / 2, !ok)) {
+                    fail = true;                           // the others see the abort flag
+                } else {
+                    fence_after_sync();
+                    // Delta = U - W S; then its pair at scale sD
+                    float ws[32];
+                    tmem_ld32(R + F_TM_D1 + 32 * half, ws);
+                    float mx = 0.f;
+#pragma unroll
+                    for (int x = 0; x < 32; ++x) {
+                        u[x] = fmaf(-ws[x], wsc, u[x]);
+                        mx = fmaxf(mx, fabsf(u[x]));
+                    }
+                    mx = warp_max(mx);
+                    float* slot = dmax + 4 * (c & 1);
+                    if (lane == 0) slot[quad + 2 * half] = mx;
+                    named_sync(kDeltaBar, NT / 2);
+                    const float4 m4 = *reinterpret_cast<const float4*>(slot);
+                    float s_D, inv_D;
+                    pow2_scale(fmaxf(fmaxf(m4.x, m4.y), fmaxf(m4.z, m4.w)), s_D, inv_D);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        st8_pair(sm + F_D, 8192, 0, row, 32 * half + 8 * q, u + 8 * q, s_D);
+                    if (tid == 0) dinv[c & 1] = inv_D;
+                    fence_async_smem();
+                    fence_before_sync();
+                    if (!(withhold && c == 0)) mbar_arrive(&bar[4]);
+                }
+            }
+            {
+                const bool ok = !fail && wait_or_abort(&bar[3], c & 1) && wait_or_abort(&bar[1], c & 1);
+                if (named_sync_or(kEpiBar, NT, !ok)) { fail = true; break; }
+            }
+            fence_after_sync();
+            const float inv_D = dinv[c & 1];
+            const float inv_S_used = inv_S;                // the scale of this chunk's D1
+            {
+                // S <- Diag(d) S + P / sD; the new state's pair at its own scale
+                const float dc = dec[row];
+                float p[32];
+                tmem_ld32(R + F_TM_P + 32 * half, p);
+                float mx = 0.f;
+#pragma unroll
+                for (int u = 0; u < 32; ++u) {
+                    S[u] = fmaf(S[u], dc, p[u] * inv_D);
+                    mx = fmaxf(mx, fabsf(S[u]));
+                }
+                pow2_scale(epi_max(mx, c), s_S, inv_S);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) st8_pair(sm + F_S, 16384, 0, row, 32 * half + 8 * q, S + 8 * q, s_S);
+            }
+            fence_async_smem();
+            fence_before_sync();
+            mbar_arrive(&bar[5]);
+            if (!dwarp) {
+                // O rows (token i = row - 64) leave TMEM, then go out from registers
+                const bool ok = wait_or_abort(&bar[7], c & 1);
+                if (ok) {
+                    fence_after_sync();
+                    float o[32], o2[32];
+                    tmem_ld32x2(R + F_TM_D1 + 32 * half, R + F_TM_O2 + 32 * half, o, o2);
+                    fence_before_sync();
+                    mbar_arrive(&bar[8 + (c & 1)]);
+                    const int i = row - 64, t = bos + c * C + i;
+                    if (t < eos) {
+                        TOut* op = out + ((int64_t)t * H + h) * DV + v0;
+#pragma unroll
+                        for (int u = 0; u < 32; ++u) {
+                            o[u] = args.scale * fmaf(o[u], inv_S_used, o2[u] * inv_D);
+                            nan_acc = fmaf(o[u], 0.f, nan_acc);
+                        }
+                        store_row32(op, o);
+                    }
+                } else {
+                    fail = true;                           // seen at the next chunk's barrier
                 }
             }
         }
+        if (fail) {
+            *abort_flag = 1;
+            if (tid == 0) report_status(args.status, KDA_ERR_TIMEOUT);
+        } else if (args.final_state != nullptr) {
+            float4* fs = reinterpret_cast<float4*>(args.final_state + (((int64_t)n * H + h) * DK + row) * DV + v0);
 #pragma unroll
-        for (int r = 0; r < 4; ++r) {
-            const float4 u4 = ld4s(ru + (i0 + r) * DV + v0 + m0);
-            *reinterpret_cast<float4*>(&D[i0 + r][m0]) =
-                make_float4(u4.x - ws[r][0], u4.y - ws[r][1], u4.z - ws[r][2], u4.w - ws[r][3]);
+            for (int u = 0; u < 32; ++u) nan_acc = fmaf(S[u], 0.f, nan_acc);
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                fs[q] = make_float4(S[4 * q], S[4 * q + 1], S[4 * q + 2], S[4 * q + 3]);
         }
-        __syncthreads();
-        // W, Q' and U of this record are read: the next one's early part may come
-        if (more && tid == 0) {
-            mbar_arrive_expect_tx(&bar[0], R_EARLY);
-            bulk_g2s(sm + F_REC, recn, R_EARLY, &bar[0]);
-        }
-        // ---- B: O = scale (Q' S + A_qk Delta), lower-triangular A_qk
-        {
-            const int tc = bos + cc * C;
-            for (int j = 0; j <= i0 + 3; j += 4) {
-                float4 a4[4];
-#pragma unroll
-                for (int r = 0; r < 4; ++r) a4[r] = ld4s(ra + (i0 + r) * C + j);
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float4 d4 = ld4s(&D[j + e][m0]);
-                    const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
-#pragma unroll
-                    for (int r = 0; r < 4; ++r) {
-                        const float av = f4at(a4[r], e);   // 0 above the diagonal
-#pragma unroll
-                        for (int x = 0; x < 4; ++x) qs[r][x] = fmaf(av, dv[x], qs[r][x]);
-                    }
-                }
-            }
-#pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                const int t = tc + i0 + r;
-                if (t < eos) {
-                    TOut* op = out + ((int64_t)t * H + h) * DV + v0 + m0;
-#pragma unroll
-                    for (int x = 0; x < 4; ++x) {
-                        const float y = args.scale * qs[r][x];
-                        if constexpr (sizeof(TOut) == 4) op[x] = y;
-                        else op[x] = __float2bfloat16_rn(y);
-                    }
-                }
-            }
-        }
-        // ---- C: S <- Diag(d) S + K''^T Delta (K = 64 tokens)
-        {
-            float sn[8][4];
-#pragma unroll
-            for (int r = 0; r < 8; ++r) {
-                const float dc = rd[c0 + r];
-                const float4 s4 = ld4s(&S[c0 + r][m0]);
-                sn[r][0] = dc * s4.x; sn[r][1] = dc * s4.y; sn[r][2] = dc * s4.z; sn[r][3] = dc * s4.w;
-            }
-            for (int i = 0; i < C; ++i) {
-                const float4 ka = ld4s(rk + i * DK + c0), kb = ld4s(rk + i * DK + c0 + 4);
-                const float kv[8] = {ka.x, ka.y, ka.z, ka.w, kb.x, kb.y, kb.z, kb.w};
-                const float4 d4 = ld4s(&D[i][m0]);
-                const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
-#pragma unroll
-                for (int r = 0; r < 8; ++r)
-#pragma unroll
-                    for (int x = 0; x < 4; ++x) sn[r][x] = fmaf(kv[r], dv[x], sn[r][x]);
-            }
-            __syncthreads();                               // every read of S and the record is done
-#pragma unroll
-            for (int r = 0; r < 8; ++r)
-                *reinterpret_cast<float4*>(&S[c0 + r][m0]) =
-                    make_float4(sn[r][0], sn[r][1], sn[r][2], sn[r][3]);
-        }
-        if (more && tid == 0) {
-            mbar_arrive_expect_tx(&bar[1], R_LATE);
-            bulk_g2s(sm + F_REC + R_KT, recn + R_KT, R_LATE, &bar[1]);
-        }
+        if (nan_acc != nan_acc) report_status(args.status, KDA_ERR_RANGE);
     }
+    fence_before_sync();
     __syncthreads();
-    if (fail_cc >= 0) {
-        // the copies of that chunk's record land (or the wait gives up) before
-        // the CTA leaves; no later copy was issued
-        if (tid == 0) {
-            report_status(args.status, KDA_ERR_TIMEOUT);
-            mbar_wait(&bar[0], fail_cc & 1);
-            mbar_wait(&bar[1], fail_cc & 1);
-        }
-        return;
-    }
-    if (args.final_state != nullptr) {
-        for (int e = tid; e < DK * VH; e += NT) {
-            const int c = e / VH, m = e % VH;
-            args.final_state[(((int64_t)n * H + h) * DK + c) * DV + v0 + m] = S[c][m];
-        }
-    }
+    if (warp == 0) tmem_dealloc(tmem, F_TM_COLS);
 }
 
 template <typename TIn, int kGate>
@@ -792,7 +1060,7 @@ cudaError_t launch_chunk_fp32_split(const ChunkArgs& a, int64_t chunks, cudaStre
     auto kern = a.out_bf16 ? fp32_scan_kernel<__nv_bfloat16> : fp32_scan_kernel<float>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)F_SMEM);
     if (e != cudaSuccess) return e;
-    kern<<<(unsigned)(2 * (int64_t)a.N * a.H), NT, F_SMEM, stream>>>(a, hdr, rec);
+    kern<<<(unsigned)(2 * (int64_t)a.N * a.H), SCAN_THREADS, F_SMEM, stream>>>(a, hdr, rec);
     return cudaGetLastError();
 }
 

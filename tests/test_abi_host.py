@@ -114,11 +114,11 @@ def test_workspace_size_bound():
         if N:
             lens[-1] += T - sum(lens)
         assert sum(-(-L // 64) for L in lens) <= T // 64 + N
-    # FP32-exact mode in two phases: the header and one 147968-byte FP32 record
+    # FP32-exact mode in two phases: the header and one 148224-byte record
     # per (chunk bound, head)
     hdr2 = -(-(4 * (2 * 2 + 9)) // 1024) * 1024
     assert workspace_size(lib, 2, 100, 3, mode=1) == (binding.KDA_OK,
-                                                      hdr2 + (100 // 64 + 2) * 3 * 147968)
+                                                      hdr2 + (100 // 64 + 2) * 3 * 148224)
     assert workspace_size(lib, 2, 100, 3, K=64)[0] == binding.KDA_ERR_UNSUPPORTED
     assert workspace_size(lib, -1, 100, 3)[0] == binding.KDA_ERR_INVALID_ARG
     assert workspace_size(lib, 2, 100, 3, mode=7)[0] == binding.KDA_ERR_INVALID_ARG
