@@ -148,3 +148,21 @@ def test_values_beyond_fp16_are_reported(path):
     v = (ri.x.v.float() * 3.0e4).to(ri.x.v.dtype)
     _, _, status = run_gpu(ri, path, v_override=v)
     assert status == KDA_ERR_RANGE
+
+
+@pytest.mark.parametrize("path", ["fp32_exact", "fp32_two_phase"])
+def test_fp32_paths_keep_fp32_range(path):
+    """|v| about 1e5, beyond FP16: the FP32-exact paths still match the oracle.
+    The two-phase path's tensor-core scan holds the state and Delta as FP16
+    pairs scaled per chunk by a power of two, so FP16's range does not apply."""
+    ri = regime("alog_0.05", "packed_5000_3000_192")
+    x = ri.x
+    v = (x.v.float() * 3.0e4).to(x.v.dtype)
+    g, beta = oracle.gate(f64(x.f), f64(x.A_log), f64(x.dt_bias), f64(x.b))
+    o_ref, S_ref = oracle.forward(f64(x.q), f64(x.k), f64(v), g, beta, x.cu_seqlens.numpy(),
+                                  x.scale)
+    out, S, status = run_gpu(ri, path, v_override=v)
+    assert status == 0
+    e_o, e_S = rel_l2(out.double().numpy(), o_ref), rel_l2(S.double().numpy(), S_ref)
+    print(f"{path} |v| ~ 1e5: out rel-L2 {e_o:.3e}, final state rel-L2 {e_S:.3e}")
+    assert e_o <= TOL[path] and e_S <= TOL[path]
