@@ -649,9 +649,10 @@ __global__ void __launch_bounds__(NT, 1) fp32_prep_kernel(ChunkArgs args,
 //             s_ready
 //   O warps (lanes 64..127): O = D1 / sS + O2 / sD once o_done has come,
 //             arrive o_read, store the chunk's output rows
-// The record comes in two parts, each into one region of shared memory: the
-// early part once the Delta warps have read U (D1's MMAs are complete by
-// then), the late part once chunk c - 1's P, O2 and Diag(d) S are done.
+// The record comes in three copies, each into one region of shared memory:
+// the [W; Q'] pairs once D1's MMAs are complete, U and 1/s_i once the Delta
+// warps have read them, the late part once chunk c - 1's P, O2 and Diag(d) S
+// are done.
 constexpr int VH = 64;
 constexpr int SCAN_THREADS = NT + 32;
 constexpr int kL2Ahead = 4;                   // records prefetched into L2 this many chunks ahead
@@ -723,15 +724,15 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) fp32_scan_kernel(ChunkArgs ar
     const int64_t rstride = (int64_t)H * R_BYTES;
     TOut* __restrict__ out = static_cast<TOut*>(args.out);
     const int v0 = VH * vh + 32 * half;                    // this thread's first column of V
-    // [0] early part, [1] late part, [2] d1_done, [3] p_done, [4] delta_ready
-    // (128), [5] s_ready (NT), [6] drain after a failure, [7] o_done, [8,9]
-    // o_read of even and odd chunks (128)
+    // [0] [W; Q'] pairs, [1] late part, [2] d1_done, [3] p_done, [4]
+    // delta_ready (128), [5] s_ready (NT), [6] drain after a failure, [7]
+    // o_done, [8,9] o_read of even and odd chunks (128), [10] U and 1/s_i
     uint64_t* bar = reinterpret_cast<uint64_t*>(sm + F_BAR);
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + F_BAR + 80);
-    volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(sm + F_BAR + 84);
-    float* smax = reinterpret_cast<float*>(sm + F_BAR + 96);      // [2][8]: state maxima by warp
-    float* dmax = reinterpret_cast<float*>(sm + F_BAR + 160);     // [2][4]: Delta maxima by warp
-    float* dinv = reinterpret_cast<float*>(sm + F_BAR + 192);     // [2]: 1/sD by chunk parity
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + F_BAR + 96);
+    volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(sm + F_BAR + 100);
+    float* smax = reinterpret_cast<float*>(sm + F_BAR + 128);     // [2][8]: state maxima by warp
+    float* dmax = reinterpret_cast<float*>(sm + F_BAR + 192);     // [2][4]: Delta maxima by warp
+    float* dinv = reinterpret_cast<float*>(sm + F_BAR + 224);     // [2]: 1/sD by chunk parity
 
     // The largest |x| over the 256 epilogue threads (exchange `k`, parity-alternating slots).
     auto epi_max = [&](float mx, int k) -> float {
@@ -771,8 +772,8 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) fp32_scan_kernel(ChunkArgs ar
         tmem_relinquish();
     }
     if (tid == 0) {
-        for (int b = 0; b < 10; ++b)
-            mbar_init(&bar[b], (b == 4 || b >= 8) ? NT / 2 : b == 5 ? NT : 1);
+        for (int b = 0; b < 11; ++b)
+            mbar_init(&bar[b], (b == 4 || b == 8 || b == 9) ? NT / 2 : b == 5 ? NT : 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -799,22 +800,29 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) fp32_scan_kernel(ChunkArgs ar
 
     if (ctrl) {
         if (lane == 0) {
-            auto issue_early = [&](int c) {
+            // the early part in two copies: [W; Q'] once D1 has read the last
+            // one, U and 1/s_i once the Delta warps have
+            auto issue_wq = [&](int c) {
+                mbar_arrive_expect_tx(&bar[0], R_WINV);
+                bulk_g2s(sm + F_E, rec0 + c * rstride, R_WINV, &bar[0]);
+            };
+            auto issue_u = [&](int c) {
                 const unsigned char* r = rec0 + c * rstride;
-                mbar_arrive_expect_tx(&bar[0], R_U + R_UHALF);
-                bulk_g2s(sm + F_E, r, R_U, &bar[0]);
-                bulk_g2s(sm + F_U, r + R_U + vh * R_UHALF, R_UHALF, &bar[0]);
+                mbar_arrive_expect_tx(&bar[10], (R_U - R_WINV) + R_UHALF);
+                bulk_g2s(sm + F_E + R_WINV, r + R_WINV, R_U - R_WINV, &bar[10]);
+                bulk_g2s(sm + F_U, r + R_U + vh * R_UHALF, R_UHALF, &bar[10]);
             };
             auto issue_late = [&](int c) {
                 mbar_arrive_expect_tx(&bar[1], R_LATE_BYTES);
                 bulk_g2s(sm + F_L, rec0 + c * rstride + R_LATE, R_LATE_BYTES, &bar[1]);
             };
-            // copies issued and copies waited for (at most one of each part in flight)
-            int e_issued = 0, l_issued = 0, e_done = 0, l_done = 0, c = 0;
+            // copies issued (at most one of each part in flight)
+            int w_issued = 0, u_issued = 0, l_issued = 0, c = 0;
             if (nch > 0) {
-                issue_early(0);
+                issue_wq(0);
+                issue_u(0);
                 issue_late(0);
-                e_issued = l_issued = 1;
+                w_issued = u_issued = l_issued = 1;
             }
             for (int cc = 1; cc < min(kL2Ahead, nch); ++cc) bulk_prefetch_l2(rec0 + cc * rstride, R_BYTES);
             bool fail = false, any_mma = false;
@@ -836,7 +844,6 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) fp32_scan_kernel(ChunkArgs ar
                 // chunk c - 2's O has left region (c & 1)
                 if (c > 1 && !wait_or_abort(&bar[8 + (c & 1)], ((c - 2) >> 1) & 1)) { fail = true; break; }
                 if (!wait_or_abort(&bar[0], c & 1)) { fail = true; break; }
-                ++e_done;
                 fence_after_sync();
 #pragma unroll
                 for (int s = 0; s < 8; ++s) {
@@ -850,14 +857,19 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) fp32_scan_kernel(ChunkArgs ar
                 commit(&bar[2]);
                 any_mma = true;
                 if (c + kL2Ahead < nch) bulk_prefetch_l2(rec0 + (c + kL2Ahead) * rstride, R_BYTES);
-                if (!wait_or_abort(&bar[4], c & 1)) { fail = true; break; }
-                // D1's MMAs are complete (the Delta warps waited for them) and U is read
                 if (c + 1 < nch) {
-                    issue_early(c + 1);
-                    ++e_issued;
+                    // D1's MMAs are complete: the next [W; Q'] may come
+                    if (!wait_or_abort(&bar[2], c & 1)) { fail = true; break; }
+                    issue_wq(c + 1);
+                    ++w_issued;
+                }
+                if (!wait_or_abort(&bar[4], c & 1)) { fail = true; break; }
+                // the Delta warps have read U and 1/s_i
+                if (c + 1 < nch) {
+                    issue_u(c + 1);
+                    ++u_issued;
                 }
                 if (!wait_or_abort(&bar[1], c & 1)) { fail = true; break; }
-                ++l_done;
                 fence_after_sync();
 #pragma unroll
                 for (int s = 0; s < 4; ++s) {
@@ -888,8 +900,10 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) fp32_scan_kernel(ChunkArgs ar
                     commit(&bar[6]);
                     mbar_wait(&bar[6], 0);
                 }
-                if (e_issued > e_done) mbar_wait(&bar[0], (e_issued - 1) & 1);
-                if (l_issued > l_done) mbar_wait(&bar[1], (l_issued - 1) & 1);
+                // the last copy of each part has landed (no later one was issued)
+                if (w_issued > 0) mbar_wait(&bar[0], (w_issued - 1) & 1);
+                if (u_issued > 0) mbar_wait(&bar[10], (u_issued - 1) & 1);
+                if (l_issued > 0) mbar_wait(&bar[1], (l_issued - 1) & 1);
             }
         }
     } else {
@@ -903,7 +917,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) fp32_scan_kernel(ChunkArgs ar
             const uint32_t R = tlane + F_TM_REGION * (c & 1);
             {
                 // (an O warp that gave up on the previous chunk carries `fail` here)
-                const bool ok = !fail && (!dwarp || wait_or_abort(&bar[0], c & 1));
+                const bool ok = !fail && (!dwarp || wait_or_abort(&bar[10], c & 1));
                 if (named_sync_or(kEpiBar, NT, !ok)) { fail = true; break; }
             }
             if (dwarp) {
