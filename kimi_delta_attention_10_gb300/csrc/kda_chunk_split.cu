@@ -28,12 +28,14 @@
 //   A_qk    fp16 [64 i][64 j]   (K-major B of [A_qk Delta]^T; strictly upper part 0)
 //   K''^T   fp16 [128 c][64 j]  (K-major B of [K''^T Delta]^T)
 //   d       fp32 [128]
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <stdint.h>
 
 #include <atomic>
+#include <cstring>
 #include <mutex>
 
 #include "kda_internal.cuh"
@@ -174,12 +176,18 @@ constexpr uint32_t P_RK = P_RQ + 256;  // 1/|k_t|
 constexpr uint32_t P_DQK = P_RK + 256; // q^_t . k^_t
 constexpr uint32_t P_BETA = P_DQK + 256;
 constexpr uint32_t P_TOT = P_BETA + 256;   // half-chunk decay fp32 [2][128]
-constexpr uint32_t P_BAR = P_TOT + 1024;   // 8 mbarriers, TMEM slot, the next units
-constexpr uint32_t P_SMEM = P_BAR + 128 + 1024;
+constexpr uint32_t P_BAR = P_TOT + 1024;   // 10 mbarriers, TMEM slot, the next units
+constexpr uint32_t P_SMEM = P_BAR + 256 + 1024;
 static_assert(P_TF + C * LDA * 4 <= P_XT, "A_kk and T fit below X'^T");
 static_assert(P_PAIR + 49152 <= P_XT, "pair-sum operands fit below X'^T");
 static_assert(2 * (P_SMEM + 1024) <= 233472, "two preparation CTAs per SM");
 constexpr uint32_t P_TM_A = 0, P_TM_W = 0, P_TM_U = 64, P_TM_COLS = 256;
+
+// TMA descriptors of the preparation's inputs, each a [T][H][128] tensor read
+// as boxes of 64 rows of one head: q, k, v (16-bit inputs only) and g or f.
+struct PrepMaps {
+    CUtensorMap q, k, v, g;
+};
 
 // Where one (chunk, head) unit lies in the packed input.
 struct UnitLoc {
@@ -189,12 +197,13 @@ struct UnitLoc {
 
 // Persistent: each CTA takes units in order from the window's counter (so CTAs
 // that start late, on SMs a scan frees, find the work already shared out) and
-// keeps its tensor memory and barriers across them.  The next unit's 16-bit
-// inputs are staged while the current one finishes: q, k (and f in BF16) as
-// soon as the inverse has freed their region, v (and an FP32 g or f) once the
-// W/U MMAs have read X'^T and V^T.
+// keeps its tensor memory and barriers across them.  The next unit's inputs
+// are staged by TMA tile loads while the current one finishes: q, k (and f in
+// BF16) as soon as the inverse has freed their region, v (and an FP32 g or f)
+// once the W/U MMAs have read X'^T and V^T.
 template <typename TIn, int kGate>
 __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(ChunkArgs args,
+                                                           const __grid_constant__ PrepMaps maps,
                                                            const int32_t* __restrict__ hdr,
                                                            unsigned char* __restrict__ records,
                                                            int64_t unit_base, int64_t units,
@@ -238,6 +247,8 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(ChunkArgs args,
     uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + P_BAR + 64);
     // [0] the CTA's first unit, [1] the unit after the current one
     UnitLoc* s_loc = reinterpret_cast<UnitLoc*>(sm + P_BAR + 80);
+    // the staging of a unit's inputs: [0] early part, [1] late part (one phase per unit)
+    uint64_t* sbar = reinterpret_cast<uint64_t*>(sm + P_BAR + 128);
     // test hook: CTA 0 withholds its first MMA group and the commit that signals it
     const bool withhold = args.fault == KDA_TEST_FAULT_PREP && blockIdx.x == 0;
 
@@ -247,9 +258,12 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(ChunkArgs args,
     const TG* __restrict__ graw =
         kGated ? static_cast<const TG*>(args.f) : reinterpret_cast<const TG*>(args.g);
     using ST = Stage<TIn>;
-    constexpr bool k16 = sizeof(TIn) == 2;                 // 16-bit inputs: staged by cp.async
+    constexpr bool k16 = sizeof(TIn) == 2;                 // 16-bit inputs: staged by TMA
     constexpr bool kGEarly = sizeof(TG) == 2;              // a BF16 f fits beside q and k
     constexpr int GP = DK * (int)sizeof(TG) / 16;          // 16-byte pieces per g/f row
+    constexpr uint32_t kRow16 = C * DK * 2, kRowG = C * DK * sizeof(TG);   // bytes of one box
+    constexpr uint32_t kEarlyBytes = (k16 ? 2 * kRow16 : 0) + (kGEarly ? kRowG : 0);
+    constexpr uint32_t kLateBytes = (k16 ? kRow16 : 0) + (kGEarly ? 0 : kRowG);
 
     // The next unit of this window, taken from its counter and located in the
     // packed input by one thread (its dependent loads of the offsets run while
@@ -274,40 +288,32 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(ChunkArgs args,
         }
         *slot = u;
     };
-    auto stage16 = [&](uint32_t so, const TIn* base, const UnitLoc& u) {
-#pragma unroll
-        for (int k = 0; k < C * 16 / NT; ++k) {
-            const int e = tid + k * NT, r = e >> 4, pc = e & 15;
-            const bool ok = r < u.L;
-            const int64_t src = ((int64_t)(u.t0 + (ok ? r : 0)) * H + u.h) * DK + pc * 8;
-            cp_async16(sm + so + r * 256 + pc * 16, base + src, ok);
-        }
-    };
-    auto stage_g = [&](const UnitLoc& u) {
-#pragma unroll
-        for (int k = 0; k < C * GP / NT; ++k) {
-            const int e = tid + k * NT, r = e / GP, pc = e % GP;
-            const bool ok = r < u.L;
-            cp_async16(sm + P_SG + e * 16,
-                       graw + ((int64_t)(u.t0 + (ok ? r : 0)) * H + u.h) * DK +
-                           pc * (16 / (int)sizeof(TG)),
-                       ok);
-        }
-    };
+    // The staging copies, issued by thread 0: 64 rows of one head, dense
+    // [64][128] in shared memory.  Rows past the end of the tensor arrive as
+    // zeros; rows of the next sequence inside a packed batch are cleared at the
+    // top of the unit.  Thread 0 counts the copies of each part issued and
+    // waited for (s_cnt: [0, 1] early, [2, 3] late).
+    int32_t* s_cnt = reinterpret_cast<int32_t*>(sm + P_BAR + 144);
     // q, k (and a BF16 f): their region is free once the inverse is done
     auto stage_early = [&](const UnitLoc& u) {
-        if constexpr (k16) {
-            stage16(P_SQ, gq, u);
-            stage16(P_SK, gk, u);
+        if (tid == 0 && kEarlyBytes > 0) {
+            mbar_arrive_expect_tx(&sbar[0], kEarlyBytes);
+            if constexpr (k16) {
+                tma_load_3d(sm + P_SQ, &maps.q, 0, u.h, u.t0, &sbar[0]);
+                tma_load_3d(sm + P_SK, &maps.k, 0, u.h, u.t0, &sbar[0]);
+            }
+            if constexpr (kGEarly) tma_load_3d(sm + P_SG, &maps.g, 0, u.h, u.t0, &sbar[0]);
+            ++s_cnt[0];
         }
-        if constexpr (kGEarly) stage_g(u);
-        cp_async_commit();
     };
     // v (and an FP32 g or f): free once the W/U MMAs have read X'^T and V^T
     auto stage_late = [&](const UnitLoc& u) {
-        if constexpr (k16) stage16(P_SV, gv, u);
-        if constexpr (!kGEarly) stage_g(u);
-        cp_async_commit();
+        if (tid == 0 && kLateBytes > 0) {
+            mbar_arrive_expect_tx(&sbar[1], kLateBytes);
+            if constexpr (k16) tma_load_3d(sm + P_SV, &maps.v, 0, u.h, u.t0, &sbar[1]);
+            if constexpr (!kGEarly) tma_load_3d(sm + P_SG, &maps.g, 0, u.h, u.t0, &sbar[1]);
+            ++s_cnt[2];
+        }
     };
 
     if (warp == 0) {
@@ -316,6 +322,9 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(ChunkArgs args,
     }
     if (tid == 0) {
         for (int b = 0; b < 8; ++b) mbar_init(&bar[b], b >= 5 ? NT : 1);
+        mbar_init(&sbar[0], 1);
+        mbar_init(&sbar[1], 1);
+        for (int i = 0; i < 4; ++i) s_cnt[i] = 0;
         fence_mbar_init();
         grab_locate(&s_loc[0]);
     }
@@ -409,8 +418,31 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(ChunkArgs args,
             sbeta[tid] = xb;
         }
         if (tid == 4 * 32) grab_locate(&s_loc[1]);          // read after the inverse
-        cp_async_wait_all();
-        __syncthreads();
+        {
+            const bool ok_e = kEarlyBytes == 0 || mbar_wait(&sbar[0], ph);
+            const bool ok_l = kLateBytes == 0 || mbar_wait(&sbar[1], ph);
+            const bool ok = ok_e && ok_l;
+            if (tid == 0) {
+                if (kEarlyBytes > 0 && ok_e) ++s_cnt[1];
+                if (kLateBytes > 0 && ok_l) ++s_cnt[3];
+            }
+            if (__syncthreads_or(!ok)) { failed = true; break; }
+        }
+        if (L < C) {
+            // the staged rows past the sequence end hold the next sequence's
+            // tokens: zero (decay 1)
+            if constexpr (k16) {
+                for (int e = tid; e < (C - L) * 16; e += NT) {
+                    const uint32_t o = (uint32_t)(L + (e >> 4)) * 256 + (e & 15) * 16;
+                    *reinterpret_cast<uint4*>(sm + P_SQ + o) = make_uint4(0, 0, 0, 0);
+                    *reinterpret_cast<uint4*>(sm + P_SK + o) = make_uint4(0, 0, 0, 0);
+                    *reinterpret_cast<uint4*>(sm + P_SV + o) = make_uint4(0, 0, 0, 0);
+                }
+            }
+            for (int e = tid; e < (C - L) * GP; e += NT)
+                *reinterpret_cast<uint4*>(sm + P_SG + (uint32_t)L * GP * 16 + e * 16) = make_uint4(0, 0, 0, 0);
+            __syncthreads();
+        }
 
         // ---- 2: row norms and q^ . k^
         chunk_norms<TIn>(sm + P_SQ, sm + P_SK, rq, rk, dqk, args.l2norm != 0, tid);
@@ -531,7 +563,9 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(ChunkArgs args,
         commit(&bar[4]);
         mbar_wait(&bar[4], 0);
     }
-    cp_async_wait_all();                                   // staging of a next unit, if any
+    // the staging of a next unit, if any, lands before the CTA leaves
+    if (tid == 0 && s_cnt[0] > s_cnt[1]) mbar_wait(&sbar[0], (s_cnt[0] - 1) & 1);
+    if (tid == 0 && s_cnt[2] > s_cnt[3]) mbar_wait(&sbar[1], (s_cnt[2] - 1) & 1);
     fence_before_sync();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, P_TM_COLS);
@@ -1231,10 +1265,67 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) chunk_scan_vh_kernel(ChunkArg
 }
 
 // ---------------------------------------------------------------- launch
+// cuTensorMapEncodeTiled from the driver (through the runtime, so the library
+// needs no link to it); null when the driver does not provide it.
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_tiled()
+{
+    static const EncodeTiledFn fn = [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return static_cast<EncodeTiledFn>(nullptr);
+        return reinterpret_cast<EncodeTiledFn>(p);
+    }();
+    return fn;
+}
+
+// The descriptor of a [T][H][128] tensor (BF16 or FP32, dense rows) read as
+// boxes of 64 tokens x 1 head x 128 values; reads past T return zeros.
+cudaError_t encode_rows(CUtensorMap* m, const void* base, bool bf16, int64_t T, int32_t H)
+{
+    const EncodeTiledFn fn = encode_tiled();
+    if (fn == nullptr) return cudaErrorNotSupported;
+    const uint32_t es = bf16 ? 2 : 4;
+    const cuuint64_t dims[3] = {(cuuint64_t)DK, (cuuint64_t)H, (cuuint64_t)T};
+    const cuuint64_t strides[2] = {(cuuint64_t)DK * es, (cuuint64_t)H * DK * es};
+    const cuuint32_t box[3] = {(cuuint32_t)DK, 1, (cuuint32_t)C};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3,
+                          const_cast<void*>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+// The preparation's descriptors for this call: q, k, v when they are 16-bit
+// (FP32 inputs are read through registers), and g or f.
+cudaError_t make_prep_maps(const ChunkArgs& a, PrepMaps* maps)
+{
+    memset(maps, 0, sizeof(*maps));
+    cudaError_t e = cudaSuccess;
+    if (a.qkv_bf16) {
+        e = encode_rows(&maps->q, a.q, true, a.T, a.H);
+        if (e == cudaSuccess) e = encode_rows(&maps->k, a.k, true, a.T, a.H);
+        if (e == cudaSuccess) e = encode_rows(&maps->v, a.v, true, a.T, a.H);
+    }
+    if (e != cudaSuccess) return e;
+    switch (gate_in(a)) {
+        case kGateF32: return encode_rows(&maps->g, a.f, false, a.T, a.H);
+        case kGateBF16: return encode_rows(&maps->g, a.f, true, a.T, a.H);
+        default: return encode_rows(&maps->g, a.g, false, a.T, a.H);
+    }
+}
+
 template <typename TIn, int kGate>
-cudaError_t launch_prep_typed(const ChunkArgs& a, const int32_t* hdr, unsigned char* rec,
-                              int64_t unit_base, int64_t units, int32_t* ctr, bool beside_scan,
-                              cudaStream_t stream)
+cudaError_t launch_prep_typed(const ChunkArgs& a, const PrepMaps& maps, const int32_t* hdr,
+                              unsigned char* rec, int64_t unit_base, int64_t units, int32_t* ctr,
+                              bool beside_scan, cudaStream_t stream)
 {
     auto kern = chunk_prep_kernel<TIn, kGate>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1252,20 +1343,20 @@ cudaError_t launch_prep_typed(const ChunkArgs& a, const int32_t* hdr, unsigned c
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = beside_scan ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, kern, a, hdr, rec, unit_base, units, ctr,
+    return cudaLaunchKernelEx(&cfg, kern, a, maps, hdr, rec, unit_base, units, ctr,
                               (int32_t)(beside_scan ? 1 : 0));
 }
 
 // Preparation of the (chunk, head) units [unit_base, unit_base + units), taken
 // from the counter `ctr` (zero at launch); `beside_scan`: launched to overlap
 // the scan just before it on the stream.
-cudaError_t launch_prep(const ChunkArgs& a, const int32_t* hdr, unsigned char* rec,
-                        int64_t unit_base, int64_t units, int32_t* ctr, bool beside_scan,
-                        cudaStream_t stream)
+cudaError_t launch_prep(const ChunkArgs& a, const PrepMaps& maps, const int32_t* hdr,
+                        unsigned char* rec, int64_t unit_base, int64_t units, int32_t* ctr,
+                        bool beside_scan, cudaStream_t stream)
 {
     if (units <= 0) return cudaSuccess;
 #define KDA_PREP(TIN, GATE) \
-    launch_prep_typed<TIN, GATE>(a, hdr, rec, unit_base, units, ctr, beside_scan, stream)
+    launch_prep_typed<TIN, GATE>(a, maps, hdr, rec, unit_base, units, ctr, beside_scan, stream)
     switch (gate_in(a)) {
         case kGateF32:
             return a.qkv_bf16 ? KDA_PREP(__nv_bfloat16, kGateF32) : KDA_PREP(float, kGateF32);
@@ -1386,8 +1477,11 @@ cudaError_t launch_chunk_split(const ChunkArgs& a, int64_t chunks, bool overlap,
     float* carry = reinterpret_cast<float*>(rec + split_chunk_bound(a.N, a.T) * a.H * (int64_t)REC_BYTES);
     const int64_t units = chunks * a.H;
     if (units > INT32_MAX || (int64_t)a.N * a.H > INT32_MAX) return cudaErrorInvalidConfiguration;
+    PrepMaps maps;
+    cudaError_t e = units > 0 ? make_prep_maps(a, &maps) : cudaSuccess;
+    if (e != cudaSuccess) return e;
     chunk_plan_kernel<<<1, 1024, 0, stream>>>(a.cu_seqlens, a.N, a.T, hdr, a.status);
-    cudaError_t e = cudaGetLastError();
+    e = cudaGetLastError();
     if (e != cudaSuccess) return e;
 
     const int sms = device_sm_count() > 0 ? device_sm_count() : 152;
@@ -1403,15 +1497,15 @@ cudaError_t launch_chunk_split(const ChunkArgs& a, int64_t chunks, bool overlap,
     const bool halves = !a.out_norm && W_shape <= 1 && 2 * heads <= sms;
     int32_t* ctr = window_counters(hdr, a.N);
     if (W <= 1) {
-        e = launch_prep(a, hdr, rec, 0, units, ctr, false, stream);
+        e = launch_prep(a, maps, hdr, rec, 0, units, ctr, false, stream);
         if (e != cudaSuccess) return e;
         return launch_scan(a, hdr, rec, ScanWindow{0, INT32_MAX, nullptr, 1}, halves, stream);
     }
     for (int w = 0; w < W && e == cudaSuccess; ++w) {
         const int32_t g0 = (int32_t)window_bound(chunks, W, w);
         const int32_t g1 = (int32_t)window_bound(chunks, W, w + 1);
-        e = launch_prep(a, hdr, rec, (int64_t)g0 * a.H, (int64_t)(g1 - g0) * a.H, ctr + w, w > 0,
-                        stream);
+        e = launch_prep(a, maps, hdr, rec, (int64_t)g0 * a.H, (int64_t)(g1 - g0) * a.H, ctr + w,
+                        w > 0, stream);
         const ScanWindow win{g0, w + 1 == W ? INT32_MAX : g1, carry, w + 1 == W ? 1 : 0};
         if (e == cudaSuccess) e = launch_scan(a, hdr, rec, win, halves, stream);
     }

@@ -240,6 +240,21 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
         : "memory");
 }
 
+// TMA tile load (cp.async.bulk.tensor, no multicast) of the box at
+// coordinates (x, y, z) of a 3-D tensor map into shared memory (128-byte
+// aligned), completing the box's bytes as transactions on `m`.  `tmap` is the
+// generic address of a __grid_constant__ CUtensorMap kernel parameter; the
+// innermost coordinate x times the element size must be a multiple of 16.
+__device__ __forceinline__ void tma_load_3d(void* dst, const void* tmap, int x, int y, int z,
+                                            uint64_t* m)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
+        "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(smem_u32(m))
+        : "memory");
+}
+
 // Hint: bring `bytes` (multiple of 16, 16-byte-aligned address) into L2.
 __device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes)
 {
