@@ -52,6 +52,9 @@ def parse_args():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--mode", choices=["bf16_tc", "fp32_exact"], default=None)
     p.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    p.add_argument("--heads", type=int, default=None,
+                   help="keep only the first H heads of the workload (a smaller case of the "
+                        "same kernels, e.g. for ncu captures that must stay a few GB)")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--unfused", action="store_true",
@@ -205,6 +208,15 @@ def max_over_ranks(x: float, device) -> float:
 def whole_job_rate(world: int, units_per_rank_step: int, steps: int, ms: float) -> float:
     """Units processed by all ranks per second (weak scaling: every rank runs a batch)."""
     return world * units_per_rank_step * steps / (ms * 1e-3)
+
+
+def first_heads(x, Hs):
+    """The first Hs heads of a workload's inputs (contiguous copies)."""
+    for n in ("q", "k", "v", "f", "b"):
+        setattr(x, n, getattr(x, n)[:, :Hs].contiguous())
+    x.A_log = x.A_log[:Hs].contiguous()
+    x.dt_bias = x.dt_bias[:Hs].contiguous()
+    return x
 
 
 def workload_config(w, mode):
@@ -398,7 +410,9 @@ def main():
     two_phase = not args.single_pass
     w = WORKLOAD_BY_NAME[args.workload]
     x = workload_inputs(w)
-    T, H, K, V, N = x.T, w.H, w.K, w.V, x.N
+    if args.heads:
+        x = first_heads(x, args.heads)
+    T, H, K, V, N = x.T, x.q.shape[1], w.K, w.V, x.N
     out_dtype = torch.float32 if mode == "fp32_exact" else x.v.dtype
     x.f = x.f.to(torch.bfloat16 if args.f_dtype == "bf16" else torch.float32)
     d = {n: getattr(x, n).to(dev) for n in ("q", "k", "v", "f", "A_log", "dt_bias", "b",
@@ -619,7 +633,9 @@ def main():
                 "algorithmic_bytes_per_launch": alg,
                 "avg_launch_ms": avg_chunk_s * 1e3}
         cfg = workload_config(w, mode)
-        cfg["T"], cfg["N"] = T, N
+        cfg["T"], cfg["N"], cfg["H"] = T, N, H
+        if H != w.H:
+            cfg["workload"] = f"{w.name}_first{H}heads"
         cfg["step"] = "kda_gate + kda_chunk_fwd" if (not args.fused) else "kda_chunk_fwd_gated"
         cfg["chunk_path"] = variant
         cfg["f_dtype"] = str(x.f.dtype).replace("torch.", "")
