@@ -581,11 +581,14 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(ChunkArgs args,
 //   control:  P^T = Delta^T K'' (4 MMAs, N = 128), commit p_done; then
 //             O^T += Delta^T A_qk^T on top of Q' S (4 MMAs, N = 64), commit o_done
 //   epilogue: S^T <- S^T Diag(d) + P^T and the fp16 copy of S^T for the next
-//             chunk; O read from TMEM; arrive s_ready; then chunk c's output
-//             rows, stored while the control warp issues chunk c + 1's MMAs
-//             into the other region
+//             chunk; arrive s_ready; then O read from TMEM once o_done has
+//             come, arrive o_read, and chunk c's output rows, stored while the
+//             control warp issues chunk c + 1's MMAs into the other region
 // so the state's chain per chunk is [W S] -> Delta -> P -> S: two short MMA
-// groups and two short epilogues; Q' S and A_qk Delta ride behind them.
+// groups and two short epilogues; Q' S and A_qk Delta ride behind them.  The
+// control waits for o_read of chunk c - 2 before it writes region (c & 1)
+// again (one barrier per chunk parity), and for o_done of chunk c - 1 before
+// it refills that chunk's record stage.
 constexpr int SCAN_THREADS = NT + 32;
 constexpr int kL2Ahead = 4;                   // records prefetched into L2 this many chunks ahead
 constexpr uint32_t kEpiBar = 1;               // named barrier of the 256 epilogue threads
@@ -675,10 +678,11 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) chunk_scan_kernel(ChunkArgs a
     const unsigned char* rec0 = records + ((int64_t)(offn + cb) * H + h) * REC_BYTES;
     TOut* __restrict__ out = static_cast<TOut*>(args.out);
     // [0,1] record stages, [2] ws_done, [3] p_done, [4] delta_ready (NT),
-    // [5] s_ready (NT), [6] drain after a failure, [7] o_done
+    // [5] s_ready (NT), [6] drain after a failure, [7] o_done, [8,9] o_read of
+    // even and odd chunks (NT)
     uint64_t* bar = reinterpret_cast<uint64_t*>(sm + S_BAR);
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + S_BAR + 64);
-    volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(sm + S_BAR + 68);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + S_BAR + 80);
+    volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(sm + S_BAR + 84);
 
     // ---- the entering state (zero, or the caller's)
     float S[64];                                           // S^T[row][64 half + c]
@@ -701,7 +705,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) chunk_scan_kernel(ChunkArgs a
         tmem_relinquish();
     }
     if (tid == 0) {
-        for (int b = 0; b < 8; ++b) mbar_init(&bar[b], (b == 4 || b == 5) ? NT : 1);
+        for (int b = 0; b < 10; ++b) mbar_init(&bar[b], (b == 4 || b == 5 || b >= 8) ? NT : 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -745,8 +749,9 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) chunk_scan_kernel(ChunkArgs a
                 const uint32_t R = tmem + S_TM_REGION * (c & 1);
                 const uint32_t sst = sb + S_STG + (c & 1) * S_STG_STRIDE;
                 if (!wait_or_abort(&bar[c & 1], (c >> 1) & 1)) { fail = true; break; }
-                // chunk c - 1 is finished: S^T is current and its stage is free
+                // chunk c - 1's state is current; chunk c - 2's O has left region (c & 1)
                 if (c > 0 && !wait_or_abort(&bar[5], (c - 1) & 1)) { fail = true; break; }
+                if (c > 1 && !wait_or_abort(&bar[8 + (c & 1)], ((c - 2) >> 1) & 1)) { fail = true; break; }
                 fence_after_sync();
 #pragma unroll
                 for (int s = 0; s < 8; ++s)
@@ -759,6 +764,9 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) chunk_scan_kernel(ChunkArgs a
                     mma_f16(R + S_TM_O, desc_kmajor(sb + S_ST, 128, s),
                             desc_mnmajor64(sst + REC_QP, s), id_ws, s > 0);
                 if (c > 0 && c + 1 < nch) {
+                    // stage (c + 1) & 1 held chunk c - 1, whose last MMA group
+                    // (A_qk Delta, signalled by o_done) must be done reading it
+                    if (!wait_or_abort(&bar[7], (c - 1) & 1)) { fail = true; break; }
                     issue_load(c + 1);
                     issued = c + 2;
                 }
@@ -916,7 +924,11 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) chunk_scan_kernel(ChunkArgs a
                     *reinterpret_cast<uint4*>(sm + S_ST + sw128_tile(128, row, (64 * half + 8 * q) * 2)) =
                         pack_h8(S + 8 * q);
             }
-            // this chunk's O leaves TMEM before the next chunk's MMAs start
+            // the next chunk's MMAs may start (into the other region) while this
+            // chunk's O is read
+            fence_async_smem();
+            fence_before_sync();
+            mbar_arrive(&bar[5]);
             {
                 const bool ok = wait_or_abort(&bar[7], c & 1);
                 if (named_sync_or(kEpiBar, NT, !ok)) { fail = true; break; }
@@ -924,9 +936,8 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) chunk_scan_kernel(ChunkArgs a
             fence_after_sync();
             float o[32];
             tmem_ld32(R + S_TM_O + 32 * half, o);
-            fence_async_smem();
             fence_before_sync();
-            mbar_arrive(&bar[5]);
+            mbar_arrive(&bar[8 + (c & 1)]);
             // its rows go out while the control warp issues the next chunk's MMAs
             store_chunk_out(c, o);
         }
