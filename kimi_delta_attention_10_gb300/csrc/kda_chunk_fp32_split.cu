@@ -400,27 +400,59 @@ __global__ void __launch_bounds__(NT, 1) fp32_prep_kernel(ChunkArgs args,
 
     // ---- 4. pairs in different sub-blocks of one 16-token block: 24 tiles of
     // 4 x 4, eight lanes per tile (a quarter warp, so that the lanes of a tile
-    // read the same Kb4 rows at once), each lane one row of A_kk or of A_qk
-    if (tid < 24 * 8) {
-        const int tile = tid >> 3, I = tile / 6, pr = tile % 6;
-        const int sa = pr == 0 ? 1 : (pr < 3 ? 2 : 3);      // (sa, sb): (1,0) (2,0) (2,1)
-        const int sb = pr == 0 ? 0 : (pr < 3 ? pr - 1 : pr - 3);   //   (3,0) (3,1) (3,2)
-        const int i = I * SB + sa * S4 + ((tid >> 1) & 3), rj = I * SB + sb * S4;
-        const bool qk = tid & 1;
-        const float* x = qk ? &sm.q[i][0] : &sm.k[i][0];
-        // sub-blocks strictly between: none, 1, 2 or 1 and 2
-        const float* midp = &sm.mid4[I][sa - sb == 1 ? 0 : (sa - sb == 3 ? 3 : sb + 1)][0];
-        float acc[S4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 4
-        for (int c = 0; c < DK; c += 4) {
-            const float4 mid = ld4s(midp + c);
-            const float4 xv = ld4s(x + c);
+    // read the same Kb4 rows at once), each lane one row of A_kk or of A_qk.
+    // Threads 0..191 sum channels 0..95 of their row; threads 192..255 sum
+    // channels 96..127 of three rows each and hand those partial sums over
+    // through the (not yet used) T array.
+    {
+        auto row_of = [&](int tl, int& i, int& rj, const float*& midp) {
+            const int tile = tl >> 3, I = tile / 6, pr = tile % 6;
+            const int sa = pr == 0 ? 1 : (pr < 3 ? 2 : 3);      // (sa, sb): (1,0) (2,0) (2,1)
+            const int sb = pr == 0 ? 0 : (pr < 3 ? pr - 1 : pr - 3);   //   (3,0) (3,1) (3,2)
+            i = I * SB + sa * S4 + ((tl >> 1) & 3);
+            rj = I * SB + sb * S4;
+            // sub-blocks strictly between: none, 1, 2 or 1 and 2
+            midp = &sm.mid4[I][sa - sb == 1 ? 0 : (sa - sb == 3 ? 3 : sb + 1)][0];
+        };
+        float acc[S4];
+        auto row_sums = [&](int tl, int c0, int c1) {
+            int i, rj;
+            const float* midp;
+            row_of(tl, i, rj, midp);
+            const float* x = (tl & 1) ? &sm.q[i][0] : &sm.k[i][0];
 #pragma unroll
-            for (int u = 0; u < S4; ++u) acc[u] = dot4(xv, mul4(ld4s(&sm.a[rj + u][c]), mid), acc[u]);
+            for (int u = 0; u < S4; ++u) acc[u] = 0.f;
+#pragma unroll 4
+            for (int c = c0; c < c1; c += 4) {
+                const float4 mid = ld4s(midp + c);
+                const float4 xv = ld4s(x + c);
+#pragma unroll
+                for (int u = 0; u < S4; ++u) acc[u] = dot4(xv, mul4(ld4s(&sm.a[rj + u][c]), mid), acc[u]);
+            }
+        };
+        float* part = &sm.tf[0][0];                         // [192 rows][4]
+        if (tid >= 24 * 8) {
+#pragma unroll 1
+            for (int k3 = 0; k3 < 3; ++k3) {
+                const int tl = tid - 24 * 8 + 64 * k3;
+                row_sums(tl, 96, DK);
+                st4s(part + tl * 4, make_float4(acc[0], acc[1], acc[2], acc[3]));
+            }
+        } else {
+            row_sums(tid, 0, 96);
         }
-        const float s = qk ? 1.f : sm.beta[i];
-        st4s(qk ? &sm.aqk[i][rj] : &sm.akk[i][rj],
-             make_float4(s * acc[0], s * acc[1], s * acc[2], s * acc[3]));
+        __syncthreads();
+        if (tid < 24 * 8) {
+            int i, rj;
+            const float* midp;
+            row_of(tid, i, rj, midp);
+            const float4 pp = ld4s(part + tid * 4);
+            const bool qk = tid & 1;
+            const float sc = qk ? 1.f : sm.beta[i];
+            st4s(qk ? &sm.aqk[i][rj] : &sm.akk[i][rj],
+                 make_float4(sc * (acc[0] + pp.x), sc * (acc[1] + pp.y), sc * (acc[2] + pp.z),
+                             sc * (acc[3] + pp.w)));
+        }
     }
     __syncthreads();
 
@@ -465,43 +497,75 @@ __global__ void __launch_bounds__(NT, 1) fp32_prep_kernel(ChunkArgs args,
     __syncthreads();
 
     // ---- 6. pairs in different 16-token blocks: one warp per block pair, each
-    // lane a 2 x 4 tile of A_kk and of A_qk over all 128 channels (rows r and
-    // r + 8: the eight lanes of a quarter warp read eight consecutive rows and
-    // one set of Kb16 rows)
-    if (tid < 6 * 32) {
-        const int pr = tid >> 5, lt = tid & 31;
-        const int I = pr == 0 ? 1 : (pr < 3 ? 2 : 3);        // (I, J): (1,0) (2,0) (2,1)
-        const int J = pr == 0 ? 0 : (pr < 3 ? pr - 1 : pr - 3);   //   (3,0) (3,1) (3,2)
-        const int ib = I * SB + (lt & 7), j0 = J * SB + (lt >> 3) * 4;
-        // blocks strictly between: none, 1, 2 or 1 and 2
-        const float* midp = &sm.mid16[I - J == 1 ? 0 : (I - J == 3 ? 3 : J + 1)][0];
+    // lane a 2 x 4 tile of A_kk and of A_qk (rows r and r + 8: the eight lanes
+    // of a quarter warp read eight consecutive rows and one set of Kb16 rows).
+    // Warps 0..5 sum channels 0..95 of their pair; warps 6 and 7 sum channels
+    // 96..127 of three pairs each and hand those partial sums over through the
+    // (not yet used) T array, so that every warp runs 96 channel steps.
+    {
         float skk[2][4], sqk[2][4];
+        auto tile_sums = [&](int pr, int c0, int c1) {
+            const int I = pr == 0 ? 1 : (pr < 3 ? 2 : 3);        // (I, J): (1,0) (2,0) (2,1)
+            const int J = pr == 0 ? 0 : (pr < 3 ? pr - 1 : pr - 3);   //   (3,0) (3,1) (3,2)
+            const int ib = I * SB + (lane & 7), j0 = J * SB + (lane >> 3) * 4;
+            // blocks strictly between: none, 1, 2 or 1 and 2
+            const float* midp = &sm.mid16[I - J == 1 ? 0 : (I - J == 3 ? 3 : J + 1)][0];
 #pragma unroll
-        for (int r = 0; r < 2; ++r)
+            for (int r = 0; r < 2; ++r)
 #pragma unroll
-            for (int x = 0; x < 4; ++x) { skk[r][x] = 0.f; sqk[r][x] = 0.f; }
+                for (int x = 0; x < 4; ++x) { skk[r][x] = 0.f; sqk[r][x] = 0.f; }
 #pragma unroll 2
-        for (int c = 0; c < DK; c += 4) {
-            const float4 mid = ld4s(midp + c);
-            float4 kb[4];
+            for (int c = c0; c < c1; c += 4) {
+                const float4 mid = ld4s(midp + c);
+                float4 kb[4];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) kb[u] = mul4(ld4s(&sm.a[j0 + u][c]), mid);
+                for (int u = 0; u < 4; ++u) kb[u] = mul4(ld4s(&sm.a[j0 + u][c]), mid);
 #pragma unroll
-            for (int r = 0; r < 2; ++r) {
-                const float4 kf = ld4s(&sm.k[ib + 8 * r][c]), qf = ld4s(&sm.q[ib + 8 * r][c]);
+                for (int r = 0; r < 2; ++r) {
+                    const float4 kf = ld4s(&sm.k[ib + 8 * r][c]), qf = ld4s(&sm.q[ib + 8 * r][c]);
 #pragma unroll
-                for (int x = 0; x < 4; ++x) {
-                    skk[r][x] = dot4(kf, kb[x], skk[r][x]);
-                    sqk[r][x] = dot4(qf, kb[x], sqk[r][x]);
+                    for (int x = 0; x < 4; ++x) {
+                        skk[r][x] = dot4(kf, kb[x], skk[r][x]);
+                        sqk[r][x] = dot4(qf, kb[x], sqk[r][x]);
+                    }
                 }
             }
-        }
+        };
+        float* part = &sm.tf[0][0];                         // [pair][16 sums][32 lanes]
+        if (warp >= 6) {
+#pragma unroll 1
+            for (int p3 = 0; p3 < 3; ++p3) {
+                const int pr = 3 * (warp - 6) + p3;
+                tile_sums(pr, 96, DK);
 #pragma unroll
-        for (int r = 0; r < 2; ++r) {
-            const float b = sm.beta[ib + 8 * r];
-            st4s(&sm.akk[ib + 8 * r][j0],
-                 make_float4(b * skk[r][0], b * skk[r][1], b * skk[r][2], b * skk[r][3]));
-            st4s(&sm.aqk[ib + 8 * r][j0], make_float4(sqk[r][0], sqk[r][1], sqk[r][2], sqk[r][3]));
+                for (int r = 0; r < 2; ++r)
+#pragma unroll
+                    for (int x = 0; x < 4; ++x) {
+                        part[(pr * 16 + 4 * r + x) * 32 + lane] = skk[r][x];
+                        part[(pr * 16 + 8 + 4 * r + x) * 32 + lane] = sqk[r][x];
+                    }
+            }
+        } else {
+            tile_sums(warp, 0, 96);
+        }
+        __syncthreads();
+        if (warp < 6) {
+            const int pr = warp;
+            const int I = pr == 0 ? 1 : (pr < 3 ? 2 : 3);
+            const int J = pr == 0 ? 0 : (pr < 3 ? pr - 1 : pr - 3);
+            const int ib = I * SB + (lane & 7), j0 = J * SB + (lane >> 3) * 4;
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+#pragma unroll
+                for (int x = 0; x < 4; ++x) {
+                    skk[r][x] += part[(pr * 16 + 4 * r + x) * 32 + lane];
+                    sqk[r][x] += part[(pr * 16 + 8 + 4 * r + x) * 32 + lane];
+                }
+                const float b = sm.beta[ib + 8 * r];
+                st4s(&sm.akk[ib + 8 * r][j0],
+                     make_float4(b * skk[r][0], b * skk[r][1], b * skk[r][2], b * skk[r][3]));
+                st4s(&sm.aqk[ib + 8 * r][j0], make_float4(sqk[r][0], sqk[r][1], sqk[r][2], sqk[r][3]));
+            }
         }
     }
     __syncthreads();
