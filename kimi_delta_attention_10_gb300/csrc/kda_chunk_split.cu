@@ -1415,14 +1415,14 @@ cudaError_t launch_scan(const ChunkArgs& a, const int32_t* hdr, const unsigned c
 // the preparation of its window, and that preparation's last CTA waits for
 // the previous scan.
 constexpr int kWindowChunks = 32;              // at least this many chunks per window
-constexpr bool kHalfLastWindow = true;         // the last window's scan runs alone: keep it short
+constexpr int kLastWindowThirds = 1;          // the last window's scan runs alone: a third as long
 
 // Window w covers the global chunks [window_bound(w), window_bound(w + 1)).
 int64_t window_bound(int64_t chunks, int W, int w)
 {
     if (w >= W) return chunks;
-    if (!kHalfLastWindow) return chunks * w / W;
-    return chunks * (2 * w) / (2 * W - 1);     // W - 1 windows of two halves, the last of one
+    // W - 1 windows of three thirds, the last of kLastWindowThirds
+    return chunks * (3 * w) / (3 * (W - 1) + kLastWindowThirds);
 }
 
 // Scratch of the no-allocation entry point (kda_chunk_fwd_static): a
