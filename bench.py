@@ -182,11 +182,11 @@ def backward_bytes(T, H, K, V, N, qkv_bytes, dout_bytes):
 
 
 def chunk_windows(N, H, chunks, sms):
-    """Chunk windows of one two-phase kda_chunk_fwd call: min(4, chunks // 32)
+    """Chunk windows of one two-phase kda_chunk_fwd call: min(3, chunks // 32)
     when N * H <= the SM count (the rule in kda_chunk_split.cu), else one.
     The call launches the plan, then one preparation and one scan per window."""
     if N * H <= sms:
-        return max(1, min(4, chunks // 32))
+        return max(1, min(3, chunks // 32))
     return 1
 
 

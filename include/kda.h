@@ -133,7 +133,7 @@ kda_status kda_gate(const void* f, int32_t f_dtype, const float* A_log, const fl
  * for bit those of one window.
  *
  * The size is a bound that holds for every cu_seqlens with these N and T:
- * a 1 KiB-aligned header of 2 N + 9 int32, then for KDA_MODE_BF16_TC
+ * a 1 KiB-aligned header of 2 N + 8 int32, then for KDA_MODE_BF16_TC
  * (T / 64 + N) * H records of 74240 bytes and N * H * K * V FP32 (the state
  * carried between windows), for KDA_MODE_FP32_EXACT (T / 64 + N) * H records
  * of 148224 bytes.

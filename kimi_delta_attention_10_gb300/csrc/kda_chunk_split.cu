@@ -73,7 +73,7 @@ static_assert(REC_BYTES % 16 == 0 && REC_BYTES < (1u << 20), "bulk copy size");
 // (zeroed by the plan).
 constexpr int kHdrOff = 4;
 constexpr int kLptMaxSeqs = 1024;
-constexpr int kMaxWindows = 4;
+constexpr int kMaxWindows = 3;
 
 int64_t header_bytes(int32_t N)
 {

@@ -106,8 +106,8 @@ def test_workspace_size_bound():
     for N, T, H in [(1, 16384, 64), (16, 32768, 64), (3, 65, 4), (0, 0, 1), (5000, 70000, 2)]:
         st, nbytes = workspace_size(lib, N, T, H)
         assert st == binding.KDA_OK
-        # flag, N + 1 offsets, N scan order, 4 chunk-window unit counters
-        hdr = -(-(4 * (2 * N + 9)) // 1024) * 1024
+        # flag, N + 1 offsets, N scan order, 3 chunk-window unit counters
+        hdr = -(-(4 * (2 * N + 8)) // 1024) * 1024
         assert nbytes == hdr + (T // 64 + N) * H * rec + N * H * 128 * 128 * 4
         # the exact chunk count of any split of T tokens into N sequences is no larger
         lens = [T // max(N, 1)] * N

@@ -77,7 +77,7 @@ def test_reference_arm_other_ranks_exit_quietly():
 
 def test_chunk_windows_rule():
     """Windows only when the scan leaves SMs idle and there are >= 64 chunks."""
-    assert bench.chunk_windows(1, 64, 256, 152) == 4          # 16384 tokens x 64 heads
+    assert bench.chunk_windows(1, 64, 256, 152) == 3          # 16384 tokens x 64 heads
     assert bench.chunk_windows(1, 64, 32, 152) == 1           # 2048 tokens: one window
     assert bench.chunk_windows(16, 64, 520, 152) == 1         # 1024 scan CTAs fill the GPU
     assert bench.chunk_windows(1, 2, 66, 152) == 2

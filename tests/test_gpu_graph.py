@@ -15,7 +15,7 @@ pytestmark = pytest.mark.gpu
 
 
 def test_fused_forward_in_a_graph_is_bitwise_eager():
-    x = make_inputs([16384], 2, 128, 128, torch.bfloat16, 101)    # four chunk windows
+    x = make_inputs([16384], 2, 128, 128, torch.bfloat16, 101)    # three chunk windows
     d = device_inputs(x)
     host = x.cu_seqlens.tolist()
     ws = torch.empty(chunk_workspace_size(x.N, x.T, x.H), dtype=torch.uint8, device="cuda")

@@ -13,7 +13,7 @@ Every forward path of the library runs each regime against the FP64 oracle
 ("Add opt-in FP32 KDA chunk computation", section Validation: an independent
 FP64 recurrence as the reference): FP32-exact mode in its single-pass kernel
 and in two phases (rel-L2 <= 1e-5, F32 output), and the BF16 tensor-core path
-(<= 3e-3, BF16 output) in two phases with a workspace (8192 tokens: four chunk
+(<= 3e-3, BF16 output) in two phases with a workspace (8192 tokens: three chunk
 windows with the FP32 state carry between them), in the single-pass kernel,
 and on the static scratch of kda_chunk_fwd_static (one window).  Output and
 final state are both checked.
@@ -32,7 +32,7 @@ from gpu_util import f64, rel_l2
 pytestmark = pytest.mark.gpu
 
 H = 4
-# one sequence of 128 chunks (four windows), and three sequences across windows
+# one sequence of 128 chunks (three windows), and three sequences across windows
 LAYOUTS = {"single_8192": [8192], "packed_5000_3000_192": [5000, 3000, 192]}
 PATHS = ("fp32_exact", "fp32_two_phase", "two_phase", "single_pass", "static")
 TOL = {"fp32_exact": 1e-5, "fp32_two_phase": 1e-5, "two_phase": 3e-3, "single_pass": 3e-3,

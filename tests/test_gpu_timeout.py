@@ -33,7 +33,7 @@ def _call(d, g, beta, x, workspace, mode):
 
 
 # (fault, mode, workspace, lengths, heads): the short problem runs the scan in V
-# halves, the 8192-token one the full-width scan in four chunk windows (its CTA
+# halves, the 8192-token one the full-width scan in three chunk windows (its CTA
 # 0 gives up once per window); the FP32-exact mode's scan is a tensor-core
 # scan in V halves too
 CASES = [(KDA_TEST_FAULT_SCAN, "bf16_tc", "auto", [300, 77], 2),

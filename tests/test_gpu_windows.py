@@ -40,9 +40,9 @@ def _both(lens, H, seed, init, host_mirror):
 
 @pytest.mark.parametrize("lens,H,init,host_mirror", [
     ([3000, 0, 1200], 2, True, True),       # a sequence across both windows, an empty one
-    ([16384], 2, False, True),              # eight windows
+    ([16384], 2, False, True),              # three windows
     ([2100, 2100], 3, True, False),         # windows from the chunk bound (no host mirror)
-    ([5000, 1, 6000, 0, 3000], 3, True, True),   # four windows, sequences across several
+    ([5000, 1, 6000, 0, 3000], 3, True, True),   # three windows, sequences across several
 ])
 def test_windows_are_bitwise_one_window(lens, H, init, host_mirror):
     _, _, (o_w, S_w), (o_1, S_1) = _both(lens, H, 91 + H, init, host_mirror)
@@ -62,7 +62,7 @@ def test_windows_match_oracle():
 
 
 def test_fused_gate_in_windows_matches_gate_then_chunk():
-    """The timed configuration's shape of schedule (four chunk windows) with the
+    """The timed configuration's shape of schedule (three chunk windows) with the
     gate fused into the preparation (its fast e^g), against kda_gate +
     kda_chunk_fwd and against the FP64 oracle."""
     x = make_inputs([16384], 2, 128, 128, torch.bfloat16, 97)
