@@ -893,6 +893,15 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) fp32_scan_kernel(ChunkArgs ar
             constexpr uint32_t id_d1 = idesc(kFmtF16, 128, VH, false, true);
             constexpr uint32_t id_p = idesc(kFmtF16, 128, VH, true, true);
             constexpr uint32_t id_o = idesc(kFmtF16, 128, VH, false, true);
+            // operand descriptors at k-step 0, computed once (every region is fixed)
+            const uint64_t dWh = desc_kmajor(sb + F_E + R_WQ, 128, 0);
+            const uint64_t dWl = desc_kmajor(sb + F_E + R_WQ_LO, 128, 0);
+            const uint64_t dSh = desc_mnmajor64(sb + F_S, 0), dSl = desc_mnmajor64(sb + F_S + 16384, 0);
+            const uint64_t dKh = desc_mnmajor128(sb + F_L + L_KT, 8192, 0);
+            const uint64_t dKl = desc_mnmajor128(sb + F_L + L_KT_LO, 8192, 0);
+            const uint64_t dAh = desc_kmajor(sb + F_L + L_AQK - 8192, 128, 0);
+            const uint64_t dAl = desc_kmajor(sb + F_L + L_AQK_LO - 8192, 128, 0);
+            const uint64_t dDh = desc_mnmajor64(sb + F_D, 0), dDl = desc_mnmajor64(sb + F_D + 8192, 0);
             for (; c < nch; ++c) {
                 const uint32_t R = tmem + F_TM_REGION * (c & 1);
                 if (c > 0) {
@@ -911,9 +920,9 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) fp32_scan_kernel(ChunkArgs ar
                 fence_after_sync();
 #pragma unroll
                 for (int s = 0; s < 8; ++s) {
-                    const uint64_t ah = desc_kmajor(sb + F_E + R_WQ, 128, s);
-                    const uint64_t al = desc_kmajor(sb + F_E + R_WQ_LO, 128, s);
-                    const uint64_t bh = desc_mnmajor64(sb + F_S, s), bl = desc_mnmajor64(sb + F_S + 16384, s);
+                    const uint64_t ah = desc_advance(dWh, kmajor_off(128, s));
+                    const uint64_t al = desc_advance(dWl, kmajor_off(128, s));
+                    const uint64_t bh = desc_advance(dSh, mnmajor_off(s)), bl = desc_advance(dSl, mnmajor_off(s));
                     mma_f16(R + F_TM_D1, ah, bh, id_d1, s > 0);
                     mma_f16(R + F_TM_D1, ah, bl, id_d1, 1);
                     mma_f16(R + F_TM_D1, al, bh, id_d1, 1);
@@ -937,9 +946,9 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) fp32_scan_kernel(ChunkArgs ar
                 fence_after_sync();
 #pragma unroll
                 for (int s = 0; s < 4; ++s) {
-                    const uint64_t ah = desc_mnmajor128(sb + F_L + L_KT, 8192, s);
-                    const uint64_t al = desc_mnmajor128(sb + F_L + L_KT_LO, 8192, s);
-                    const uint64_t bh = desc_mnmajor64(sb + F_D, s), bl = desc_mnmajor64(sb + F_D + 8192, s);
+                    const uint64_t ah = desc_advance(dKh, mnmajor_off(s));
+                    const uint64_t al = desc_advance(dKl, mnmajor_off(s));
+                    const uint64_t bh = desc_advance(dDh, mnmajor_off(s)), bl = desc_advance(dDl, mnmajor_off(s));
                     mma_f16(R + F_TM_P, ah, bh, id_p, s > 0);
                     mma_f16(R + F_TM_P, ah, bl, id_p, 1);
                     mma_f16(R + F_TM_P, al, bh, id_p, 1);
@@ -947,9 +956,9 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) fp32_scan_kernel(ChunkArgs ar
                 commit(&bar[3]);
 #pragma unroll
                 for (int s = 0; s < 4; ++s) {
-                    const uint64_t ah = desc_kmajor(sb + F_L + L_AQK - 8192, 128, s);
-                    const uint64_t al = desc_kmajor(sb + F_L + L_AQK_LO - 8192, 128, s);
-                    const uint64_t bh = desc_mnmajor64(sb + F_D, s), bl = desc_mnmajor64(sb + F_D + 8192, s);
+                    const uint64_t ah = desc_advance(dAh, kmajor_off(128, s));
+                    const uint64_t al = desc_advance(dAl, kmajor_off(128, s));
+                    const uint64_t bh = desc_advance(dDh, mnmajor_off(s)), bl = desc_advance(dDl, mnmajor_off(s));
                     mma_f16(R + F_TM_O2, ah, bh, id_o, s > 0);
                     mma_f16(R + F_TM_O2, ah, bl, id_o, 1);
                     mma_f16(R + F_TM_O2, al, bh, id_o, 1);

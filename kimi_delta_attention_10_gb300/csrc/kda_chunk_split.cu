@@ -353,10 +353,12 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(ChunkArgs args,
                 failed = true;                             // no commit: the others time out too
             } else {
                 fence_after_sync();
+                const uint64_t da = desc_mnmajor128(sb + P_PAIR, 16384, 0);
+                const uint64_t db = desc_mnmajor64(sb + P_PAIR + 32768, 0);
 #pragma unroll
                 for (int s = 0; s < 8; ++s)
-                    mma_f16(tmem + P_TM_A + 64 * rnd, desc_mnmajor128(sb + P_PAIR, 16384, s),
-                            desc_mnmajor64(sb + P_PAIR + 32768, s), id_pairs, s > 0);
+                    mma_f16(tmem + P_TM_A + 64 * rnd, desc_advance(da, mnmajor_off(s)),
+                            desc_advance(db, mnmajor_off(s)), id_pairs, s > 0);
                 commit(&bar[rnd]);
             }
         }
@@ -524,14 +526,16 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(ChunkArgs args,
         if (tid == 0) {
             fence_after_sync();
             constexpr uint32_t id = idesc(kFmtF16, 128, 64);
+            const uint64_t dx = desc_kmajor(sb + P_XT, 128, 0), dv = desc_kmajor(sb + P_SV, 128, 0);
+            const uint64_t dt = desc_kmajor(sb + P_TP, 64, 0);
 #pragma unroll
             for (int s = 0; s < 4; ++s)
-                mma_f16(tmem + P_TM_W, desc_kmajor(sb + P_XT, 128, s), desc_kmajor(sb + P_TP, 64, s),
-                        id, s > 0);
+                mma_f16(tmem + P_TM_W, desc_advance(dx, kmajor_off(128, s)),
+                        desc_advance(dt, kmajor_off(64, s)), id, s > 0);
 #pragma unroll
             for (int s = 0; s < 4; ++s)
-                mma_f16(tmem + P_TM_U, desc_kmajor(sb + P_SV, 128, s), desc_kmajor(sb + P_TP, 64, s),
-                        id, s > 0);
+                mma_f16(tmem + P_TM_U, desc_advance(dv, kmajor_off(128, s)),
+                        desc_advance(dt, kmajor_off(64, s)), id, s > 0);
             commit(&bar[3]);
         }
         {
@@ -745,43 +749,54 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) chunk_scan_kernel(ChunkArgs a
             constexpr uint32_t id_ws = idesc(kFmtF16, 128, 64, false, true);
             constexpr uint32_t id_p = idesc(kFmtF16, 128, 128);
             constexpr uint32_t id_o = idesc(kFmtF16, 128, 64);
+            // operand descriptors at k-step 0, computed once (stage 0 and 1)
+            const uint64_t dS = desc_kmajor(sb + S_ST, 128, 0), dDt = desc_kmajor(sb + S_DT, 128, 0);
+            const uint32_t st0 = sb + S_STG, st1 = sb + S_STG + S_STG_STRIDE;
+            const uint64_t dW0 = desc_mnmajor64(st0 + REC_W, 0), dW1 = desc_mnmajor64(st1 + REC_W, 0);
+            const uint64_t dQ0 = desc_mnmajor64(st0 + REC_QP, 0), dQ1 = desc_mnmajor64(st1 + REC_QP, 0);
+            const uint64_t dK0 = desc_kmajor(st0 + REC_KT, 128, 0), dK1 = desc_kmajor(st1 + REC_KT, 128, 0);
+            const uint64_t dA0 = desc_kmajor(st0 + REC_AQK, 64, 0), dA1 = desc_kmajor(st1 + REC_AQK, 64, 0);
             for (; c < nch; ++c) {
                 const uint32_t R = tmem + S_TM_REGION * (c & 1);
-                const uint32_t sst = sb + S_STG + (c & 1) * S_STG_STRIDE;
-                if (!wait_or_abort(&bar[c & 1], (c >> 1) & 1)) { fail = true; break; }
                 // chunk c - 1's state is current; chunk c - 2's O has left region (c & 1)
                 if (c > 0 && !wait_or_abort(&bar[5], (c - 1) & 1)) { fail = true; break; }
-                if (c > 1 && !wait_or_abort(&bar[8 + (c & 1)], ((c - 2) >> 1) & 1)) { fail = true; break; }
-                fence_after_sync();
-#pragma unroll
-                for (int s = 0; s < 8; ++s)
-                    mma_f16(R + S_TM_WS, desc_kmajor(sb + S_ST, 128, s),
-                            desc_mnmajor64(sst + REC_W, s), id_ws, s > 0);
-                commit(&bar[2]);
-                any_mma = true;
-#pragma unroll
-                for (int s = 0; s < 8; ++s)
-                    mma_f16(R + S_TM_O, desc_kmajor(sb + S_ST, 128, s),
-                            desc_mnmajor64(sst + REC_QP, s), id_ws, s > 0);
                 if (c > 0 && c + 1 < nch) {
                     // stage (c + 1) & 1 held chunk c - 1, whose last MMA group
-                    // (A_qk Delta, signalled by o_done) must be done reading it
+                    // (A_qk Delta, signalled by o_done, done by now in practice)
+                    // must be done reading it; the copy then has this chunk's
+                    // whole chain to land
                     if (!wait_or_abort(&bar[7], (c - 1) & 1)) { fail = true; break; }
                     issue_load(c + 1);
                     issued = c + 2;
                 }
+                if (c > 1 && !wait_or_abort(&bar[8 + (c & 1)], ((c - 2) >> 1) & 1)) { fail = true; break; }
+                if (!wait_or_abort(&bar[c & 1], (c >> 1) & 1)) { fail = true; break; }
+                fence_after_sync();
+                const bool odd = c & 1;
+                const uint64_t dW = odd ? dW1 : dW0, dQ = odd ? dQ1 : dQ0;
+                const uint64_t dK = odd ? dK1 : dK0, dA = odd ? dA1 : dA0;
+#pragma unroll
+                for (int s = 0; s < 8; ++s)
+                    mma_f16(R + S_TM_WS, desc_advance(dS, kmajor_off(128, s)),
+                            desc_advance(dW, mnmajor_off(s)), id_ws, s > 0);
+                commit(&bar[2]);
+                any_mma = true;
+#pragma unroll
+                for (int s = 0; s < 8; ++s)
+                    mma_f16(R + S_TM_O, desc_advance(dS, kmajor_off(128, s)),
+                            desc_advance(dQ, mnmajor_off(s)), id_ws, s > 0);
                 if (c + kL2Ahead < nch) bulk_prefetch_l2(rec0 + (c + kL2Ahead) * rstride, REC_BYTES);
                 if (!wait_or_abort(&bar[4], c & 1)) { fail = true; break; }
                 fence_after_sync();
 #pragma unroll
                 for (int s = 0; s < 4; ++s)
-                    mma_f16(R + S_TM_P, desc_kmajor(sb + S_DT, 128, s),
-                            desc_kmajor(sst + REC_KT, 128, s), id_p, s > 0);
+                    mma_f16(R + S_TM_P, desc_advance(dDt, kmajor_off(128, s)),
+                            desc_advance(dK, kmajor_off(128, s)), id_p, s > 0);
                 commit(&bar[3]);
 #pragma unroll
                 for (int s = 0; s < 4; ++s)
-                    mma_f16(R + S_TM_O, desc_kmajor(sb + S_DT, 128, s),
-                            desc_kmajor(sst + REC_AQK, 64, s), id_o, 1);
+                    mma_f16(R + S_TM_O, desc_advance(dDt, kmajor_off(128, s)),
+                            desc_advance(dA, kmajor_off(64, s)), id_o, 1);
                 commit(&bar[7]);
             }
             if (fail) {
@@ -1124,41 +1139,51 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) chunk_scan_vh_kernel(ChunkArg
             bool fail = false, any_mma = false;
             constexpr uint32_t id_d1 = idesc(kFmtF16, 128, VH, true, true);
             constexpr uint32_t id_pv = idesc(kFmtF16, 128, VH, false, true);
+            // operand descriptors at k-step 0, computed once (stage 0 and 1)
+            const uint64_t dS = desc_mnmajor64(sb + V_ST, 0), dDl = desc_mnmajor64(sb + V_DT, 0);
+            const uint32_t st0 = sb + V_STG, st1 = sb + V_STG + S_STG_STRIDE;
+            const uint64_t dW0 = desc_mnmajor128(st0 + REC_W, 16384, 0);
+            const uint64_t dW1 = desc_mnmajor128(st1 + REC_W, 16384, 0);
+            const uint64_t dK0 = desc_kmajor(st0 + REC_KT, 128, 0), dK1 = desc_kmajor(st1 + REC_KT, 128, 0);
+            const uint64_t dA0 = desc_kmajor(st0 + REC_AQK - 8192, 128, 0);
+            const uint64_t dA1 = desc_kmajor(st1 + REC_AQK - 8192, 128, 0);
             for (; c < nch; ++c) {
                 const uint32_t R = tmem + V_TM_REGION * (c & 1);
-                const uint32_t sst = sb + V_STG + (c & 1) * S_STG_STRIDE;
-                if (!wait_or_abort(&bar[c & 1], (c >> 1) & 1)) { fail = true; break; }
                 // chunk c - 1's state is current; chunk c - 2's O has left region (c & 1)
                 if (c > 0 && !wait_or_abort(&bar[5], (c - 1) & 1)) { fail = true; break; }
-                if (c > 1 && !wait_or_abort(&bar[8 + (c & 1)], ((c - 2) >> 1) & 1)) { fail = true; break; }
-                fence_after_sync();
-#pragma unroll
-                for (int s = 0; s < 8; ++s)
-                    mma_f16(R + V_TM_D1, desc_mnmajor128(sst + REC_W, 16384, s),
-                            desc_mnmajor64(sb + V_ST, s), id_d1, s > 0);
-                commit(&bar[2]);
-                any_mma = true;
                 if (c > 0 && c + 1 < nch) {
                     // stage (c + 1) & 1 held chunk c - 1, whose last MMA group
-                    // (A_qk Delta, signalled by o_done) must be done reading it
+                    // (A_qk Delta, signalled by o_done) must be done reading it;
+                    // the copy then has this chunk's whole chain to land
                     if (!wait_or_abort(&bar[7], (c - 1) & 1)) { fail = true; break; }
                     issue_load(c + 1);
                     issued = c + 2;
                 }
+                if (c > 1 && !wait_or_abort(&bar[8 + (c & 1)], ((c - 2) >> 1) & 1)) { fail = true; break; }
+                if (!wait_or_abort(&bar[c & 1], (c >> 1) & 1)) { fail = true; break; }
+                fence_after_sync();
+                const bool odd = c & 1;
+                const uint64_t dW = odd ? dW1 : dW0, dK = odd ? dK1 : dK0, dA = odd ? dA1 : dA0;
+#pragma unroll
+                for (int s = 0; s < 8; ++s)
+                    mma_f16(R + V_TM_D1, desc_advance(dW, mnmajor_off(s)),
+                            desc_advance(dS, mnmajor_off(s)), id_d1, s > 0);
+                commit(&bar[2]);
+                any_mma = true;
                 if (c + kL2Ahead < nch) bulk_prefetch_l2(rec0 + (c + kL2Ahead) * rstride, REC_BYTES);
                 if (!wait_or_abort(&bar[4], c & 1)) { fail = true; break; }
                 fence_after_sync();
 #pragma unroll
                 for (int s = 0; s < 4; ++s)
-                    mma_f16(R + V_TM_P, desc_kmajor(sst + REC_KT, 128, s),
-                            desc_mnmajor64(sb + V_DT, s), id_pv, s > 0);
+                    mma_f16(R + V_TM_P, desc_advance(dK, kmajor_off(128, s)),
+                            desc_advance(dDl, mnmajor_off(s)), id_pv, s > 0);
                 commit(&bar[3]);
                 // rows 0..63 of this A operand are the 8 KiB before A_qk in the
                 // record (finite FP16 values of U^T); they add into the dead W S rows
 #pragma unroll
                 for (int s = 0; s < 4; ++s)
-                    mma_f16(R + V_TM_D1, desc_kmajor(sst + REC_AQK - 8192, 128, s),
-                            desc_mnmajor64(sb + V_DT, s), id_pv, 1);
+                    mma_f16(R + V_TM_D1, desc_advance(dA, kmajor_off(128, s)),
+                            desc_advance(dDl, mnmajor_off(s)), id_pv, 1);
                 commit(&bar[7]);
             }
             if (fail) {

@@ -324,10 +324,12 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(ChunkArgs args)
             __syncthreads();
             if (tid == 0 && !(withhold && rnd == 0)) {
                 fence_after_sync();
+                const uint64_t da = desc_mnmajor128(sb + buf, 16384, 0);
+                const uint64_t db = desc_mnmajor64(sb + buf + 32768, 0);
 #pragma unroll
                 for (int s = 0; s < 8; ++s)
-                    mma_f16(tmem + TM_A + 64 * rnd, desc_mnmajor128(sb + buf, 16384, s),
-                            desc_mnmajor64(sb + buf + 32768, s), id_pairs, s > 0);
+                    mma_f16(tmem + TM_A + 64 * rnd, desc_advance(da, mnmajor_off(s)),
+                            desc_advance(db, mnmajor_off(s)), id_pairs, s > 0);
                 commit(&bar[rnd]);
             }
         };
@@ -342,12 +344,16 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(ChunkArgs args)
             // [X'S]^T = S^T X'^T and [Q'S]^T = S^T Q'^T need only this chunk's X', Q'
             // and the entering state; the next commit covers them.
             constexpr uint32_t ids = idesc(kFmtF16, 128, 64, false, true);
+            const uint64_t dS = desc_kmajor(sb + OFF_ST, 128, 0);
+            const uint64_t dX = desc_mnmajor64(sb + OFF_XT, 0), dQ = desc_mnmajor64(sb + OFF_QP, 0);
 #pragma unroll
             for (int s = 0; s < 8; ++s)
-                mma_f16(tmem + TM_XS, desc_kmajor(sb + OFF_ST, 128, s), desc_mnmajor64(sb + OFF_XT, s), ids, s > 0);
+                mma_f16(tmem + TM_XS, desc_advance(dS, kmajor_off(128, s)), desc_advance(dX, mnmajor_off(s)), ids,
+                        s > 0);
 #pragma unroll
             for (int s = 0; s < 8; ++s)
-                mma_f16(tmem + TM_O, desc_kmajor(sb + OFF_ST, 128, s), desc_mnmajor64(sb + OFF_QP, s), ids, s > 0);
+                mma_f16(tmem + TM_O, desc_advance(dS, kmajor_off(128, s)), desc_advance(dQ, mnmajor_off(s)), ids,
+                        s > 0);
         }
         {
             // V^T fp16 K-major [v][j] into the q staging (q is no longer read)
@@ -413,9 +419,11 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(ChunkArgs args)
         if (tid == 0) {
             fence_after_sync();
             constexpr uint32_t id = idesc(kFmtF16, 128, 64);
+            const uint64_t dA = desc_kmajor(sb + OFF_SQ, 128, 0), dT = desc_kmajor(sb + OFF_TP, 64, 0);
 #pragma unroll
             for (int s = 0; s < 4; ++s)
-                mma_f16(tmem + TM_XS, desc_kmajor(sb + OFF_SQ, 128, s), desc_kmajor(sb + OFF_TP, 64, s), id, s > 0);
+                mma_f16(tmem + TM_XS, desc_advance(dA, kmajor_off(128, s)), desc_advance(dT, kmajor_off(64, s)), id,
+                        s > 0);
             commit(&bar[3]);
         }
         {
@@ -440,12 +448,16 @@ __global__ void __launch_bounds__(NT, 1) chunk_tc_kernel(ChunkArgs args)
             fence_after_sync();
             constexpr uint32_t ido = idesc(kFmtF16, 128, 64);
             constexpr uint32_t idp = idesc(kFmtF16, 128, 128);
+            const uint64_t dD = desc_kmajor(sb + OFF_XT, 128, 0);
+            const uint64_t dAq = desc_kmajor(sb + OFF_AQK, 64, 0), dK = desc_kmajor(sb + OFF_KT, 128, 0);
 #pragma unroll
             for (int s = 0; s < 4; ++s)
-                mma_f16(tmem + TM_O, desc_kmajor(sb + OFF_XT, 128, s), desc_kmajor(sb + OFF_AQK, 64, s), ido, 1);
+                mma_f16(tmem + TM_O, desc_advance(dD, kmajor_off(128, s)), desc_advance(dAq, kmajor_off(64, s)), ido,
+                        1);
 #pragma unroll
             for (int s = 0; s < 4; ++s)
-                mma_f16(tmem + TM_P, desc_kmajor(sb + OFF_XT, 128, s), desc_kmajor(sb + OFF_KT, 128, s), idp, s > 0);
+                mma_f16(tmem + TM_P, desc_advance(dD, kmajor_off(128, s)), desc_advance(dK, kmajor_off(128, s)), idp,
+                        s > 0);
             commit(&bar[4]);
         }
         {

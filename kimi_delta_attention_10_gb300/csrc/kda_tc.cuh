@@ -65,6 +65,23 @@ __device__ __forceinline__ uint64_t desc_mnmajor128(uint32_t base, uint32_t grou
     return desc_sw128(base + s * 2048u, group_bytes, 1024u);
 }
 
+// Byte offsets of k-step s within the operands above, for desc_advance.
+__host__ __device__ constexpr uint32_t kmajor_off(uint32_t rows, uint32_t s)
+{
+    return (s >> 2) * rows * 128u + (s & 3u) * 32u;
+}
+__host__ __device__ constexpr uint32_t mnmajor_off(uint32_t s) { return s * 2048u; }
+
+// The descriptor of the same operand `bytes` further on (a multiple of 16).
+// The start field holds the shared-memory address >> 4 in its low 14 bits;
+// every shared-memory address fits, so the sum never carries out of it.
+// Issuing from descriptors computed once keeps the issuing thread's integer
+// work per MMA to one addition.
+__device__ __forceinline__ uint64_t desc_advance(uint64_t d, uint32_t bytes)
+{
+    return d + (bytes >> 4);
+}
+
 // Instruction descriptor (kind::f16 with F16 or BF16 operands, or kind::tf32), FP32 D.
 //   bits 4-5 D format (1 = F32), 7-9 A format, 10-12 B format (0 = F16,
 //   1 = BF16, 2 = TF32), 15/16 A/B major (0 = K, 1 = MN), 17-22 N >> 3, 24-28 M >> 4.
