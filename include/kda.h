@@ -126,8 +126,9 @@ kda_status kda_gate(const void* f, int32_t f_dtype, const float* A_log, const fl
  * not agree bit for bit.
  *
  * When N * H is at most the GPU's SM count (the scan then leaves SMs idle)
- * and there are at least 64 chunks, the chunks are cut into up to 4 windows
- * launched as prep(0), scan(0), prep(1), scan(1), ... on the caller's stream,
+ * and there are at least 64 chunks, the chunks are cut into min(3, chunks /
+ * 32) windows, the last a third as long as the others, launched as prep(0),
+ * scan(0), prep(1), scan(1), ... on the caller's stream,
  * each preparation after the first with programmatic dependent launch, so
  * that it runs on the SMs the scan before it leaves free.  Results are bit
  * for bit those of one window.
