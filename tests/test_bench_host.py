@@ -1,5 +1,5 @@
 """bench.py host logic on the CPU: the multi-rank reduction (gloo, world size 2),
-the whole-job rate, and the reference arm's JSON line."""
+the whole-job rate, the reference arm's JSON line, the head subset and the traffic lookup."""
 import json
 import os
 import socket
@@ -96,3 +96,31 @@ def test_chunk_windows_mirror_matches_the_library_constants():
     for chunks in (0, 31, 32, 63, 64, 100, 256, 10000):
         assert bench.chunk_windows(1, 64, chunks, 152) == max(1, min(max_w, chunks // per_w))
     assert bench.chunk_windows(3, 64, 10000, 152) == 1
+
+
+def test_first_heads_keeps_the_leading_heads():
+    from kimi_delta_attention_10_gb300.inputs import make_inputs
+    full = make_inputs([70, 5], 6, 128, 128, torch.bfloat16, 3)
+    ref = make_inputs([70, 5], 6, 128, 128, torch.bfloat16, 3)
+    x = bench.first_heads(full, 4)
+    for n in ("q", "k", "v", "f"):
+        assert getattr(x, n).shape == (75, 4, 128) and getattr(x, n).is_contiguous()
+        assert torch.equal(getattr(x, n), getattr(ref, n)[:, :4])
+    assert torch.equal(x.b, ref.b[:, :4]) and x.b.is_contiguous()
+    assert torch.equal(x.A_log, ref.A_log[:4]) and torch.equal(x.dt_bias, ref.dt_bias[:4])
+    assert torch.equal(x.cu_seqlens, ref.cu_seqlens)
+
+
+def test_kernel_traffic_only_while_the_sources_match(tmp_path, monkeypatch):
+    src = tmp_path / "k.cu"
+    src.write_bytes(b"kernel v1")
+    import hashlib
+    sha = hashlib.sha256(b"kernel v1").hexdigest()[:16]
+    (tmp_path / "profiles").mkdir()
+    (tmp_path / "profiles" / "traffic.json").write_text(json.dumps(
+        {"key": {"sources": ["k.cu"], "sources_sha256_16": sha, "dram_bytes_per_call": 1234}}))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.kernel_traffic("key") == 1234
+    assert bench.kernel_traffic("other") is None
+    src.write_bytes(b"kernel v2")                    # changed since the capture
+    assert bench.kernel_traffic("key") is None
