@@ -472,18 +472,32 @@ __device__ __forceinline__ void chunk_inverse_f32(float (*akk)[LDA], float (*Tf)
     __syncthreads();
 }
 
+// kBetaInTp: beta lies inside the T' tile, so each thread reads its beta_j
+// before the inverse's last barrier (once T' is being written it is gone).
+template <bool kBetaInTp = false>
 __device__ __forceinline__ void chunk_inverse(float (*akk)[LDA], float (*Tf)[LDA],
                                               const float* sbeta, unsigned char* tp, int tid,
                                               int warp, int lane)
 {
+    float4 bq[2][2];
+    auto read_beta = [&] {
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int j0 = ((tid + u * NT) % 8) * 8;
+            bq[u][0] = ld4(sbeta + j0);
+            bq[u][1] = ld4(sbeta + j0 + 4);
+        }
+    };
+    if constexpr (kBetaInTp) read_beta();
     chunk_inverse_f32(akk, Tf, tid, warp, lane);
+    if constexpr (!kBetaInTp) read_beta();
     // T'[i][j] = T[i][j] beta_j (j <= i), row i, 8 columns per store
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
         const int e = tid + u * NT;                  // 512 pieces of 8
         const int i = e / 8, j0 = (e % 8) * 8;
         const float4 ta = ld4(&Tf[i][j0]), tb = ld4(&Tf[i][j0 + 4]);
-        const float4 ba = ld4(sbeta + j0), bb = ld4(sbeta + j0 + 4);
+        const float4 ba = bq[u][0], bb = bq[u][1];
         float v8[8];
 #pragma unroll
         for (int x = 0; x < 8; ++x) {

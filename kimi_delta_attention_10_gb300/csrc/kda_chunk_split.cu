@@ -171,16 +171,29 @@ constexpr uint32_t P_XT = 49152;       // X'^T fp16 K-major [128 c][64 j]
 constexpr uint32_t P_SV = 65536;       // v staging -> V^T fp16 K-major [128 v][64 j]
 constexpr uint32_t P_AQK = 81920;      // A_qk fp16 [64 i][64 j]
 constexpr uint32_t P_TP = 90112;       // T' fp16 [64 i][64 j]
-constexpr uint32_t P_RQ = 98304;       // 1/|q_t| fp32 [64]
-constexpr uint32_t P_RK = P_RQ + 256;  // 1/|k_t|
-constexpr uint32_t P_DQK = P_RK + 256; // q^_t . k^_t
-constexpr uint32_t P_BETA = P_DQK + 256;
-constexpr uint32_t P_TOT = P_BETA + 256;   // half-chunk decay fp32 [2][128]
-constexpr uint32_t P_BAR = P_TOT + 1024;   // 10 mbarriers, TMEM slot, the next units
-constexpr uint32_t P_SMEM = P_BAR + 256 + 1024;
+// Until T' is written (the end of the inverse) its region holds the unit's
+// small vectors: beta (read into registers before the inverse's last
+// barrier), the norms, q^.k^ and the half-chunk decay products.
+constexpr uint32_t P_BETA = P_TP;          // beta fp32 [64]
+constexpr uint32_t P_RQ = P_TP + 256;      // 1/|q_t| fp32 [64]
+constexpr uint32_t P_RK = P_RQ + 256;      // 1/|k_t|
+constexpr uint32_t P_DQK = P_RK + 256;     // q^_t . k^_t
+constexpr uint32_t P_TOT = P_DQK + 256;    // half-chunk decay fp32 [2][128]
+constexpr uint32_t P_BAR = 98304;          // 10 mbarriers, TMEM slot, the next units
+constexpr uint32_t P_LAYOUT = P_BAR + 256;
+// 97 KiB per CTA, so that two CTAs (with the 1 KiB each that the system
+// keeps) fit the 196 KiB shared-memory carveout and leave the SM 60 KiB of
+// L1 (the next carveout, 228 KiB, leaves 28 KiB, less than the two CTAs'
+// register-spill slots).  The layout needs 1024-byte alignment: the slack
+// covers a dynamic base aligned to 256 bytes; a CTA that finds less reports
+// KDA_ERR_ALIGNMENT and leaves.
+constexpr uint32_t P_SMEM = 99328;
+constexpr int P_CARVEOUT_PCT = 85;         // of 228 KiB, rounded up to the 196 KiB carveout
+static_assert(P_TOT + 1024 <= P_TP + 8192, "the small vectors fit in the T' region");
 static_assert(P_TF + C * LDA * 4 <= P_XT, "A_kk and T fit below X'^T");
 static_assert(P_PAIR + 49152 <= P_XT, "pair-sum operands fit below X'^T");
-static_assert(2 * (P_SMEM + 1024) <= 233472, "two preparation CTAs per SM");
+static_assert(P_LAYOUT + 768 <= P_SMEM, "slack for a 256-byte-aligned base");
+static_assert(2 * (P_SMEM + 1024) <= 200704, "two preparation CTAs in the 196 KiB carveout");
 constexpr uint32_t P_TM_A = 0, P_TM_W = 0, P_TM_U = 64, P_TM_COLS = 256;
 
 // TMA descriptors of the preparation's inputs, each a [T][H][128] tensor read
@@ -226,6 +239,10 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(ChunkArgs args,
     // dependent launch) completes only after that scan: its last CTA waits for
     // it, so the next scan, launched after this grid, sees the state carry.
     if (wait_primary && blockIdx.x == gridDim.x - 1 && tid == 0) grid_dependency_wait();
+    if (pad + P_LAYOUT > P_SMEM) {                         // the same for every CTA
+        if (tid == 0) report_status(args.status, KDA_ERR_ALIGNMENT);
+        return;
+    }
     const int32_t* off = hdr + kHdrOff;
 
     float (*akk)[LDA] = reinterpret_cast<float (*)[LDA]>(sm + P_AKK);
@@ -515,7 +532,7 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(ChunkArgs args,
         __syncthreads();
 
         // ---- 6: T' = (I + A_kk)^-1 diag(beta)
-        chunk_inverse(akk, Tf, sbeta, sm + P_TP, tid, warp, lane);
+        chunk_inverse<true>(akk, Tf, sbeta, sm + P_TP, tid, warp, lane);
         fence_async_smem();
         fence_before_sync();
         __syncthreads();
@@ -1366,6 +1383,9 @@ cudaError_t launch_prep_typed(const ChunkArgs& a, const PrepMaps& maps, const in
     auto kern = chunk_prep_kernel<TIn, kGate>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)P_SMEM);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 P_CARVEOUT_PCT);
     if (e != cudaSuccess) return e;
     const int sms = device_sm_count();
     const int64_t ctas = std::min<int64_t>(units, 2 * (int64_t)(sms > 0 ? sms : 152));
